@@ -1,0 +1,426 @@
+"""Benchmark of the paged decode path (one JSON line on stdout).
+
+A step is one pass of the whole hot path over one batch: the copy-on-write
+block copies (when the workload has any), the cache write of the new tokens,
+and paged decode attention.  The default workload is the Llama-2-7B-shaped
+decode (64 sequences of 512..4096 tokens, 32/32 heads, head_dim 128, fp16,
+block size 16); ``--config`` selects another named workload for profiling.
+
+Metric: KV bytes read per step (every K and V element of every sequence's
+tokens, counted once per distinct slot) / step time, in GB/s; also
+sequence·layer/s.  Inputs are resident in HBM before timing starts; the KV
+working set (2.4 GB for the default workload) is far larger than L2, so no
+flush is needed between steps.
+
+``--impl reference`` times the CPU oracle (float64 NumPy) on a bounded
+sample of the same workload on the host cores instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as W  # noqa: E402
+
+METRIC = "paged decode attention: KV-read HBM GB/s vs GB300 peak; seq·layer/s"
+DEFAULT_CONFIG = "llama2-7b"
+SMI_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "decode_traffic.txt")
+DECODE_SOURCES = [os.path.join(ROOT, "paged_kv_cache_54_gb300", "csrc", f)
+                  for f in ("pa_decode.cuh", "pa_decode_params.h", "pa_common.cuh")]
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=500)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--config", default=DEFAULT_CONFIG, choices=W.CONFIG_ORDER)
+    ap.add_argument("--seed", type=int, default=None)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f), "measured"
+    except OSError:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}, "fallback"
+
+
+def decode_source_hash() -> str:
+    h = hashlib.sha256()
+    for p in DECODE_SOURCES:
+        with open(p, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(config: str):
+    """DRAM bytes per decode launch from the committed ncu summary, if it was
+    taken on the current decode source; else None."""
+    try:
+        lines = open(TRAFFIC_FILE).read().splitlines()
+    except OSError:
+        return None
+    src, val = None, None
+    for ln in lines:
+        if ln.startswith("source_sha:"):
+            src = ln.split(":", 1)[1].strip()
+        if ln.startswith(f"bytes_per_launch[{config}]:"):
+            val = float(ln.split(":", 1)[1].strip())
+    if src != decode_source_hash():
+        return None
+    return val
+
+
+class ClockSampler:
+    def __init__(self, index: int):
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={SMI_FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-i", str(index)], stdout=subprocess.PIPE,
+                stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        self.t_on = self.t_off = None
+
+    def mark_start(self):
+        self.t_on = time.time()
+
+    def mark_end(self):
+        self.t_off = time.time()
+
+    def finish(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        rows = [r.split(",") for r in out.strip().splitlines() if r.count(",") >= 8]
+        # samples are not time-stamped: keep the ones taken while under load
+        sm = [float(r[1]) for r in rows if r[1].strip().replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].strip().replace(".", "").isdigit()]
+        load = [r for r in rows if float(r[3] or 0) > 200.0] if rows else []
+        use = load or rows
+        sm_load = [float(r[1]) for r in use] if use else sm
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in use:
+            for i, n in enumerate(names):
+                if r[5 + i].strip() == "Active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm_load) if sm_load else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": sorted(reasons),
+                "samples": len(rows), "samples_under_load": len(load)}
+
+
+def workload_bytes(w):
+    kv = w.kv_unique_bytes()
+    qo = 2 * w.S * w.Hq * w.d * 2
+    tables = int(sum(-(-int(L) // w.bs) for L in w.seq_lens)) * 4 + w.S * 4
+    return kv, kv + qo + tables
+
+
+# ---------------------------------------------------------------------------
+# the GPU arm
+# ---------------------------------------------------------------------------
+def run_ours(args, rank, world, local):
+    import torch
+    import paged_kv_cache_54_gb300 as pa
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device(f"cuda:{local}"))
+    torch.cuda.set_device(local)
+    dev = f"cuda:{local}"
+    seed = args.seed if args.seed is not None else W.CONFIG_ORDER.index(args.config) + 1
+    w = W.make_workload(args.config, seed, device=dev)
+    shape = (w.num_blocks, w.Hkv, w.bs, w.d)
+    if w.cache_dtype in ("e4m3", "e5m2"):
+        kc = torch.zeros(shape, dtype=torch.uint8, device=dev)
+        vc = torch.zeros(shape, dtype=torch.uint8, device=dev)
+    else:
+        dt = torch.float16 if w.cache_dtype == "f16" else torch.bfloat16
+        kc = torch.zeros(shape, dtype=dt, device=dev)
+        vc = torch.zeros(shape, dtype=dt, device=dev)
+    kw = dict(cache_dtype=w.cache_dtype, k_scale=w.k_scale, v_scale=w.v_scale)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    pa.pa_reshape_and_cache(w.ctx_k, w.ctx_v, torch.from_numpy(w.ctx_slots).to(dev), kc, vc,
+                            device_error=err, **kw)
+    w.ctx_k = w.ctx_v = None
+    torch.cuda.synchronize()
+    bt = torch.from_numpy(w.block_tables).to(dev)
+    sl = torch.from_numpy(w.seq_lens).to(dev)
+    slots = torch.from_numpy(w.new_slots).to(dev)
+    pairs = torch.from_numpy(w.cow_pairs).to(dev)
+    out = torch.empty_like(w.q)
+    P = w.partition_size
+    ws = torch.empty(pa.pa_decode_workspace_size(w.S, w.Hq, w.Hkv, w.d, w.max_seq_len, P),
+                     dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    n_pairs = len(w.cow_pairs)
+    max_parts_gt1 = w.max_seq_len > (P or _auto_partition(w))
+    launches_per_step = (1 if n_pairs else 0) + 1 + 2 + (1 if max_parts_gt1 else 0)
+
+    def step(dec_events=None):
+        if n_pairs:
+            pa.pa_copy_blocks(kc, vc, pairs, cache_dtype=w.cache_dtype, device_error=err)
+        pa.pa_reshape_and_cache(w.new_k, w.new_v, slots, kc, vc, device_error=err, **kw)
+        if dec_events is not None:
+            dec_events[0].record(stream)
+        pa.pa_decode(out, w.q, kc, vc, bt, sl, w.max_seq_len, w.scale, partition_size=P,
+                     workspace=ws, device_error=err, **kw)
+        if dec_events is not None:
+            dec_events[1].record(stream)
+
+    sampler = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(K)]
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    if sampler:
+        sampler.mark_start()
+    torch.cuda.synchronize()
+    t0.record(stream)
+    for i in range(K):
+        step(ev[i])
+    t1.record(stream)
+    torch.cuda.synchronize()
+    if sampler:
+        sampler.mark_end()
+    if world > 1:
+        dist.barrier()
+    elapsed = t0.elapsed_time(t1) / 1e3
+    dec_ms = [a.elapsed_time(b) for a, b in ev]
+    dec_avg = statistics.mean(dec_ms) / 1e3
+    if world > 1:
+        t = torch.tensor([elapsed], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed = float(t.item())
+    derr = int(err.item())
+
+    # end to end through the C ABI with host buffers (pinned), copies inside
+    host = {
+        "q": w.q.cpu().pin_memory(), "k": w.new_k.cpu().pin_memory(),
+        "v": w.new_v.cpu().pin_memory(), "slots": slots.cpu().pin_memory(),
+        "bt": bt.cpu().pin_memory(), "sl": sl.cpu().pin_memory(),
+        "pairs": pairs.cpu().pin_memory(),
+    }
+    out_host = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    dq, dk, dv = torch.empty_like(w.q), torch.empty_like(w.new_k), torch.empty_like(w.new_v)
+    dslots, dbt, dsl, dpairs = (torch.empty_like(slots), torch.empty_like(bt),
+                                torch.empty_like(sl), torch.empty_like(pairs))
+    h2d = sum(t.numel() * t.element_size() for k, t in host.items() if k != "pairs" or n_pairs)
+    d2h = out.numel() * out.element_size()
+
+    def e2e_step():
+        dq.copy_(host["q"], non_blocking=True)
+        dk.copy_(host["k"], non_blocking=True)
+        dv.copy_(host["v"], non_blocking=True)
+        dslots.copy_(host["slots"], non_blocking=True)
+        dbt.copy_(host["bt"], non_blocking=True)
+        dsl.copy_(host["sl"], non_blocking=True)
+        if n_pairs:
+            dpairs.copy_(host["pairs"], non_blocking=True)
+            pa.pa_copy_blocks(kc, vc, dpairs, cache_dtype=w.cache_dtype, device_error=err)
+        pa.pa_reshape_and_cache(dk, dv, dslots, kc, vc, device_error=err, **kw)
+        pa.pa_decode(out, dq, kc, vc, dbt, dsl, w.max_seq_len, w.scale, partition_size=P,
+                     workspace=ws, device_error=err, **kw)
+        out_host.copy_(out, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    KE = max(10, K // 5)
+    e0.record(stream)
+    for _ in range(KE):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_t = e0.elapsed_time(e1) / 1e3 / KE
+    clocks = sampler.finish() if sampler else None
+    if world > 1:
+        dist.destroy_process_group()
+    if rank != 0:
+        return
+    kv_bytes, alg_bytes = workload_bytes(w)
+    step_t = elapsed / K
+    peaks, peak_kind = measured_peaks()
+    achieved = alg_bytes / dec_avg / 1e9
+    traffic = recorded_traffic(args.config)
+    line = {
+        "metric": METRIC,
+        "value": round(world * kv_bytes / step_t / 1e9, 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": args.warmup,
+        "ms_per_step": round(step_t * 1e3, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": w.cache_dtype,
+        "data": "synthetic (seeded N(0,1) K/V/q, seeded lengths and shuffled block pool)",
+        "config": {
+            "workload": f"{args.config}: {_describe(w)}",
+            "num_seqs": w.S, "q_heads": w.Hq, "kv_heads": w.Hkv, "head_dim": w.d,
+            "block_size": w.bs, "cache_dtype": w.cache_dtype, "q_dtype": w.q_dtype,
+            "partition_size": P or _auto_partition(w),
+            "kv_bytes_per_step": kv_bytes, "seed": seed,
+            "l2": "inputs larger than L2 (KV working set %.2f GB vs 129 MB L2)" % (kv_bytes / 1e9),
+            "parallelism": f"replicas x{world}",
+        },
+        "seq_layer_per_s": round(world * w.S / step_t, 1),
+        "gpu_launches": launches_per_step * K,
+        "device_error": derr,
+        "roofline": {
+            "kernel": "pa_decode (plan + persistent decode + merge, CUDA events)",
+            "bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
+            "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
+            "peak_kind": f"{peak_kind} (copy, burst)",
+            "traffic": traffic,
+            "algorithmic_bytes_per_launch": alg_bytes,
+            "avg_launch_ms": round(dec_avg * 1e3, 4),
+            "frac_of_nominal_8tbs": round(achieved / 8000.0, 4),
+        },
+        "e2e": {"value": round(kv_bytes / e2e_t / 1e9, 2), "unit": "GB/s",
+                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+                "ms_per_step": round(e2e_t * 1e3, 4)},
+        "clocks": clocks,
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(args.config, seed, budget_s=12.0)
+    print(json.dumps(line), flush=True)
+
+
+def _auto_partition(w):
+    P = 512
+    while P > 64 and w.S * w.Hkv * (-(-w.max_seq_len // P)) < 1024:
+        P //= 2
+    return P
+
+
+def _describe(w):
+    lens = w.seq_lens
+    return (f"{w.S} seqs, L {int(lens.min())}..{int(lens.max())} (mean {float(lens.mean()):.0f}), "
+            f"{w.Hq}q/{w.Hkv}kv heads, d {w.d}, bs {w.bs}, {w.cache_dtype} KV, {w.num_blocks} blocks")
+
+
+# ---------------------------------------------------------------------------
+# the CPU oracle, timed on a bounded sample
+# ---------------------------------------------------------------------------
+def _oracle_sample(config: str, seed: int, n_seqs: int):
+    """Oracle paged cache holding the first n_seqs sequences of the workload
+    (their blocks renumbered into a compact pool, fresh seeded values)."""
+    import torch
+    from oracle.cache import PagedKVCache, bits_to_f64
+    full = W.make_workload(config, seed, values=False)
+    w = W.subset(full, range(min(n_seqs, full.S)), seed)
+
+    def bits(t):
+        return t.contiguous().view(torch.int16).numpy().view(np.uint16)
+
+    c = PagedKVCache(w.num_blocks, w.Hkv, w.bs, w.d, w.cache_dtype, w.k_scale, w.v_scale)
+    c.reshape_and_cache(bits(w.ctx_k), bits(w.ctx_v), w.src_dtype, w.ctx_slots)
+    c.reshape_and_cache(bits(w.new_k), bits(w.new_v), w.src_dtype, w.new_slots)
+    qv = bits_to_f64(bits(w.q), w.q_dtype)
+    kv = int(w.seq_lens.astype(np.int64).sum()) * w.Hkv * w.d * w.elt_bytes() * 2
+    return w, c, w.block_tables, w.seq_lens, qv, kv
+
+
+def cpu_baseline(config: str, seed: int, budget_s: float = 12.0, n_seqs: int = 4):
+    from oracle import attention as A
+    w, c, tables, lens, qv, kv = _oracle_sample(config, seed, n_seqs)
+    t0 = time.perf_counter()
+    reps = 0
+    while True:
+        A.paged_decode(qv, c.k, c.v, w.cache_dtype, tables, lens, w.scale, w.k_scale, w.v_scale)
+        reps += 1
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    dt = (time.perf_counter() - t0) / reps
+    return {"value": round(kv / dt / 1e9, 4), "unit": "GB/s", "cores": _cores(),
+            "kind": "oracle",
+            "sample": f"first {len(lens)} sequences of {config} (all {w.Hq} query heads, "
+                      f"{int(lens.sum())} tokens), float64 NumPy oracle, {reps} passes in {budget_s:.0f} s",
+            "seq_layer_per_s": round(len(lens) / dt, 3)}
+
+
+def _cores() -> int:
+    try:
+        from threadpoolctl import threadpool_info
+        n = max((i.get("num_threads", 1) for i in threadpool_info()), default=1)
+        return int(n)
+    except Exception:
+        return len(os.sched_getaffinity(0))
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    seed = args.seed if args.seed is not None else W.CONFIG_ORDER.index(args.config) + 1
+    from oracle import attention as A
+    w, c, tables, lens, qv, kv = _oracle_sample(args.config, seed, 2)
+    for _ in range(args.warmup):
+        A.paged_decode(qv, c.k, c.v, w.cache_dtype, tables, lens, w.scale, w.k_scale, w.v_scale)
+    steps = min(args.steps, 20)
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        A.paged_decode(qv, c.k, c.v, w.cache_dtype, tables, lens, w.scale, w.k_scale, w.v_scale)
+    dt = (time.perf_counter() - t0) / steps
+    val = round(kv / dt / 1e9, 4)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": val, "unit": "GB/s", "n_gpus": world,
+        "steps": steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": f"{args.config} (bounded sample: 2 sequences)"},
+        "cpu_baseline": {"value": val, "unit": "GB/s", "cores": _cores(), "kind": "oracle",
+                         "sample": f"first 2 sequences of {args.config}, all query heads"},
+        "e2e": {"value": val, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        run_ours(args, rank, world, local)
+
+
+if __name__ == "__main__":
+    main()

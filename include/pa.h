@@ -1,0 +1,205 @@
+/*
+ * pa.h — C ABI of libpa, the GB300 (sm_103a) paged KV-cache decode path.
+ *
+ * Three device operations, each asynchronous on the caller's stream:
+ *
+ *   pa_reshape_and_cache  write new tokens' K and V into fixed-size physical
+ *                         blocks through a slot mapping (optionally as FP8
+ *                         with a per-tensor scale);
+ *   pa_decode             single-query decode attention over the paged cache,
+ *                         reached through per-sequence block tables;
+ *   pa_copy_blocks        whole-block copies, the copy step of copy-on-write.
+ *
+ * Pages that state the problem (cited by title and section):
+ *   [P1] "【性能飞跃】从 OOM 到丝滑推理:深度工程化 RAG 架构下的内存管理艺术"
+ *        §2.1 (logical blocks mapped to scattered physical blocks through a
+ *        block table; fixed block size, default 16), §3.2 (prefix sharing and
+ *        copy-on-write), §6.1 (beam search shares blocks, copies only the
+ *        last one).
+ *   [P2] "大模型推理引擎显存优化：从 KV Cache 管理到连续批处理的工程实践"
+ *        §2.2 (block table per request, blocks from a global pool), §三
+ *        (refcounted block manager).
+ *   [P3] m.lsln.cn/news/213354 (KV-cache memory article; title not
+ *        preserved) §3.2 (paging), §4.3 (reference counts), §6.1–§6.3 (FP8:
+ *        store value / scale, read back × scale; e4m3 and e5m2; default
+ *        scale 1.0, per tensor).
+ *   [P4] "第3章 vLLM架构与显存使用：PagedAttention、KV Cache管理与显存池化技术"
+ *        §3.2 (block life cycle, shared blocks), §3.3 (copy-on-write: take a
+ *        new block, copy the old one, write the new one).
+ * The pages do not write the attention formula or any kernel down; the
+ * attention computed here is the textbook scaled dot-product attention of
+ * one query row over the sequence's tokens.
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * - Ownership: the caller owns every buffer, including the decode workspace.
+ *   The library allocates no device or host memory and never synchronises.
+ * - Pointers: every array argument is a DEVICE pointer except `cache`
+ *   (a host struct read during the call).  Device arrays must be 16-byte
+ *   aligned and densely packed in the layouts stated below.
+ * - Streams: `stream` is a cudaStream_t (NULL = the legacy default stream).
+ *   Work is only enqueued; results are ready when the stream reaches them.
+ * - Errors: invalid arguments are rejected on the host before anything is
+ *   launched (PA_ERR_INVALID / PA_ERR_UNSUPPORTED).  A failed launch returns
+ *   PA_ERR_CUDA.  Data that only the device can see (a block id outside the
+ *   pool, a slot outside the cache, a length beyond the table width) is
+ *   checked in the kernels: the bad access is skipped and a nonzero code is
+ *   written to *device_error (when the pointer is not NULL; the first error
+ *   wins), which the caller reads after synchronising.  Kernels never trap.
+ * - Device error codes: 1 block id out of range, 2 slot out of range,
+ *   3 sequence length out of range, 4 a pipeline wait exceeded its time
+ *   limit, 5 copy pair out of range.
+ */
+#ifndef PA_H_
+#define PA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define PA_API __attribute__((visibility("default")))
+#else
+#define PA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *pa_stream_t; /* same type as cudaStream_t */
+
+typedef enum {
+  PA_OK = 0,
+  PA_ERR_INVALID = 1,      /* null pointer, negative size, misalignment, ... */
+  PA_ERR_UNSUPPORTED = 2,  /* valid but outside the supported set below */
+  PA_ERR_CUDA = 3,         /* a CUDA runtime call or launch failed */
+  PA_ERR_DEVICE_CHECK = 4  /* for callers that map a nonzero *device_error */
+} pa_status;
+
+typedef enum {
+  PA_F16 = 0,       /* IEEE binary16 */
+  PA_BF16 = 1,      /* bfloat16 */
+  PA_FP8_E4M3 = 2,  /* OCP E4M3 (max 448, no inf), one byte */
+  PA_FP8_E5M2 = 3   /* OCP E5M2 (max 57344), one byte */
+} pa_dtype;
+
+/*
+ * Description of one paged cache pair (K and V).
+ * Layout of k_cache and v_cache: [num_blocks, kv_heads, block_size, head_dim]
+ * elements of `dtype`, row-major.  Physical block b holds block_size token
+ * slots of every KV head; flat slot = b * block_size + offset.
+ * For FP8 caches a stored code c means c * k_scale (K) or c * v_scale (V):
+ * values are stored as value / scale ([P3] §6.1; default 1.0, §6.3).
+ * Supported set: block_size in {8, 16, 32}; head_dim in {64, 128}.
+ */
+typedef struct {
+  int32_t num_blocks;
+  int32_t kv_heads;
+  int32_t block_size;
+  int32_t head_dim;
+  int32_t dtype;     /* pa_dtype */
+  float k_scale;     /* FP8 only; must be > 0 and finite */
+  float v_scale;
+} pa_cache_desc;
+
+/*
+ * pa_reshape_and_cache — write T new tokens into the paged caches.
+ * ([P1] §2.1 / [P2] §2.2 block tables; [P3] §6.1 FP8 with a scale.)
+ *
+ *   key, value     device, [num_tokens, kv_heads, head_dim] of src_dtype
+ *                  (PA_F16 or PA_BF16), row-major.
+ *   slot_mapping   device int64 [num_tokens]: flat slot of token t;
+ *                  -1 marks a padding row that is skipped.
+ *   k_cache/v_cache  device caches described by *cache.
+ * For every token t with slot >= 0 and every head h:
+ *   cache[slot / block_size, h, slot % block_size, :] = enc(row[t, h, :])
+ * where enc is a bit copy for 16-bit caches (src_dtype must equal
+ * cache->dtype) and, for FP8 caches, round-to-nearest-even with saturation
+ * to the largest finite value of (float)x / scale computed in IEEE float32.
+ * Slots must be distinct among the call's tokens.  A slot >= num_blocks *
+ * block_size is skipped and reported as device error 2.
+ */
+PA_API pa_status pa_reshape_and_cache(const void *key, const void *value,
+                               int32_t src_dtype, const int64_t *slot_mapping,
+                               int32_t num_tokens, void *k_cache, void *v_cache,
+                               const pa_cache_desc *cache, int *device_error,
+                               pa_stream_t stream);
+
+/*
+ * pa_decode_workspace_size — bytes of device workspace pa_decode needs for
+ * these sizes (same arguments as pa_decode; 0 partition_size = automatic).
+ * Returns 0 for arguments pa_decode would reject.
+ */
+PA_API size_t pa_decode_workspace_size(int32_t num_seqs, int32_t num_q_heads,
+                                int32_t num_kv_heads, int32_t head_dim,
+                                int32_t max_seq_len, int32_t partition_size);
+
+/*
+ * pa_decode — single-query decode attention over the paged cache.
+ *
+ * For every sequence s < num_seqs and query head hq < num_q_heads, with
+ * G = num_q_heads / kv_heads and KV head h = hq / G (a group of G query heads
+ * shares one KV head):
+ *   out[s, hq, :] = sum_{i < L_s} softmax_i(scale * <q[s, hq, :], k_i>) v_i
+ * where L_s = seq_lens[s] and token i of sequence s is read from physical
+ * block block_tables[s, i / block_size] at offset i % block_size
+ * ([P1] §2.1, [P2] §2.2, [P3] §3.2; FP8 codes are multiplied by the scales
+ * of *cache, [P3] §6.1).  L_s = 0 gives zeros.
+ *
+ *   out            device [num_seqs, num_q_heads, head_dim], q_dtype.
+ *   q              device [num_seqs, num_q_heads, head_dim], q_dtype
+ *                  (PA_F16 or PA_BF16; for 16-bit caches it must equal the
+ *                  cache dtype).
+ *   block_tables   device int32 [num_seqs, max_blocks_per_seq]; only the
+ *                  first ceil(L_s / block_size) entries of a row are read.
+ *   seq_lens       device int32 [num_seqs]; each must satisfy
+ *                  0 <= L_s <= min(max_seq_len, max_blocks_per_seq * block_size).
+ *   max_seq_len    host upper bound of seq_lens, used to size the work.
+ *   scale          softmax scale (e.g. 1/sqrt(head_dim)).
+ *   partition_size 0 = automatic; else the number of tokens one work item
+ *                  covers (multiple of 64 and of block_size, <= 1024).
+ *                  Sequences longer than one partition are split and merged
+ *                  exactly (flash-decoding), so the result does not depend
+ *                  on it beyond rounding.
+ *   workspace      device scratch of at least pa_decode_workspace_size(...)
+ *                  bytes, 256-byte aligned; contents need no initialisation.
+ *                  Calls sharing one workspace must be stream-ordered.
+ * Supported set: num_q_heads / kv_heads in {1, 2, 4, 8}; cache dtypes of
+ * pa_cache_desc; FP8 caches accept q in PA_F16 or PA_BF16.
+ */
+PA_API pa_status pa_decode(void *out, const void *q, int32_t q_dtype,
+                    int32_t num_seqs, int32_t num_q_heads,
+                    const void *k_cache, const void *v_cache,
+                    const pa_cache_desc *cache, const int32_t *block_tables,
+                    int32_t max_blocks_per_seq, const int32_t *seq_lens,
+                    int32_t max_seq_len, float scale, int32_t partition_size,
+                    void *workspace, size_t workspace_bytes, int *device_error,
+                    pa_stream_t stream);
+
+/*
+ * pa_copy_blocks — copy-on-write block copies ([P4] §3.3; [P1] §6.1: a
+ * forked beam copies only the shared last block).
+ *
+ *   block_mapping  device int64 [num_pairs, 2]: (src, dst) physical blocks.
+ * For each pair, block dst of k_cache and of v_cache becomes a bit-exact copy
+ * of block src (all kv_heads * block_size * head_dim elements).
+ * Destinations must be distinct and never also a source, so the result does
+ * not depend on the order of the copies.  Out-of-range ids are skipped and
+ * reported as device error 5.
+ */
+PA_API pa_status pa_copy_blocks(void *k_cache, void *v_cache, const pa_cache_desc *cache,
+                         const int64_t *block_mapping, int32_t num_pairs,
+                         int *device_error, pa_stream_t stream);
+
+/* Static description of a status code. */
+PA_API const char *pa_status_string(pa_status status);
+
+/* Last CUDA error text seen by a call that returned PA_ERR_CUDA on this
+ * thread (static storage; empty if none). */
+PA_API const char *pa_last_cuda_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PA_H_ */

@@ -78,8 +78,7 @@ class PagedKVCache:
             if src_dtype != self.dtype:
                 raise ValueError("16-bit caches take rows of their own dtype")
             return np.asarray(src_bits, dtype=np.uint16)
-        vals = bits_to_f64(src_bits, src_dtype).astype(np.float32)  # exact
-        return _fp8.quantize(vals, scale, self.dtype)
+        return _fp8.quantize_bits16(src_bits, src_dtype, scale, self.dtype)
 
     def reshape_and_cache(self, key_bits: np.ndarray, value_bits: np.ndarray,
                           src_dtype: str, slot_mapping: np.ndarray) -> None:

@@ -25,6 +25,7 @@ from __future__ import annotations
 
 import math
 from dataclasses import dataclass
+from functools import lru_cache
 
 import numpy as np
 
@@ -134,3 +135,25 @@ def quantize(values_f32: np.ndarray, scale: float, fmt_name: str) -> np.ndarray:
                       for u in uniq.view(np.float32)], dtype=np.uint8)
     out[:] = codes[inv.reshape(-1)]
     return out.reshape(q.shape)
+
+
+def _bits16_to_f32(bits: np.ndarray, src_dtype: str) -> np.ndarray:
+    b = np.asarray(bits, dtype=np.uint16)
+    if src_dtype == "f16":
+        return b.view(np.float16).astype(np.float32)
+    if src_dtype == "bf16":
+        return (b.astype(np.uint32) << 16).view(np.float32)
+    raise ValueError(src_dtype)
+
+
+@lru_cache(maxsize=16)
+def _table16(src_dtype: str, scale: float, fmt_name: str) -> np.ndarray:
+    """Code of every 16-bit source pattern (same rule as ``quantize``)."""
+    allbits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    with np.errstate(invalid="ignore", over="ignore"):   # NaN / inf patterns included
+        return quantize(_bits16_to_f32(allbits, src_dtype), scale, fmt_name)
+
+
+def quantize_bits16(bits: np.ndarray, src_dtype: str, scale: float, fmt_name: str) -> np.ndarray:
+    """``quantize`` of fp16/bf16 values given as bit patterns, by table."""
+    return _table16(src_dtype, float(scale), fmt_name)[np.asarray(bits, dtype=np.uint16)]

@@ -1,0 +1,192 @@
+"""Python binding of libpa, the sm_103a paged KV-cache decode path.
+
+Argument marshalling only: every step runs in the CUDA kernels of
+``libpa.so`` (built in-tree by ``paged_kv_cache_54_gb300.build``).  The
+functions carry the C ABI's names:
+
+    pa_reshape_and_cache   write new tokens' K/V into the paged caches
+    pa_decode              paged single-query decode attention
+    pa_copy_blocks         whole-block copies (copy-on-write)
+    pa_decode_workspace_size
+
+PyTorch supplies the device memory and the stream; there is no CPU or
+PyTorch fallback: if ``libpa.so`` is missing, every call raises.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libpa.so")
+
+PA_F16, PA_BF16, PA_FP8_E4M3, PA_FP8_E5M2 = 0, 1, 2, 3
+DTYPE_CODES = {"f16": PA_F16, "bf16": PA_BF16, "e4m3": PA_FP8_E4M3, "e5m2": PA_FP8_E5M2}
+_TORCH_CODES = {torch.float16: PA_F16, torch.bfloat16: PA_BF16}
+if hasattr(torch, "float8_e4m3fn"):
+    _TORCH_CODES[torch.float8_e4m3fn] = PA_FP8_E4M3
+if hasattr(torch, "float8_e5m2"):
+    _TORCH_CODES[torch.float8_e5m2] = PA_FP8_E5M2
+
+EXPORTED = ("pa_reshape_and_cache", "pa_decode_workspace_size", "pa_decode",
+            "pa_copy_blocks", "pa_status_string", "pa_last_cuda_error")
+
+
+class PaCacheDesc(ctypes.Structure):
+    _fields_ = [("num_blocks", ctypes.c_int32), ("kv_heads", ctypes.c_int32),
+                ("block_size", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+                ("dtype", ctypes.c_int32), ("k_scale", ctypes.c_float),
+                ("v_scale", ctypes.c_float)]
+
+
+class PaError(RuntimeError):
+    pass
+
+
+_lib = None
+
+
+def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load libpa.so and declare its C signatures (raises if it is absent)."""
+    global _lib
+    if _lib is not None and path == LIB_PATH:
+        return _lib
+    if not os.path.exists(path):
+        raise ImportError(f"{path} is not built; run paged_kv_cache_54_gb300.build.build()")
+    lib = ctypes.CDLL(path)
+    vp, i32, i64p = ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p
+    lib.pa_reshape_and_cache.argtypes = [vp, vp, i32, i64p, i32, vp, vp,
+                                         ctypes.POINTER(PaCacheDesc), vp, vp]
+    lib.pa_reshape_and_cache.restype = ctypes.c_int
+    lib.pa_decode_workspace_size.argtypes = [i32] * 6
+    lib.pa_decode_workspace_size.restype = ctypes.c_size_t
+    lib.pa_decode.argtypes = [vp, vp, i32, i32, i32, vp, vp, ctypes.POINTER(PaCacheDesc),
+                              vp, i32, vp, i32, ctypes.c_float, i32, vp, ctypes.c_size_t,
+                              vp, vp]
+    lib.pa_decode.restype = ctypes.c_int
+    lib.pa_copy_blocks.argtypes = [vp, vp, ctypes.POINTER(PaCacheDesc), vp, i32, vp, vp]
+    lib.pa_copy_blocks.restype = ctypes.c_int
+    lib.pa_status_string.argtypes = [ctypes.c_int]
+    lib.pa_status_string.restype = ctypes.c_char_p
+    lib.pa_last_cuda_error.argtypes = []
+    lib.pa_last_cuda_error.restype = ctypes.c_char_p
+    if path == LIB_PATH:
+        _lib = lib
+    return lib
+
+
+def pa_status_string(status: int) -> str:
+    return load_library().pa_status_string(status).decode()
+
+
+def _check(status: int, what: str) -> None:
+    if status != 0:
+        lib = load_library()
+        msg = lib.pa_status_string(status).decode()
+        if status == 3:
+            msg += ": " + lib.pa_last_cuda_error().decode()
+        raise PaError(f"{what} failed: {msg} (status {status})")
+
+
+def _ptr(t) -> int | None:
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _cache_code(k_cache: torch.Tensor, cache_dtype) -> int:
+    if cache_dtype is not None:
+        return DTYPE_CODES[cache_dtype] if isinstance(cache_dtype, str) else int(cache_dtype)
+    if k_cache.dtype in _TORCH_CODES:
+        return _TORCH_CODES[k_cache.dtype]
+    raise ValueError("cache_dtype is required for a byte-typed FP8 cache")
+
+
+def cache_desc(k_cache: torch.Tensor, cache_dtype=None, k_scale: float = 1.0,
+               v_scale: float = 1.0) -> PaCacheDesc:
+    if k_cache.dim() != 4:
+        raise ValueError("cache must be [num_blocks, kv_heads, block_size, head_dim]")
+    nb, h, bs, d = k_cache.shape
+    return PaCacheDesc(nb, h, bs, d, _cache_code(k_cache, cache_dtype), k_scale, v_scale)
+
+
+def _require(t: torch.Tensor, name: str) -> None:
+    if not t.is_cuda or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous CUDA tensor")
+
+
+def pa_reshape_and_cache(key, value, slot_mapping, k_cache, v_cache, cache_dtype=None,
+                         k_scale: float = 1.0, v_scale: float = 1.0, device_error=None,
+                         stream=None) -> None:
+    """Write rows ``key/value [T, kv_heads, head_dim]`` into the caches."""
+    for t, n in ((key, "key"), (value, "value"), (slot_mapping, "slot_mapping"),
+                 (k_cache, "k_cache"), (v_cache, "v_cache")):
+        _require(t, n)
+    if slot_mapping.dtype != torch.int64:
+        raise ValueError("slot_mapping must be int64")
+    desc = cache_desc(k_cache, cache_dtype, k_scale, v_scale)
+    src = _TORCH_CODES.get(key.dtype)
+    if src is None or key.dtype != value.dtype:
+        raise ValueError("key/value must be float16 or bfloat16 of one dtype")
+    lib = load_library()
+    _check(lib.pa_reshape_and_cache(key.data_ptr(), value.data_ptr(), src,
+                                    slot_mapping.data_ptr(), slot_mapping.numel(),
+                                    k_cache.data_ptr(), v_cache.data_ptr(),
+                                    ctypes.byref(desc), _ptr(device_error), _stream(stream)),
+           "pa_reshape_and_cache")
+
+
+def pa_decode_workspace_size(num_seqs: int, num_q_heads: int, num_kv_heads: int,
+                             head_dim: int, max_seq_len: int, partition_size: int = 0) -> int:
+    return int(load_library().pa_decode_workspace_size(
+        num_seqs, num_q_heads, num_kv_heads, head_dim, max_seq_len, partition_size))
+
+
+def pa_decode(out, q, k_cache, v_cache, block_tables, seq_lens, max_seq_len: int,
+              scale: float, cache_dtype=None, k_scale: float = 1.0, v_scale: float = 1.0,
+              partition_size: int = 0, workspace=None, device_error=None,
+              stream=None) -> torch.Tensor:
+    """Paged decode attention; writes ``out [S, Hq, head_dim]`` (q's dtype)."""
+    for t, n in ((out, "out"), (q, "q"), (k_cache, "k_cache"), (v_cache, "v_cache"),
+                 (block_tables, "block_tables"), (seq_lens, "seq_lens")):
+        _require(t, n)
+    if block_tables.dtype != torch.int32 or seq_lens.dtype != torch.int32:
+        raise ValueError("block_tables and seq_lens must be int32")
+    desc = cache_desc(k_cache, cache_dtype, k_scale, v_scale)
+    S, Hq, D = q.shape
+    qcode = _TORCH_CODES.get(q.dtype)
+    if qcode not in (PA_F16, PA_BF16) or out.dtype != q.dtype or tuple(out.shape) != (S, Hq, D):
+        raise ValueError("q/out must be float16 or bfloat16 [S, Hq, head_dim] of one dtype")
+    need = pa_decode_workspace_size(S, Hq, desc.kv_heads, D, max_seq_len, partition_size)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    lib = load_library()
+    _check(lib.pa_decode(out.data_ptr(), q.data_ptr(), qcode, S, Hq, k_cache.data_ptr(),
+                         v_cache.data_ptr(), ctypes.byref(desc), block_tables.data_ptr(),
+                         block_tables.shape[1], seq_lens.data_ptr(), max_seq_len, scale,
+                         partition_size, workspace.data_ptr(), workspace.numel(),
+                         _ptr(device_error), _stream(stream)),
+           "pa_decode")
+    return out
+
+
+def pa_copy_blocks(k_cache, v_cache, block_mapping, cache_dtype=None, device_error=None,
+                   stream=None) -> None:
+    """For each (src, dst) row of ``block_mapping [n, 2]`` copy block src to dst."""
+    for t, n in ((k_cache, "k_cache"), (v_cache, "v_cache"), (block_mapping, "block_mapping")):
+        _require(t, n)
+    if block_mapping.dtype != torch.int64:
+        raise ValueError("block_mapping must be int64")
+    desc = cache_desc(k_cache, cache_dtype)
+    lib = load_library()
+    _check(lib.pa_copy_blocks(k_cache.data_ptr(), v_cache.data_ptr(), ctypes.byref(desc),
+                              block_mapping.data_ptr(), block_mapping.shape[0],
+                              _ptr(device_error), _stream(stream)),
+           "pa_copy_blocks")

@@ -1,0 +1,161 @@
+// Shared device helpers for libpa: dtype tags, conversions, mbarrier and
+// bulk-copy PTX wrappers, bounded waits.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace pa {
+
+enum DType : int { kF16 = 0, kBF16 = 1, kE4M3 = 2, kE5M2 = 3 };
+
+enum DevErr : int {
+  kErrNone = 0,
+  kErrBlockIndex = 1,
+  kErrSlot = 2,
+  kErrSeqLen = 3,
+  kErrTimeout = 4,
+  kErrCopyIndex = 5,
+};
+
+// Wait limit for every spin on an mbarrier: 2 s of %globaltimer.
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;
+
+__host__ __device__ constexpr int elt_bytes(int dt) { return (dt == kE4M3 || dt == kE5M2) ? 1 : 2; }
+__host__ __device__ constexpr bool is_fp8(int dt) { return dt == kE4M3 || dt == kE5M2; }
+
+__device__ __forceinline__ void record_error(int *err, int code) {
+  if (err != nullptr) atomicCAS(err, 0, code);
+}
+
+// ----------------------------------------------------------------------------
+// conversions
+// ----------------------------------------------------------------------------
+template <int DT>
+__device__ __forceinline__ float2 half2_bits_to_float2(uint32_t w) {
+  if constexpr (DT == kF16) {
+    __half2 h = *reinterpret_cast<const __half2 *>(&w);
+    return __half22float2(h);
+  } else {
+    __nv_bfloat162 h = *reinterpret_cast<const __nv_bfloat162 *>(&w);
+    return __bfloat1622float2(h);
+  }
+}
+
+// two FP8 codes (low byte = first element) -> __half2 bits (exact)
+template <int DT>
+__device__ __forceinline__ uint32_t fp8x2_to_half2_bits(uint32_t two_codes) {
+  __half2_raw r = __nv_cvt_fp8x2_to_halfraw2(
+      static_cast<__nv_fp8x2_storage_t>(two_codes & 0xFFFFu),
+      DT == kE4M3 ? __NV_E4M3 : __NV_E5M2);
+  return static_cast<uint32_t>(r.x) | (static_cast<uint32_t>(r.y) << 16);
+}
+
+template <int DT>
+__device__ __forceinline__ float2 fp8x2_to_float2(uint32_t two_codes) {
+  uint32_t h = fp8x2_to_half2_bits<DT>(two_codes);
+  return __half22float2(*reinterpret_cast<const __half2 *>(&h));
+}
+
+template <int DT>
+__device__ __forceinline__ uint16_t float_to_storage16(float x) {
+  if constexpr (DT == kF16) {
+    return __half_as_ushort(__float2half_rn(x));
+  } else {
+    return __bfloat16_as_ushort(__float2bfloat16_rn(x));
+  }
+}
+
+template <int DT>
+__device__ __forceinline__ uint32_t pack2_rn(float lo, float hi) {
+  if constexpr (DT == kF16) {
+    __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&h);
+  } else {
+    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&h);
+  }
+}
+
+// ----------------------------------------------------------------------------
+// shared-memory addressing, mbarriers, bulk copies
+// ----------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_addr(const void *p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count)
+               : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ unsigned long long global_timer_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Wait for the phase of `bar` with the given parity to complete.  Returns
+// false if it did not within kWaitLimitNs, or if *abort became nonzero.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, const volatile int *abort) {
+  const uint32_t a = smem_addr(bar);
+  if (mbar_try_wait(a, parity)) return true;
+  const unsigned long long t0 = global_timer_ns();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try_wait(a, parity)) return true;
+    if ((i & 63u) == 0) {
+      if (abort != nullptr && *abort) return false;
+      if (global_timer_ns() - t0 > kWaitLimitNs) return false;
+    }
+  }
+}
+
+// Bulk (TMA) copy global -> shared of `bytes` (multiple of 16, both addresses
+// 16-byte aligned), completing on the mbarrier's transaction count.
+__device__ __forceinline__ void bulk_g2s(void *smem_dst, const void *gmem_src, uint32_t bytes,
+                                         uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_addr(smem_dst)),
+      "l"(gmem_src), "r"(bytes), "r"(smem_addr(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void named_bar_sync(int id, int threads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+__device__ __forceinline__ uint4 lds128(const void *p) {
+  return *reinterpret_cast<const uint4 *>(p);
+}
+
+}  // namespace pa

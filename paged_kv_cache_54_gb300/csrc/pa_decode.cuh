@@ -1,0 +1,903 @@
+// Paged decode attention for sm_103a.
+//
+// Work decomposition.  A work item is one (KV head h, sequence s, partition
+// p): the tokens [p*P, min((p+1)*P, L_s)) of one sequence, for the G query
+// heads that share KV head h.  A plan kernel lists the (s, p) pairs; a
+// persistent kernel (one CTA per SM) claims items from an atomic counter in
+// the order (h, s, p), so that CTAs running at the same time read the same
+// KV head of neighbouring sequences — the beams of one prompt and the
+// sequences of one shared prefix meet in L2.  Sequences with more than one
+// partition leave (m, l, o) partials that a merge kernel combines exactly
+// (the flash-decoding reduction).
+//
+// CTA = 1 producer warp + 4 consumer warps.  The producer walks the block
+// table and stages whole (block, head) tiles of K and V — contiguous
+// block_size * head_dim runs in the [num_blocks, kv_heads, block_size,
+// head_dim] layout — into shared memory with bulk asynchronous copies (TMA,
+// cp.async.bulk) completing on a per-stage mbarrier.  A stage holds 64
+// tokens; consumer warp c owns tokens [16c, 16c + 16) of each stage and keeps
+// its own online-softmax state; the four states are combined at the end of
+// each item.  Block-table entries, the next item's claim and its metadata
+// are fetched one item ahead so the copy engine never waits on them.
+//
+// Consumers compute, per 16-token slice:
+//   G <= 2  (SIMT):  two lanes per token, warp-shuffle dot products in fp32;
+//                    lanes own head_dim columns for the P*V accumulation.
+//   G >= 4  (MMA):   S^T = K Q^T and O^T = V^T P^T on mma.sync m16n8k16
+//                    (tokens and head_dim as M, the query group as N = 8),
+//                    fp32 accumulation; FP8 codes are widened exactly to
+//                    fp16 in registers.
+// Softmax is kept in base-2 units (scores pre-multiplied by log2 e) with a
+// lazily updated running maximum: the accumulators are rescaled only when
+// the maximum grows by more than 2^8, which leaves o / l unchanged.
+#pragma once
+
+#include <type_traits>
+
+#include "pa_common.cuh"
+#include "pa_decode_params.h"
+
+namespace pa {
+namespace {  // kernels are private to each translation unit
+
+constexpr float kLazyRescale = 8.0f;
+
+__device__ __forceinline__ uint32_t w32(const uint4 &v, int i) {
+  return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
+}
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+  return d;
+}
+
+__device__ __forceinline__ int clamp_len(int L, int cap, int *err) {
+  if (L < 0 || L > cap) {
+    record_error(err, kErrSeqLen);
+    return L < 0 ? 0 : cap;
+  }
+  return L;
+}
+
+// ----------------------------------------------------------------------------
+// plan: list (s, p) pairs in sequence order; reset the claim counter
+// ----------------------------------------------------------------------------
+__global__ void __launch_bounds__(1024) plan_kernel(const DecodeParams p) {
+  __shared__ int warp_tot[32];
+  __shared__ int base;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (tid == 0) base = 0;
+  __syncthreads();
+  for (int b0 = 0; b0 < p.num_seqs; b0 += 1024) {
+    const int s = b0 + tid;
+    int nP = 0;
+    if (s < p.num_seqs) {
+      const int L = clamp_len(__ldg(p.seq_lens + s), p.len_cap, p.err);
+      nP = max(1, (L + p.partition_size - 1) / p.partition_size);
+    }
+    int x = nP;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
+    }
+    if (lane == 31) warp_tot[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+      int t = warp_tot[lane];
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, t, o);
+        if (lane >= o) t += y;
+      }
+      warp_tot[lane] = t;  // inclusive over warps
+    }
+    __syncthreads();
+    const int excl = base + (warp ? warp_tot[warp - 1] : 0) + x - nP;
+    for (int q = 0; q < nP; ++q) p.pairs[excl + q] = make_int2(s, q);
+    __syncthreads();
+    if (tid == 0) base += warp_tot[31];
+    __syncthreads();
+  }
+  if (tid == 0) {
+    p.work[1] = base;
+    p.work[0] = 0;
+  }
+}
+
+// ----------------------------------------------------------------------------
+// merge: combine the partials of sequences split into several partitions
+// ----------------------------------------------------------------------------
+template <int QT, int D>
+__global__ void __launch_bounds__(256) merge_kernel(const DecodeParams p) {
+  const int lane = threadIdx.x & 31;
+  const long long gw = (blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x) >> 5;
+  if (gw >= static_cast<long long>(p.num_seqs) * p.num_q_heads) return;
+  const int s = static_cast<int>(gw / p.num_q_heads);
+  const int hq = static_cast<int>(gw % p.num_q_heads);
+  const int L = min(max(__ldg(p.seq_lens + s), 0), p.len_cap);
+  const int nP = max(1, (L + p.partition_size - 1) / p.partition_size);
+  if (nP <= 1) return;
+  const size_t base = static_cast<size_t>(s) * p.max_parts * p.num_q_heads + hq;
+  float M = -INFINITY;
+  for (int q = lane; q < nP; q += 32) M = fmaxf(M, p.part_ml[base + static_cast<size_t>(q) * p.num_q_heads].x);
+#pragma unroll
+  for (int o = 16; o; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  constexpr int E = D / 32;
+  float acc[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) acc[e] = 0.f;
+  float den = 0.f;
+  for (int q = 0; q < nP; ++q) {
+    const size_t idx = base + static_cast<size_t>(q) * p.num_q_heads;
+    const float2 ml = p.part_ml[idx];
+    const float w = (ml.y > 0.f) ? exp2f(ml.x - M) * ml.y : 0.f;
+    den += w;
+    const float *po = p.part_o + idx * D + lane * E;
+#pragma unroll
+    for (int e = 0; e < E; ++e) acc[e] += w * po[e];
+  }
+  const float inv = den > 0.f ? 1.f / den : 0.f;
+  uint16_t *out = static_cast<uint16_t *>(p.out) + (static_cast<size_t>(s) * p.num_q_heads + hq) * D + lane * E;
+#pragma unroll
+  for (int e = 0; e < E; ++e) out[e] = float_to_storage16<QT>(den > 0.f ? acc[e] * inv : 0.f);
+}
+
+// ----------------------------------------------------------------------------
+// producer warp
+// ----------------------------------------------------------------------------
+template <int KV, int D, int G>
+__device__ __forceinline__ void producer_warp(const DecodeParams &p, uint8_t *smem) {
+  SmemHeader &hdr = *reinterpret_cast<SmemHeader *>(smem);
+  uint8_t *stages = smem + p.stages_off;
+  const volatile int *abort = &hdr.abort;
+  const int lane = threadIdx.x & 31;
+  constexpr int ROWB = D * elt_bytes(KV);
+  const int bs = p.block_size;
+  const uint32_t tile = static_cast<uint32_t>(bs) * ROWB;
+  const int bps = kStageTok / bs;
+  const int P = p.partition_size;
+  const int bpp = P / bs;  // <= 128
+  const int NS = p.num_stages;
+  const int n_pairs = p.work[1];
+  const int total = n_pairs * p.num_kv_heads;
+  constexpr uint32_t qbytes = G * D * 2;
+
+  auto claim = [&]() -> int {
+    int w = 0;
+    if (lane == 0) w = atomicAdd(p.work, 1);
+    return __shfl_sync(0xffffffffu, w, 0);
+  };
+  auto load_pair = [&](int w) -> int2 {
+    return (w < total) ? p.pairs[w % n_pairs] : make_int2(0, 0);
+  };
+  auto load_len = [&](int w, int2 pr) -> int {
+    return (w < total) ? __ldg(p.seq_lens + pr.x) : 0;
+  };
+  auto load_table = [&](int w, int2 pr, int L, int (&ph)[4]) {
+    const int nblk = (w < total) ? (min(max(L, 0), p.len_cap) + bs - 1) / bs : 0;
+    const int32_t *row = p.block_tables + static_cast<size_t>(pr.x) * p.max_blocks;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const int ib = lane + 32 * c;
+      const int j = pr.y * bpp + ib;
+      ph[c] = (ib < bpp && j < nblk) ? __ldg(row + j) : 0;
+    }
+  };
+
+  // current item
+  int w_c = claim();
+  int2 pr_c = load_pair(w_c);
+  int L_c = load_len(w_c, pr_c);
+  int ph_c[4];
+  load_table(w_c, pr_c, L_c, ph_c);
+  // next item, fetched step by step while the current one is issued
+  int w_n = 0, L_n = 0, pf = 0;
+  int2 pr_n = make_int2(0, 0);
+  int ph_n[4] = {0, 0, 0, 0};
+  auto pf_step = [&]() {
+    switch (pf) {
+      case 0: w_n = claim(); break;
+      case 1: pr_n = load_pair(w_n); break;
+      case 2: L_n = load_len(w_n, pr_n); break;
+      default: load_table(w_n, pr_n, L_n, ph_n); break;
+    }
+    ++pf;
+  };
+
+  int it = 0;
+  bool ok = true;
+  while (w_c < total) {
+    const int h = w_c / n_pairs;
+    const int s = pr_c.x, pi = pr_c.y;
+    const int L = clamp_len(L_c, p.len_cap, lane == 0 ? p.err : nullptr);
+    const int t_begin = pi * P;
+    const int t_end = min(L, t_begin + P);
+    const int ntok_item = max(0, t_end - t_begin);
+    const int nstages = max(1, (ntok_item + kStageTok - 1) / kStageTok);
+    const int nP = max(1, (L + P - 1) / P);
+    for (int st = 0; st < nstages; ++st) {
+      const int tok0 = t_begin + st * kStageTok;
+      const int ntok = max(0, min(kStageTok, t_end - tok0));
+      const int nb = (ntok + bs - 1) / bs;
+      const int ib0 = st * bps;
+      const int c = ib0 >> 5;
+      const int reg = c == 0 ? ph_c[0] : c == 1 ? ph_c[1] : c == 2 ? ph_c[2] : ph_c[3];
+      const int phys = __shfl_sync(0xffffffffu, reg, (ib0 & 31) + (lane < nb ? lane : 0));
+      const int stage = it % NS;
+      const uint32_t par = ((it / NS) & 1) ^ 1;
+      if (!mbar_wait(&hdr.empty[stage], par, abort)) {
+        ok = false;
+        break;
+      }
+      uint8_t *sb = stages + static_cast<size_t>(stage) * p.stage_bytes;
+      if (lane == 0) {
+        StageInfo &inf = hdr.info[stage];
+        inf.s = s;
+        inf.h = h;
+        inf.p = pi;
+        inf.tok0 = tok0;
+        inf.ntok = ntok;
+        inf.L = L;
+        inf.nP = nP;
+        inf.flags = (st == 0 ? kFirst : 0) | (st == nstages - 1 ? kLast : 0);
+        mbar_arrive_expect_tx(&hdr.full[stage], nb * 2 * tile + (st == 0 ? qbytes : 0u));
+      }
+      __syncwarp();
+      if (lane < nb) {
+        int b = phys;
+        if (static_cast<unsigned>(b) >= static_cast<unsigned>(p.num_blocks)) {
+          record_error(p.err, kErrBlockIndex);
+          b = 0;
+        }
+        const size_t off = (static_cast<size_t>(b) * p.num_kv_heads + h) * tile;
+        bulk_g2s(sb + p.k_off + lane * tile, p.k_cache + off, tile, &hdr.full[stage]);
+        bulk_g2s(sb + p.v_off + lane * tile, p.v_cache + off, tile, &hdr.full[stage]);
+      }
+      if (st == 0 && lane == 31) {
+        const uint8_t *qsrc = p.q + (static_cast<size_t>(s) * p.num_q_heads + static_cast<size_t>(h) * G) * D * 2;
+        bulk_g2s(sb + p.q_off, qsrc, qbytes, &hdr.full[stage]);
+      }
+      ++it;
+      if (pf < 4) pf_step();
+    }
+    if (!ok) break;
+    while (pf < 4) pf_step();
+    w_c = w_n;
+    pr_c = pr_n;
+    L_c = L_n;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) ph_c[c] = ph_n[c];
+    pf = 0;
+  }
+  if (ok) {
+    const int stage = it % NS;
+    const uint32_t par = ((it / NS) & 1) ^ 1;
+    if (mbar_wait(&hdr.empty[stage], par, abort)) {
+      if (lane == 0) {
+        hdr.info[stage].flags = kEnd;
+        mbar_arrive(&hdr.full[stage]);
+      }
+    } else {
+      ok = false;
+    }
+  }
+  if (!ok) {
+    if (lane == 0) {
+      record_error(p.err, kErrTimeout);
+      hdr.abort = 1;
+    }
+    // wait, within the limit, for the copies this warp started
+    if (lane == 0) {
+      for (int j = max(0, it - NS); j < it; ++j) mbar_wait(&hdr.full[j % NS], (j / NS) & 1, nullptr);
+    }
+    __syncwarp();
+  }
+}
+
+// ----------------------------------------------------------------------------
+// consumer state: SIMT (G <= 2)
+// ----------------------------------------------------------------------------
+template <int KV, int QT, int D, int G>
+struct SimtState {
+  static constexpr int ELT = elt_bytes(KV);
+  static constexpr int ROWB = D * ELT;
+  static constexpr int NCH = ROWB / 16;  // 16-byte chunks per token row
+  static constexpr int NCHL = NCH / 2;   // chunks per lane (two lanes per token)
+  static constexpr int EPC = 16 / ELT;   // elements per chunk
+  static constexpr int EPL = D / 32;     // P*V columns per lane
+  static constexpr int QS = G;           // query rows kept in the combine scratch
+
+  float qf[G][NCHL][EPC];
+  float o[G][EPL];
+  float m[G], l[G];
+
+  __device__ __forceinline__ void start(const uint8_t *qs, float qk_scale) {
+    const int lane = threadIdx.x & 31;
+    const int t = lane >> 1, hh = lane & 1;
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+#pragma unroll
+      for (int i = 0; i < NCHL; ++i) {
+        const int c = (2 * i + hh + 2 * t) % NCH;
+        const uint8_t *src = qs + (static_cast<size_t>(g) * D + c * EPC) * 2;
+#pragma unroll
+        for (int e = 0; e < EPC; e += 2) {
+          const float2 f = half2_bits_to_float2<QT>(*reinterpret_cast<const uint32_t *>(src + e * 2));
+          qf[g][i][e] = f.x * qk_scale;
+          qf[g][i][e + 1] = f.y * qk_scale;
+        }
+      }
+#pragma unroll
+      for (int e = 0; e < EPL; ++e) o[g][e] = 0.f;
+      m[g] = -INFINITY;
+      l[g] = 0.f;
+    }
+  }
+
+  __device__ __forceinline__ void chunk_to_float(const uint4 &v, float (&f)[EPC]) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const uint32_t w = w32(v, k);
+      if constexpr (ELT == 2) {
+        const float2 a = half2_bits_to_float2<KV>(w);
+        f[2 * k] = a.x;
+        f[2 * k + 1] = a.y;
+      } else {
+        const float2 a = fp8x2_to_float2<KV>(w);
+        const float2 b = fp8x2_to_float2<KV>(w >> 16);
+        f[4 * k] = a.x;
+        f[4 * k + 1] = a.y;
+        f[4 * k + 2] = b.x;
+        f[4 * k + 3] = b.y;
+      }
+    }
+  }
+
+  __device__ __forceinline__ void load_v(const uint8_t *row, float (&f)[EPL]) {
+    const int lane = threadIdx.x & 31;
+    const uint8_t *src = row + lane * EPL * ELT;
+    if constexpr (ELT == 2) {
+#pragma unroll
+      for (int e = 0; e < EPL; e += 2) {
+        const float2 a = half2_bits_to_float2<KV>(*reinterpret_cast<const uint32_t *>(src + e * 2));
+        f[e] = a.x;
+        f[e + 1] = a.y;
+      }
+    } else {
+#pragma unroll
+      for (int e = 0; e < EPL; e += 2) {
+        const float2 a = fp8x2_to_float2<KV>(*reinterpret_cast<const uint16_t *>(src + e));
+        f[e] = a.x;
+        f[e + 1] = a.y;
+      }
+    }
+  }
+
+  // one 16-token slice: rows Ks[0..15], Vs[0..15]; n valid tokens (1..16)
+  __device__ __forceinline__ void slice(const uint8_t *Ks, const uint8_t *Vs, int n, float v_scale) {
+    const int lane = threadIdx.x & 31;
+    const int t = lane >> 1, hh = lane & 1;
+    float acc[G];
+#pragma unroll
+    for (int g = 0; g < G; ++g) acc[g] = 0.f;
+    const uint8_t *krow = Ks + t * ROWB;
+#pragma unroll
+    for (int i = 0; i < NCHL; ++i) {
+      const int c = (2 * i + hh + 2 * t) % NCH;
+      float kf[EPC];
+      chunk_to_float(lds128(krow + c * 16), kf);
+#pragma unroll
+      for (int g = 0; g < G; ++g)
+#pragma unroll
+        for (int e = 0; e < EPC; ++e) acc[g] = fmaf(qf[g][i][e], kf[e], acc[g]);
+    }
+    float pr[G];
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      float sc = acc[g] + __shfl_xor_sync(0xffffffffu, acc[g], 1);
+      sc = (t < n) ? sc : -INFINITY;
+      float mx = sc;
+#pragma unroll
+      for (int o2 = 2; o2 < 32; o2 <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o2));
+      if (mx > m[g] + kLazyRescale) {  // warp-uniform
+        const float alpha = exp2f(m[g] - mx);
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) o[g][e] *= alpha;
+        l[g] *= alpha;
+        m[g] = mx;
+      }
+      pr[g] = exp2f(sc - m[g]);
+      if (hh == 0) l[g] += pr[g];
+    }
+    // P * V: lane owns EPL columns; tokens broadcast from their lane pair
+#pragma unroll
+    for (int tt = 0; tt < 16; ++tt) {
+      if (tt < n) {
+        float vf[EPL];
+        load_v(Vs + tt * ROWB, vf);
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+          const float pt = __shfl_sync(0xffffffffu, pr[g], 2 * tt) * v_scale;
+#pragma unroll
+          for (int e = 0; e < EPL; ++e) o[g][e] = fmaf(pt, vf[e], o[g][e]);
+        }
+      }
+    }
+  }
+
+  __device__ __forceinline__ void to_scratch(float *so, float *sm, float *sl, int cw) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      float ls = l[g];
+#pragma unroll
+      for (int o2 = 1; o2 < 32; o2 <<= 1) ls += __shfl_xor_sync(0xffffffffu, ls, o2);
+      float *dst = so + (static_cast<size_t>(cw) * QS + g) * D + lane * EPL;
+#pragma unroll
+      for (int e = 0; e < EPL; ++e) dst[e] = o[g][e];
+      if (lane == 0) {
+        sm[cw * QS + g] = m[g];
+        sl[cw * QS + g] = ls;
+      }
+    }
+  }
+};
+
+// ----------------------------------------------------------------------------
+// consumer state: tensor-core mma.sync (G in {4, 8}; query group padded to 8)
+// ----------------------------------------------------------------------------
+template <int MT>
+__device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+  if constexpr (MT == kF16) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+  } else {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+  }
+}
+
+// Fragment layout of m16n8k16 (lane = 4*gq + tq):
+//   A regs: (row gq, cols 2tq..+1), (row gq+8, same), (row gq, cols 2tq+8..+9), (row gq+8, same)
+//   B regs: (rows 2tq..+1, col gq), (rows 2tq+8..+9, col gq)
+//   C regs: (row gq, cols 2tq, 2tq+1), (row gq+8, cols 2tq, 2tq+1)
+// Scores S^T = K Q^T: M = slice token (row r is token r), N = query, K = head_dim.
+//   The head_dim order is permuted so that lane tq reads contiguous 16-byte
+//   chunks {tq, tq+4, ...} of a row: local element e of lane tq is column
+//   (tq + 4 * (e / CE)) * CE + e % CE, and k-step kk uses local e = 4kk..4kk+3.
+// Output O^T = V^T P^T: M = head_dim, N = query, K = slice token.
+//   Token order of the K dimension: k = 2tq -> token 2tq, 2tq+1 -> 2tq+8,
+//   2tq+8 -> 2tq+1, 2tq+9 -> 2tq+9, which makes each B register of P^T a pair
+//   of scores one lane already holds (C rows gq and gq+8).
+//   Head_dim order of the M dimension: lane gq owns columns
+//   [gq*DPL, gq*DPL + DPL); m-tile mi row gq -> gq*DPL + mi, row gq+8 ->
+//   gq*DPL + MTILES + mi.
+template <int KV, int QT, int D, int G>
+struct MmaState {
+  static constexpr bool KV8 = is_fp8(KV);
+  static constexpr int MT = KV8 ? kF16 : KV;  // mma input type
+  static constexpr int ELT = elt_bytes(KV);
+  static constexpr int ROWB = D * ELT;
+  static constexpr int KSTEPS = D / 16;
+  static constexpr int MTILES = D / 16;
+  static constexpr int CE = 16 / ELT;       // elements per 16-byte chunk
+  static constexpr int LCH = (D / 4) / CE;  // chunks of a K row per lane
+  static constexpr int DPL = D / 8;         // output columns per lane group
+  static constexpr int QS = G;
+
+  uint32_t qb[KSTEPS][2];
+  float oacc[MTILES][4];
+  float m2[2], l2[2];
+  float qk_mult;
+
+  __device__ __forceinline__ static int kcol(int tq, int e) { return (tq + 4 * (e / CE)) * CE + e % CE; }
+
+  __device__ __forceinline__ void start(const uint8_t *qs, float qk_scale) {
+    const int lane = threadIdx.x & 31;
+    const int gq = lane >> 2, tq = lane & 3;
+    const bool real = gq < G;
+    const uint16_t *qrow = reinterpret_cast<const uint16_t *>(qs) + static_cast<size_t>(real ? gq : 0) * D;
+    float f = 1.f;
+    if constexpr (KV8 && QT == kBF16) {
+      // fp16 operands: scale q by a power of two so the group's largest
+      // entry fits fp16's range; the factor is undone on the scores.
+      float amax = 0.f;
+#pragma unroll
+      for (int kk = 0; kk < KSTEPS; ++kk)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float v = __bfloat162float(__ushort_as_bfloat16(qrow[kcol(tq, 4 * kk + e)]));
+          amax = fmaxf(amax, fabsf(real ? v : 0.f));
+        }
+#pragma unroll
+      for (int o2 = 1; o2 < 32; o2 <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o2));
+      if (amax > 16384.f) {
+        int ex;
+        frexpf(amax, &ex);
+        f = ldexpf(1.f, 14 - ex);
+      }
+    }
+#pragma unroll
+    for (int kk = 0; kk < KSTEPS; ++kk) {
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        const int d0 = kcol(tq, 4 * kk + 2 * r);  // d0 + 1 is the next column
+        uint32_t w = 0;
+        if (real) {
+          if constexpr (KV8 && QT == kBF16) {
+            const float a = __bfloat162float(__ushort_as_bfloat16(qrow[d0])) * f;
+            const float b = __bfloat162float(__ushort_as_bfloat16(qrow[d0 + 1])) * f;
+            w = pack2_rn<kF16>(a, b);
+          } else {
+            w = *reinterpret_cast<const uint32_t *>(qrow + d0);
+          }
+        }
+        qb[kk][r] = w;
+      }
+    }
+    qk_mult = qk_scale / f;
+#pragma unroll
+    for (int mi = 0; mi < MTILES; ++mi)
+#pragma unroll
+      for (int k = 0; k < 4; ++k) oacc[mi][k] = 0.f;
+    m2[0] = m2[1] = -INFINITY;
+    l2[0] = l2[1] = 0.f;
+  }
+
+  // A register of K for k-step kk from the row's LCH chunks; r = 0 (cols
+  // 2tq..+1) or 1 (cols 2tq+8..+9)
+  __device__ __forceinline__ static uint32_t k_reg(const uint4 (&ch)[LCH], int kk, int r) {
+    if constexpr (ELT == 2) {
+      const int e = 4 * kk + 2 * r;  // local element (even)
+      return w32(ch[e / CE], (e % CE) / 2);
+    } else {
+      const int e = 4 * kk;
+      const uint32_t w = w32(ch[e / CE], (e % CE) / 4);
+      return fp8x2_to_half2_bits<KV>(r ? (w >> 16) : w);
+    }
+  }
+
+  // A register of V^T: pair (row ra, row rb) of output column index `col`
+  // within the lane's DPL columns
+  __device__ __forceinline__ static uint32_t v_pair(const uint32_t *ra, const uint32_t *rb, int col) {
+    if constexpr (ELT == 2) {
+      const uint32_t a = ra[col / 2], b = rb[col / 2];
+      return prmt(a, b, (col & 1) ? 0x7632u : 0x5410u);
+    } else {
+      const int byte = col & 3;
+      const uint32_t a = ra[col / 4], b = rb[col / 4];
+      const uint32_t two = prmt(a, b, static_cast<uint32_t>(byte | ((4 + byte) << 4)));
+      return fp8x2_to_half2_bits<KV>(two);
+    }
+  }
+
+  __device__ __forceinline__ void slice(const uint8_t *Ks, const uint8_t *Vs, int n, float v_scale) {
+    const int lane = threadIdx.x & 31;
+    const int gq = lane >> 2, tq = lane & 3;
+    // ---- S^T = K Q^T ----
+    uint4 k0[LCH], k1[LCH];
+#pragma unroll
+    for (int j = 0; j < LCH; ++j) {
+      k0[j] = lds128(Ks + gq * ROWB + (tq + 4 * j) * 16);
+      k1[j] = lds128(Ks + (gq + 8) * ROWB + (tq + 4 * j) * 16);
+    }
+    float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int kk = 0; kk < KSTEPS; ++kk) {
+      const uint32_t a0 = k_reg(k0, kk, 0), a1 = k_reg(k1, kk, 0);
+      const uint32_t a2 = k_reg(k0, kk, 1), a3 = k_reg(k1, kk, 1);
+      if (kk & 1)
+        mma16816<MT>(sb, a0, a1, a2, a3, qb[kk][0], qb[kk][1]);
+      else
+        mma16816<MT>(sa, a0, a1, a2, a3, qb[kk][0], qb[kk][1]);
+    }
+    float sc[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) sc[k] = (sa[k] + sb[k]) * qk_mult;
+    // rows gq (regs 0,1) and gq+8 (regs 2,3); columns 2tq, 2tq+1
+    if (gq >= n) sc[0] = sc[1] = -INFINITY;
+    if (gq + 8 >= n) sc[2] = sc[3] = -INFINITY;
+    float mx0 = fmaxf(sc[0], sc[2]), mx1 = fmaxf(sc[1], sc[3]);
+#pragma unroll
+    for (int o2 = 4; o2 < 32; o2 <<= 1) {
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o2));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o2));
+    }
+    const bool up0 = mx0 > m2[0] + kLazyRescale, up1 = mx1 > m2[1] + kLazyRescale;
+    if (__any_sync(0xffffffffu, up0 || up1)) {
+      const float al0 = up0 ? exp2f(m2[0] - mx0) : 1.f;
+      const float al1 = up1 ? exp2f(m2[1] - mx1) : 1.f;
+      if (up0) m2[0] = mx0;
+      if (up1) m2[1] = mx1;
+#pragma unroll
+      for (int mi = 0; mi < MTILES; ++mi) {
+        oacc[mi][0] *= al0;
+        oacc[mi][2] *= al0;
+        oacc[mi][1] *= al1;
+        oacc[mi][3] *= al1;
+      }
+      l2[0] *= al0;
+      l2[1] *= al1;
+    }
+    const float p0 = exp2f(sc[0] - m2[0]), p1 = exp2f(sc[1] - m2[1]);
+    const float p2 = exp2f(sc[2] - m2[0]), p3 = exp2f(sc[3] - m2[1]);
+    l2[0] += p0 + p2;
+    l2[1] += p1 + p3;
+    // P^T as the B operand: query gq, tokens (2tq, 2tq+8) and (2tq+1, 2tq+9)
+    const uint32_t packA = pack2_rn<MT>(p0, p2);  // query 2tq
+    const uint32_t packB = pack2_rn<MT>(p1, p3);  // query 2tq+1
+    const int src0 = (2 * tq) * 4 + (gq >> 1), src1 = (2 * tq + 1) * 4 + (gq >> 1);
+    const uint32_t xA0 = __shfl_sync(0xffffffffu, packA, src0), xB0 = __shfl_sync(0xffffffffu, packB, src0);
+    const uint32_t xA1 = __shfl_sync(0xffffffffu, packA, src1), xB1 = __shfl_sync(0xffffffffu, packB, src1);
+    const uint32_t b0 = (gq & 1) ? xB0 : xA0;
+    const uint32_t b1 = (gq & 1) ? xB1 : xA1;
+    // ---- O^T += V^T P^T ----
+    constexpr int VW = DPL * ELT / 4;  // 32-bit words of a row the lane reads
+    uint32_t r0[VW], r1[VW], r2[VW], r3[VW];
+    const uint8_t *vb = Vs + gq * DPL * ELT;
+    const int t0 = 2 * tq, t1 = 2 * tq + 8, t2 = 2 * tq + 1, t3 = 2 * tq + 9;
+#pragma unroll
+    for (int w = 0; w < VW; w += 2) {
+      const uint2 a = *reinterpret_cast<const uint2 *>(vb + t0 * ROWB + w * 4);
+      const uint2 b = *reinterpret_cast<const uint2 *>(vb + t1 * ROWB + w * 4);
+      const uint2 c = *reinterpret_cast<const uint2 *>(vb + t2 * ROWB + w * 4);
+      const uint2 d = *reinterpret_cast<const uint2 *>(vb + t3 * ROWB + w * 4);
+      r0[w] = a.x; r0[w + 1] = a.y;
+      r1[w] = b.x; r1[w + 1] = b.y;
+      r2[w] = c.x; r2[w + 1] = c.y;
+      r3[w] = d.x; r3[w + 1] = d.y;
+    }
+    if (n < 16) {  // stale rows may hold NaN: zero them so 0 * NaN never reaches the sum
+#pragma unroll
+      for (int w = 0; w < VW; ++w) {
+        if (t0 >= n) r0[w] = 0u;
+        if (t1 >= n) r1[w] = 0u;
+        if (t2 >= n) r2[w] = 0u;
+        if (t3 >= n) r3[w] = 0u;
+      }
+    }
+#pragma unroll
+    for (int mi = 0; mi < MTILES; ++mi) {
+      const uint32_t a0 = v_pair(r0, r1, mi);
+      const uint32_t a1 = v_pair(r0, r1, MTILES + mi);
+      const uint32_t a2 = v_pair(r2, r3, mi);
+      const uint32_t a3 = v_pair(r2, r3, MTILES + mi);
+      mma16816<MT>(oacc[mi], a0, a1, a2, a3, b0, b1);
+    }
+    (void)v_scale;
+  }
+
+  __device__ __forceinline__ void to_scratch(float *so, float *sm, float *sl, int cw, float v_scale) {
+    const int lane = threadIdx.x & 31;
+    const int gq = lane >> 2, tq = lane & 3;
+    float ls0 = l2[0], ls1 = l2[1];
+#pragma unroll
+    for (int o2 = 4; o2 < 32; o2 <<= 1) {
+      ls0 += __shfl_xor_sync(0xffffffffu, ls0, o2);
+      ls1 += __shfl_xor_sync(0xffffffffu, ls1, o2);
+    }
+    const int qa = 2 * tq, qb2 = 2 * tq + 1;
+#pragma unroll
+    for (int mi = 0; mi < MTILES; ++mi) {
+      const int d0 = gq * DPL + mi, d1 = gq * DPL + MTILES + mi;
+      if (qa < G) {
+        so[(static_cast<size_t>(cw) * QS + qa) * D + d0] = oacc[mi][0] * v_scale;
+        so[(static_cast<size_t>(cw) * QS + qa) * D + d1] = oacc[mi][2] * v_scale;
+      }
+      if (qb2 < G) {
+        so[(static_cast<size_t>(cw) * QS + qb2) * D + d0] = oacc[mi][1] * v_scale;
+        so[(static_cast<size_t>(cw) * QS + qb2) * D + d1] = oacc[mi][3] * v_scale;
+      }
+    }
+    if (gq == 0) {
+      if (qa < G) {
+        sm[cw * QS + qa] = m2[0];
+        sl[cw * QS + qa] = ls0;
+      }
+      if (qb2 < G) {
+        sm[cw * QS + qb2] = m2[1];
+        sl[cw * QS + qb2] = ls1;
+      }
+    }
+  }
+};
+
+// ----------------------------------------------------------------------------
+// combine the four consumer warps' states and write the item's result
+// ----------------------------------------------------------------------------
+template <int QT, int D, int G>
+__device__ __forceinline__ void combine_item(const DecodeParams &p, const StageInfo &inf, const float *so,
+                                             const float *sm, const float *sl) {
+  const int ct = threadIdx.x - 32;
+  for (int e = ct; e < G * D; e += kConsumerThreads) {
+    const int g = e / D, dd = e % D;
+    float M = -INFINITY;
+#pragma unroll
+    for (int c = 0; c < kConsumerWarps; ++c) M = fmaxf(M, sm[c * G + g]);
+    float wsum = 0.f, acc = 0.f;
+#pragma unroll
+    for (int c = 0; c < kConsumerWarps; ++c) {
+      const float mc = sm[c * G + g];
+      const float w = (mc == -INFINITY) ? 0.f : exp2f(mc - M);
+      wsum = fmaf(w, sl[c * G + g], wsum);
+      acc = fmaf(w, so[(static_cast<size_t>(c) * G + g) * D + dd], acc);
+    }
+    const float val = wsum > 0.f ? acc / wsum : 0.f;
+    const int hq = inf.h * G + g;
+    if (inf.nP == 1) {
+      uint16_t *out = static_cast<uint16_t *>(p.out);
+      out[(static_cast<size_t>(inf.s) * p.num_q_heads + hq) * D + dd] = float_to_storage16<QT>(val);
+    } else {
+      const size_t idx = (static_cast<size_t>(inf.s) * p.max_parts + inf.p) * p.num_q_heads + hq;
+      p.part_o[idx * D + dd] = val;
+      if (dd == 0) p.part_ml[idx] = make_float2(M, wsum);
+    }
+  }
+}
+
+// ----------------------------------------------------------------------------
+// the persistent decode kernel
+// ----------------------------------------------------------------------------
+template <int KV, int QT, int D, int G, bool MMA>
+__global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams p) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  SmemHeader &hdr = *reinterpret_cast<SmemHeader *>(smem);
+  const int warp = threadIdx.x >> 5;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < p.num_stages; ++i) {
+      mbar_init(&hdr.full[i], 1);
+      mbar_init(&hdr.empty[i], kConsumerWarps);
+    }
+    mbar_init(&hdr.combine, kConsumerThreads);
+    hdr.abort = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (warp == 0) {
+    producer_warp<KV, D, G>(p, smem);
+    return;
+  }
+  const int cw = warp - 1;
+  const int lane = threadIdx.x & 31;
+  const volatile int *abort = &hdr.abort;
+  uint8_t *stages = smem + p.stages_off;
+  float *so = reinterpret_cast<float *>(smem + p.scratch_off);
+  float *sm = so + kConsumerWarps * G * D;
+  float *sl = sm + kConsumerWarps * G;
+  constexpr int ROWB = D * elt_bytes(KV);
+  using State = typename std::conditional<MMA, MmaState<KV, QT, D, G>, SimtState<KV, QT, D, G>>::type;
+  State st;
+  int it = 0, ncomb = 0;
+  bool failed = false;
+  while (true) {
+    const int stage = it % p.num_stages;
+    const uint32_t par = (it / p.num_stages) & 1;
+    if (!mbar_wait(&hdr.full[stage], par, abort)) {
+      failed = true;
+      break;
+    }
+    const StageInfo inf = hdr.info[stage];
+    if (inf.flags & kEnd) break;
+    const uint8_t *sb = stages + static_cast<size_t>(stage) * p.stage_bytes;
+    if (inf.flags & kFirst) st.start(sb + p.q_off, p.qk_scale_log2);
+    const int n = min(16, inf.ntok - 16 * cw);
+    if (n > 0) st.slice(sb + p.k_off + 16 * cw * ROWB, sb + p.v_off + 16 * cw * ROWB, n, p.v_scale);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&hdr.empty[stage]);
+    if (inf.flags & kLast) {
+      if constexpr (MMA) {
+        st.to_scratch(so, sm, sl, cw, p.v_scale);
+      } else {
+        st.to_scratch(so, sm, sl, cw);
+      }
+      mbar_arrive(&hdr.combine);
+      if (!mbar_wait(&hdr.combine, (2 * ncomb) & 1, abort)) {
+        failed = true;
+        break;
+      }
+      combine_item<QT, D, G>(p, inf, so, sm, sl);
+      mbar_arrive(&hdr.combine);
+      if (!mbar_wait(&hdr.combine, (2 * ncomb + 1) & 1, abort)) {
+        failed = true;
+        break;
+      }
+      ++ncomb;
+    }
+    ++it;
+  }
+  if (failed && lane == 0) {
+    record_error(p.err, kErrTimeout);
+    hdr.abort = 1;
+  }
+}
+
+// Shared-memory plan of one decode instantiation.
+struct DecodeSmemPlan {
+  int stage_bytes, k_off, v_off, q_off, scratch_off, stages_off, num_stages, total;
+};
+
+template <int KV, int D, int G>
+inline DecodeSmemPlan plan_smem(int max_smem) {
+  constexpr int ROWB = D * elt_bytes(KV);
+  DecodeSmemPlan s{};
+  s.k_off = 0;
+  s.v_off = kStageTok * ROWB;
+  s.q_off = 2 * kStageTok * ROWB;
+  s.stage_bytes = (s.q_off + G * D * 2 + 127) / 128 * 128;
+  s.scratch_off = (static_cast<int>(sizeof(SmemHeader)) + 127) / 128 * 128;
+  const int scratch = kConsumerWarps * (G * D + 2 * G) * 4;
+  s.stages_off = (s.scratch_off + scratch + 1023) / 1024 * 1024;
+  int ns = (max_smem - s.stages_off) / s.stage_bytes;
+  if (ns > kMaxStages) ns = kMaxStages;
+  s.num_stages = ns;
+  s.total = s.stages_off + ns * s.stage_bytes;
+  return s;
+}
+
+// ----------------------------------------------------------------------------
+// host launch of one instantiation: plan, persistent decode, merge
+// ----------------------------------------------------------------------------
+template <int KV, int QT, int D, int G, bool MMA>
+pa_status launch_decode(DecodeParams p, const DeviceInfo &dev, cudaStream_t stream) {
+  const DecodeSmemPlan sp = plan_smem<KV, D, G>(dev.max_smem_optin);
+  if (sp.num_stages < 2) return PA_ERR_UNSUPPORTED;
+  p.num_stages = sp.num_stages;
+  p.stage_bytes = sp.stage_bytes;
+  p.k_off = sp.k_off;
+  p.v_off = sp.v_off;
+  p.q_off = sp.q_off;
+  p.scratch_off = sp.scratch_off;
+  p.stages_off = sp.stages_off;
+  auto kern = decode_kernel<KV, QT, D, G, MMA>;
+  static int configured_bytes[64];  // per device: dynamic smem already allowed
+  int dev_id = 0;
+  cudaError_t e = cudaGetDevice(&dev_id);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (dev_id < 0 || dev_id >= 64 || configured_bytes[dev_id] < sp.total) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, sp.total);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (dev_id >= 0 && dev_id < 64) configured_bytes[dev_id] = sp.total;
+  }
+  plan_kernel<<<1, 1024, 0, stream>>>(p);
+  const long long items = static_cast<long long>(p.num_seqs) * p.max_parts * p.num_kv_heads;
+  const int grid = static_cast<int>(items < dev.sm_count ? items : dev.sm_count);
+  kern<<<grid, kThreads, sp.total, stream>>>(p);
+  if (p.max_parts > 1) {
+    const long long warps = static_cast<long long>(p.num_seqs) * p.num_q_heads;
+    const int blocks = static_cast<int>((warps * 32 + 255) / 256);
+    merge_kernel<QT, D><<<blocks, 256, 0, stream>>>(p);
+  }
+  e = cudaGetLastError();
+  return e == cudaSuccess ? PA_OK : cuda_fail(e);
+}
+
+template <int KV, int QT, int D>
+pa_status launch_by_group(int group, const DecodeParams &p, const DeviceInfo &dev, cudaStream_t s) {
+  switch (group) {
+    case 1: return launch_decode<KV, QT, D, 1, false>(p, dev, s);
+    case 2: return launch_decode<KV, QT, D, 2, false>(p, dev, s);
+    case 4: return launch_decode<KV, QT, D, 4, true>(p, dev, s);
+    case 8: return launch_decode<KV, QT, D, 8, true>(p, dev, s);
+  }
+  return PA_ERR_UNSUPPORTED;
+}
+
+template <int KV, int QT>
+pa_status launch_by_dim(int head_dim, int group, const DecodeParams &p, const DeviceInfo &dev,
+                        cudaStream_t s) {
+  if (head_dim == 64) return launch_by_group<KV, QT, 64>(group, p, dev, s);
+  if (head_dim == 128) return launch_by_group<KV, QT, 128>(group, p, dev, s);
+  return PA_ERR_UNSUPPORTED;
+}
+
+}  // namespace
+}  // namespace pa

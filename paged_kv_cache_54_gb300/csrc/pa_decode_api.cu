@@ -1,0 +1,132 @@
+// Host entry points of the decode path: argument checks, partition choice,
+// workspace layout, dispatch by cache dtype.
+#include <math.h>
+
+#include "pa_decode_params.h"
+
+namespace pa {
+namespace {
+
+// Tokens per work item.  512 unless that leaves fewer than ~1024 items
+// (about 7 per SM), in which case it halves, down to one 64-token stage.
+int choose_partition(int num_seqs, int kv_heads, int max_seq_len, int requested) {
+  if (requested > 0) return requested;
+  int P = 512;
+  while (P > kStageTok &&
+         static_cast<long long>(num_seqs) * kv_heads * ((max_seq_len + P - 1) / P) < 1024)
+    P >>= 1;
+  return P;
+}
+
+struct WorkspaceLayout {
+  size_t pairs_off, ml_off, o_off, total;
+  int partition, max_parts;
+};
+
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+bool layout_for(int num_seqs, int num_q_heads, int kv_heads, int head_dim, int max_seq_len,
+                int partition_size, WorkspaceLayout *out) {
+  if (num_seqs < 0 || num_q_heads <= 0 || kv_heads <= 0 || head_dim <= 0 || max_seq_len < 0)
+    return false;
+  if (partition_size < 0 || partition_size > kMaxPartition || partition_size % kStageTok) return false;
+  WorkspaceLayout w;
+  w.partition = choose_partition(num_seqs, kv_heads, max_seq_len, partition_size);
+  w.max_parts = max_seq_len > 0 ? (max_seq_len + w.partition - 1) / w.partition : 1;
+  const size_t units = static_cast<size_t>(num_seqs) * w.max_parts;
+  w.pairs_off = 256;
+  w.ml_off = align256(w.pairs_off + units * sizeof(int2));
+  w.o_off = align256(w.ml_off + units * num_q_heads * sizeof(float2));
+  w.total = align256(w.o_off + units * num_q_heads * head_dim * sizeof(float));
+  *out = w;
+  return true;
+}
+
+}  // namespace
+}  // namespace pa
+
+using namespace pa;
+
+extern "C" size_t pa_decode_workspace_size(int32_t num_seqs, int32_t num_q_heads,
+                                           int32_t num_kv_heads, int32_t head_dim,
+                                           int32_t max_seq_len, int32_t partition_size) {
+  WorkspaceLayout w;
+  if (!layout_for(num_seqs, num_q_heads, num_kv_heads, head_dim, max_seq_len, partition_size, &w))
+    return 0;
+  return w.total;
+}
+
+extern "C" pa_status pa_decode(void *out, const void *q, int32_t q_dtype, int32_t num_seqs,
+                               int32_t num_q_heads, const void *k_cache, const void *v_cache,
+                               const pa_cache_desc *cache, const int32_t *block_tables,
+                               int32_t max_blocks_per_seq, const int32_t *seq_lens,
+                               int32_t max_seq_len, float scale, int32_t partition_size,
+                               void *workspace, size_t workspace_bytes, int *device_error,
+                               pa_stream_t stream) {
+  if (!valid_cache_desc(cache) || num_seqs < 0 || num_q_heads <= 0 || max_seq_len < 0 ||
+      max_blocks_per_seq <= 0 || !isfinite(scale))
+    return PA_ERR_INVALID;
+  if (num_seqs == 0) return PA_OK;
+  if (!out || !q || !k_cache || !v_cache || !block_tables || !seq_lens || !workspace)
+    return PA_ERR_INVALID;
+  if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) ||
+      (reinterpret_cast<uintptr_t>(block_tables) & 3u) || (reinterpret_cast<uintptr_t>(seq_lens) & 3u) ||
+      (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return PA_ERR_INVALID;
+  if (num_q_heads % cache->kv_heads) return PA_ERR_INVALID;
+  const int G = num_q_heads / cache->kv_heads;
+  if (G != 1 && G != 2 && G != 4 && G != 8) return PA_ERR_UNSUPPORTED;
+  if (!supported_cache_shape(cache)) return PA_ERR_UNSUPPORTED;
+  if (q_dtype != PA_F16 && q_dtype != PA_BF16) return PA_ERR_UNSUPPORTED;
+  const bool fp8 = cache->dtype == PA_FP8_E4M3 || cache->dtype == PA_FP8_E5M2;
+  if (!fp8 && q_dtype != cache->dtype) return PA_ERR_UNSUPPORTED;
+  if (partition_size != 0 &&
+      (partition_size < kStageTok || partition_size > kMaxPartition ||
+       partition_size % kStageTok || partition_size % cache->block_size))
+    return PA_ERR_INVALID;
+  WorkspaceLayout w;
+  if (!layout_for(num_seqs, num_q_heads, cache->kv_heads, cache->head_dim, max_seq_len,
+                  partition_size, &w))
+    return PA_ERR_INVALID;
+  if (workspace_bytes < w.total) return PA_ERR_INVALID;
+  DeviceInfo dev;
+  if (!current_device_info(&dev)) return cuda_fail(cudaGetLastError());
+
+  const long long cap_table = static_cast<long long>(max_blocks_per_seq) * cache->block_size;
+  const long long cap_parts = static_cast<long long>(w.max_parts) * w.partition;
+  const long long cap = cap_table < cap_parts ? cap_table : cap_parts;
+
+  uint8_t *ws = static_cast<uint8_t *>(workspace);
+  DecodeParams p{};
+  p.out = out;
+  p.q = static_cast<const uint8_t *>(q);
+  p.k_cache = static_cast<const uint8_t *>(k_cache);
+  p.v_cache = static_cast<const uint8_t *>(v_cache);
+  p.block_tables = block_tables;
+  p.seq_lens = seq_lens;
+  p.num_seqs = num_seqs;
+  p.num_q_heads = num_q_heads;
+  p.num_kv_heads = cache->kv_heads;
+  p.num_blocks = cache->num_blocks;
+  p.block_size = cache->block_size;
+  p.max_blocks = max_blocks_per_seq;
+  p.partition_size = w.partition;
+  p.max_parts = w.max_parts;
+  p.len_cap = static_cast<int>(cap > 0x7fffffff ? 0x7fffffff : cap);
+  p.qk_scale_log2 = scale * (fp8 ? cache->k_scale : 1.0f) * 1.4426950408889634f;
+  p.v_scale = fp8 ? cache->v_scale : 1.0f;
+  p.work = reinterpret_cast<int *>(ws);
+  p.pairs = reinterpret_cast<int2 *>(ws + w.pairs_off);
+  p.part_ml = reinterpret_cast<float2 *>(ws + w.ml_off);
+  p.part_o = reinterpret_cast<float *>(ws + w.o_off);
+  p.err = device_error;
+
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  switch (cache->dtype) {
+    case PA_F16: return dispatch_decode_f16(q_dtype, cache->head_dim, G, p, dev, s);
+    case PA_BF16: return dispatch_decode_bf16(q_dtype, cache->head_dim, G, p, dev, s);
+    case PA_FP8_E4M3: return dispatch_decode_e4m3(q_dtype, cache->head_dim, G, p, dev, s);
+    case PA_FP8_E5M2: return dispatch_decode_e5m2(q_dtype, cache->head_dim, G, p, dev, s);
+  }
+  return PA_ERR_UNSUPPORTED;
+}

@@ -1,0 +1,68 @@
+// Parameters shared by the decode kernels and the host entry point.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "pa.h"
+#include "pa_host.h"
+
+namespace pa {
+
+constexpr int kStageTok = 64;          // tokens per pipeline stage
+constexpr int kConsumerWarps = 4;      // each owns 16 tokens of a stage
+constexpr int kThreads = 32 * (1 + kConsumerWarps);
+constexpr int kConsumerThreads = 32 * kConsumerWarps;
+constexpr int kMaxStages = 16;
+constexpr int kMaxPartition = 1024;
+
+enum StageFlags : int { kFirst = 1, kLast = 2, kEnd = 4 };
+
+struct StageInfo {
+  int s, h, p;
+  int tok0;   // sequence position of the stage's first token
+  int ntok;   // valid tokens in the stage (0..64)
+  int flags;
+  int L;      // sequence length (clamped to the table capacity)
+  int nP;     // number of partitions of the sequence
+};
+
+struct SmemHeader {
+  uint64_t full[kMaxStages];
+  uint64_t empty[kMaxStages];
+  uint64_t combine;
+  StageInfo info[kMaxStages];
+  int abort;
+};
+
+struct DecodeParams {
+  void *out;
+  const uint8_t *q;
+  const uint8_t *k_cache;
+  const uint8_t *v_cache;
+  const int32_t *block_tables;
+  const int32_t *seq_lens;
+  int num_seqs, num_q_heads, num_kv_heads, num_blocks, block_size, max_blocks;
+  int partition_size, max_parts, len_cap;
+  float qk_scale_log2;  // softmax scale * k_scale * log2(e)
+  float v_scale;
+  int num_stages, stage_bytes, k_off, v_off, q_off, scratch_off, stages_off;
+  int *work;  // [0] claim counter, [1] number of (s, p) pairs
+  int2 *pairs;
+  float2 *part_ml;  // [S * max_parts * Hq] (max in log2 units, sum)
+  float *part_o;    // [S * max_parts * Hq * D], normalised by its own sum
+  int *err;
+};
+
+
+// One instantiation family per cache dtype (separate translation units).
+pa_status dispatch_decode_f16(int q_dtype, int head_dim, int group, DecodeParams p,
+                              const DeviceInfo &dev, cudaStream_t stream);
+pa_status dispatch_decode_bf16(int q_dtype, int head_dim, int group, DecodeParams p,
+                               const DeviceInfo &dev, cudaStream_t stream);
+pa_status dispatch_decode_e4m3(int q_dtype, int head_dim, int group, DecodeParams p,
+                               const DeviceInfo &dev, cudaStream_t stream);
+pa_status dispatch_decode_e5m2(int q_dtype, int head_dim, int group, DecodeParams p,
+                               const DeviceInfo &dev, cudaStream_t stream);
+
+}  // namespace pa

@@ -1,0 +1,137 @@
+"""Helpers for the GPU parity tests: run a workload through the C ABI and
+build the oracle's view of the same inputs."""
+import numpy as np
+import torch
+
+import paged_kv_cache_54_gb300 as pa
+from oracle import attention as A
+from oracle import fp8 as F
+from oracle.cache import NAN_CODE, PagedKVCache, bits_to_f64
+
+DEV = "cuda:0"
+TOL = {"f16": 2e-3, "bf16": 1e-2}
+FP8_TOL = 1e-2
+
+
+def bits(t):
+    t = t.detach().cpu().contiguous()
+    if t.element_size() == 1:
+        return t.view(torch.uint8).numpy()
+    return t.view(torch.int16).numpy().view(np.uint16)
+
+
+def new_caches(w):
+    shape = (w.num_blocks, w.Hkv, w.bs, w.d)
+    if w.cache_dtype in ("e4m3", "e5m2"):
+        kc = torch.full(shape, NAN_CODE[w.cache_dtype], dtype=torch.uint8, device=DEV)
+        vc = torch.full(shape, NAN_CODE[w.cache_dtype], dtype=torch.uint8, device=DEV)
+    else:
+        dt = torch.float16 if w.cache_dtype == "f16" else torch.bfloat16
+        kc = torch.full(shape, float("nan"), dtype=dt, device=DEV)
+        vc = torch.full(shape, float("nan"), dtype=dt, device=DEV)
+    return kc, vc
+
+
+class GpuRun:
+    """Set-up (context write) and one step (copies, new tokens, decode)."""
+
+    def __init__(self, w, partition_size=None):
+        self.w = w
+        self.P = w.partition_size if partition_size is None else partition_size
+        self.kc, self.vc = new_caches(w)
+        self.err = torch.zeros(1, dtype=torch.int32, device=DEV)
+        self.bt = torch.from_numpy(w.block_tables).to(DEV)
+        self.sl = torch.from_numpy(w.seq_lens).to(DEV)
+        self.new_slots = torch.from_numpy(w.new_slots).to(DEV)
+        self.pairs = torch.from_numpy(w.cow_pairs).to(DEV)
+        self.out = torch.empty_like(w.q)
+        self.kw = dict(cache_dtype=w.cache_dtype, k_scale=w.k_scale, v_scale=w.v_scale)
+        self.ws = torch.empty(max(256, pa.pa_decode_workspace_size(
+            w.S, w.Hq, w.Hkv, w.d, w.max_seq_len, self.P)), dtype=torch.uint8, device=DEV)
+
+    def setup(self):
+        w = self.w
+        if len(w.ctx_slots):
+            slots = torch.from_numpy(w.ctx_slots).to(DEV)
+            pa.pa_reshape_and_cache(w.ctx_k, w.ctx_v, slots, self.kc, self.vc,
+                                    device_error=self.err, **self.kw)
+        return self
+
+    def step(self):
+        w = self.w
+        if len(w.cow_pairs):
+            pa.pa_copy_blocks(self.kc, self.vc, self.pairs, cache_dtype=w.cache_dtype,
+                              device_error=self.err)
+        pa.pa_reshape_and_cache(w.new_k, w.new_v, self.new_slots, self.kc, self.vc,
+                                device_error=self.err, **self.kw)
+        self.decode()
+        return self
+
+    def decode(self):
+        w = self.w
+        pa.pa_decode(self.out, w.q, self.kc, self.vc, self.bt, self.sl, w.max_seq_len,
+                     w.scale, partition_size=self.P, workspace=self.ws,
+                     device_error=self.err, **self.kw)
+        return self.out
+
+
+def oracle_cache(w):
+    """The oracle's own cache after set-up and one step (small workloads)."""
+    c = PagedKVCache(w.num_blocks, w.Hkv, w.bs, w.d, w.cache_dtype, w.k_scale, w.v_scale)
+    c.reshape_and_cache(bits(w.ctx_k), bits(w.ctx_v), w.src_dtype, w.ctx_slots)
+    c.copy_blocks(w.cow_pairs)
+    c.reshape_and_cache(bits(w.new_k), bits(w.new_v), w.src_dtype, w.new_slots)
+    return c
+
+
+def q_values(w):
+    return bits_to_f64(bits(w.q), w.q_dtype)
+
+
+def oracle_decode(w, c, rows=None):
+    return A.paged_decode(q_values(w), c.k, c.v, w.cache_dtype, w.block_tables, w.seq_lens,
+                          w.scale, w.k_scale, w.v_scale, rows=rows)
+
+
+def logical_kv(w, s, h):
+    """float64 [L, d] K and V of sequence s, KV head h, from the input rows."""
+    rows = w.token_rows(s)
+    ctx_idx = [i for k, i in rows if k == "ctx"]
+    new_idx = [i for k, i in rows if k == "new"]
+    out = []
+    for src_ctx, src_new, scale in ((w.ctx_k, w.new_k, w.k_scale), (w.ctx_v, w.new_v, w.v_scale)):
+        parts = []
+        if ctx_idx:
+            parts.append(bits(src_ctx[torch.tensor(ctx_idx, device=src_ctx.device), h]))
+        if new_idx:
+            parts.append(bits(src_new[torch.tensor(new_idx, device=src_new.device), h]))
+        raw = np.concatenate(parts) if parts else np.zeros((0, w.d), np.uint16)
+        if w.cache_dtype in ("e4m3", "e5m2"):
+            vals = F.decode(F.quantize_bits16(raw, w.src_dtype, scale, w.cache_dtype),
+                            w.cache_dtype) * scale
+        else:
+            vals = bits_to_f64(raw, w.src_dtype)
+        out.append(vals)
+    return out
+
+
+def oracle_rows(w, rows):
+    """Oracle output for sampled (s, hq) rows, from the logical sequences."""
+    q = q_values(w)
+    res = {}
+    for s, hq in rows:
+        h = hq // w.G
+        K, V = logical_kv(w, s, h)
+        res[(s, hq)] = A.attend(q[s, hq], K, V, w.scale)[0]
+    return res
+
+
+def ulp(x, dtype):
+    """Spacing of the output dtype at |x| (fp16: 11 significant bits, bf16: 8)."""
+    mant = 10 if dtype == "f16" else 7
+    e = np.floor(np.log2(np.maximum(np.abs(x), 2.0 ** -14)))
+    return 2.0 ** (e - mant)
+
+
+def tolerance(w):
+    return FP8_TOL if w.cache_dtype in ("e4m3", "e5m2") else TOL[w.q_dtype]

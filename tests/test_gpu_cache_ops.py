@@ -1,0 +1,96 @@
+"""Cache write and block copy on the GPU: bit-exact against the oracle."""
+import numpy as np
+import pytest
+import torch
+
+import workloads as W
+from tests import _gpu as G
+
+pytestmark = pytest.mark.gpu
+
+DTYPES = [("f16", "f16"), ("bf16", "bf16"), ("e4m3", "bf16"), ("e4m3", "f16"),
+          ("e5m2", "f16"), ("e5m2", "bf16")]
+
+
+@pytest.mark.parametrize("cache_dtype,src", DTYPES)
+@pytest.mark.parametrize("d,bs", [(64, 16), (128, 8), (128, 32)])
+def test_reshape_and_cache_bit_exact(cache_dtype, src, d, bs):
+    scales = (0.37, 2.5) if cache_dtype in ("e4m3", "e5m2") else (1.0, 1.0)
+    w = W.random_case(5, 5, 4, 2, d, bs, cache_dtype, src, [1, bs - 1, bs, bs + 1, 77],
+                      device=G.DEV, k_scale=scales[0], v_scale=scales[1])
+    run = G.GpuRun(w).setup()
+    run.step()
+    torch.cuda.synchronize()
+    assert int(run.err.item()) == 0
+    c = G.oracle_cache(w)
+    np.testing.assert_array_equal(G.bits(run.kc), c.k)
+    np.testing.assert_array_equal(G.bits(run.vc), c.v)
+
+
+@pytest.mark.parametrize("cache_dtype", ["f16", "e4m3"])
+def test_reshape_and_cache_large_values_saturate(cache_dtype):
+    w = W.random_case(6, 2, 2, 2, 128, 16, cache_dtype, "bf16" if cache_dtype == "e4m3" else "f16",
+                      [40, 33], device=G.DEV, k_scale=0.01, v_scale=0.02)
+    w.ctx_k.mul_(100)   # many values beyond 448 * scale: saturate to the largest code
+    w.new_v.mul_(300)
+    run = G.GpuRun(w).setup()
+    run.step()
+    torch.cuda.synchronize()
+    c = G.oracle_cache(w)
+    np.testing.assert_array_equal(G.bits(run.kc), c.k)
+    np.testing.assert_array_equal(G.bits(run.vc), c.v)
+
+
+def test_padding_slots_are_skipped():
+    import paged_kv_cache_54_gb300 as pa
+    kc = torch.zeros((8, 2, 16, 64), dtype=torch.float16, device=G.DEV)
+    vc = torch.zeros_like(kc)
+    key = torch.randn((4, 2, 64), device=G.DEV).half()
+    val = torch.randn((4, 2, 64), device=G.DEV).half()
+    slots = torch.tensor([3, -1, 17, -1], dtype=torch.int64, device=G.DEV)
+    pa.pa_reshape_and_cache(key, val, slots, kc, vc)
+    torch.cuda.synchronize()
+    assert torch.equal(kc[0, :, 3], key[0]) and torch.equal(vc[1, :, 1], val[2])
+    assert int((kc != 0).sum()) == int((key[0] != 0).sum() + (key[2] != 0).sum())
+
+
+@pytest.mark.parametrize("cache_dtype", ["f16", "bf16", "e4m3"])
+@pytest.mark.parametrize("bs", [8, 16, 32])
+def test_copy_blocks_bit_exact(cache_dtype, bs):
+    import paged_kv_cache_54_gb300 as pa
+    nb, H, d = 40, 3, 128
+    g = torch.Generator(device=G.DEV).manual_seed(bs)
+    if cache_dtype == "e4m3":
+        kc = torch.randint(0, 256, (nb, H, bs, d), generator=g, device=G.DEV, dtype=torch.int32).to(torch.uint8)
+        vc = torch.randint(0, 256, (nb, H, bs, d), generator=g, device=G.DEV, dtype=torch.int32).to(torch.uint8)
+    else:
+        dt = torch.float16 if cache_dtype == "f16" else torch.bfloat16
+        kc = torch.randn((nb, H, bs, d), generator=g, device=G.DEV).to(dt)
+        vc = torch.randn((nb, H, bs, d), generator=g, device=G.DEV).to(dt)
+    rng = np.random.default_rng(bs)
+    perm = rng.permutation(nb)
+    pairs = np.stack([perm[:12], perm[12:24]], axis=1)      # dst never a src
+    ref_k, ref_v = G.bits(kc).copy(), G.bits(vc).copy()
+    for s, t in pairs:
+        ref_k[t] = ref_k[s]
+        ref_v[t] = ref_v[s]
+    pa.pa_copy_blocks(kc, vc, torch.from_numpy(pairs).to(G.DEV), cache_dtype=cache_dtype)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(G.bits(kc), ref_k)
+    np.testing.assert_array_equal(G.bits(vc), ref_v)
+
+
+def test_out_of_range_slot_and_pair_are_reported():
+    import paged_kv_cache_54_gb300 as pa
+    kc = torch.zeros((4, 1, 16, 64), dtype=torch.float16, device=G.DEV)
+    vc = torch.zeros_like(kc)
+    err = torch.zeros(1, dtype=torch.int32, device=G.DEV)
+    key = torch.ones((2, 1, 64), dtype=torch.float16, device=G.DEV)
+    pa.pa_reshape_and_cache(key, key, torch.tensor([5, 64], device=G.DEV), kc, vc, device_error=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 2
+    assert float(kc.sum()) == 64.0          # the valid row was still written
+    err.zero_()
+    pa.pa_copy_blocks(kc, vc, torch.tensor([[0, 9]], device=G.DEV), device_error=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 5

@@ -1,0 +1,132 @@
+"""pa_decode against the float64 oracle on small seeded cases (GPU)."""
+import itertools
+
+import numpy as np
+import pytest
+import torch
+
+import workloads as W
+from tests import _gpu as G
+
+pytestmark = pytest.mark.gpu
+
+DTYPES = [("f16", "f16"), ("bf16", "bf16"), ("e4m3", "bf16"), ("e4m3", "f16"),
+          ("e5m2", "f16"), ("e5m2", "bf16")]
+
+
+def _check(w, got, ref, extra_ulp=True):
+    tol = G.tolerance(w)
+    got = got.float().cpu().numpy().astype(np.float64)
+    bound = np.maximum(tol, G.ulp(ref, w.q_dtype)) if extra_ulp else tol
+    err = np.abs(got - ref)
+    bad = err > bound
+    assert not bad.any(), (f"max |err| {err.max():.3e} at {np.argwhere(bad)[:5].tolist()}, "
+                           f"tol {tol}")
+    return float(err.max())
+
+
+def _lens(bs, P):
+    return [0, 1, bs - 1, bs, bs + 1, 63, 64, 65, P - 1, P, P + 1, 2 * P + 17, 700]
+
+
+@pytest.mark.parametrize("cache_dtype,q_dtype", DTYPES)
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("bs", [8, 16, 32])
+@pytest.mark.parametrize("group", [1, 2, 4, 8])
+def test_decode_matches_oracle(cache_dtype, q_dtype, d, bs, group):
+    Hkv = 2
+    P = 128
+    lens = _lens(bs, P)
+    fp8 = cache_dtype in ("e4m3", "e5m2")
+    w = W.random_case(hash((cache_dtype, q_dtype, d, bs, group)) % 1000, len(lens), Hkv * group,
+                      Hkv, d, bs, cache_dtype, q_dtype, lens, device=G.DEV,
+                      k_scale=0.5 if fp8 else 1.0, v_scale=1.5 if fp8 else 1.0)
+    run = G.GpuRun(w, partition_size=P).setup()
+    run.step()
+    torch.cuda.synchronize()
+    assert int(run.err.item()) == 0
+    ref = G.oracle_decode(w, G.oracle_cache(w))
+    _check(w, run.out, ref)
+    assert torch.all(run.out[0] == 0)          # length 0 gives zeros
+
+
+@pytest.mark.parametrize("cache_dtype,q_dtype,group", [("f16", "f16", 1), ("bf16", "bf16", 2),
+                                                       ("e4m3", "bf16", 8), ("f16", "f16", 4)])
+def test_partition_size_does_not_change_the_result(cache_dtype, q_dtype, group):
+    lens = [1, 100, 511, 512, 513, 1500, 2049]
+    w = W.random_case(9, len(lens), 2 * group, 2, 128, 16, cache_dtype, q_dtype, lens,
+                      device=G.DEV)
+    c = G.oracle_cache(w)
+    ref = G.oracle_decode(w, c)
+    outs = []
+    for P in (64, 192, 512, 1024, 0):
+        run = G.GpuRun(w, partition_size=P).setup()
+        run.step()
+        torch.cuda.synchronize()
+        assert int(run.err.item()) == 0
+        _check(w, run.out, ref)
+        outs.append(run.out.float())
+    tol = G.tolerance(w)
+    for o in outs[1:]:
+        assert float((o - outs[0]).abs().max()) <= 2 * tol
+
+
+def test_equal_keys_give_mean_of_values():
+    lens = [1, 37, 300, 1000]
+    w = W.random_case(3, len(lens), 2, 2, 128, 16, "f16", "f16", lens, device=G.DEV)
+    w.ctx_k.copy_(w.ctx_k[:1].expand_as(w.ctx_k))
+    w.new_k.copy_(w.ctx_k[:1].expand_as(w.new_k))
+    run = G.GpuRun(w, partition_size=128).setup()
+    run.step()
+    torch.cuda.synchronize()
+    for s in range(w.S):
+        for hq in range(w.Hq):
+            _, V = G.logical_kv(w, s, hq)
+            np.testing.assert_allclose(run.out[s, hq].float().cpu().numpy(), V.mean(axis=0),
+                                       atol=2e-3)
+
+
+def test_repeated_calls_are_deterministic():
+    lens = [5, 900, 1700, 3]
+    w = W.random_case(4, len(lens), 8, 1, 128, 16, "e4m3", "bf16", lens, device=G.DEV)
+    run = G.GpuRun(w, partition_size=256).setup()
+    run.step()
+    a = run.out.clone()
+    for _ in range(3):
+        run.decode()
+    torch.cuda.synchronize()
+    assert torch.equal(a, run.out)
+
+
+def test_large_query_values_with_fp8_cache():
+    lens = [50, 300]
+    w = W.random_case(8, 2, 8, 1, 128, 16, "e4m3", "bf16", lens, device=G.DEV)
+    # entries beyond fp16's range (the fp16 tensor-core path rescales q by a
+    # power of two); the softmax scale shrinks by the same factor so that the
+    # scores, and the conditioning of the problem, stay as before
+    w.q.mul_(3.0e4)
+    w.scale /= 3.0e4
+    run = G.GpuRun(w).setup()
+    run.step()
+    torch.cuda.synchronize()
+    ref = G.oracle_decode(w, G.oracle_cache(w))
+    _check(w, run.out, ref)
+
+
+def test_bad_block_id_and_length_are_reported():
+    lens = [40, 20]
+    w = W.random_case(1, 2, 2, 2, 64, 16, "f16", "f16", lens, device=G.DEV)
+    run = G.GpuRun(w).setup()
+    run.step()
+    torch.cuda.synchronize()
+    assert int(run.err.item()) == 0
+    run.bt[0, 1] = w.num_blocks + 5
+    run.decode()
+    torch.cuda.synchronize()
+    assert int(run.err.item()) == 1
+    run.err.zero_()
+    run.bt.copy_(torch.from_numpy(w.block_tables).to(G.DEV))
+    run.sl[1] = w.block_tables.shape[1] * w.bs + 1
+    run.decode()
+    torch.cuda.synchronize()
+    assert int(run.err.item()) == 3

@@ -97,3 +97,16 @@ def test_quantize_divides_by_scale_in_float32():
     assert codes.tolist() == expect
     back = fp8.decode(codes, "e4m3") * float(scale)
     assert np.all(np.abs(back - x) <= np.abs(x) / 16 + 2.0 ** -9 * float(scale))
+
+
+@pytest.mark.parametrize("src", ["f16", "bf16"])
+@pytest.mark.parametrize("name", ["e4m3", "e5m2"])
+def test_table_quantizer_equals_direct(src, name):
+    rng = np.random.default_rng(3)
+    bits = rng.integers(0, 65536, 4000).astype(np.uint16)
+    vals = fp8._bits16_to_f32(bits, src)
+    keep = np.isfinite(vals)
+    for scale in (1.0, 0.37, 3.5):
+        a = fp8.quantize_bits16(bits[keep], src, scale, name)
+        b = fp8.quantize(vals[keep], scale, name)
+        np.testing.assert_array_equal(a, b)

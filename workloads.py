@@ -227,7 +227,8 @@ def build_structure(name: str, seed: int, overrides: Optional[dict] = None,
             for p in range(L - 1):
                 r.append(("ctx", len(ctx_slots)))
                 ctx_slots.append(slot(t, p))
-            r.append(("new", s))
+            if L > 0:
+                r.append(("new", s))
             new_slots.append(slot(t, L - 1) if L > 0 else -1)
             rows.append(r)
     elif kind == "prefix":
@@ -342,3 +343,57 @@ def random_case(seed: int, S: int, Hq: int, Hkv: int, d: int, bs: int,
     if cache_dtype in ("e4m3", "e5m2"):
         cfg["src_dtype"] = q_dtype
     return make_workload(None, seed, device=device, overrides=cfg, lens=lens)
+
+
+def subset(w: Workload, seqs, seed: int, device: str = "cpu") -> Workload:
+    """The sequences ``seqs`` of ``w`` on their own: their blocks renumbered
+    into a compact pool (same block-table structure and sharing), and fresh
+    seeded values for just their tokens.  Used for bounded CPU samples."""
+    seqs = list(seqs)
+    bs = w.bs
+    used = []
+    for s in seqs:
+        used += w.block_tables[s, :-(-int(w.seq_lens[s]) // bs)].tolist()
+    remap = {b: i for i, b in enumerate(dict.fromkeys(used))}
+    width = max(1, max(-(-int(w.seq_lens[s]) // bs) for s in seqs))
+    bt = np.zeros((len(seqs), width), dtype=np.int32)
+    for i, s in enumerate(seqs):
+        n = -(-int(w.seq_lens[s]) // bs)
+        bt[i, :n] = [remap[b] for b in w.block_tables[s, :n]]
+    ctx_map: Dict[int, int] = {}
+    rows, ctx_slots, new_slots = [], [], []
+    for i, s in enumerate(seqs):
+        r = []
+        for p, (kind, idx) in enumerate(w.token_rows(s)):
+            slot = int(bt[i, p // bs]) * bs + p % bs
+            if kind == "ctx":
+                if idx not in ctx_map:
+                    ctx_map[idx] = len(ctx_slots)
+                    ctx_slots.append(slot)
+                r.append(("ctx", ctx_map[idx]))
+            else:
+                r.append(("new", i))
+        L = int(w.seq_lens[s])
+        new_slots.append(int(bt[i, (L - 1) // bs]) * bs + (L - 1) % bs if L > 0 else -1)
+        rows.append(r)
+    sub = Workload(
+        name=f"{w.name}[{len(seqs)} seqs]", S=len(seqs), Hq=w.Hq, Hkv=w.Hkv, d=w.d, bs=bs,
+        num_blocks=max(1, len(remap)), cache_dtype=w.cache_dtype, q_dtype=w.q_dtype,
+        src_dtype=w.src_dtype, scale=w.scale, k_scale=w.k_scale, v_scale=w.v_scale,
+        partition_size=w.partition_size, seq_lens=w.seq_lens[seqs].copy(), block_tables=bt,
+        pool_order=np.arange(max(1, len(remap))), ctx_slots=np.asarray(ctx_slots, np.int64),
+        new_slots=np.asarray(new_slots, np.int64), cow_pairs=np.zeros((0, 2), np.int64),
+        rows=rows, kind=w.kind)
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    sd, qd = TORCH_DTYPES[w.src_dtype], TORCH_DTYPES[w.q_dtype]
+
+    def randn(*shape, dtype):
+        return torch.randn(*shape, generator=g, device=device, dtype=torch.float32).to(dtype)
+
+    sub.ctx_k = randn(len(ctx_slots), w.Hkv, w.d, dtype=sd)
+    sub.ctx_v = randn(len(ctx_slots), w.Hkv, w.d, dtype=sd)
+    sub.new_k = randn(sub.S, w.Hkv, w.d, dtype=sd)
+    sub.new_v = randn(sub.S, w.Hkv, w.d, dtype=sd)
+    sub.q = randn(sub.S, w.Hq, w.d, dtype=qd)
+    return sub
