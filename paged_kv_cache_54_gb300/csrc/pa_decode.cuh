@@ -164,17 +164,6 @@ __device__ __forceinline__ void producer_warp(const DecodeParams &p, uint8_t *sm
   const int total = n_pairs * p.num_kv_heads;
   constexpr uint32_t qbytes = G * D * 2;
 
-  auto claim = [&]() -> int {
-    int w = 0;
-    if (lane == 0) w = atomicAdd(p.work, 1);
-    return __shfl_sync(0xffffffffu, w, 0);
-  };
-  auto load_pair = [&](int w) -> int2 {
-    return (w < total) ? p.pairs[w % n_pairs] : make_int2(0, 0);
-  };
-  auto load_len = [&](int w, int2 pr) -> int {
-    return (w < total) ? __ldg(p.seq_lens + pr.x) : 0;
-  };
   auto load_table = [&](int w, int2 pr, int L, int (&ph)[4]) {
     const int nblk = (w < total) ? (min(max(L, 0), p.len_cap) + bs - 1) / bs : 0;
     const int32_t *row = p.block_tables + static_cast<size_t>(pr.x) * p.max_blocks;
@@ -186,22 +175,35 @@ __device__ __forceinline__ void producer_warp(const DecodeParams &p, uint8_t *sm
     }
   };
 
-  // current item
-  int w_c = claim();
-  int2 pr_c = load_pair(w_c);
-  int L_c = load_len(w_c, pr_c);
+  // current item (loaded synchronously once)
+  int w_c = 0;
+  if (lane == 0) w_c = atomicAdd(p.work, 1);
+  w_c = __shfl_sync(0xffffffffu, w_c, 0);
+  int2 pr_c = (w_c < total) ? p.pairs[w_c % n_pairs] : make_int2(0, 0);
+  int L_c = (w_c < total) ? __ldg(p.seq_lens + pr_c.x) : 0;
   int ph_c[4];
   load_table(w_c, pr_c, L_c, ph_c);
-  // next item, fetched step by step while the current one is issued
-  int w_n = 0, L_n = 0, pf = 0;
+  // Next item, fetched one dependent step per issued stage: each step only
+  // issues a load whose result the following step consumes, so the warp
+  // never waits on a round trip while stages are being refilled.
+  int w_raw = 0, w_n = 0, L_n = 0, pf = 0;
   int2 pr_n = make_int2(0, 0);
   int ph_n[4] = {0, 0, 0, 0};
   auto pf_step = [&]() {
     switch (pf) {
-      case 0: w_n = claim(); break;
-      case 1: pr_n = load_pair(w_n); break;
-      case 2: L_n = load_len(w_n, pr_n); break;
-      default: load_table(w_n, pr_n, L_n, ph_n); break;
+      case 0:
+        if (lane == 0) w_raw = atomicAdd(p.work, 1);
+        break;
+      case 1:
+        w_n = __shfl_sync(0xffffffffu, w_raw, 0);
+        pr_n = (w_n < total) ? p.pairs[w_n % n_pairs] : make_int2(0, 0);
+        break;
+      case 2:
+        L_n = (w_n < total) ? __ldg(p.seq_lens + pr_n.x) : 0;
+        break;
+      default:
+        load_table(w_n, pr_n, L_n, ph_n);
+        break;
     }
     ++pf;
   };
@@ -748,7 +750,7 @@ __device__ __forceinline__ void combine_item(const DecodeParams &p, const StageI
 // the persistent decode kernel
 // ----------------------------------------------------------------------------
 template <int KV, int QT, int D, int G, bool MMA>
-__global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams p) {
+__global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_kernel(const DecodeParams p) {
   extern __shared__ __align__(1024) uint8_t smem[];
   SmemHeader &hdr = *reinterpret_cast<SmemHeader *>(smem);
   const int warp = threadIdx.x >> 5;
@@ -848,7 +850,11 @@ inline DecodeSmemPlan plan_smem(int max_smem) {
 // ----------------------------------------------------------------------------
 template <int KV, int QT, int D, int G, bool MMA>
 pa_status launch_decode(DecodeParams p, const DeviceInfo &dev, cudaStream_t stream) {
-  const DecodeSmemPlan sp = plan_smem<KV, D, G>(dev.max_smem_optin);
+  // shared memory a CTA may use when kCtasPerSm of them share an SM (the
+  // hardware reserves 1 KB per resident CTA)
+  int budget = dev.max_smem_optin;
+  if (kCtasPerSm > 1) budget = min(budget, dev.smem_per_sm / kCtasPerSm - 1024);
+  const DecodeSmemPlan sp = plan_smem<KV, D, G>(budget);
   if (sp.num_stages < 2) return PA_ERR_UNSUPPORTED;
   p.num_stages = sp.num_stages;
   p.stage_bytes = sp.stage_bytes;
@@ -869,7 +875,8 @@ pa_status launch_decode(DecodeParams p, const DeviceInfo &dev, cudaStream_t stre
   }
   plan_kernel<<<1, 1024, 0, stream>>>(p);
   const long long items = static_cast<long long>(p.num_seqs) * p.max_parts * p.num_kv_heads;
-  const int grid = static_cast<int>(items < dev.sm_count ? items : dev.sm_count);
+  const long long slots = static_cast<long long>(dev.sm_count) * kCtasPerSm;
+  const int grid = static_cast<int>(items < slots ? items : slots);
   kern<<<grid, kThreads, sp.total, stream>>>(p);
   if (p.max_parts > 1) {
     const long long warps = static_cast<long long>(p.num_seqs) * p.num_q_heads;

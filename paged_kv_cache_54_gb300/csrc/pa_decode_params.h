@@ -15,6 +15,10 @@ constexpr int kThreads = 32 * (1 + kConsumerWarps);
 constexpr int kConsumerThreads = 32 * kConsumerWarps;
 constexpr int kMaxStages = 16;
 constexpr int kMaxPartition = 1024;
+#ifndef PA_DECODE_CTAS_PER_SM
+#define PA_DECODE_CTAS_PER_SM 1
+#endif
+constexpr int kCtasPerSm = PA_DECODE_CTAS_PER_SM;  // resident decode CTAs per SM
 
 enum StageFlags : int { kFirst = 1, kLast = 2, kEnd = 4 };
 

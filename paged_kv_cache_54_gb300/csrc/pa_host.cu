@@ -26,6 +26,9 @@ bool current_device_info(DeviceInfo *out) {
     if (cudaDeviceGetAttribute(&d.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
         cudaSuccess)
       return false;
+    if (cudaDeviceGetAttribute(&d.smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) !=
+        cudaSuccess)
+      return false;
     g_info[dev] = d;
     g_have[dev] = true;
   }

@@ -12,6 +12,7 @@ namespace pa {
 struct DeviceInfo {
   int sm_count = 0;
   int max_smem_optin = 0;  // bytes of dynamic shared memory a block may opt into
+  int smem_per_sm = 0;     // bytes of shared memory per SM
 };
 
 // Properties of the current device, queried once per device.
