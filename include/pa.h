@@ -177,6 +177,41 @@ PA_API pa_status pa_decode(void *out, const void *q, int32_t q_dtype,
                     pa_stream_t stream);
 
 /*
+ * pa_decode_static_scratch — pa_decode for callers that cannot allocate.
+ *
+ * The pages have no counterpart to this call; it exists for callers of this
+ * library that may not allocate device memory at decode time: a plugin whose
+ * host framework owns all GPU memory through its own pool (an allocation
+ * outside the pool escapes its accounting and can fail once the KV pool has
+ * been sized to fill the device), or a serving loop that allows no
+ * allocation after start-up because cudaMalloc may synchronise the device.
+ *
+ * Same arguments and result as pa_decode, without `workspace`.  Its scratch
+ * is a fixed device array of PA_DECODE_STATIC_SCRATCH_BYTES (16 MiB) inside
+ * the library, held by every GPU that loads the library until the process
+ * exits.  The call allocates nothing (no cudaMalloc / cudaFree, no library
+ * routine that allocates).
+ * - Limit: a call whose pa_decode_workspace_size(...) exceeds
+ *   PA_DECODE_STATIC_SCRATCH_BYTES returns PA_ERR_UNSUPPORTED and launches
+ *   nothing; pass a caller-owned workspace to pa_decode instead.
+ * - First call on each device: it looks up the array's device address with
+ *   cudaGetSymbolAddress (with that device current) and caches it, so make
+ *   that first call before any stream capture begins.
+ * - Sharing: every call uses the same array and it keeps the last call's
+ *   contents; nothing in it needs to start at zero (each call rewrites its
+ *   work list and claim counter first).  Calls whose execution overlaps on
+ *   the GPU (different streams, or different threads without ordering) race
+ *   on the array; order them on one stream.
+ */
+#define PA_DECODE_STATIC_SCRATCH_BYTES (16u << 20)
+PA_API pa_status pa_decode_static_scratch(
+    void *out, const void *q, int32_t q_dtype, int32_t num_seqs, int32_t num_q_heads,
+    const void *k_cache, const void *v_cache, const pa_cache_desc *cache,
+    const int32_t *block_tables, int32_t max_blocks_per_seq, const int32_t *seq_lens,
+    int32_t max_seq_len, float scale, int32_t partition_size, int *device_error,
+    pa_stream_t stream);
+
+/*
  * pa_copy_blocks — copy-on-write block copies ([P4] §3.3; [P1] §6.1: a
  * forked beam copies only the shared last block).
  *

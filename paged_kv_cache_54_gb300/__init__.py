@@ -32,7 +32,9 @@ if hasattr(torch, "float8_e5m2"):
     _TORCH_CODES[torch.float8_e5m2] = PA_FP8_E5M2
 
 EXPORTED = ("pa_reshape_and_cache", "pa_decode_workspace_size", "pa_decode",
-            "pa_copy_blocks", "pa_status_string", "pa_last_cuda_error")
+            "pa_decode_static_scratch", "pa_copy_blocks", "pa_status_string",
+            "pa_last_cuda_error")
+STATIC_SCRATCH_BYTES = 16 << 20   # PA_DECODE_STATIC_SCRATCH_BYTES
 
 
 class PaCacheDesc(ctypes.Structure):
@@ -67,6 +69,10 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
                               vp, i32, vp, i32, ctypes.c_float, i32, vp, ctypes.c_size_t,
                               vp, vp]
     lib.pa_decode.restype = ctypes.c_int
+    lib.pa_decode_static_scratch.argtypes = [vp, vp, i32, i32, i32, vp, vp,
+                                             ctypes.POINTER(PaCacheDesc), vp, i32, vp, i32,
+                                             ctypes.c_float, i32, vp, vp]
+    lib.pa_decode_static_scratch.restype = ctypes.c_int
     lib.pa_copy_blocks.argtypes = [vp, vp, ctypes.POINTER(PaCacheDesc), vp, i32, vp, vp]
     lib.pa_copy_blocks.restype = ctypes.c_int
     lib.pa_status_string.argtypes = [ctypes.c_int]
@@ -174,6 +180,36 @@ def pa_decode(out, q, k_cache, v_cache, block_tables, seq_lens, max_seq_len: int
                          partition_size, workspace.data_ptr(), workspace.numel(),
                          _ptr(device_error), _stream(stream)),
            "pa_decode")
+    return out
+
+
+def pa_decode_static_scratch(out, q, k_cache, v_cache, block_tables, seq_lens,
+                             max_seq_len: int, scale: float, cache_dtype=None,
+                             k_scale: float = 1.0, v_scale: float = 1.0,
+                             partition_size: int = 0, device_error=None,
+                             stream=None) -> torch.Tensor:
+    """``pa_decode`` for callers that cannot allocate device memory.
+
+    Uses the library's own fixed 16 MiB device scratch instead of a
+    workspace, so nothing is allocated here either; shapes that need more
+    scratch than that are rejected (use ``pa_decode`` with a workspace).
+    Calls that overlap on the GPU race on the shared scratch.
+    """
+    for t, n in ((out, "out"), (q, "q"), (k_cache, "k_cache"), (v_cache, "v_cache"),
+                 (block_tables, "block_tables"), (seq_lens, "seq_lens")):
+        _require(t, n)
+    desc = cache_desc(k_cache, cache_dtype, k_scale, v_scale)
+    S, Hq, D = q.shape
+    need = pa_decode_workspace_size(S, Hq, desc.kv_heads, D, max_seq_len, partition_size)
+    if need > STATIC_SCRATCH_BYTES:
+        raise PaError(f"pa_decode_static_scratch: these sizes need {need} bytes of scratch, "
+                      f"more than its fixed {STATIC_SCRATCH_BYTES}; use pa_decode")
+    lib = load_library()
+    _check(lib.pa_decode_static_scratch(
+        out.data_ptr(), q.data_ptr(), _TORCH_CODES.get(q.dtype, -1), S, Hq,
+        k_cache.data_ptr(), v_cache.data_ptr(), ctypes.byref(desc), block_tables.data_ptr(),
+        block_tables.shape[1], seq_lens.data_ptr(), max_seq_len, scale, partition_size,
+        _ptr(device_error), _stream(stream)), "pa_decode_static_scratch")
     return out
 
 
