@@ -54,6 +54,23 @@ __device__ __forceinline__ uint32_t fp8x2_to_half2_bits(uint32_t two_codes) {
   return static_cast<uint32_t>(r.x) | (static_cast<uint32_t>(r.y) << 16);
 }
 
+// four FP8 codes in one word -> two __half2 (codes 0,1 -> lo; codes 2,3 -> hi),
+// exact: every e4m3 / e5m2 value is an fp16 value
+template <int DT>
+__device__ __forceinline__ void fp8x4_to_half2x2(uint32_t w, uint32_t &lo, uint32_t &hi) {
+  if constexpr (DT == kE4M3) {
+    asm("{\n\t.reg .b16 a, b;\n\tmov.b32 {a, b}, %2;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %0, a;\n\tcvt.rn.f16x2.e4m3x2 %1, b;\n\t}"
+        : "=r"(lo), "=r"(hi)
+        : "r"(w));
+  } else {
+    asm("{\n\t.reg .b16 a, b;\n\tmov.b32 {a, b}, %2;\n\t"
+        "cvt.rn.f16x2.e5m2x2 %0, a;\n\tcvt.rn.f16x2.e5m2x2 %1, b;\n\t}"
+        : "=r"(lo), "=r"(hi)
+        : "r"(w));
+  }
+}
+
 template <int DT>
 __device__ __forceinline__ float2 fp8x2_to_float2(uint32_t two_codes) {
   uint32_t h = fp8x2_to_half2_bits<DT>(two_codes);
@@ -106,8 +123,25 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t by
                : "memory");
 }
 
+#ifndef PA_WAIT_HINT_NS
+#define PA_WAIT_HINT_NS 0
+#endif
+
+// One test of an mbarrier phase.  The instruction may suspend the thread
+// until the phase completes or a time limit passes; with PA_WAIT_HINT_NS > 0
+// that limit is raised to the given number of nanoseconds, so a waiting warp
+// sleeps instead of re-issuing the test.
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
+#if PA_WAIT_HINT_NS > 0
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "n"(PA_WAIT_HINT_NS)
+      : "memory");
+#else
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
       "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
@@ -115,6 +149,7 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
       : "=r"(ok)
       : "r"(bar), "r"(parity)
       : "memory");
+#endif
   return ok != 0;
 }
 

@@ -1,14 +1,17 @@
 // Paged decode attention for sm_103a.
 //
-// Work decomposition.  A work item is one (KV head h, sequence s, partition
-// p): the tokens [p*P, min((p+1)*P, L_s)) of one sequence, for the G query
-// heads that share KV head h.  A plan kernel lists the (s, p) pairs; a
-// persistent kernel (one CTA per SM) claims items from an atomic counter in
-// the order (h, s, p), so that CTAs running at the same time read the same
-// KV head of neighbouring sequences — the beams of one prompt and the
-// sequences of one shared prefix meet in L2.  Sequences with more than one
-// partition leave (m, l, o) partials that a merge kernel combines exactly
-// (the flash-decoding reduction).
+// Work decomposition.  A work item is one (KV head h, partition p, and a run
+// of k >= 1 consecutive sequences s..s+k-1): the tokens [p*P, min((p+1)*P,
+// L_s)) for the G query heads that share KV head h.  k > 1 when the
+// sequences' block tables name the same physical blocks over the whole
+// partition (a shared prefix, the beams of one prompt: blocks shared through
+// reference counts and copy-on-write), so each shared tile is read once for
+// all k * G queries.  A plan kernel lists the items; a persistent kernel
+// (several CTAs per SM) claims them from an atomic counter in the order
+// (h, s, p), so CTAs running at the same time read the same KV head of
+// neighbouring sequences.  Sequences with more than one partition leave
+// (m, l, o) partials that a merge kernel combines exactly (the
+// flash-decoding reduction).
 //
 // CTA = 1 producer warp + 4 consumer warps.  The producer walks the block
 // table and stages whole (block, head) tiles of K and V — contiguous
@@ -21,12 +24,15 @@
 // are fetched one item ahead so the copy engine never waits on them.
 //
 // Consumers compute, per 16-token slice:
-//   G <= 2  (SIMT):  two lanes per token, warp-shuffle dot products in fp32;
-//                    lanes own head_dim columns for the P*V accumulation.
-//   G >= 4  (MMA):   S^T = K Q^T and O^T = V^T P^T on mma.sync m16n8k16
-//                    (tokens and head_dim as M, the query group as N = 8),
-//                    fp32 accumulation; FP8 codes are widened exactly to
-//                    fp16 in registers.
+//   one query per tile (G == 1, nothing shared)  (SIMT): four lanes per
+//                    token, warp-shuffle dot products in fp32; lanes own
+//                    head_dim columns for the P*V accumulation.
+//   several queries per tile (G >= 2, or sequences sharing the blocks)
+//                    (MMA): S^T = K Q^T and O^T = V^T P^T are small dense
+//                    contractions: mma.sync m16n8k16 with tokens and head_dim
+//                    as M and the queries as N (padded to 8), fp32
+//                    accumulation; FP8 codes are widened exactly to fp16 in
+//                    registers.
 // Softmax is kept in base-2 units (scores pre-multiplied by log2 e) with a
 // lazily updated running maximum: the accumulators are rescaled only when
 // the maximum grows by more than 2^8, which leaves o / l unchanged.
@@ -60,23 +66,50 @@ __device__ __forceinline__ int clamp_len(int L, int cap, int *err) {
   return L;
 }
 
+// Query rows one item can hold: 4 for G == 1 (a beam of four), 8 otherwise
+// (one mma N tile).  Sequences per shared item: kmax = QM / G.
+__host__ __device__ constexpr int query_capacity(int G) { return G == 1 ? 4 : 8; }
+
 // ----------------------------------------------------------------------------
-// plan: list (s, p) pairs in sequence order; reset the claim counter
+// plan: list the work items in sequence order; reset the claim counter
 // ----------------------------------------------------------------------------
+// Partition q of sequence s is "full" when all its P tokens exist.  Sequence
+// s joins the item of s-1 for partition q when both partitions are full, s is
+// not at a multiple of kmax, and their block-table entries over the
+// partition are equal; otherwise it leads an item of its own.
+__device__ __forceinline__ bool same_blocks(const DecodeParams &p, int s, int q, int bpp) {
+  const int32_t *a = p.block_tables + static_cast<size_t>(s) * p.max_blocks + static_cast<size_t>(q) * bpp;
+  const int32_t *b = a - p.max_blocks;
+  for (int j = 0; j < bpp; ++j)
+    if (__ldg(a + j) != __ldg(b + j)) return false;
+  return true;
+}
+
+__device__ __forceinline__ bool joins_previous(const DecodeParams &p, int s, int q, int bpp) {
+  if (s % p.kmax == 0) return false;
+  const int P = p.partition_size;
+  const int Lprev = min(max(__ldg(p.seq_lens + s - 1), 0), p.len_cap);
+  const int L = min(max(__ldg(p.seq_lens + s), 0), p.len_cap);
+  if (L < (q + 1) * P || Lprev < (q + 1) * P) return false;
+  return same_blocks(p, s, q, bpp);
+}
+
 __global__ void __launch_bounds__(1024) plan_kernel(const DecodeParams p) {
   __shared__ int warp_tot[32];
   __shared__ int base;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int bpp = p.partition_size / p.block_size;
   if (tid == 0) base = 0;
   __syncthreads();
   for (int b0 = 0; b0 < p.num_seqs; b0 += 1024) {
     const int s = b0 + tid;
-    int nP = 0;
+    int nP = 0, cnt = 0;
     if (s < p.num_seqs) {
       const int L = clamp_len(__ldg(p.seq_lens + s), p.len_cap, p.err);
       nP = max(1, (L + p.partition_size - 1) / p.partition_size);
+      for (int q = 0; q < nP; ++q) cnt += (p.kmax > 1 && joins_previous(p, s, q, bpp)) ? 0 : 1;
     }
-    int x = nP;
+    int x = cnt;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const int y = __shfl_up_sync(0xffffffffu, x, o);
@@ -94,8 +127,13 @@ __global__ void __launch_bounds__(1024) plan_kernel(const DecodeParams p) {
       warp_tot[lane] = t;  // inclusive over warps
     }
     __syncthreads();
-    const int excl = base + (warp ? warp_tot[warp - 1] : 0) + x - nP;
-    for (int q = 0; q < nP; ++q) p.pairs[excl + q] = make_int2(s, q);
+    int idx = base + (warp ? warp_tot[warp - 1] : 0) + x - cnt;
+    for (int q = 0; q < nP; ++q) {
+      if (p.kmax > 1 && joins_previous(p, s, q, bpp)) continue;
+      int k = 1;
+      while (p.kmax > 1 && s + k < p.num_seqs && joins_previous(p, s + k, q, bpp)) ++k;
+      p.items[idx++] = make_int4(s, q, k, 0);
+    }
     __syncthreads();
     if (tid == 0) base += warp_tot[31];
     __syncthreads();
@@ -120,28 +158,41 @@ __global__ void __launch_bounds__(256) merge_kernel(const DecodeParams p) {
   const int nP = max(1, (L + p.partition_size - 1) / p.partition_size);
   if (nP <= 1) return;
   const size_t base = static_cast<size_t>(s) * p.max_parts * p.num_q_heads + hq;
+  // pass 1: the largest partition maximum (lane q reads partition q, q + 32, ...)
   float M = -INFINITY;
   for (int q = lane; q < nP; q += 32) M = fmaxf(M, p.part_ml[base + static_cast<size_t>(q) * p.num_q_heads].x);
 #pragma unroll
   for (int o = 16; o; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  // pass 2: weights w_q = exp2(m_q - M) * l_q, 32 partitions per round;
+  // every lane then accumulates its head_dim columns of each partition
   constexpr int E = D / 32;
   float acc[E];
 #pragma unroll
   for (int e = 0; e < E; ++e) acc[e] = 0.f;
   float den = 0.f;
-  for (int q = 0; q < nP; ++q) {
-    const size_t idx = base + static_cast<size_t>(q) * p.num_q_heads;
-    const float2 ml = p.part_ml[idx];
-    const float w = (ml.y > 0.f) ? exp2f(ml.x - M) * ml.y : 0.f;
-    den += w;
-    const float *po = p.part_o + idx * D + lane * E;
+  for (int q0 = 0; q0 < nP; q0 += 32) {
+    const int q = q0 + lane;
+    float w = 0.f;
+    if (q < nP) {
+      const float2 ml = p.part_ml[base + static_cast<size_t>(q) * p.num_q_heads];
+      w = (ml.y > 0.f) ? exp2f(ml.x - M) * ml.y : 0.f;
+    }
+    float ws = w;
 #pragma unroll
-    for (int e = 0; e < E; ++e) acc[e] += w * po[e];
+    for (int o = 16; o; o >>= 1) ws += __shfl_xor_sync(0xffffffffu, ws, o);
+    den += ws;
+    const int cnt = min(32, nP - q0);
+    for (int k = 0; k < cnt; ++k) {
+      const float wk = __shfl_sync(0xffffffffu, w, k);
+      const float *po = p.part_o + (base + static_cast<size_t>(q0 + k) * p.num_q_heads) * D + lane * E;
+#pragma unroll
+      for (int e = 0; e < E; ++e) acc[e] = fmaf(wk, po[e], acc[e]);
+    }
   }
   const float inv = den > 0.f ? 1.f / den : 0.f;
   uint16_t *out = static_cast<uint16_t *>(p.out) + (static_cast<size_t>(s) * p.num_q_heads + hq) * D + lane * E;
 #pragma unroll
-  for (int e = 0; e < E; ++e) out[e] = float_to_storage16<QT>(den > 0.f ? acc[e] * inv : 0.f);
+  for (int e = 0; e < E; ++e) out[e] = float_to_storage16<QT>(acc[e] * inv);
 }
 
 // ----------------------------------------------------------------------------
@@ -160,11 +211,11 @@ __device__ __forceinline__ void producer_warp(const DecodeParams &p, uint8_t *sm
   const int P = p.partition_size;
   const int bpp = P / bs;  // <= 128
   const int NS = p.num_stages;
-  const int n_pairs = p.work[1];
-  const int total = n_pairs * p.num_kv_heads;
-  constexpr uint32_t qbytes = G * D * 2;
+  const int n_items = p.work[1];
+  const int total = n_items * p.num_kv_heads;
+  constexpr uint32_t qbytes = G * D * 2;  // query rows of one sequence's group
 
-  auto load_table = [&](int w, int2 pr, int L, int (&ph)[4]) {
+  auto load_table = [&](int w, int4 pr, int L, int (&ph)[4]) {
     const int nblk = (w < total) ? (min(max(L, 0), p.len_cap) + bs - 1) / bs : 0;
     const int32_t *row = p.block_tables + static_cast<size_t>(pr.x) * p.max_blocks;
 #pragma unroll
@@ -179,7 +230,7 @@ __device__ __forceinline__ void producer_warp(const DecodeParams &p, uint8_t *sm
   int w_c = 0;
   if (lane == 0) w_c = atomicAdd(p.work, 1);
   w_c = __shfl_sync(0xffffffffu, w_c, 0);
-  int2 pr_c = (w_c < total) ? p.pairs[w_c % n_pairs] : make_int2(0, 0);
+  int4 pr_c = (w_c < total) ? p.items[w_c % n_items] : make_int4(0, 0, 1, 0);
   int L_c = (w_c < total) ? __ldg(p.seq_lens + pr_c.x) : 0;
   int ph_c[4];
   load_table(w_c, pr_c, L_c, ph_c);
@@ -187,7 +238,7 @@ __device__ __forceinline__ void producer_warp(const DecodeParams &p, uint8_t *sm
   // issues a load whose result the following step consumes, so the warp
   // never waits on a round trip while stages are being refilled.
   int w_raw = 0, w_n = 0, L_n = 0, pf = 0;
-  int2 pr_n = make_int2(0, 0);
+  int4 pr_n = make_int4(0, 0, 1, 0);
   int ph_n[4] = {0, 0, 0, 0};
   auto pf_step = [&]() {
     switch (pf) {
@@ -196,7 +247,7 @@ __device__ __forceinline__ void producer_warp(const DecodeParams &p, uint8_t *sm
         break;
       case 1:
         w_n = __shfl_sync(0xffffffffu, w_raw, 0);
-        pr_n = (w_n < total) ? p.pairs[w_n % n_pairs] : make_int2(0, 0);
+        pr_n = (w_n < total) ? p.items[w_n % n_items] : make_int4(0, 0, 1, 0);
         break;
       case 2:
         L_n = (w_n < total) ? __ldg(p.seq_lens + pr_n.x) : 0;
@@ -208,11 +259,13 @@ __device__ __forceinline__ void producer_warp(const DecodeParams &p, uint8_t *sm
     ++pf;
   };
 
-  int it = 0;
+  int it = 0;            // stages issued so far
+  int stage = 0;         // it % NS
+  uint32_t phase = 0;    // (it / NS) & 1
   bool ok = true;
   while (w_c < total) {
-    const int h = w_c / n_pairs;
-    const int s = pr_c.x, pi = pr_c.y;
+    const int h = w_c / n_items;
+    const int s = pr_c.x, pi = pr_c.y, kseq = pr_c.z;
     const int L = clamp_len(L_c, p.len_cap, lane == 0 ? p.err : nullptr);
     const int t_begin = pi * P;
     const int t_end = min(L, t_begin + P);
@@ -227,9 +280,7 @@ __device__ __forceinline__ void producer_warp(const DecodeParams &p, uint8_t *sm
       const int c = ib0 >> 5;
       const int reg = c == 0 ? ph_c[0] : c == 1 ? ph_c[1] : c == 2 ? ph_c[2] : ph_c[3];
       const int phys = __shfl_sync(0xffffffffu, reg, (ib0 & 31) + (lane < nb ? lane : 0));
-      const int stage = it % NS;
-      const uint32_t par = ((it / NS) & 1) ^ 1;
-      if (!mbar_wait(&hdr.empty[stage], par, abort)) {
+      if (!mbar_wait(&hdr.empty[stage], phase ^ 1u, abort)) {
         ok = false;
         break;
       }
@@ -243,8 +294,9 @@ __device__ __forceinline__ void producer_warp(const DecodeParams &p, uint8_t *sm
         inf.ntok = ntok;
         inf.L = L;
         inf.nP = nP;
+        inf.k = kseq;
         inf.flags = (st == 0 ? kFirst : 0) | (st == nstages - 1 ? kLast : 0);
-        mbar_arrive_expect_tx(&hdr.full[stage], nb * 2 * tile + (st == 0 ? qbytes : 0u));
+        mbar_arrive_expect_tx(&hdr.full[stage], nb * 2 * tile + (st == 0 ? kseq * qbytes : 0u));
       }
       __syncwarp();
       if (lane < nb) {
@@ -257,11 +309,17 @@ __device__ __forceinline__ void producer_warp(const DecodeParams &p, uint8_t *sm
         bulk_g2s(sb + p.k_off + lane * tile, p.k_cache + off, tile, &hdr.full[stage]);
         bulk_g2s(sb + p.v_off + lane * tile, p.v_cache + off, tile, &hdr.full[stage]);
       }
-      if (st == 0 && lane == 31) {
-        const uint8_t *qsrc = p.q + (static_cast<size_t>(s) * p.num_q_heads + static_cast<size_t>(h) * G) * D * 2;
-        bulk_g2s(sb + p.q_off, qsrc, qbytes, &hdr.full[stage]);
+      if (st == 0 && lane >= 24 && lane - 24 < kseq) {  // one q copy per sequence of the item
+        const int i = lane - 24;
+        const uint8_t *qsrc =
+            p.q + (static_cast<size_t>(s + i) * p.num_q_heads + static_cast<size_t>(h) * G) * D * 2;
+        bulk_g2s(sb + p.q_off + i * qbytes, qsrc, qbytes, &hdr.full[stage]);
       }
       ++it;
+      if (++stage == NS) {
+        stage = 0;
+        phase ^= 1u;
+      }
       if (pf < 4) pf_step();
     }
     if (!ok) break;
@@ -274,9 +332,7 @@ __device__ __forceinline__ void producer_warp(const DecodeParams &p, uint8_t *sm
     pf = 0;
   }
   if (ok) {
-    const int stage = it % NS;
-    const uint32_t par = ((it / NS) & 1) ^ 1;
-    if (mbar_wait(&hdr.empty[stage], par, abort)) {
+    if (mbar_wait(&hdr.empty[stage], phase ^ 1u, abort)) {
       if (lane == 0) {
         hdr.info[stage].flags = kEnd;
         mbar_arrive(&hdr.full[stage]);
@@ -299,31 +355,37 @@ __device__ __forceinline__ void producer_warp(const DecodeParams &p, uint8_t *sm
 }
 
 // ----------------------------------------------------------------------------
-// consumer state: SIMT (G <= 2)
+// consumer state: SIMT (one query per KV head, nothing shared)
 // ----------------------------------------------------------------------------
-template <int KV, int QT, int D, int G>
+template <int KV, int QT, int D, int G, int QM>
 struct SimtState {
+  // Lane = 4 * t8 + qd: four lanes per token, eight tokens per pass, two
+  // passes per 16-token slice.  Lane qd of a token owns the 16-byte chunks
+  // c == qd (mod 4) of the token's K row, visited in an order rotated by t8
+  // so that the eight lanes of a shared-memory phase hit eight different
+  // bank groups.  For P*V, lane l owns head_dim columns [l*EPL, l*EPL+EPL).
   static constexpr int ELT = elt_bytes(KV);
   static constexpr int ROWB = D * ELT;
   static constexpr int NCH = ROWB / 16;  // 16-byte chunks per token row
-  static constexpr int NCHL = NCH / 2;   // chunks per lane (two lanes per token)
+  static constexpr int NCHL = NCH / 4;   // chunks per lane
   static constexpr int EPC = 16 / ELT;   // elements per chunk
   static constexpr int EPL = D / 32;     // P*V columns per lane
-  static constexpr int QS = G;           // query rows kept in the combine scratch
+  static constexpr int QS = QM;          // query rows per warp in the combine scratch
 
   float qf[G][NCHL][EPC];
   float o[G][EPL];
   float m[G], l[G];
 
-  __device__ __forceinline__ void start(const uint8_t *qs, float qk_scale) {
+  __device__ __forceinline__ static int chunk(int i, int qd, int t8) { return (4 * i + qd + 4 * t8) % NCH; }
+
+  __device__ __forceinline__ void start(const uint8_t *qs, float qk_scale, int /*ncols*/) {
     const int lane = threadIdx.x & 31;
-    const int t = lane >> 1, hh = lane & 1;
+    const int t8 = lane >> 2, qd = lane & 3;
 #pragma unroll
     for (int g = 0; g < G; ++g) {
 #pragma unroll
       for (int i = 0; i < NCHL; ++i) {
-        const int c = (2 * i + hh + 2 * t) % NCH;
-        const uint8_t *src = qs + (static_cast<size_t>(g) * D + c * EPC) * 2;
+        const uint8_t *src = qs + (static_cast<size_t>(g) * D + chunk(i, qd, t8) * EPC) * 2;
 #pragma unroll
         for (int e = 0; e < EPC; e += 2) {
           const float2 f = half2_bits_to_float2<QT>(*reinterpret_cast<const uint32_t *>(src + e * 2));
@@ -380,29 +442,40 @@ struct SimtState {
   // one 16-token slice: rows Ks[0..15], Vs[0..15]; n valid tokens (1..16)
   __device__ __forceinline__ void slice(const uint8_t *Ks, const uint8_t *Vs, int n, float v_scale) {
     const int lane = threadIdx.x & 31;
-    const int t = lane >> 1, hh = lane & 1;
-    float acc[G];
+    const int t8 = lane >> 2, qd = lane & 3;
+    float acc[2][G][2];
 #pragma unroll
-    for (int g = 0; g < G; ++g) acc[g] = 0.f;
-    const uint8_t *krow = Ks + t * ROWB;
+    for (int ps = 0; ps < 2; ++ps)
 #pragma unroll
-    for (int i = 0; i < NCHL; ++i) {
-      const int c = (2 * i + hh + 2 * t) % NCH;
-      float kf[EPC];
-      chunk_to_float(lds128(krow + c * 16), kf);
+      for (int g = 0; g < G; ++g) acc[ps][g][0] = acc[ps][g][1] = 0.f;
 #pragma unroll
-      for (int g = 0; g < G; ++g)
+    for (int ps = 0; ps < 2; ++ps) {
+      const uint8_t *krow = Ks + (8 * ps + t8) * ROWB;
 #pragma unroll
-        for (int e = 0; e < EPC; ++e) acc[g] = fmaf(qf[g][i][e], kf[e], acc[g]);
+      for (int i = 0; i < NCHL; ++i) {
+        float kf[EPC];
+        chunk_to_float(lds128(krow + chunk(i, qd, t8) * 16), kf);
+#pragma unroll
+        for (int g = 0; g < G; ++g)
+#pragma unroll
+          for (int e = 0; e < EPC; ++e)
+            acc[ps][g][e & 1] = fmaf(qf[g][i][e], kf[e], acc[ps][g][e & 1]);
+      }
     }
-    float pr[G];
+    float pr[2][G];
 #pragma unroll
     for (int g = 0; g < G; ++g) {
-      float sc = acc[g] + __shfl_xor_sync(0xffffffffu, acc[g], 1);
-      sc = (t < n) ? sc : -INFINITY;
-      float mx = sc;
+      float sc[2];
 #pragma unroll
-      for (int o2 = 2; o2 < 32; o2 <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o2));
+      for (int ps = 0; ps < 2; ++ps) {
+        float x = acc[ps][g][0] + acc[ps][g][1];
+        x += __shfl_xor_sync(0xffffffffu, x, 1);
+        x += __shfl_xor_sync(0xffffffffu, x, 2);
+        sc[ps] = (8 * ps + t8 < n) ? x : -INFINITY;
+      }
+      float mx = fmaxf(sc[0], sc[1]);
+#pragma unroll
+      for (int o2 = 4; o2 < 32; o2 <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o2));
       if (mx > m[g] + kLazyRescale) {  // warp-uniform
         const float alpha = exp2f(m[g] - mx);
 #pragma unroll
@@ -410,10 +483,11 @@ struct SimtState {
         l[g] *= alpha;
         m[g] = mx;
       }
-      pr[g] = exp2f(sc - m[g]);
-      if (hh == 0) l[g] += pr[g];
+      pr[0][g] = exp2f(sc[0] - m[g]);
+      pr[1][g] = exp2f(sc[1] - m[g]);
+      if (qd == 0) l[g] += pr[0][g] + pr[1][g];
     }
-    // P * V: lane owns EPL columns; tokens broadcast from their lane pair
+    // P * V: lane owns EPL columns; token tt's weight lives in lane 4*(tt%8)
 #pragma unroll
     for (int tt = 0; tt < 16; ++tt) {
       if (tt < n) {
@@ -421,7 +495,7 @@ struct SimtState {
         load_v(Vs + tt * ROWB, vf);
 #pragma unroll
         for (int g = 0; g < G; ++g) {
-          const float pt = __shfl_sync(0xffffffffu, pr[g], 2 * tt) * v_scale;
+          const float pt = __shfl_sync(0xffffffffu, pr[tt >> 3][g], 4 * (tt & 7)) * v_scale;
 #pragma unroll
           for (int e = 0; e < EPL; ++e) o[g][e] = fmaf(pt, vf[e], o[g][e]);
         }
@@ -429,7 +503,8 @@ struct SimtState {
     }
   }
 
-  __device__ __forceinline__ void to_scratch(float *so, float *sm, float *sl, int cw) {
+  __device__ __forceinline__ void to_scratch(float *so, float *sm, float *sl, int cw, float /*v_scale*/,
+                                             int /*ncols*/) {
     const int lane = threadIdx.x & 31;
 #pragma unroll
     for (int g = 0; g < G; ++g) {
@@ -448,7 +523,7 @@ struct SimtState {
 };
 
 // ----------------------------------------------------------------------------
-// consumer state: tensor-core mma.sync (G in {4, 8}; query group padded to 8)
+// consumer state: tensor-core mma.sync (several queries share the K/V tile)
 // ----------------------------------------------------------------------------
 template <int MT>
 __device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
@@ -483,7 +558,7 @@ __device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1
 //   Head_dim order of the M dimension: lane gq owns columns
 //   [gq*DPL, gq*DPL + DPL); m-tile mi row gq -> gq*DPL + mi, row gq+8 ->
 //   gq*DPL + MTILES + mi.
-template <int KV, int QT, int D, int G>
+template <int KV, int QT, int D, int G, int QM>
 struct MmaState {
   static constexpr bool KV8 = is_fp8(KV);
   static constexpr int MT = KV8 ? kF16 : KV;  // mma input type
@@ -494,7 +569,7 @@ struct MmaState {
   static constexpr int CE = 16 / ELT;       // elements per 16-byte chunk
   static constexpr int LCH = (D / 4) / CE;  // chunks of a K row per lane
   static constexpr int DPL = D / 8;         // output columns per lane group
-  static constexpr int QS = G;
+  static constexpr int QS = QM;  // query rows per warp in the combine scratch
 
   uint32_t qb[KSTEPS][2];
   float oacc[MTILES][4];
@@ -503,10 +578,12 @@ struct MmaState {
 
   __device__ __forceinline__ static int kcol(int tq, int e) { return (tq + 4 * (e / CE)) * CE + e % CE; }
 
-  __device__ __forceinline__ void start(const uint8_t *qs, float qk_scale) {
+  // q rows [ncols][D] in shared memory: the query heads of the group, for
+  // each sequence that shares the item's blocks; columns >= ncols are zero
+  __device__ __forceinline__ void start(const uint8_t *qs, float qk_scale, int ncols) {
     const int lane = threadIdx.x & 31;
     const int gq = lane >> 2, tq = lane & 3;
-    const bool real = gq < G;
+    const bool real = gq < ncols;
     const uint16_t *qrow = reinterpret_cast<const uint16_t *>(qs) + static_cast<size_t>(real ? gq : 0) * D;
     float f = 1.f;
     if constexpr (KV8 && QT == kBF16) {
@@ -582,6 +659,14 @@ struct MmaState {
     }
   }
 
+  // FP8 V^T: (row ra, row rb) pairs of output columns col and col+1 (col even)
+  __device__ __forceinline__ static void v_pair2(const uint32_t *ra, const uint32_t *rb, int col,
+                                                 uint32_t &lo, uint32_t &hi) {
+    const uint32_t b = col & 3;
+    const uint32_t two = prmt(ra[col / 4], rb[col / 4], b | ((4 + b) << 4) | ((b + 1) << 8) | ((5 + b) << 12));
+    fp8x4_to_half2x2<KV>(two, lo, hi);
+  }
+
   __device__ __forceinline__ void slice(const uint8_t *Ks, const uint8_t *Vs, int n, float v_scale) {
     const int lane = threadIdx.x & 31;
     const int gq = lane >> 2, tq = lane & 3;
@@ -592,19 +677,31 @@ struct MmaState {
       k0[j] = lds128(Ks + gq * ROWB + (tq + 4 * j) * 16);
       k1[j] = lds128(Ks + (gq + 8) * ROWB + (tq + 4 * j) * 16);
     }
-    float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+    // four independent accumulators so the k-steps do not form one chain
+    float sacc[4][4];
+#pragma unroll
+    for (int a = 0; a < 4; ++a)
+#pragma unroll
+      for (int k = 0; k < 4; ++k) sacc[a][k] = 0.f;
 #pragma unroll
     for (int kk = 0; kk < KSTEPS; ++kk) {
-      const uint32_t a0 = k_reg(k0, kk, 0), a1 = k_reg(k1, kk, 0);
-      const uint32_t a2 = k_reg(k0, kk, 1), a3 = k_reg(k1, kk, 1);
-      if (kk & 1)
-        mma16816<MT>(sb, a0, a1, a2, a3, qb[kk][0], qb[kk][1]);
-      else
-        mma16816<MT>(sa, a0, a1, a2, a3, qb[kk][0], qb[kk][1]);
+      uint32_t a0, a1, a2, a3;
+      if constexpr (ELT == 2) {
+        a0 = k_reg(k0, kk, 0);
+        a1 = k_reg(k1, kk, 0);
+        a2 = k_reg(k0, kk, 1);
+        a3 = k_reg(k1, kk, 1);
+      } else {  // local elements 4kk..4kk+3 are one word of the row's chunk
+        const int e = 4 * kk;
+        fp8x4_to_half2x2<KV>(w32(k0[e / CE], (e % CE) / 4), a0, a2);
+        fp8x4_to_half2x2<KV>(w32(k1[e / CE], (e % CE) / 4), a1, a3);
+      }
+      mma16816<MT>(sacc[kk & 3], a0, a1, a2, a3, qb[kk][0], qb[kk][1]);
     }
     float sc[4];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) sc[k] = (sa[k] + sb[k]) * qk_mult;
+    for (int k = 0; k < 4; ++k)
+      sc[k] = ((sacc[0][k] + sacc[1][k]) + (sacc[2][k] + sacc[3][k])) * qk_mult;
     // rows gq (regs 0,1) and gq+8 (regs 2,3); columns 2tq, 2tq+1
     if (gq >= n) sc[0] = sc[1] = -INFINITY;
     if (gq + 8 >= n) sc[2] = sc[3] = -INFINITY;
@@ -667,18 +764,33 @@ struct MmaState {
         if (t3 >= n) r3[w] = 0u;
       }
     }
+    if constexpr (ELT == 2) {
 #pragma unroll
-    for (int mi = 0; mi < MTILES; ++mi) {
-      const uint32_t a0 = v_pair(r0, r1, mi);
-      const uint32_t a1 = v_pair(r0, r1, MTILES + mi);
-      const uint32_t a2 = v_pair(r2, r3, mi);
-      const uint32_t a3 = v_pair(r2, r3, MTILES + mi);
-      mma16816<MT>(oacc[mi], a0, a1, a2, a3, b0, b1);
+      for (int mi = 0; mi < MTILES; ++mi) {
+        const uint32_t a0 = v_pair(r0, r1, mi);
+        const uint32_t a1 = v_pair(r0, r1, MTILES + mi);
+        const uint32_t a2 = v_pair(r2, r3, mi);
+        const uint32_t a3 = v_pair(r2, r3, MTILES + mi);
+        mma16816<MT>(oacc[mi], a0, a1, a2, a3, b0, b1);
+      }
+    } else {
+      // bytes (c, c+1) of rows (ra, rb) -> pairs for m-tiles c and c+1
+#pragma unroll
+      for (int mi = 0; mi < MTILES; mi += 2) {
+        uint32_t x0[2], x1[2], x2[2], x3[2];
+        v_pair2(r0, r1, mi, x0[0], x0[1]);
+        v_pair2(r0, r1, MTILES + mi, x1[0], x1[1]);
+        v_pair2(r2, r3, mi, x2[0], x2[1]);
+        v_pair2(r2, r3, MTILES + mi, x3[0], x3[1]);
+        mma16816<MT>(oacc[mi], x0[0], x1[0], x2[0], x3[0], b0, b1);
+        mma16816<MT>(oacc[mi + 1], x0[1], x1[1], x2[1], x3[1], b0, b1);
+      }
     }
     (void)v_scale;
   }
 
-  __device__ __forceinline__ void to_scratch(float *so, float *sm, float *sl, int cw, float v_scale) {
+  __device__ __forceinline__ void to_scratch(float *so, float *sm, float *sl, int cw, float v_scale,
+                                             int ncols) {
     const int lane = threadIdx.x & 31;
     const int gq = lane >> 2, tq = lane & 3;
     float ls0 = l2[0], ls1 = l2[1];
@@ -691,21 +803,21 @@ struct MmaState {
 #pragma unroll
     for (int mi = 0; mi < MTILES; ++mi) {
       const int d0 = gq * DPL + mi, d1 = gq * DPL + MTILES + mi;
-      if (qa < G) {
+      if (qa < ncols) {
         so[(static_cast<size_t>(cw) * QS + qa) * D + d0] = oacc[mi][0] * v_scale;
         so[(static_cast<size_t>(cw) * QS + qa) * D + d1] = oacc[mi][2] * v_scale;
       }
-      if (qb2 < G) {
+      if (qb2 < ncols) {
         so[(static_cast<size_t>(cw) * QS + qb2) * D + d0] = oacc[mi][1] * v_scale;
         so[(static_cast<size_t>(cw) * QS + qb2) * D + d1] = oacc[mi][3] * v_scale;
       }
     }
     if (gq == 0) {
-      if (qa < G) {
+      if (qa < ncols) {
         sm[cw * QS + qa] = m2[0];
         sl[cw * QS + qa] = ls0;
       }
-      if (qb2 < G) {
+      if (qb2 < ncols) {
         sm[cw * QS + qb2] = m2[1];
         sl[cw * QS + qb2] = ls1;
       }
@@ -716,42 +828,119 @@ struct MmaState {
 // ----------------------------------------------------------------------------
 // combine the four consumer warps' states and write the item's result
 // ----------------------------------------------------------------------------
-template <int QT, int D, int G>
-__device__ __forceinline__ void combine_item(const DecodeParams &p, const StageInfo &inf, const float *so,
-                                             const float *sm, const float *sl) {
+// Query column j of an item is head h*G + j%G of sequence s + j/G.
+template <int QT, int D, int G, int QM>
+__device__ __forceinline__ void combine_item(const DecodeParams &p, const StageInfo &inf, int ncols,
+                                             const float *so, float *sm, const float *sl, uint64_t *bar,
+                                             int ncomb, const volatile int *abort, bool &ok) {
   const int ct = threadIdx.x - 32;
-  for (int e = ct; e < G * D; e += kConsumerThreads) {
-    const int g = e / D, dd = e % D;
+  const int P = p.partition_size;
+  // 1) per column j: weights w_c = exp2(m_c - M) / sum_c exp2(m_c - M) l_c,
+  //    written over the maxima in place
+  if (ct < ncols) {
+    const int j = ct;
     float M = -INFINITY;
 #pragma unroll
-    for (int c = 0; c < kConsumerWarps; ++c) M = fmaxf(M, sm[c * G + g]);
-    float wsum = 0.f, acc = 0.f;
+    for (int c = 0; c < kConsumerWarps; ++c) M = fmaxf(M, sm[c * QM + j]);
+    float w[kConsumerWarps], wsum = 0.f;
 #pragma unroll
     for (int c = 0; c < kConsumerWarps; ++c) {
-      const float mc = sm[c * G + g];
-      const float w = (mc == -INFINITY) ? 0.f : exp2f(mc - M);
-      wsum = fmaf(w, sl[c * G + g], wsum);
-      acc = fmaf(w, so[(static_cast<size_t>(c) * G + g) * D + dd], acc);
+      const float mc = sm[c * QM + j];
+      w[c] = (mc == -INFINITY) ? 0.f : exp2f(mc - M);
+      wsum = fmaf(w[c], sl[c * QM + j], wsum);
     }
-    const float val = wsum > 0.f ? acc / wsum : 0.f;
-    const int hq = inf.h * G + g;
-    if (inf.nP == 1) {
-      uint16_t *out = static_cast<uint16_t *>(p.out);
-      out[(static_cast<size_t>(inf.s) * p.num_q_heads + hq) * D + dd] = float_to_storage16<QT>(val);
+    const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+#pragma unroll
+    for (int c = 0; c < kConsumerWarps; ++c) sm[c * QM + j] = w[c] * inv;
+    const int sj = inf.s + j / G;
+    const int Lj = min(max(__ldg(p.seq_lens + sj), 0), p.len_cap);
+    if ((Lj + P - 1) / P > 1) {
+      const size_t idx = (static_cast<size_t>(sj) * p.max_parts + inf.p) * p.num_q_heads + inf.h * G + j % G;
+      p.part_ml[idx] = make_float2(M, wsum);
+    }
+  }
+  mbar_arrive(bar);
+  if (!mbar_wait(bar, (3 * ncomb + 1) & 1, abort)) {
+    ok = false;
+    return;
+  }
+  // 2) out[j, d] = sum_c w_c * o_c[j, d], two adjacent columns per thread
+  for (int e = 2 * ct; e < ncols * D; e += 2 * kConsumerThreads) {
+    const int j = e / D, dd = e % D;
+    float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+    for (int c = 0; c < kConsumerWarps; ++c) {
+      const float wc = sm[c * QM + j];
+      const float2 oc = *reinterpret_cast<const float2 *>(so + (static_cast<size_t>(c) * QM + j) * D + dd);
+      a0 = fmaf(wc, oc.x, a0);
+      a1 = fmaf(wc, oc.y, a1);
+    }
+    const int sj = inf.s + j / G;
+    const int hq = inf.h * G + j % G;
+    const int Lj = (G == 1 && inf.k == 1) ? inf.L : min(max(__ldg(p.seq_lens + sj), 0), p.len_cap);
+    if ((Lj + P - 1) / P <= 1) {
+      uint32_t *out = reinterpret_cast<uint32_t *>(static_cast<uint16_t *>(p.out) +
+                                                   (static_cast<size_t>(sj) * p.num_q_heads + hq) * D + dd);
+      *out = pack2_rn<QT>(a0, a1);
     } else {
-      const size_t idx = (static_cast<size_t>(inf.s) * p.max_parts + inf.p) * p.num_q_heads + hq;
-      p.part_o[idx * D + dd] = val;
-      if (dd == 0) p.part_ml[idx] = make_float2(M, wsum);
+      const size_t idx = (static_cast<size_t>(sj) * p.max_parts + inf.p) * p.num_q_heads + hq;
+      *reinterpret_cast<float2 *>(p.part_o + idx * D + dd) = make_float2(a0, a1);
     }
   }
 }
 
 // ----------------------------------------------------------------------------
+// one work item, from its first (already waited) stage to its combine
+// ----------------------------------------------------------------------------
+template <int KV, int QT, int D, int G, int QM, class State>
+__device__ __forceinline__ bool run_item(const DecodeParams &p, SmemHeader &hdr, uint8_t *stages, float *so,
+                                         float *sm, float *sl, int cw, int &stage, uint32_t &phase,
+                                         int &ncomb, StageInfo inf, const volatile int *abort) {
+  constexpr int ROWB = D * elt_bytes(KV);
+  const int lane = threadIdx.x & 31;
+  const int ncols = inf.k * G;
+  State st;
+  st.start(stages + static_cast<size_t>(stage) * p.stage_bytes + p.q_off, p.qk_scale_log2, ncols);
+  while (true) {
+    const uint8_t *sb = stages + static_cast<size_t>(stage) * p.stage_bytes;
+    const int n = min(16, inf.ntok - 16 * cw);
+    if (n > 0) st.slice(sb + p.k_off + 16 * cw * ROWB, sb + p.v_off + 16 * cw * ROWB, n, p.v_scale);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&hdr.empty[stage]);
+    const bool last = (inf.flags & kLast) != 0;
+    if (++stage == p.num_stages) {
+      stage = 0;
+      phase ^= 1u;
+    }
+    if (last) break;
+    if (!mbar_wait(&hdr.full[stage], phase, abort)) return false;
+    const StageInfo nxt = hdr.info[stage];
+    inf.ntok = nxt.ntok;
+    inf.flags = nxt.flags;
+  }
+  // three consumer-wide barriers: states written, weights computed, scratch
+  // read (so that the next item may overwrite it)
+  st.to_scratch(so, sm, sl, cw, p.v_scale, ncols);
+  mbar_arrive(&hdr.combine);
+  if (!mbar_wait(&hdr.combine, (3 * ncomb) & 1, abort)) return false;
+  bool ok = true;
+  combine_item<QT, D, G, QM>(p, inf, ncols, so, sm, sl, &hdr.combine, ncomb, abort, ok);
+  if (!ok) return false;
+  mbar_arrive(&hdr.combine);
+  if (!mbar_wait(&hdr.combine, (3 * ncomb + 2) & 1, abort)) return false;
+  ++ncomb;
+  return true;
+}
+
+// ----------------------------------------------------------------------------
 // the persistent decode kernel
 // ----------------------------------------------------------------------------
+// MMA: every item runs on the tensor-core path; otherwise items whose tile
+// serves a single query run on the SIMT path and shared items on the MMA one.
 template <int KV, int QT, int D, int G, bool MMA>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_kernel(const DecodeParams p) {
-  extern __shared__ __align__(1024) uint8_t smem[];
+  constexpr int QM = query_capacity(G);
+  extern __shared__ __align__(128) uint8_t smem[];
   SmemHeader &hdr = *reinterpret_cast<SmemHeader *>(smem);
   const int warp = threadIdx.x >> 5;
   if (threadIdx.x == 0) {
@@ -773,48 +962,33 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_kernel(const Deco
   const volatile int *abort = &hdr.abort;
   uint8_t *stages = smem + p.stages_off;
   float *so = reinterpret_cast<float *>(smem + p.scratch_off);
-  float *sm = so + kConsumerWarps * G * D;
-  float *sl = sm + kConsumerWarps * G;
-  constexpr int ROWB = D * elt_bytes(KV);
-  using State = typename std::conditional<MMA, MmaState<KV, QT, D, G>, SimtState<KV, QT, D, G>>::type;
-  State st;
-  int it = 0, ncomb = 0;
+  float *sm = so + kConsumerWarps * QM * D;
+  float *sl = sm + kConsumerWarps * QM;
+  using Mma = MmaState<KV, QT, D, G, QM>;
+  int stage = 0, ncomb = 0;
+  uint32_t phase = 0;
   bool failed = false;
   while (true) {
-    const int stage = it % p.num_stages;
-    const uint32_t par = (it / p.num_stages) & 1;
-    if (!mbar_wait(&hdr.full[stage], par, abort)) {
+    if (!mbar_wait(&hdr.full[stage], phase, abort)) {
       failed = true;
       break;
     }
     const StageInfo inf = hdr.info[stage];
     if (inf.flags & kEnd) break;
-    const uint8_t *sb = stages + static_cast<size_t>(stage) * p.stage_bytes;
-    if (inf.flags & kFirst) st.start(sb + p.q_off, p.qk_scale_log2);
-    const int n = min(16, inf.ntok - 16 * cw);
-    if (n > 0) st.slice(sb + p.k_off + 16 * cw * ROWB, sb + p.v_off + 16 * cw * ROWB, n, p.v_scale);
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&hdr.empty[stage]);
-    if (inf.flags & kLast) {
-      if constexpr (MMA) {
-        st.to_scratch(so, sm, sl, cw, p.v_scale);
-      } else {
-        st.to_scratch(so, sm, sl, cw);
-      }
-      mbar_arrive(&hdr.combine);
-      if (!mbar_wait(&hdr.combine, (2 * ncomb) & 1, abort)) {
-        failed = true;
-        break;
-      }
-      combine_item<QT, D, G>(p, inf, so, sm, sl);
-      mbar_arrive(&hdr.combine);
-      if (!mbar_wait(&hdr.combine, (2 * ncomb + 1) & 1, abort)) {
-        failed = true;
-        break;
-      }
-      ++ncomb;
+    bool ok;
+    if constexpr (MMA) {
+      ok = run_item<KV, QT, D, G, QM, Mma>(p, hdr, stages, so, sm, sl, cw, stage, phase, ncomb, inf, abort);
+    } else {
+      using Simt = SimtState<KV, QT, D, G, QM>;
+      if (inf.k > 1)
+        ok = run_item<KV, QT, D, G, QM, Mma>(p, hdr, stages, so, sm, sl, cw, stage, phase, ncomb, inf, abort);
+      else
+        ok = run_item<KV, QT, D, G, QM, Simt>(p, hdr, stages, so, sm, sl, cw, stage, phase, ncomb, inf, abort);
     }
-    ++it;
+    if (!ok) {
+      failed = true;
+      break;
+    }
   }
   if (failed && lane == 0) {
     record_error(p.err, kErrTimeout);
@@ -830,14 +1004,15 @@ struct DecodeSmemPlan {
 template <int KV, int D, int G>
 inline DecodeSmemPlan plan_smem(int max_smem) {
   constexpr int ROWB = D * elt_bytes(KV);
+  constexpr int QM = query_capacity(G);
   DecodeSmemPlan s{};
   s.k_off = 0;
   s.v_off = kStageTok * ROWB;
   s.q_off = 2 * kStageTok * ROWB;
-  s.stage_bytes = (s.q_off + G * D * 2 + 127) / 128 * 128;
+  s.stage_bytes = (s.q_off + QM * D * 2 + 127) / 128 * 128;
   s.scratch_off = (static_cast<int>(sizeof(SmemHeader)) + 127) / 128 * 128;
-  const int scratch = kConsumerWarps * (G * D + 2 * G) * 4;
-  s.stages_off = (s.scratch_off + scratch + 1023) / 1024 * 1024;
+  const int scratch = kConsumerWarps * (QM * D + 2 * QM) * 4;
+  s.stages_off = (s.scratch_off + scratch + 127) / 128 * 128;
   int ns = (max_smem - s.stages_off) / s.stage_bytes;
   if (ns > kMaxStages) ns = kMaxStages;
   s.num_stages = ns;
@@ -850,12 +1025,17 @@ inline DecodeSmemPlan plan_smem(int max_smem) {
 // ----------------------------------------------------------------------------
 template <int KV, int QT, int D, int G, bool MMA>
 pa_status launch_decode(DecodeParams p, const DeviceInfo &dev, cudaStream_t stream) {
-  // shared memory a CTA may use when kCtasPerSm of them share an SM (the
-  // hardware reserves 1 KB per resident CTA)
-  int budget = dev.max_smem_optin;
-  if (kCtasPerSm > 1) budget = min(budget, dev.smem_per_sm / kCtasPerSm - 1024);
-  const DecodeSmemPlan sp = plan_smem<KV, D, G>(budget);
-  if (sp.num_stages < 2) return PA_ERR_UNSUPPORTED;
+  // As many resident CTAs per SM (up to kCtasPerSm) as leave each of them at
+  // least two pipeline stages; the hardware reserves 1 KB per resident CTA.
+  DecodeSmemPlan sp{};
+  int ctas = kCtasPerSm;
+  for (; ctas >= 1; --ctas) {
+    int budget = dev.max_smem_optin;
+    if (ctas > 1) budget = min(budget, dev.smem_per_sm / ctas - 1024);
+    sp = plan_smem<KV, D, G>(budget);
+    if (sp.num_stages >= 2) break;
+  }
+  if (ctas < 1 || sp.num_stages < 2) return PA_ERR_UNSUPPORTED;
   p.num_stages = sp.num_stages;
   p.stage_bytes = sp.stage_bytes;
   p.k_off = sp.k_off;
@@ -863,6 +1043,7 @@ pa_status launch_decode(DecodeParams p, const DeviceInfo &dev, cudaStream_t stre
   p.q_off = sp.q_off;
   p.scratch_off = sp.scratch_off;
   p.stages_off = sp.stages_off;
+  p.kmax = query_capacity(G) / G;
   auto kern = decode_kernel<KV, QT, D, G, MMA>;
   static int configured_bytes[64];  // per device: dynamic smem already allowed
   int dev_id = 0;
@@ -875,7 +1056,7 @@ pa_status launch_decode(DecodeParams p, const DeviceInfo &dev, cudaStream_t stre
   }
   plan_kernel<<<1, 1024, 0, stream>>>(p);
   const long long items = static_cast<long long>(p.num_seqs) * p.max_parts * p.num_kv_heads;
-  const long long slots = static_cast<long long>(dev.sm_count) * kCtasPerSm;
+  const long long slots = static_cast<long long>(dev.sm_count) * ctas;
   const int grid = static_cast<int>(items < slots ? items : slots);
   kern<<<grid, kThreads, sp.total, stream>>>(p);
   if (p.max_parts > 1) {
@@ -887,11 +1068,15 @@ pa_status launch_decode(DecodeParams p, const DeviceInfo &dev, cudaStream_t stre
   return e == cudaSuccess ? PA_OK : cuda_fail(e);
 }
 
+#ifndef PA_MMA_MIN_GROUP
+#define PA_MMA_MIN_GROUP 2
+#endif
+
 template <int KV, int QT, int D>
 pa_status launch_by_group(int group, const DecodeParams &p, const DeviceInfo &dev, cudaStream_t s) {
   switch (group) {
-    case 1: return launch_decode<KV, QT, D, 1, false>(p, dev, s);
-    case 2: return launch_decode<KV, QT, D, 2, false>(p, dev, s);
+    case 1: return launch_decode<KV, QT, D, 1, (PA_MMA_MIN_GROUP <= 1)>(p, dev, s);
+    case 2: return launch_decode<KV, QT, D, 2, (PA_MMA_MIN_GROUP <= 2)>(p, dev, s);
     case 4: return launch_decode<KV, QT, D, 4, true>(p, dev, s);
     case 8: return launch_decode<KV, QT, D, 8, true>(p, dev, s);
   }

@@ -35,7 +35,7 @@ bool layout_for(int num_seqs, int num_q_heads, int kv_heads, int head_dim, int m
   w.max_parts = max_seq_len > 0 ? (max_seq_len + w.partition - 1) / w.partition : 1;
   const size_t units = static_cast<size_t>(num_seqs) * w.max_parts;
   w.pairs_off = 256;
-  w.ml_off = align256(w.pairs_off + units * sizeof(int2));
+  w.ml_off = align256(w.pairs_off + units * sizeof(int4));
   w.o_off = align256(w.ml_off + units * num_q_heads * sizeof(float2));
   w.total = align256(w.o_off + units * num_q_heads * head_dim * sizeof(float));
   *out = w;
@@ -116,7 +116,7 @@ extern "C" pa_status pa_decode(void *out, const void *q, int32_t q_dtype, int32_
   p.qk_scale_log2 = scale * (fp8 ? cache->k_scale : 1.0f) * 1.4426950408889634f;
   p.v_scale = fp8 ? cache->v_scale : 1.0f;
   p.work = reinterpret_cast<int *>(ws);
-  p.pairs = reinterpret_cast<int2 *>(ws + w.pairs_off);
+  p.items = reinterpret_cast<int4 *>(ws + w.pairs_off);
   p.part_ml = reinterpret_cast<float2 *>(ws + w.ml_off);
   p.part_o = reinterpret_cast<float *>(ws + w.o_off);
   p.err = device_error;

@@ -13,10 +13,10 @@ constexpr int kStageTok = 64;          // tokens per pipeline stage
 constexpr int kConsumerWarps = 4;      // each owns 16 tokens of a stage
 constexpr int kThreads = 32 * (1 + kConsumerWarps);
 constexpr int kConsumerThreads = 32 * kConsumerWarps;
-constexpr int kMaxStages = 16;
+constexpr int kMaxStages = 12;
 constexpr int kMaxPartition = 1024;
 #ifndef PA_DECODE_CTAS_PER_SM
-#define PA_DECODE_CTAS_PER_SM 1
+#define PA_DECODE_CTAS_PER_SM 3
 #endif
 constexpr int kCtasPerSm = PA_DECODE_CTAS_PER_SM;  // resident decode CTAs per SM
 
@@ -29,6 +29,7 @@ struct StageInfo {
   int flags;
   int L;      // sequence length (clamped to the table capacity)
   int nP;     // number of partitions of the sequence
+  int k;      // sequences sharing the item's blocks (s .. s+k-1)
 };
 
 struct SmemHeader {
@@ -51,8 +52,9 @@ struct DecodeParams {
   float qk_scale_log2;  // softmax scale * k_scale * log2(e)
   float v_scale;
   int num_stages, stage_bytes, k_off, v_off, q_off, scratch_off, stages_off;
-  int *work;  // [0] claim counter, [1] number of (s, p) pairs
-  int2 *pairs;
+  int kmax;   // most sequences one item may batch
+  int *work;  // [0] claim counter, [1] number of items
+  int4 *items;  // (first sequence, partition, sequences, 0)
   float2 *part_ml;  // [S * max_parts * Hq] (max in log2 units, sum)
   float *part_o;    // [S * max_parts * Hq * D], normalised by its own sum
   int *err;

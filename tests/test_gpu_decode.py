@@ -130,3 +130,42 @@ def test_bad_block_id_and_length_are_reported():
     run.decode()
     torch.cuda.synchronize()
     assert int(run.err.item()) == 3
+
+
+SHARED_DTYPES = [("f16", "f16"), ("bf16", "bf16"), ("e4m3", "bf16")]
+
+
+@pytest.mark.parametrize("cache_dtype,q_dtype", SHARED_DTYPES)
+@pytest.mark.parametrize("group", [1, 2, 4, 8])
+@pytest.mark.parametrize("bs", [8, 16, 32])
+def test_shared_prefix_matches_oracle(cache_dtype, q_dtype, group, bs):
+    """Sequences whose tables name the same blocks over whole partitions are
+    decoded together; every output still equals the oracle's."""
+    Hkv = 2
+    w = W.make_workload("qwen3-prefix", 31 + group + bs, device=G.DEV, overrides=dict(
+        S=11, prefix=256, suffix_lo=1, suffix_hi=300, Hq=Hkv * group, Hkv=Hkv, d=128, bs=bs,
+        cache_dtype=cache_dtype, q_dtype=q_dtype, src_dtype=q_dtype))
+    for P in (64, 128):
+        run = G.GpuRun(w, partition_size=P).setup()
+        run.step()
+        torch.cuda.synchronize()
+        assert int(run.err.item()) == 0
+        ref = G.oracle_decode(w, G.oracle_cache(w))
+        _check(w, run.out, ref)
+
+
+@pytest.mark.parametrize("cache_dtype,q_dtype", SHARED_DTYPES)
+@pytest.mark.parametrize("bs", [16, 32])
+@pytest.mark.parametrize("heads", [(2, 2), (4, 2), (8, 1)])
+def test_beam_fork_matches_oracle(cache_dtype, q_dtype, bs, heads):
+    Hq, Hkv = heads
+    w = W.make_workload("opt13b-beam", 7 + bs + Hq, device=G.DEV, overrides=dict(
+        prompts=5, len_lo=100, len_hi=700, Hq=Hq, Hkv=Hkv, d=64 if Hq == 8 else 128, bs=bs,
+        cache_dtype=cache_dtype, q_dtype=q_dtype, src_dtype=q_dtype))
+    for P in (64, 256):
+        run = G.GpuRun(w, partition_size=P).setup()
+        run.step()
+        torch.cuda.synchronize()
+        assert int(run.err.item()) == 0
+        ref = G.oracle_decode(w, G.oracle_cache(w))
+        _check(w, run.out, ref)
