@@ -68,7 +68,10 @@ __device__ __forceinline__ int clamp_len(int L, int cap, int *err) {
 
 // Query rows one item can hold: 4 for G == 1 (a beam of four), 8 otherwise
 // (one mma N tile).  Sequences per shared item: kmax = QM / G.
-__host__ __device__ constexpr int query_capacity(int G) { return G == 1 ? 4 : 8; }
+#ifndef PA_SHARE_G1
+#define PA_SHARE_G1 1
+#endif
+__host__ __device__ constexpr int query_capacity(int G) { return G == 1 ? (PA_SHARE_G1 ? 4 : 1) : 8; }
 
 // ----------------------------------------------------------------------------
 // plan: list the work items in sequence order; reset the claim counter
@@ -77,65 +80,127 @@ __host__ __device__ constexpr int query_capacity(int G) { return G == 1 ? 4 : 8;
 // s joins the item of s-1 for partition q when both partitions are full, s is
 // not at a multiple of kmax, and their block-table entries over the
 // partition are equal; otherwise it leads an item of its own.
+
+// Exclusive prefix sum over the 1024 threads of the block; *total = sum.
+__device__ __forceinline__ int block_exclusive_scan(int x, int *warp_tot, int *total) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  int v = x;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += y;
+  }
+  if (lane == 31) warp_tot[warp] = v;
+  __syncthreads();
+  if (warp == 0) {
+    int t = warp_tot[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, t, o);
+      if (lane >= o) t += y;
+    }
+    warp_tot[lane] = t;  // inclusive over warps
+  }
+  __syncthreads();
+  const int ex = (warp ? warp_tot[warp - 1] : 0) + v - x;
+  *total = warp_tot[31];
+  __syncthreads();
+  return ex;
+}
+
+// Rows s and s-1 of the block table agree over partition q (bpp entries);
+// loads go out eight at a time so a mismatch costs one round trip.
 __device__ __forceinline__ bool same_blocks(const DecodeParams &p, int s, int q, int bpp) {
   const int32_t *a = p.block_tables + static_cast<size_t>(s) * p.max_blocks + static_cast<size_t>(q) * bpp;
   const int32_t *b = a - p.max_blocks;
-  for (int j = 0; j < bpp; ++j)
-    if (__ldg(a + j) != __ldg(b + j)) return false;
+  for (int j0 = 0; j0 < bpp; j0 += 8) {
+    int x[8], y[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const bool in = j0 + u < bpp;
+      x[u] = in ? __ldg(a + j0 + u) : 0;
+      y[u] = in ? __ldg(b + j0 + u) : 0;
+    }
+    bool eq = true;
+#pragma unroll
+    for (int u = 0; u < 8; ++u) eq = eq && (x[u] == y[u]);
+    if (!eq) return false;
+  }
   return true;
-}
-
-__device__ __forceinline__ bool joins_previous(const DecodeParams &p, int s, int q, int bpp) {
-  if (s % p.kmax == 0) return false;
-  const int P = p.partition_size;
-  const int Lprev = min(max(__ldg(p.seq_lens + s - 1), 0), p.len_cap);
-  const int L = min(max(__ldg(p.seq_lens + s), 0), p.len_cap);
-  if (L < (q + 1) * P || Lprev < (q + 1) * P) return false;
-  return same_blocks(p, s, q, bpp);
 }
 
 __global__ void __launch_bounds__(1024) plan_kernel(const DecodeParams p) {
   __shared__ int warp_tot[32];
   __shared__ int base;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int bpp = p.partition_size / p.block_size;
+  const int tid = threadIdx.x;
+  const int P = p.partition_size;
+  const int bpp = P / p.block_size;
+  const int S = p.num_seqs;
+  launch_dependents();  // the decode grid may become resident; it waits for us
+  // A) lengths, partition counts, and the (s, q) pair list in sequence order
   if (tid == 0) base = 0;
   __syncthreads();
-  for (int b0 = 0; b0 < p.num_seqs; b0 += 1024) {
+  for (int b0 = 0; b0 < S; b0 += 1024) {
     const int s = b0 + tid;
-    int nP = 0, cnt = 0;
-    if (s < p.num_seqs) {
+    int nP = 0;
+    if (s < S) {
       const int L = clamp_len(__ldg(p.seq_lens + s), p.len_cap, p.err);
-      nP = max(1, (L + p.partition_size - 1) / p.partition_size);
-      for (int q = 0; q < nP; ++q) cnt += (p.kmax > 1 && joins_previous(p, s, q, bpp)) ? 0 : 1;
+      nP = max(1, (L + P - 1) / P);
+      p.plan_len[s] = L;
     }
-    int x = cnt;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, x, o);
-      if (lane >= o) x += y;
+    int tot;
+    const int ex = block_exclusive_scan(nP, warp_tot, &tot);
+    const int b = base;  // every thread reads the running base ...
+    if (s < S) {
+      const int o = b + ex;
+      p.plan_off[s] = o;
+      for (int q = 0; q < nP; ++q) p.plan_pairs[o + q] = make_int2(s, q);
     }
-    if (lane == 31) warp_tot[warp] = x;
+    __syncthreads();     // ... before thread 0 advances it
+    if (tid == 0) base = b + tot;
     __syncthreads();
-    if (warp == 0) {
-      int t = warp_tot[lane];
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, t, o);
-        if (lane >= o) t += y;
+  }
+  const int npairs = base;
+  if (tid == 0) p.plan_off[S] = npairs;
+  __syncthreads();
+  // B) does pair (s, q) join the item of (s-1, q)?  One thread per pair.
+  if (p.kmax > 1) {
+    for (int k = tid; k < npairs; k += 1024) {
+      const int2 sq = p.plan_pairs[k];
+      bool join = false;
+      if (sq.x % p.kmax != 0) {
+        const int need = (sq.y + 1) * P;
+        if (p.plan_len[sq.x] >= need && p.plan_len[sq.x - 1] >= need) join = same_blocks(p, sq.x, sq.y, bpp);
       }
-      warp_tot[lane] = t;  // inclusive over warps
+      p.plan_join[k] = join ? 1 : 0;
     }
     __syncthreads();
-    int idx = base + (warp ? warp_tot[warp - 1] : 0) + x - cnt;
-    for (int q = 0; q < nP; ++q) {
-      if (p.kmax > 1 && joins_previous(p, s, q, bpp)) continue;
-      int k = 1;
-      while (p.kmax > 1 && s + k < p.num_seqs && joins_previous(p, s + k, q, bpp)) ++k;
-      p.items[idx++] = make_int4(s, q, k, 0);
+  }
+  // C) every pair that does not join leads an item of itself and the pairs
+  //    (s+1, q), (s+2, q), ... that join it; items keep sequence order
+  if (tid == 0) base = 0;
+  __syncthreads();
+  for (int k0 = 0; k0 < npairs; k0 += 1024) {
+    const int k = k0 + tid;
+    int lead = 0, ksz = 1;
+    int2 sq = make_int2(0, 0);
+    if (k < npairs) {
+      sq = p.plan_pairs[k];
+      lead = (p.kmax > 1) ? (p.plan_join[k] == 0) : 1;
+      if (lead && p.kmax > 1) {
+        for (int j = 1; j < p.kmax && sq.x + j < S; ++j) {
+          const int idx = p.plan_off[sq.x + j] + sq.y;
+          if (idx >= p.plan_off[sq.x + j + 1] || p.plan_join[idx] == 0) break;
+          ++ksz;
+        }
+      }
     }
+    int tot;
+    const int ex = block_exclusive_scan(lead, warp_tot, &tot);
+    const int b = base;
+    if (lead) p.items[b + ex] = make_int4(sq.x, sq.y, ksz, 0);
     __syncthreads();
-    if (tid == 0) base += warp_tot[31];
+    if (tid == 0) base = b + tot;
     __syncthreads();
   }
   if (tid == 0) {
@@ -149,6 +214,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(const DecodeParams p) {
 // ----------------------------------------------------------------------------
 template <int QT, int D>
 __global__ void __launch_bounds__(256) merge_kernel(const DecodeParams p) {
+  grid_dependency_wait();  // partials of the decode grid
   const int lane = threadIdx.x & 31;
   const long long gw = (blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x) >> 5;
   if (gw >= static_cast<long long>(p.num_seqs) * p.num_q_heads) return;
@@ -182,11 +248,29 @@ __global__ void __launch_bounds__(256) merge_kernel(const DecodeParams p) {
     for (int o = 16; o; o >>= 1) ws += __shfl_xor_sync(0xffffffffu, ws, o);
     den += ws;
     const int cnt = min(32, nP - q0);
-    for (int k = 0; k < cnt; ++k) {
-      const float wk = __shfl_sync(0xffffffffu, w, k);
-      const float *po = p.part_o + (base + static_cast<size_t>(q0 + k) * p.num_q_heads) * D + lane * E;
+    // eight partitions per batch: their loads are all in flight before the FMAs
+    for (int k0 = 0; k0 < cnt; k0 += 8) {
+      float v[8][E];
 #pragma unroll
-      for (int e = 0; e < E; ++e) acc[e] = fmaf(wk, po[e], acc[e]);
+      for (int u = 0; u < 8; ++u) {
+        if (k0 + u < cnt) {
+          const float *po = p.part_o + (base + static_cast<size_t>(q0 + k0 + u) * p.num_q_heads) * D + lane * E;
+#pragma unroll
+          for (int e = 0; e < E; e += 2) {
+            const float2 t = *reinterpret_cast<const float2 *>(po + e);
+            v[u][e] = t.x;
+            v[u][e + 1] = t.y;
+          }
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const float wk = __shfl_sync(0xffffffffu, w, (k0 + u) & 31);
+        if (k0 + u < cnt) {
+#pragma unroll
+          for (int e = 0; e < E; ++e) acc[e] = fmaf(wk, v[u][e], acc[e]);
+        }
+      }
     }
   }
   const float inv = den > 0.f ? 1.f / den : 0.f;
@@ -953,6 +1037,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_kernel(const Deco
     fence_mbar_init();
   }
   __syncthreads();
+  // the plan (and every kernel before it: the cache writes) must be complete
+  grid_dependency_wait();
+  launch_dependents();
   if (warp == 0) {
     producer_warp<KV, D, G>(p, smem);
     return;
@@ -980,7 +1067,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_kernel(const Deco
       ok = run_item<KV, QT, D, G, QM, Mma>(p, hdr, stages, so, sm, sl, cw, stage, phase, ncomb, inf, abort);
     } else {
       using Simt = SimtState<KV, QT, D, G, QM>;
-      if (inf.k > 1)
+      if (QM > G && inf.k > 1)
         ok = run_item<KV, QT, D, G, QM, Mma>(p, hdr, stages, so, sm, sl, cw, stage, phase, ncomb, inf, abort);
       else
         ok = run_item<KV, QT, D, G, QM, Simt>(p, hdr, stages, so, sm, sl, cw, stage, phase, ncomb, inf, abort);
@@ -1058,11 +1145,27 @@ pa_status launch_decode(DecodeParams p, const DeviceInfo &dev, cudaStream_t stre
   const long long items = static_cast<long long>(p.num_seqs) * p.max_parts * p.num_kv_heads;
   const long long slots = static_cast<long long>(dev.sm_count) * ctas;
   const int grid = static_cast<int>(items < slots ? items : slots);
-  kern<<<grid, kThreads, sp.total, stream>>>(p);
+  // decode and merge are launched as programmatic dependents of the kernel
+  // before them, so their launch overlaps its tail (each waits on the device)
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = sp.total;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, kern, p);
+  if (e != cudaSuccess) return cuda_fail(e);
   if (p.max_parts > 1) {
     const long long warps = static_cast<long long>(p.num_seqs) * p.num_q_heads;
-    const int blocks = static_cast<int>((warps * 32 + 255) / 256);
-    merge_kernel<QT, D><<<blocks, 256, 0, stream>>>(p);
+    cfg.gridDim = dim3(static_cast<unsigned>((warps * 32 + 255) / 256));
+    cfg.blockDim = dim3(256);
+    cfg.dynamicSmemBytes = 0;
+    e = cudaLaunchKernelEx(&cfg, merge_kernel<QT, D>, p);
+    if (e != cudaSuccess) return cuda_fail(e);
   }
   e = cudaGetLastError();
   return e == cudaSuccess ? PA_OK : cuda_fail(e);

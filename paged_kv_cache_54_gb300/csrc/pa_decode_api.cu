@@ -19,7 +19,7 @@ int choose_partition(int num_seqs, int kv_heads, int max_seq_len, int requested)
 }
 
 struct WorkspaceLayout {
-  size_t pairs_off, ml_off, o_off, total;
+  size_t pairs_off, len_off, seqoff_off, plist_off, join_off, ml_off, o_off, total;
   int partition, max_parts;
 };
 
@@ -34,8 +34,12 @@ bool layout_for(int num_seqs, int num_q_heads, int kv_heads, int head_dim, int m
   w.partition = choose_partition(num_seqs, kv_heads, max_seq_len, partition_size);
   w.max_parts = max_seq_len > 0 ? (max_seq_len + w.partition - 1) / w.partition : 1;
   const size_t units = static_cast<size_t>(num_seqs) * w.max_parts;
-  w.pairs_off = 256;
-  w.ml_off = align256(w.pairs_off + units * sizeof(int4));
+  w.pairs_off = 256;                                            // items (int4)
+  w.len_off = align256(w.pairs_off + units * sizeof(int4));      // lengths
+  w.seqoff_off = align256(w.len_off + num_seqs * sizeof(int));   // pair offsets
+  w.plist_off = align256(w.seqoff_off + (num_seqs + 1) * sizeof(int));
+  w.join_off = align256(w.plist_off + units * sizeof(int2));
+  w.ml_off = align256(w.join_off + units);
   w.o_off = align256(w.ml_off + units * num_q_heads * sizeof(float2));
   w.total = align256(w.o_off + units * num_q_heads * head_dim * sizeof(float));
   *out = w;
@@ -117,6 +121,10 @@ extern "C" pa_status pa_decode(void *out, const void *q, int32_t q_dtype, int32_
   p.v_scale = fp8 ? cache->v_scale : 1.0f;
   p.work = reinterpret_cast<int *>(ws);
   p.items = reinterpret_cast<int4 *>(ws + w.pairs_off);
+  p.plan_len = reinterpret_cast<int *>(ws + w.len_off);
+  p.plan_off = reinterpret_cast<int *>(ws + w.seqoff_off);
+  p.plan_pairs = reinterpret_cast<int2 *>(ws + w.plist_off);
+  p.plan_join = ws + w.join_off;
   p.part_ml = reinterpret_cast<float2 *>(ws + w.ml_off);
   p.part_o = reinterpret_cast<float *>(ws + w.o_off);
   p.err = device_error;

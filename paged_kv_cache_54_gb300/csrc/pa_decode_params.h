@@ -55,6 +55,10 @@ struct DecodeParams {
   int kmax;   // most sequences one item may batch
   int *work;  // [0] claim counter, [1] number of items
   int4 *items;  // (first sequence, partition, sequences, 0)
+  int *plan_len;       // [S] clamped lengths
+  int *plan_off;       // [S + 1] first (s, q) pair of each sequence
+  int2 *plan_pairs;    // [S * max_parts] (s, q) pairs in sequence order
+  uint8_t *plan_join;  // [S * max_parts] pair joins the previous sequence's item
   float2 *part_ml;  // [S * max_parts * Hq] (max in log2 units, sum)
   float *part_o;    // [S * max_parts * Hq * D], normalised by its own sum
   int *err;
