@@ -108,11 +108,29 @@ __device__ __forceinline__ int block_exclusive_scan(int x, int *warp_tot, int *t
   return ex;
 }
 
-// Rows s and s-1 of the block table agree over partition q (bpp entries);
-// loads go out eight at a time so a mismatch costs one round trip.
+// Rows s and s-1 of the block table agree over partition q (bpp entries).
+// 16-byte loads when both row segments are aligned, else eight scalar loads
+// at a time; either way a mismatch usually costs one round trip.
 __device__ __forceinline__ bool same_blocks(const DecodeParams &p, int s, int q, int bpp) {
   const int32_t *a = p.block_tables + static_cast<size_t>(s) * p.max_blocks + static_cast<size_t>(q) * bpp;
   const int32_t *b = a - p.max_blocks;
+  if ((bpp & 3) == 0 && ((reinterpret_cast<uintptr_t>(a) | reinterpret_cast<uintptr_t>(b)) & 15) == 0) {
+    for (int j0 = 0; j0 < bpp; j0 += 32) {
+      int4 x[8], y[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const bool in = j0 + 4 * u < bpp;
+        x[u] = in ? __ldg(reinterpret_cast<const int4 *>(a + j0) + u) : make_int4(0, 0, 0, 0);
+        y[u] = in ? __ldg(reinterpret_cast<const int4 *>(b + j0) + u) : make_int4(0, 0, 0, 0);
+      }
+      bool eq = true;
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        eq = eq && x[u].x == y[u].x && x[u].y == y[u].y && x[u].z == y[u].z && x[u].w == y[u].w;
+      if (!eq) return false;
+    }
+    return true;
+  }
   for (int j0 = 0; j0 < bpp; j0 += 8) {
     int x[8], y[8];
 #pragma unroll
@@ -129,14 +147,23 @@ __device__ __forceinline__ bool same_blocks(const DecodeParams &p, int s, int q,
   return true;
 }
 
+// Plan tables live in shared memory when they fit, else in the workspace.
+constexpr int kPlanSmemSeqs = 4096;
+constexpr int kPlanSmemPairs = 12288;
+
 __global__ void __launch_bounds__(1024) plan_kernel(const DecodeParams p) {
   __shared__ int warp_tot[32];
   __shared__ int base;
+  __shared__ int s_len[kPlanSmemSeqs];
+  __shared__ int s_off[kPlanSmemSeqs + 1];
+  __shared__ uint8_t s_join[kPlanSmemPairs];
   const int tid = threadIdx.x;
   const int P = p.partition_size;
   const int bpp = P / p.block_size;
   const int S = p.num_seqs;
   launch_dependents();  // the decode grid may become resident; it waits for us
+  int *len = S <= kPlanSmemSeqs ? s_len : p.plan_len;
+  int *off = S <= kPlanSmemSeqs ? s_off : p.plan_off;
   // A) lengths, partition counts, and the (s, q) pair list in sequence order
   if (tid == 0) base = 0;
   __syncthreads();
@@ -146,14 +173,14 @@ __global__ void __launch_bounds__(1024) plan_kernel(const DecodeParams p) {
     if (s < S) {
       const int L = clamp_len(__ldg(p.seq_lens + s), p.len_cap, p.err);
       nP = max(1, (L + P - 1) / P);
-      p.plan_len[s] = L;
+      len[s] = L;
     }
     int tot;
     const int ex = block_exclusive_scan(nP, warp_tot, &tot);
     const int b = base;  // every thread reads the running base ...
     if (s < S) {
       const int o = b + ex;
-      p.plan_off[s] = o;
+      off[s] = o;
       for (int q = 0; q < nP; ++q) p.plan_pairs[o + q] = make_int2(s, q);
     }
     __syncthreads();     // ... before thread 0 advances it
@@ -161,18 +188,19 @@ __global__ void __launch_bounds__(1024) plan_kernel(const DecodeParams p) {
     __syncthreads();
   }
   const int npairs = base;
-  if (tid == 0) p.plan_off[S] = npairs;
+  if (tid == 0) off[S] = npairs;
+  uint8_t *join = npairs <= kPlanSmemPairs ? s_join : p.plan_join;
   __syncthreads();
   // B) does pair (s, q) join the item of (s-1, q)?  One thread per pair.
   if (p.kmax > 1) {
     for (int k = tid; k < npairs; k += 1024) {
       const int2 sq = p.plan_pairs[k];
-      bool join = false;
+      bool jn = false;
       if (sq.x % p.kmax != 0) {
         const int need = (sq.y + 1) * P;
-        if (p.plan_len[sq.x] >= need && p.plan_len[sq.x - 1] >= need) join = same_blocks(p, sq.x, sq.y, bpp);
+        if (len[sq.x] >= need && len[sq.x - 1] >= need) jn = same_blocks(p, sq.x, sq.y, bpp);
       }
-      p.plan_join[k] = join ? 1 : 0;
+      join[k] = jn ? 1 : 0;
     }
     __syncthreads();
   }
@@ -186,11 +214,11 @@ __global__ void __launch_bounds__(1024) plan_kernel(const DecodeParams p) {
     int2 sq = make_int2(0, 0);
     if (k < npairs) {
       sq = p.plan_pairs[k];
-      lead = (p.kmax > 1) ? (p.plan_join[k] == 0) : 1;
+      lead = (p.kmax > 1) ? (join[k] == 0) : 1;
       if (lead && p.kmax > 1) {
         for (int j = 1; j < p.kmax && sq.x + j < S; ++j) {
-          const int idx = p.plan_off[sq.x + j] + sq.y;
-          if (idx >= p.plan_off[sq.x + j + 1] || p.plan_join[idx] == 0) break;
+          const int idx = off[sq.x + j] + sq.y;
+          if (idx >= off[sq.x + j + 1] || join[idx] == 0) break;
           ++ksz;
         }
       }

@@ -169,3 +169,33 @@ def test_beam_fork_matches_oracle(cache_dtype, q_dtype, bs, heads):
         assert int(run.err.item()) == 0
         ref = G.oracle_decode(w, G.oracle_cache(w))
         _check(w, run.out, ref)
+
+
+@pytest.mark.parametrize("cache_dtype,q_dtype,heads", [("f16", "f16", (1, 1)),
+                                                       ("bf16", "bf16", (2, 1))])
+def test_many_sequences_exceed_plan_shared_memory(cache_dtype, q_dtype, heads):
+    """5000 sequences and > 12288 (sequence, partition) pairs: the plan's
+    tables spill from shared memory to the workspace."""
+    rng = np.random.default_rng(5)
+    lens = rng.integers(1, 330, 5000).tolist()
+    Hq, Hkv = heads
+    w = W.random_case(12, len(lens), Hq, Hkv, 64, 16, cache_dtype, q_dtype, lens, device=G.DEV)
+    run = G.GpuRun(w, partition_size=64).setup()
+    run.step()
+    torch.cuda.synchronize()
+    assert int(run.err.item()) == 0
+    ref = G.oracle_decode(w, G.oracle_cache(w))
+    _check(w, run.out, ref)
+
+
+def test_shared_prefix_across_plan_chunks():
+    """Sharing runs that cross the plan kernel's 1024-sequence chunks."""
+    w = W.make_workload("qwen3-prefix", 77, device=G.DEV, overrides=dict(
+        S=2100, prefix=128, suffix_lo=1, suffix_hi=40, Hq=2, Hkv=1, d=64, bs=16,
+        cache_dtype="bf16", q_dtype="bf16", src_dtype="bf16"))
+    run = G.GpuRun(w, partition_size=64).setup()
+    run.step()
+    torch.cuda.synchronize()
+    assert int(run.err.item()) == 0
+    ref = G.oracle_decode(w, G.oracle_cache(w))
+    _check(w, run.out, ref)
