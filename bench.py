@@ -47,8 +47,8 @@ DECODE_SOURCES = [os.path.join(ROOT, "paged_kv_cache_54_gb300", "csrc", f)
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=500)
-    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", default=DEFAULT_CONFIG, choices=W.CONFIG_ORDER)
     ap.add_argument("--seed", type=int, default=None)
@@ -102,7 +102,7 @@ class ClockSampler:
         self.proc = None
         try:
             self.proc = subprocess.Popen(
-                ["nvidia-smi", f"--query-gpu={SMI_FIELDS}", "--format=csv,noheader,nounits",
+                ["nvidia-smi", f"--query-gpu=timestamp,{SMI_FIELDS}", "--format=csv,noheader,nounits",
                  "-lms", "100", "-i", str(index)], stdout=subprocess.PIPE,
                 stderr=subprocess.DEVNULL, text=True)
         except OSError:
@@ -121,22 +121,24 @@ class ClockSampler:
         time.sleep(0.25)
         self.proc.terminate()
         out, _ = self.proc.communicate(timeout=10)
-        rows = [r.split(",") for r in out.strip().splitlines() if r.count(",") >= 8]
-        # samples are not time-stamped: keep the ones taken while under load
-        sm = [float(r[1]) for r in rows if r[1].strip().replace(".", "").isdigit()]
-        mx = [float(r[2]) for r in rows if r[2].strip().replace(".", "").isdigit()]
-        load = [r for r in rows if float(r[3] or 0) > 200.0] if rows else []
-        use = load or rows
-        sm_load = [float(r[1]) for r in use] if use else sm
-        reasons = set()
+        rows = []
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 10:
+                continue
+            try:
+                ts = time.mktime(time.strptime(f[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                rows.append((ts, float(f[2]), float(f[3]), f[6:10]))
+            except ValueError:
+                continue
+        # samples inside the timed region (second resolution, so widen by 1 s)
+        inside = [r for r in rows if self.t_on - 1 <= r[0] <= self.t_off + 1] or rows
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for r in use:
-            for i, n in enumerate(names):
-                if r[5 + i].strip() == "Active":
-                    reasons.add(n)
-        return {"sm_mhz": statistics.median(sm_load) if sm_load else None,
-                "sm_max_mhz": max(mx) if mx else None, "reasons": sorted(reasons),
-                "samples": len(rows), "samples_under_load": len(load)}
+        reasons = sorted({n for r in inside for n, v in zip(names, r[3]) if v == "Active"})
+        sm = [r[1] for r in inside]
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(r[2] for r in rows) if rows else None,
+                "reasons": reasons, "samples": len(inside)}
 
 
 def workload_bytes(w):
