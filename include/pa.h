@@ -48,7 +48,8 @@
  *   wins), which the caller reads after synchronising.  Kernels never trap.
  * - Device error codes: 1 block id out of range, 2 slot out of range,
  *   3 sequence length out of range, 4 a pipeline wait exceeded its time
- *   limit, 5 copy pair out of range.
+ *   limit, 5 copy pair out of range, 6 shared memory not aligned as the
+ *   swizzled tile layout needs (nothing computed).
  */
 #ifndef PA_H_
 #define PA_H_

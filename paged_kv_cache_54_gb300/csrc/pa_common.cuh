@@ -2,6 +2,7 @@
 // bulk-copy PTX wrappers, bounded waits.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
@@ -19,6 +20,7 @@ enum DevErr : int {
   kErrSeqLen = 3,
   kErrTimeout = 4,
   kErrCopyIndex = 5,
+  kErrSmemAlign = 6,
 };
 
 // Wait limit for every spin on an mbarrier: 2 s of %globaltimer.
@@ -183,6 +185,26 @@ __device__ __forceinline__ void bulk_g2s(void *smem_dst, const void *gmem_src, u
           smem_addr(smem_dst)),
       "l"(gmem_src), "r"(bytes), "r"(smem_addr(bar))
       : "memory");
+}
+
+// Tiled TMA load of one tile of a 2-D ([rows, 128 B]) or 3-D ([rows, 2, 128 B])
+// tensor view, rows [row0, row0 + box rows), completing on the mbarrier's
+// transaction count.  The tensor map lives in the kernel's parameter space.
+template <bool kThreeD>
+__device__ __forceinline__ void tma_load_tile(void *smem_dst, const CUtensorMap *map, int row0, uint64_t *bar) {
+  if constexpr (kThreeD) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_addr(smem_dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(0), "r"(row0), "r"(smem_addr(bar))
+        : "memory");
+  } else {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_addr(smem_dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(row0), "r"(smem_addr(bar))
+        : "memory");
+  }
 }
 
 __device__ __forceinline__ void named_bar_sync(int id, int threads) {

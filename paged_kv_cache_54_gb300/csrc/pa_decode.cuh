@@ -48,6 +48,31 @@ namespace {  // kernels are private to each translation unit
 
 constexpr float kLazyRescale = 8.0f;
 
+// Stage buffers are written by tiled TMA with the 128-byte swizzle when a
+// token row is at least 128 bytes: within every 1024-byte atom, the 16-byte
+// chunk at byte offset `off` lands at off ^ (((off >> 7) & 7) << 4).  Every
+// shared-memory read of K or V goes through swz<SW>() on the offset relative
+// to the (1024-byte aligned) K or V region of the stage.
+// Used for the kernels whose items always run on the tensor-core path
+// (G >= 2): there the swizzle makes the fragment reads conflict-free.  The
+// G == 1 kernels keep the linear layout, on which the SIMT path's reads are
+// already conflict-free.
+template <int KV, int D, int G>
+__host__ __device__ constexpr bool swizzled() { return D * elt_bytes(KV) >= 128 && G >= 2; }
+
+template <bool SW>
+__device__ __forceinline__ int swz(int off) {
+  return SW ? (off ^ (((off >> 7) & 7) << 4)) : off;
+}
+
+// Combine scratch: row r (warp c, query j: r = c * QM + j) holds D floats in
+// 16-byte units; unit u is stored at u ^ ((r >> 1) & 3) so that the end-of-item
+// stores of the four lanes that share a unit index land in different banks.
+template <int D>
+__device__ __forceinline__ int scr(int row, int d) {
+  return row * D + ((((d >> 2) ^ (row >> 1)) & 3) | ((d >> 2) & ~3)) * 4 + (d & 3);
+}
+
 __device__ __forceinline__ uint32_t w32(const uint4 &v, int i) {
   return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
 }
@@ -151,7 +176,7 @@ __device__ __forceinline__ bool same_blocks(const DecodeParams &p, int s, int q,
 constexpr int kPlanSmemSeqs = 4096;
 constexpr int kPlanSmemPairs = 12288;
 
-__global__ void __launch_bounds__(1024) plan_kernel(const DecodeParams p) {
+__global__ void __launch_bounds__(1024) plan_kernel(const __grid_constant__ DecodeParams p) {
   __shared__ int warp_tot[32];
   __shared__ int base;
   __shared__ int s_len[kPlanSmemSeqs];
@@ -241,7 +266,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(const DecodeParams p) {
 // merge: combine the partials of sequences split into several partitions
 // ----------------------------------------------------------------------------
 template <int QT, int D>
-__global__ void __launch_bounds__(256) merge_kernel(const DecodeParams p) {
+__global__ void __launch_bounds__(256) merge_kernel(const __grid_constant__ DecodeParams p) {
   grid_dependency_wait();  // partials of the decode grid
   const int lane = threadIdx.x & 31;
   const long long gw = (blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x) >> 5;
@@ -417,9 +442,16 @@ __device__ __forceinline__ void producer_warp(const DecodeParams &p, uint8_t *sm
           record_error(p.err, kErrBlockIndex);
           b = 0;
         }
-        const size_t off = (static_cast<size_t>(b) * p.num_kv_heads + h) * tile;
-        bulk_g2s(sb + p.k_off + lane * tile, p.k_cache + off, tile, &hdr.full[stage]);
-        bulk_g2s(sb + p.v_off + lane * tile, p.v_cache + off, tile, &hdr.full[stage]);
+        if constexpr (swizzled<KV, D, G>()) {
+          // tile rows [row0, row0 + bs) of the [num_blocks * kv_heads * bs, d] view
+          const int row0 = (b * p.num_kv_heads + h) * bs;
+          tma_load_tile<(D * elt_bytes(KV) > 128)>(sb + p.k_off + lane * tile, &p.tmap_k, row0, &hdr.full[stage]);
+          tma_load_tile<(D * elt_bytes(KV) > 128)>(sb + p.v_off + lane * tile, &p.tmap_v, row0, &hdr.full[stage]);
+        } else {
+          const size_t off = (static_cast<size_t>(b) * p.num_kv_heads + h) * tile;
+          bulk_g2s(sb + p.k_off + lane * tile, p.k_cache + off, tile, &hdr.full[stage]);
+          bulk_g2s(sb + p.v_off + lane * tile, p.v_cache + off, tile, &hdr.full[stage]);
+        }
       }
       if (st == 0 && lane >= 24 && lane - 24 < kseq) {  // one q copy per sequence of the item
         const int i = lane - 24;
@@ -471,6 +503,7 @@ __device__ __forceinline__ void producer_warp(const DecodeParams &p, uint8_t *sm
 // ----------------------------------------------------------------------------
 template <int KV, int QT, int D, int G, int QM>
 struct SimtState {
+  static constexpr bool SW = swizzled<KV, D, G>();
   // Lane = 4 * t8 + qd: four lanes per token, eight tokens per pass, two
   // passes per 16-token slice.  Lane qd of a token owns the 16-byte chunks
   // c == qd (mod 4) of the token's K row, visited in an order rotated by t8
@@ -531,9 +564,9 @@ struct SimtState {
     }
   }
 
-  __device__ __forceinline__ void load_v(const uint8_t *row, float (&f)[EPL]) {
+  __device__ __forceinline__ void load_v(const uint8_t *Vb, int row, float (&f)[EPL]) {
     const int lane = threadIdx.x & 31;
-    const uint8_t *src = row + lane * EPL * ELT;
+    const uint8_t *src = Vb + swz<SW>(row * ROWB + lane * EPL * ELT);
     if constexpr (ELT == 2) {
 #pragma unroll
       for (int e = 0; e < EPL; e += 2) {
@@ -551,8 +584,9 @@ struct SimtState {
     }
   }
 
-  // one 16-token slice: rows Ks[0..15], Vs[0..15]; n valid tokens (1..16)
-  __device__ __forceinline__ void slice(const uint8_t *Ks, const uint8_t *Vs, int n, float v_scale) {
+  // one 16-token slice: rows row0..row0+15 of the stage's K and V regions
+  // Kb, Vb; n valid tokens (1..16)
+  __device__ __forceinline__ void slice(const uint8_t *Kb, const uint8_t *Vb, int row0, int n, float v_scale) {
     const int lane = threadIdx.x & 31;
     const int t8 = lane >> 2, qd = lane & 3;
     float acc[2][G][2];
@@ -562,11 +596,11 @@ struct SimtState {
       for (int g = 0; g < G; ++g) acc[ps][g][0] = acc[ps][g][1] = 0.f;
 #pragma unroll
     for (int ps = 0; ps < 2; ++ps) {
-      const uint8_t *krow = Ks + (8 * ps + t8) * ROWB;
+      const int krow = (row0 + 8 * ps + t8) * ROWB;
 #pragma unroll
       for (int i = 0; i < NCHL; ++i) {
         float kf[EPC];
-        chunk_to_float(lds128(krow + chunk(i, qd, t8) * 16), kf);
+        chunk_to_float(lds128(Kb + swz<SW>(krow + chunk(i, qd, t8) * 16)), kf);
 #pragma unroll
         for (int g = 0; g < G; ++g)
 #pragma unroll
@@ -604,7 +638,7 @@ struct SimtState {
     for (int tt = 0; tt < 16; ++tt) {
       if (tt < n) {
         float vf[EPL];
-        load_v(Vs + tt * ROWB, vf);
+        load_v(Vb, row0 + tt, vf);
 #pragma unroll
         for (int g = 0; g < G; ++g) {
           const float pt = __shfl_sync(0xffffffffu, pr[tt >> 3][g], 4 * (tt & 7)) * v_scale;
@@ -623,9 +657,13 @@ struct SimtState {
       float ls = l[g];
 #pragma unroll
       for (int o2 = 1; o2 < 32; o2 <<= 1) ls += __shfl_xor_sync(0xffffffffu, ls, o2);
-      float *dst = so + (static_cast<size_t>(cw) * QS + g) * D + lane * EPL;
+      const int row = cw * QS + g;
+      if constexpr (EPL == 4) {
+        *reinterpret_cast<float4 *>(so + scr<D>(row, lane * 4)) = make_float4(o[g][0], o[g][1], o[g][2], o[g][3]);
+      } else {
 #pragma unroll
-      for (int e = 0; e < EPL; ++e) dst[e] = o[g][e];
+        for (int e = 0; e < EPL; ++e) so[scr<D>(row, lane * EPL + e)] = o[g][e];
+      }
       if (lane == 0) {
         sm[cw * QS + g] = m[g];
         sl[cw * QS + g] = ls;
@@ -660,18 +698,22 @@ __device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1
 //   B regs: (rows 2tq..+1, col gq), (rows 2tq+8..+9, col gq)
 //   C regs: (row gq, cols 2tq, 2tq+1), (row gq+8, cols 2tq, 2tq+1)
 // Scores S^T = K Q^T: M = slice token (row r is token r), N = query, K = head_dim.
-//   The head_dim order is permuted so that lane tq reads contiguous 16-byte
-//   chunks {tq, tq+4, ...} of a row: local element e of lane tq is column
-//   (tq + 4 * (e / CE)) * CE + e % CE, and k-step kk uses local e = 4kk..4kk+3.
+//   The head_dim order is permuted so that lane tq reads whole 16-byte chunks
+//   kchunk(tq, j) of a row: local element e of lane tq is column
+//   kchunk(tq, e / CE) * CE + e % CE, and k-step kk uses local e = 4kk..4kk+3.
 // Output O^T = V^T P^T: M = head_dim, N = query, K = slice token.
 //   Token order of the K dimension: k = 2tq -> token 2tq, 2tq+1 -> 2tq+8,
 //   2tq+8 -> 2tq+1, 2tq+9 -> 2tq+9, which makes each B register of P^T a pair
 //   of scores one lane already holds (C rows gq and gq+8).
-//   Head_dim order of the M dimension: lane gq owns columns
-//   [gq*DPL, gq*DPL + DPL); m-tile mi row gq -> gq*DPL + mi, row gq+8 ->
-//   gq*DPL + MTILES + mi.
+//   Head_dim order of the M dimension: lane gq owns DPL columns, read as the
+//   16-byte chunks gq, gq+8, ... of a row (or 8 bytes at 8*gq when a row is
+//   64 bytes); local column c maps to head_dim column vcol(gq, c); m-tile mi
+//   uses local columns mi (row gq) and MTILES + mi (row gq+8).
+//   These orders make every read of the swizzled stage conflict-free except
+//   for 256-byte rows, where the V reads are 2-way.
 template <int KV, int QT, int D, int G, int QM>
 struct MmaState {
+  static constexpr bool SW = swizzled<KV, D, G>();
   static constexpr bool KV8 = is_fp8(KV);
   static constexpr int MT = KV8 ? kF16 : KV;  // mma input type
   static constexpr int ELT = elt_bytes(KV);
@@ -688,27 +730,53 @@ struct MmaState {
   float m2[2], l2[2];
   float qk_mult;
 
-  __device__ __forceinline__ static int kcol(int tq, int e) { return (tq + 4 * (e / CE)) * CE + e % CE; }
+  // 16-byte chunk j of a K row read by lane tq: contiguous chunks on the
+  // swizzled layout, chunks tq, tq+4, ... on the linear one (fewest bank
+  // conflicts for each)
+  __device__ __forceinline__ static int kchunk(int tq, int j) { return SW ? LCH * tq + j : tq + 4 * j; }
+  __device__ __forceinline__ static int kcol(int tq, int e) { return kchunk(tq, e / CE) * CE + e % CE; }
+  // head_dim column of the lane's local V column c
+  __device__ __forceinline__ static int vcol(int gq, int c) {
+    if constexpr (DPL * ELT >= 16) {
+      return (gq + 8 * (c / CE)) * CE + c % CE;
+    } else {
+      return gq * DPL + c;
+    }
+  }
 
   // q rows [ncols][D] in shared memory: the query heads of the group, for
-  // each sequence that shares the item's blocks; columns >= ncols are zero
+  // each sequence that shares the item's blocks; columns >= ncols are zero.
+  // Lane (gq, tq) needs row gq's local elements 0..D/4-1: chunk j of them
+  // is the CE columns at kchunk(tq, j) * CE, read with 16-byte loads.
   __device__ __forceinline__ void start(const uint8_t *qs, float qk_scale, int ncols) {
     const int lane = threadIdx.x & 31;
     const int gq = lane >> 2, tq = lane & 3;
     const bool real = gq < ncols;
-    const uint16_t *qrow = reinterpret_cast<const uint16_t *>(qs) + static_cast<size_t>(real ? gq : 0) * D;
+    constexpr int QW = D / 8;  // 32-bit words of q the lane holds (two elements each)
+    uint32_t qw[QW];
+    const uint8_t *qrow = qs + static_cast<size_t>(real ? gq : 0) * D * 2;
+#pragma unroll
+    for (int j = 0; j < LCH; ++j) {
+#pragma unroll
+      for (int h = 0; h < CE / 8; ++h) {  // CE q elements = CE * 2 bytes
+        const uint4 v = real ? lds128(qrow + kchunk(tq, j) * CE * 2 + 16 * h) : make_uint4(0u, 0u, 0u, 0u);
+        const int w0 = j * (CE / 2) + 4 * h;
+        qw[w0] = v.x;
+        qw[w0 + 1] = v.y;
+        qw[w0 + 2] = v.z;
+        qw[w0 + 3] = v.w;
+      }
+    }
     float f = 1.f;
     if constexpr (KV8 && QT == kBF16) {
       // fp16 operands: scale q by a power of two so the group's largest
       // entry fits fp16's range; the factor is undone on the scores.
       float amax = 0.f;
 #pragma unroll
-      for (int kk = 0; kk < KSTEPS; ++kk)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float v = __bfloat162float(__ushort_as_bfloat16(qrow[kcol(tq, 4 * kk + e)]));
-          amax = fmaxf(amax, fabsf(real ? v : 0.f));
-        }
+      for (int w = 0; w < QW; ++w) {
+        const float2 x = half2_bits_to_float2<kBF16>(qw[w]);
+        amax = fmaxf(amax, fmaxf(fabsf(x.x), fabsf(x.y)));
+      }
 #pragma unroll
       for (int o2 = 1; o2 < 32; o2 <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o2));
       if (amax > 16384.f) {
@@ -716,24 +784,18 @@ struct MmaState {
         frexpf(amax, &ex);
         f = ldexpf(1.f, 14 - ex);
       }
+#pragma unroll
+      for (int w = 0; w < QW; ++w) {
+        const float2 x = half2_bits_to_float2<kBF16>(qw[w]);
+        qw[w] = pack2_rn<kF16>(x.x * f, x.y * f);
+      }
     }
+    // k-step kk uses local elements 4kk..4kk+3: words 2kk (cols 2tq, 2tq+1)
+    // and 2kk + 1 (cols 2tq+8, 2tq+9)
 #pragma unroll
     for (int kk = 0; kk < KSTEPS; ++kk) {
-#pragma unroll
-      for (int r = 0; r < 2; ++r) {
-        const int d0 = kcol(tq, 4 * kk + 2 * r);  // d0 + 1 is the next column
-        uint32_t w = 0;
-        if (real) {
-          if constexpr (KV8 && QT == kBF16) {
-            const float a = __bfloat162float(__ushort_as_bfloat16(qrow[d0])) * f;
-            const float b = __bfloat162float(__ushort_as_bfloat16(qrow[d0 + 1])) * f;
-            w = pack2_rn<kF16>(a, b);
-          } else {
-            w = *reinterpret_cast<const uint32_t *>(qrow + d0);
-          }
-        }
-        qb[kk][r] = w;
-      }
+      qb[kk][0] = qw[2 * kk];
+      qb[kk][1] = qw[2 * kk + 1];
     }
     qk_mult = qk_scale / f;
 #pragma unroll
@@ -779,15 +841,15 @@ struct MmaState {
     fp8x4_to_half2x2<KV>(two, lo, hi);
   }
 
-  __device__ __forceinline__ void slice(const uint8_t *Ks, const uint8_t *Vs, int n, float v_scale) {
+  __device__ __forceinline__ void slice(const uint8_t *Kb, const uint8_t *Vb, int row0, int n, float v_scale) {
     const int lane = threadIdx.x & 31;
     const int gq = lane >> 2, tq = lane & 3;
     // ---- S^T = K Q^T ----
     uint4 k0[LCH], k1[LCH];
 #pragma unroll
     for (int j = 0; j < LCH; ++j) {
-      k0[j] = lds128(Ks + gq * ROWB + (tq + 4 * j) * 16);
-      k1[j] = lds128(Ks + (gq + 8) * ROWB + (tq + 4 * j) * 16);
+      k0[j] = lds128(Kb + swz<SW>((row0 + gq) * ROWB + kchunk(tq, j) * 16));
+      k1[j] = lds128(Kb + swz<SW>((row0 + gq + 8) * ROWB + kchunk(tq, j) * 16));
     }
     // four independent accumulators so the k-steps do not form one chain
     float sacc[4][4];
@@ -854,18 +916,30 @@ struct MmaState {
     // ---- O^T += V^T P^T ----
     constexpr int VW = DPL * ELT / 4;  // 32-bit words of a row the lane reads
     uint32_t r0[VW], r1[VW], r2[VW], r3[VW];
-    const uint8_t *vb = Vs + gq * DPL * ELT;
     const int t0 = 2 * tq, t1 = 2 * tq + 8, t2 = 2 * tq + 1, t3 = 2 * tq + 9;
+    if constexpr (VW >= 4) {  // whole 16-byte chunks gq, gq + 8, ...
 #pragma unroll
-    for (int w = 0; w < VW; w += 2) {
-      const uint2 a = *reinterpret_cast<const uint2 *>(vb + t0 * ROWB + w * 4);
-      const uint2 b = *reinterpret_cast<const uint2 *>(vb + t1 * ROWB + w * 4);
-      const uint2 c = *reinterpret_cast<const uint2 *>(vb + t2 * ROWB + w * 4);
-      const uint2 d = *reinterpret_cast<const uint2 *>(vb + t3 * ROWB + w * 4);
-      r0[w] = a.x; r0[w + 1] = a.y;
-      r1[w] = b.x; r1[w + 1] = b.y;
-      r2[w] = c.x; r2[w + 1] = c.y;
-      r3[w] = d.x; r3[w + 1] = d.y;
+      for (int j = 0; j < VW / 4; ++j) {
+        const int cb = (gq + 8 * j) * 16;
+        const uint4 a = lds128(Vb + swz<SW>((row0 + t0) * ROWB + cb));
+        const uint4 b = lds128(Vb + swz<SW>((row0 + t1) * ROWB + cb));
+        const uint4 c = lds128(Vb + swz<SW>((row0 + t2) * ROWB + cb));
+        const uint4 d = lds128(Vb + swz<SW>((row0 + t3) * ROWB + cb));
+        r0[4 * j] = a.x; r0[4 * j + 1] = a.y; r0[4 * j + 2] = a.z; r0[4 * j + 3] = a.w;
+        r1[4 * j] = b.x; r1[4 * j + 1] = b.y; r1[4 * j + 2] = b.z; r1[4 * j + 3] = b.w;
+        r2[4 * j] = c.x; r2[4 * j + 1] = c.y; r2[4 * j + 2] = c.z; r2[4 * j + 3] = c.w;
+        r3[4 * j] = d.x; r3[4 * j + 1] = d.y; r3[4 * j + 2] = d.z; r3[4 * j + 3] = d.w;
+      }
+    } else {  // 64-byte rows: 8 bytes at 8 * gq
+      const int cb = gq * 8;
+      const uint2 a = *reinterpret_cast<const uint2 *>(Vb + swz<SW>((row0 + t0) * ROWB + cb));
+      const uint2 b = *reinterpret_cast<const uint2 *>(Vb + swz<SW>((row0 + t1) * ROWB + cb));
+      const uint2 c = *reinterpret_cast<const uint2 *>(Vb + swz<SW>((row0 + t2) * ROWB + cb));
+      const uint2 d = *reinterpret_cast<const uint2 *>(Vb + swz<SW>((row0 + t3) * ROWB + cb));
+      r0[0] = a.x; r0[1] = a.y;
+      r1[0] = b.x; r1[1] = b.y;
+      r2[0] = c.x; r2[1] = c.y;
+      r3[0] = d.x; r3[1] = d.y;
     }
     if (n < 16) {  // stale rows may hold NaN: zero them so 0 * NaN never reaches the sum
 #pragma unroll
@@ -912,17 +986,22 @@ struct MmaState {
       ls1 += __shfl_xor_sync(0xffffffffu, ls1, o2);
     }
     const int qa = 2 * tq, qb2 = 2 * tq + 1;
+    // local column c holds oacc[c][0|1] (c < MTILES) or oacc[c - MTILES][2|3];
+    // runs of four local columns are four consecutive head_dim columns
 #pragma unroll
-    for (int mi = 0; mi < MTILES; ++mi) {
-      const int d0 = gq * DPL + mi, d1 = gq * DPL + MTILES + mi;
-      if (qa < ncols) {
-        so[(static_cast<size_t>(cw) * QS + qa) * D + d0] = oacc[mi][0] * v_scale;
-        so[(static_cast<size_t>(cw) * QS + qa) * D + d1] = oacc[mi][2] * v_scale;
+    for (int c0 = 0; c0 < DPL; c0 += 4) {
+      float va[4], vb[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int c = c0 + u;
+        va[u] = (c < MTILES ? oacc[c % MTILES][0] : oacc[c % MTILES][2]) * v_scale;
+        vb[u] = (c < MTILES ? oacc[c % MTILES][1] : oacc[c % MTILES][3]) * v_scale;
       }
-      if (qb2 < ncols) {
-        so[(static_cast<size_t>(cw) * QS + qb2) * D + d0] = oacc[mi][1] * v_scale;
-        so[(static_cast<size_t>(cw) * QS + qb2) * D + d1] = oacc[mi][3] * v_scale;
-      }
+      const int d = vcol(gq, c0);
+      if (qa < ncols)
+        *reinterpret_cast<float4 *>(so + scr<D>(cw * QS + qa, d)) = make_float4(va[0], va[1], va[2], va[3]);
+      if (qb2 < ncols)
+        *reinterpret_cast<float4 *>(so + scr<D>(cw * QS + qb2, d)) = make_float4(vb[0], vb[1], vb[2], vb[3]);
     }
     if (gq == 0) {
       if (qa < ncols) {
@@ -983,7 +1062,7 @@ __device__ __forceinline__ void combine_item(const DecodeParams &p, const StageI
 #pragma unroll
     for (int c = 0; c < kConsumerWarps; ++c) {
       const float wc = sm[c * QM + j];
-      const float2 oc = *reinterpret_cast<const float2 *>(so + (static_cast<size_t>(c) * QM + j) * D + dd);
+      const float2 oc = *reinterpret_cast<const float2 *>(so + scr<D>(c * QM + j, dd));
       a0 = fmaf(wc, oc.x, a0);
       a1 = fmaf(wc, oc.y, a1);
     }
@@ -1008,7 +1087,6 @@ template <int KV, int QT, int D, int G, int QM, class State>
 __device__ __forceinline__ bool run_item(const DecodeParams &p, SmemHeader &hdr, uint8_t *stages, float *so,
                                          float *sm, float *sl, int cw, int &stage, uint32_t &phase,
                                          int &ncomb, StageInfo inf, const volatile int *abort) {
-  constexpr int ROWB = D * elt_bytes(KV);
   const int lane = threadIdx.x & 31;
   const int ncols = inf.k * G;
   State st;
@@ -1016,7 +1094,7 @@ __device__ __forceinline__ bool run_item(const DecodeParams &p, SmemHeader &hdr,
   while (true) {
     const uint8_t *sb = stages + static_cast<size_t>(stage) * p.stage_bytes;
     const int n = min(16, inf.ntok - 16 * cw);
-    if (n > 0) st.slice(sb + p.k_off + 16 * cw * ROWB, sb + p.v_off + 16 * cw * ROWB, n, p.v_scale);
+    if (n > 0) st.slice(sb + p.k_off, sb + p.v_off, 16 * cw, n, p.v_scale);
     __syncwarp();
     if (lane == 0) mbar_arrive(&hdr.empty[stage]);
     const bool last = (inf.flags & kLast) != 0;
@@ -1050,7 +1128,7 @@ __device__ __forceinline__ bool run_item(const DecodeParams &p, SmemHeader &hdr,
 // MMA: every item runs on the tensor-core path; otherwise items whose tile
 // serves a single query run on the SIMT path and shared items on the MMA one.
 template <int KV, int QT, int D, int G, bool MMA>
-__global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_kernel(const DecodeParams p) {
+__device__ __forceinline__ void decode_body(const DecodeParams &p) {
   constexpr int QM = query_capacity(G);
   extern __shared__ __align__(128) uint8_t smem[];
   SmemHeader &hdr = *reinterpret_cast<SmemHeader *>(smem);
@@ -1065,6 +1143,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_kernel(const Deco
     fence_mbar_init();
   }
   __syncthreads();
+  if ((smem_addr(smem + p.stages_off) & 1023u) != 0) {  // the swizzle needs 1024-byte atoms
+    if (threadIdx.x == 0) record_error(p.err, kErrSmemAlign);
+    return;
+  }
   // the plan (and every kernel before it: the cache writes) must be complete
   grid_dependency_wait();
   launch_dependents();
@@ -1117,17 +1199,19 @@ struct DecodeSmemPlan {
 };
 
 template <int KV, int D, int G>
-inline DecodeSmemPlan plan_smem(int max_smem) {
+__host__ __device__ constexpr DecodeSmemPlan plan_smem(int max_smem) {
   constexpr int ROWB = D * elt_bytes(KV);
   constexpr int QM = query_capacity(G);
-  DecodeSmemPlan s{};
+  DecodeSmemPlan s{0, 0, 0, 0, 0, 0, 0, 0};
   s.k_off = 0;
   s.v_off = kStageTok * ROWB;
   s.q_off = 2 * kStageTok * ROWB;
-  s.stage_bytes = (s.q_off + QM * D * 2 + 127) / 128 * 128;
+  // stages and their K / V regions start on 1024-byte boundaries (the
+  // swizzle atom of the tensor copies)
+  s.stage_bytes = (s.q_off + QM * D * 2 + 1023) / 1024 * 1024;
   s.scratch_off = (static_cast<int>(sizeof(SmemHeader)) + 127) / 128 * 128;
   const int scratch = kConsumerWarps * (QM * D + 2 * QM) * 4;
-  s.stages_off = (s.scratch_off + scratch + 127) / 128 * 128;
+  s.stages_off = (s.scratch_off + scratch + 1023) / 1024 * 1024;
   int ns = (max_smem - s.stages_off) / s.stage_bytes;
   if (ns > kMaxStages) ns = kMaxStages;
   s.num_stages = ns;
@@ -1135,21 +1219,51 @@ inline DecodeSmemPlan plan_smem(int max_smem) {
   return s;
 }
 
+// Resident CTAs per SM for a shared-memory budget: as many (up to kCtasPerSm)
+// as leave each at least two pipeline stages; the hardware reserves 1 KB per
+// resident CTA.
+template <int KV, int D, int G>
+__host__ __device__ constexpr int resident_ctas(int smem_per_sm, int smem_optin) {
+  for (int ctas = kCtasPerSm; ctas >= 1; --ctas) {
+    int budget = smem_optin;
+    if (ctas > 1 && smem_per_sm / ctas - 1024 < budget) budget = smem_per_sm / ctas - 1024;
+    if (plan_smem<KV, D, G>(budget).num_stages >= 2) return ctas;
+  }
+  return 0;
+}
+
+template <int KV, int D, int G>
+__host__ __device__ constexpr int kernel_regs() {
+  return regs_for_ctas(resident_ctas<KV, D, G>(kSmemPerSm, kSmemOptin) > 0
+                           ? resident_ctas<KV, D, G>(kSmemPerSm, kSmemOptin)
+                           : 1);
+}
+
+// The tiled TMA reads the tensor maps from the kernel's parameter space, so
+// the swizzled kernels take their parameters as grid constants; the others
+// take them by value.
+template <int KV, int QT, int D, int G, bool MMA>
+__global__ void __maxnreg__((kernel_regs<KV, D, G>())) decode_kernel_tma(const __grid_constant__ DecodeParams p) {
+  decode_body<KV, QT, D, G, MMA>(p);
+}
+
+template <int KV, int QT, int D, int G, bool MMA>
+__global__ void __maxnreg__((kernel_regs<KV, D, G>())) decode_kernel(const DecodeParams p) {
+  decode_body<KV, QT, D, G, MMA>(p);
+}
+
+
+
+
 // ----------------------------------------------------------------------------
 // host launch of one instantiation: plan, persistent decode, merge
 // ----------------------------------------------------------------------------
 template <int KV, int QT, int D, int G, bool MMA>
 pa_status launch_decode(DecodeParams p, const DeviceInfo &dev, cudaStream_t stream) {
-  // As many resident CTAs per SM (up to kCtasPerSm) as leave each of them at
-  // least two pipeline stages; the hardware reserves 1 KB per resident CTA.
-  DecodeSmemPlan sp{};
-  int ctas = kCtasPerSm;
-  for (; ctas >= 1; --ctas) {
-    int budget = dev.max_smem_optin;
-    if (ctas > 1) budget = min(budget, dev.smem_per_sm / ctas - 1024);
-    sp = plan_smem<KV, D, G>(budget);
-    if (sp.num_stages >= 2) break;
-  }
+  const int ctas = resident_ctas<KV, D, G>(dev.smem_per_sm, dev.max_smem_optin);
+  int budget = dev.max_smem_optin;
+  if (ctas > 1) budget = min(budget, dev.smem_per_sm / ctas - 1024);
+  const DecodeSmemPlan sp = plan_smem<KV, D, G>(budget);
   if (ctas < 1 || sp.num_stages < 2) return PA_ERR_UNSUPPORTED;
   p.num_stages = sp.num_stages;
   p.stage_bytes = sp.stage_bytes;
@@ -1159,7 +1273,12 @@ pa_status launch_decode(DecodeParams p, const DeviceInfo &dev, cudaStream_t stre
   p.scratch_off = sp.scratch_off;
   p.stages_off = sp.stages_off;
   p.kmax = query_capacity(G) / G;
-  auto kern = decode_kernel<KV, QT, D, G, MMA>;
+  void (*kern)(DecodeParams);
+  if constexpr (swizzled<KV, D, G>()) {
+    kern = decode_kernel_tma<KV, QT, D, G, MMA>;
+  } else {
+    kern = decode_kernel<KV, QT, D, G, MMA>;
+  }
   static int configured_bytes[64];  // per device: dynamic smem already allowed
   int dev_id = 0;
   cudaError_t e = cudaGetDevice(&dev_id);

@@ -1,6 +1,9 @@
 // Host entry points of the decode path: argument checks, partition choice,
 // workspace layout, dispatch by cache dtype.
+#include <cudaTypedefs.h>
 #include <math.h>
+
+#include <mutex>
 
 #include "pa_decode_params.h"
 
@@ -44,6 +47,51 @@ bool layout_for(int num_seqs, int num_q_heads, int kv_heads, int head_dim, int m
   w.total = align256(w.o_off + units * num_q_heads * head_dim * sizeof(float));
   *out = w;
   return true;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  return fn;
+}
+
+// Tiled view of a cache as rows of head_dim elements, one row per (block,
+// head, token slot): 2-D [rows, 128 B] when a row is 128 bytes, 3-D
+// [rows, 2, 128 B] when it is 256 bytes; the box is one (block, head) tile
+// of block_size rows, written to shared memory with the 128-byte swizzle.
+bool encode_cache_map(CUtensorMap *map, const void *cache, const pa_cache_desc *c) {
+  const int elt = (c->dtype == PA_FP8_E4M3 || c->dtype == PA_FP8_E5M2) ? 1 : 2;
+  const int rowb = c->head_dim * elt;
+  if (rowb < 128) return true;  // 64-byte rows use plain bulk copies
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (enc == nullptr) return false;
+  const CUtensorMapDataType dt = elt == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_UINT16;
+  const cuuint64_t rows = static_cast<cuuint64_t>(c->num_blocks) * c->kv_heads * c->block_size;
+  const cuuint32_t inner = 128 / elt;  // elements in 128 bytes
+  const cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r;
+  if (rowb == 128) {
+    const cuuint64_t dims[2] = {inner, rows};
+    const cuuint64_t strides[1] = {128};
+    const cuuint32_t box[2] = {inner, static_cast<cuuint32_t>(c->block_size)};
+    r = enc(map, dt, 2, const_cast<void *>(cache), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  } else {
+    const cuuint64_t dims[3] = {inner, 2, rows};
+    const cuuint64_t strides[2] = {128, 256};
+    const cuuint32_t box[3] = {inner, 2, static_cast<cuuint32_t>(c->block_size)};
+    r = enc(map, dt, 3, const_cast<void *>(cache), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  }
+  return r == CUDA_SUCCESS;
 }
 
 }  // namespace
@@ -128,6 +176,10 @@ extern "C" pa_status pa_decode(void *out, const void *q, int32_t q_dtype, int32_
   p.part_ml = reinterpret_cast<float2 *>(ws + w.ml_off);
   p.part_o = reinterpret_cast<float *>(ws + w.o_off);
   p.err = device_error;
+
+  if (G >= 2 && (!encode_cache_map(&p.tmap_k, k_cache, cache) ||
+                 !encode_cache_map(&p.tmap_v, v_cache, cache)))  // tiled views for the swizzled kernels
+    return cuda_fail(cudaErrorInvalidValue);
 
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   switch (cache->dtype) {

@@ -1,6 +1,7 @@
 // Parameters shared by the decode kernels and the host entry point.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -19,6 +20,22 @@ constexpr int kMaxPartition = 1024;
 #define PA_DECODE_CTAS_PER_SM 3
 #endif
 constexpr int kCtasPerSm = PA_DECODE_CTAS_PER_SM;  // resident decode CTAs per SM
+// Registers per thread that still let kCtasPerSm CTAs of kThreads reside on
+// one SM.  The 64K-entry register file is split between the SM's four
+// sub-partitions and a warp takes all its registers from one of them, so the
+// sub-partition holding the most warps, ceil(warps / 4), sets the limit
+// (registers are allocated in units of 8 per thread).
+constexpr int regs_for_ctas(int ctas) {
+  return (16384 / (((ctas * (kThreads / 32) + 3) / 4) * 32)) / 8 * 8 > 255
+             ? 255
+             : (16384 / (((ctas * (kThreads / 32) + 3) / 4) * 32)) / 8 * 8;
+}
+constexpr int kMaxRegs = regs_for_ctas(kCtasPerSm);
+// Shared memory of the GB300 (sm_103a) SM, used to plan each kernel's
+// resident CTAs (and so its register budget) at compile time; the launch
+// re-plans from the device's own figures.
+constexpr int kSmemPerSm = 233472;
+constexpr int kSmemOptin = 232448;
 
 enum StageFlags : int { kFirst = 1, kLast = 2, kEnd = 4 };
 
@@ -41,6 +58,9 @@ struct SmemHeader {
 };
 
 struct DecodeParams {
+  // tiled views of the caches for the TMA (unused when a row is < 128 bytes)
+  CUtensorMap tmap_k;
+  CUtensorMap tmap_v;
   void *out;
   const uint8_t *q;
   const uint8_t *k_cache;
