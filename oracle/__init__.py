@@ -14,6 +14,8 @@ allocator   Block pool with FIFO free list and reference counts, block tables,
             slot mapping, copy-on-write decisions.
 fp8         OCP 8-bit floating point (E4M3 / E5M2) encode and decode, written
             from the format definition (sign, biased exponent, mantissa).
+int8        Symmetric int8 KV codes (round half to even, saturate), the
+            integer one-byte format the pages name beside FP8.
 cache       Host paged KV cache: the cache write through a slot mapping and
             the whole-block copy used by copy-on-write.
 attention   Single-query decode attention over the paged cache in float64.
@@ -29,4 +31,4 @@ Every function here is pinned by ``-m "not gpu"`` tests in ``tests/`` to
 values the pages print, closed forms, library routines or brute force.
 """
 
-from . import allocator, attention, cache, fp8  # noqa: F401
+from . import allocator, attention, cache, fp8, int8  # noqa: F401

@@ -26,12 +26,13 @@ from __future__ import annotations
 
 import numpy as np
 
-from .cache import values
+from .cache import head_scale, values
 
 
 def gather(codes: np.ndarray, dtype: str, scale: float, table_row, length: int,
            kv_head: int, block_size: int) -> np.ndarray:
-    """[length, head_dim] float64 rows of one KV head of one sequence."""
+    """[length, head_dim] float64 rows of one KV head of one sequence
+    (``scale``: that head's scale)."""
     pos = np.arange(length)
     blocks = np.asarray(table_row, dtype=np.int64)[pos // block_size]
     return values(codes[blocks, kv_head, pos % block_size, :], dtype, scale)
@@ -49,13 +50,13 @@ def attend(q: np.ndarray, K: np.ndarray, V: np.ndarray, scale: float) -> np.ndar
 
 def paged_decode(q: np.ndarray, k_codes: np.ndarray, v_codes: np.ndarray,
                  dtype: str, block_tables, seq_lens, scale: float,
-                 k_scale: float = 1.0, v_scale: float = 1.0,
-                 rows=None) -> np.ndarray:
+                 k_scale=1.0, v_scale=1.0, rows=None) -> np.ndarray:
     """Decode attention for every (s, hq), or only for the (s, hq) in ``rows``.
 
     q: [S, Hq, d] float64 query values; k_codes/v_codes: the cache codes
-    [num_blocks, Hkv, block_size, d].  Returns float64 [S, Hq, d] (rows not
-    requested are left as NaN).
+    [num_blocks, Hkv, block_size, d]; k_scale / v_scale: one number, or one
+    per KV head ([P3] §6.3).  Returns float64 [S, Hq, d] (rows not requested
+    are left as NaN).
     """
     S, Hq, d = q.shape
     Hkv, bs = k_codes.shape[1], k_codes.shape[2]
@@ -71,7 +72,7 @@ def paged_decode(q: np.ndarray, k_codes: np.ndarray, v_codes: np.ndarray,
                      if wanted is None or (s, h * G + g) in wanted]
             if not heads:
                 continue
-            K = gather(k_codes, dtype, k_scale, block_tables[s], L, h, bs)
-            V = gather(v_codes, dtype, v_scale, block_tables[s], L, h, bs)
+            K = gather(k_codes, dtype, head_scale(k_scale, h), block_tables[s], L, h, bs)
+            V = gather(v_codes, dtype, head_scale(v_scale, h), block_tables[s], L, h, bs)
             out[s, heads] = attend(q[s, heads], K, V, scale)
     return out

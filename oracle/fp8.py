@@ -137,7 +137,7 @@ def quantize(values_f32: np.ndarray, scale: float, fmt_name: str) -> np.ndarray:
     return out.reshape(q.shape)
 
 
-def _bits16_to_f32(bits: np.ndarray, src_dtype: str) -> np.ndarray:
+def bits16_to_f32(bits: np.ndarray, src_dtype: str) -> np.ndarray:
     b = np.asarray(bits, dtype=np.uint16)
     if src_dtype == "f16":
         return b.view(np.float16).astype(np.float32)
@@ -146,12 +146,12 @@ def _bits16_to_f32(bits: np.ndarray, src_dtype: str) -> np.ndarray:
     raise ValueError(src_dtype)
 
 
-@lru_cache(maxsize=16)
+@lru_cache(maxsize=64)
 def _table16(src_dtype: str, scale: float, fmt_name: str) -> np.ndarray:
     """Code of every 16-bit source pattern (same rule as ``quantize``)."""
     allbits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
     with np.errstate(invalid="ignore", over="ignore"):   # NaN / inf patterns included
-        return quantize(_bits16_to_f32(allbits, src_dtype), scale, fmt_name)
+        return quantize(bits16_to_f32(allbits, src_dtype), scale, fmt_name)
 
 
 def quantize_bits16(bits: np.ndarray, src_dtype: str, scale: float, fmt_name: str) -> np.ndarray:

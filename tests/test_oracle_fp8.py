@@ -104,7 +104,7 @@ def test_quantize_divides_by_scale_in_float32():
 def test_table_quantizer_equals_direct(src, name):
     rng = np.random.default_rng(3)
     bits = rng.integers(0, 65536, 4000).astype(np.uint16)
-    vals = fp8._bits16_to_f32(bits, src)
+    vals = fp8.bits16_to_f32(bits, src)
     keep = np.isfinite(vals)
     for scale in (1.0, 0.37, 3.5):
         a = fp8.quantize_bits16(bits[keep], src, scale, name)

@@ -81,8 +81,27 @@ CONFIGS: Dict[str, dict] = {
         Hq=64, Hkv=8, d=128, bs=16, pool_factor=1.25, cache_dtype="e4m3",
         q_dtype="bf16", src_dtype="bf16", k_scale=1.0, v_scale=1.0,
         partition_size=512, layers_of_model=80),
+    # The gqa-fp8 shapes with an int8 cache and one scale per KV head: 127
+    # codes span about 5 standard deviations of the N(0, 1) values, a little
+    # more for each further head.
+    "gqa-int8": dict(
+        kind="independent", S=128, len_lo=256, len_hi=32768, log_uniform=True,
+        Hq=64, Hkv=8, d=128, bs=16, pool_factor=1.25, cache_dtype="int8",
+        q_dtype="bf16", src_dtype="bf16",
+        k_scale=tuple(0.04 + 0.0025 * h for h in range(8)),
+        v_scale=tuple(0.045 - 0.0025 * h for h in range(8)),
+        partition_size=512, layers_of_model=80),
 }
 CONFIG_ORDER = ["tiny", "llama2-7b", "qwen3-prefix", "opt13b-beam", "gqa-fp8"]
+EXTRA_CONFIGS = ["gqa-int8"]
+BYTE_DTYPES = ("e4m3", "e5m2", "int8")
+
+
+def _scale(x):
+    """A scale as given: one number, or a tuple of one per KV head."""
+    if np.ndim(x) == 0:
+        return float(x)
+    return tuple(float(v) for v in x)
 
 
 @dataclass
@@ -98,8 +117,8 @@ class Workload:
     q_dtype: str
     src_dtype: str
     scale: float
-    k_scale: float
-    v_scale: float
+    k_scale: object               # float, or a tuple of one per KV head
+    v_scale: object
     partition_size: int
     seq_lens: np.ndarray          # int32 [S]
     block_tables: np.ndarray      # int32 [S, width]
@@ -128,7 +147,7 @@ class Workload:
 
     # -- byte counts for the measurement ---------------------------------
     def elt_bytes(self) -> int:
-        return 1 if self.cache_dtype in ("e4m3", "e5m2") else 2
+        return 1 if self.cache_dtype in BYTE_DTYPES else 2
 
     def kv_logical_bytes(self) -> int:
         """Bytes of K and V the definition reads: sum_s L_s * Hkv * d * elt * 2."""
@@ -304,7 +323,7 @@ def make_workload(name: Optional[str], seed: int, device: str = "cpu",
         num_blocks=st["num_blocks"], cache_dtype=cache_dtype,
         q_dtype=cfg["q_dtype"], src_dtype=src_dtype,
         scale=float(cfg.get("scale") or 1.0 / math.sqrt(d)),
-        k_scale=float(cfg.get("k_scale", 1.0)), v_scale=float(cfg.get("v_scale", 1.0)),
+        k_scale=_scale(cfg.get("k_scale", 1.0)), v_scale=_scale(cfg.get("v_scale", 1.0)),
         partition_size=int(cfg.get("partition_size", 0)),
         seq_lens=st["seq_lens"], block_tables=st["block_tables"],
         pool_order=st["pool_order"], ctx_slots=st["ctx_slots"],
@@ -333,14 +352,14 @@ def make_workload(name: Optional[str], seed: int, device: str = "cpu",
 def random_case(seed: int, S: int, Hq: int, Hkv: int, d: int, bs: int,
                 cache_dtype: str, q_dtype: str, lens, device: str = "cpu",
                 pool_factor: float = 1.5, scale: Optional[float] = None,
-                k_scale: float = 1.0, v_scale: float = 1.0,
+                k_scale=1.0, v_scale=1.0,
                 partition_size: int = 0) -> Workload:
     """A small independent-sequence workload with the given lengths."""
     cfg = dict(kind="independent", S=S, Hq=Hq, Hkv=Hkv, d=d, bs=bs,
                cache_dtype=cache_dtype, q_dtype=q_dtype, pool_factor=pool_factor,
                scale=scale, k_scale=k_scale, v_scale=v_scale,
                partition_size=partition_size)
-    if cache_dtype in ("e4m3", "e5m2"):
+    if cache_dtype in BYTE_DTYPES:
         cfg["src_dtype"] = q_dtype
     return make_workload(None, seed, device=device, overrides=cfg, lens=lens)
 
