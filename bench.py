@@ -50,7 +50,7 @@ def parse():
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--config", default=DEFAULT_CONFIG, choices=W.CONFIG_ORDER)
+    ap.add_argument("--config", default=DEFAULT_CONFIG, choices=W.ALL_CONFIGS)
     ap.add_argument("--seed", type=int, default=None)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args()
@@ -159,17 +159,21 @@ def run_ours(args, rank, world, local):
         dist.init_process_group("nccl", device_id=torch.device(f"cuda:{local}"))
     torch.cuda.set_device(local)
     dev = f"cuda:{local}"
-    seed = args.seed if args.seed is not None else W.CONFIG_ORDER.index(args.config) + 1
+    seed = args.seed if args.seed is not None else W.config_seed(args.config)
     w = W.make_workload(args.config, seed, device=dev)
     shape = (w.num_blocks, w.Hkv, w.bs, w.d)
-    if w.cache_dtype in ("e4m3", "e5m2"):
+    if w.cache_dtype in W.BYTE_DTYPES:
         kc = torch.zeros(shape, dtype=torch.uint8, device=dev)
         vc = torch.zeros(shape, dtype=torch.uint8, device=dev)
     else:
         dt = torch.float16 if w.cache_dtype == "f16" else torch.bfloat16
         kc = torch.zeros(shape, dtype=dt, device=dev)
         vc = torch.zeros(shape, dtype=dt, device=dev)
-    kw = dict(cache_dtype=w.cache_dtype, k_scale=w.k_scale, v_scale=w.v_scale)
+
+    def scale_arg(x):   # a number, or one float32 scale per KV head on the device
+        return float(x) if np.ndim(x) == 0 else torch.tensor(x, dtype=torch.float32, device=dev)
+
+    kw = dict(cache_dtype=w.cache_dtype, k_scale=scale_arg(w.k_scale), v_scale=scale_arg(w.v_scale))
     err = torch.zeros(1, dtype=torch.int32, device=dev)
     pa.pa_reshape_and_cache(w.ctx_k, w.ctx_v, torch.from_numpy(w.ctx_slots).to(dev), kc, vc,
                             device_error=err, **kw)
@@ -337,7 +341,8 @@ def _auto_partition(w):
 def _describe(w):
     lens = w.seq_lens
     return (f"{w.S} seqs, L {int(lens.min())}..{int(lens.max())} (mean {float(lens.mean()):.0f}), "
-            f"{w.Hq}q/{w.Hkv}kv heads, d {w.d}, bs {w.bs}, {w.cache_dtype} KV, {w.num_blocks} blocks")
+            f"{w.Hq}q/{w.Hkv}kv heads, d {w.d}, bs {w.bs}, {w.cache_dtype} KV"
+            f"{', per-head scales' if np.ndim(w.k_scale) else ''}, {w.num_blocks} blocks")
 
 
 # ---------------------------------------------------------------------------
@@ -392,7 +397,7 @@ def _cores() -> int:
 def run_reference(args, rank, world):
     if rank != 0:
         return
-    seed = args.seed if args.seed is not None else W.CONFIG_ORDER.index(args.config) + 1
+    seed = args.seed if args.seed is not None else W.config_seed(args.config)
     from oracle import attention as A
     w, c, tables, lens, qv, kv = _oracle_sample(args.config, seed, 2)
     for _ in range(args.warmup):

@@ -5,7 +5,7 @@
  *
  *   pa_reshape_and_cache  write new tokens' K and V into fixed-size physical
  *                         blocks through a slot mapping (optionally as FP8
- *                         with a per-tensor scale);
+ *                         or INT8 with a scale per tensor or per KV head);
  *   pa_decode             single-query decode attention over the paged cache,
  *                         reached through per-sequence block tables;
  *   pa_copy_blocks        whole-block copies, the copy step of copy-on-write.
@@ -20,9 +20,10 @@
  *        §2.2 (block table per request, blocks from a global pool), §三
  *        (refcounted block manager).
  *   [P3] m.lsln.cn/news/213354 (KV-cache memory article; title not
- *        preserved) §3.2 (paging), §4.3 (reference counts), §6.1–§6.3 (FP8:
- *        store value / scale, read back × scale; e4m3 and e5m2; default
- *        scale 1.0, per tensor).
+ *        preserved) §3.2 (paging), §4.3 (reference counts), §6 (FP8 or INT8
+ *        halve the cache), §6.1–§6.3 (store value / scale, read back
+ *        × scale; e4m3 and e5m2; default scale 1.0 per tensor, optionally
+ *        one per attention head).
  *   [P4] "第3章 vLLM架构与显存使用：PagedAttention、KV Cache管理与显存池化技术"
  *        §3.2 (block life cycle, shared blocks), §3.3 (copy-on-write: take a
  *        new block, copy the old one, write the new one).
@@ -81,7 +82,8 @@ typedef enum {
   PA_F16 = 0,       /* IEEE binary16 */
   PA_BF16 = 1,      /* bfloat16 */
   PA_FP8_E4M3 = 2,  /* OCP E4M3 (max 448, no inf), one byte */
-  PA_FP8_E5M2 = 3   /* OCP E5M2 (max 57344), one byte */
+  PA_FP8_E5M2 = 3,  /* OCP E5M2 (max 57344), one byte */
+  PA_INT8 = 4       /* two's-complement int8 code, one byte */
 } pa_dtype;
 
 /*
@@ -89,8 +91,11 @@ typedef enum {
  * Layout of k_cache and v_cache: [num_blocks, kv_heads, block_size, head_dim]
  * elements of `dtype`, row-major.  Physical block b holds block_size token
  * slots of every KV head; flat slot = b * block_size + offset.
- * For FP8 caches a stored code c means c * k_scale (K) or c * v_scale (V):
- * values are stored as value / scale ([P3] §6.1; default 1.0, §6.3).
+ * For the one-byte caches (FP8, INT8) a stored code c of KV head h means
+ * c * sk(h) in K and c * sv(h) in V: values are stored as value / scale
+ * ([P3] §6.1; default 1.0 per tensor, one per head optionally, §6.3).
+ * sk(h) is k_head_scales[h] when that pointer is not NULL, else k_scale
+ * (likewise for V).
  * Supported set: block_size in {8, 16, 32}; head_dim in {64, 128}.
  */
 typedef struct {
@@ -99,8 +104,14 @@ typedef struct {
   int32_t block_size;
   int32_t head_dim;
   int32_t dtype;     /* pa_dtype */
-  float k_scale;     /* FP8 only; must be > 0 and finite */
+  float k_scale;     /* one-byte caches only; must be > 0 and finite */
   float v_scale;
+  /* One-byte caches only, else must be NULL: DEVICE float32 [kv_heads],
+   * one scale per KV head (each > 0 and finite; not checked), or NULL for
+   * the per-tensor scales above.  Read by the kernels, so they must stay
+   * valid until the calls that use them have run. */
+  const float *k_head_scales;
+  const float *v_head_scales;
 } pa_cache_desc;
 
 /*
@@ -115,8 +126,11 @@ typedef struct {
  * For every token t with slot >= 0 and every head h:
  *   cache[slot / block_size, h, slot % block_size, :] = enc(row[t, h, :])
  * where enc is a bit copy for 16-bit caches (src_dtype must equal
- * cache->dtype) and, for FP8 caches, round-to-nearest-even with saturation
- * to the largest finite value of (float)x / scale computed in IEEE float32.
+ * cache->dtype); for FP8 caches, round-to-nearest-even with saturation to
+ * the largest finite value of (float)x / scale computed in IEEE float32;
+ * for INT8 caches, the same quotient rounded to the nearest integer (ties
+ * to even) and saturated to [-128, 127], with NaN stored as 0.  The scale
+ * is head h's (see pa_cache_desc).
  * Slots must be distinct among the call's tokens.  A slot >= num_blocks *
  * block_size is skipped and reported as device error 2.
  */
@@ -144,8 +158,8 @@ PA_API size_t pa_decode_workspace_size(int32_t num_seqs, int32_t num_q_heads,
  *   out[s, hq, :] = sum_{i < L_s} softmax_i(scale * <q[s, hq, :], k_i>) v_i
  * where L_s = seq_lens[s] and token i of sequence s is read from physical
  * block block_tables[s, i / block_size] at offset i % block_size
- * ([P1] §2.1, [P2] §2.2, [P3] §3.2; FP8 codes are multiplied by the scales
- * of *cache, [P3] §6.1).  L_s = 0 gives zeros.
+ * ([P1] §2.1, [P2] §2.2, [P3] §3.2; one-byte codes are multiplied by
+ * their head's scales of *cache, [P3] §6.1 and §6.3).  L_s = 0 gives zeros.
  *
  *   out            device [num_seqs, num_q_heads, head_dim], q_dtype.
  *   q              device [num_seqs, num_q_heads, head_dim], q_dtype
@@ -166,7 +180,7 @@ PA_API size_t pa_decode_workspace_size(int32_t num_seqs, int32_t num_q_heads,
  *                  bytes, 256-byte aligned; contents need no initialisation.
  *                  Calls sharing one workspace must be stream-ordered.
  * Supported set: num_q_heads / kv_heads in {1, 2, 4, 8}; cache dtypes of
- * pa_cache_desc; FP8 caches accept q in PA_F16 or PA_BF16.
+ * pa_cache_desc; one-byte caches accept q in PA_F16 or PA_BF16.
  */
 PA_API pa_status pa_decode(void *out, const void *q, int32_t q_dtype,
                     int32_t num_seqs, int32_t num_q_heads,

@@ -23,9 +23,10 @@ import torch
 HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libpa.so")
 
-PA_F16, PA_BF16, PA_FP8_E4M3, PA_FP8_E5M2 = 0, 1, 2, 3
-DTYPE_CODES = {"f16": PA_F16, "bf16": PA_BF16, "e4m3": PA_FP8_E4M3, "e5m2": PA_FP8_E5M2}
-_TORCH_CODES = {torch.float16: PA_F16, torch.bfloat16: PA_BF16}
+PA_F16, PA_BF16, PA_FP8_E4M3, PA_FP8_E5M2, PA_INT8 = 0, 1, 2, 3, 4
+DTYPE_CODES = {"f16": PA_F16, "bf16": PA_BF16, "e4m3": PA_FP8_E4M3, "e5m2": PA_FP8_E5M2,
+               "int8": PA_INT8}
+_TORCH_CODES = {torch.float16: PA_F16, torch.bfloat16: PA_BF16, torch.int8: PA_INT8}
 if hasattr(torch, "float8_e4m3fn"):
     _TORCH_CODES[torch.float8_e4m3fn] = PA_FP8_E4M3
 if hasattr(torch, "float8_e5m2"):
@@ -41,7 +42,8 @@ class PaCacheDesc(ctypes.Structure):
     _fields_ = [("num_blocks", ctypes.c_int32), ("kv_heads", ctypes.c_int32),
                 ("block_size", ctypes.c_int32), ("head_dim", ctypes.c_int32),
                 ("dtype", ctypes.c_int32), ("k_scale", ctypes.c_float),
-                ("v_scale", ctypes.c_float)]
+                ("v_scale", ctypes.c_float), ("k_head_scales", ctypes.c_void_p),
+                ("v_head_scales", ctypes.c_void_p)]
 
 
 class PaError(RuntimeError):
@@ -115,12 +117,29 @@ def _cache_code(k_cache: torch.Tensor, cache_dtype) -> int:
     raise ValueError("cache_dtype is required for a byte-typed FP8 cache")
 
 
-def cache_desc(k_cache: torch.Tensor, cache_dtype=None, k_scale: float = 1.0,
-               v_scale: float = 1.0) -> PaCacheDesc:
+def _scale_arg(scale, kv_heads: int, name: str):
+    """(per-tensor value, per-head device pointer) of a scale argument: a
+    number, or a contiguous float32 CUDA tensor of one scale per KV head."""
+    if isinstance(scale, torch.Tensor):
+        if (not scale.is_cuda or scale.dtype != torch.float32 or not scale.is_contiguous()
+                or scale.numel() != kv_heads):
+            raise ValueError(f"{name}: per-head scales must be a contiguous float32 CUDA "
+                             f"tensor of {kv_heads} elements")
+        return 1.0, scale.data_ptr()
+    return float(scale), None
+
+
+def cache_desc(k_cache: torch.Tensor, cache_dtype=None, k_scale=1.0,
+               v_scale=1.0) -> PaCacheDesc:
+    """Descriptor of a cache pair; k_scale / v_scale are numbers (per tensor)
+    or float32 CUDA tensors [kv_heads] (per head; the tensors must outlive
+    the calls that use the descriptor)."""
     if k_cache.dim() != 4:
         raise ValueError("cache must be [num_blocks, kv_heads, block_size, head_dim]")
     nb, h, bs, d = k_cache.shape
-    return PaCacheDesc(nb, h, bs, d, _cache_code(k_cache, cache_dtype), k_scale, v_scale)
+    ks, kp = _scale_arg(k_scale, h, "k_scale")
+    vs, vp = _scale_arg(v_scale, h, "v_scale")
+    return PaCacheDesc(nb, h, bs, d, _cache_code(k_cache, cache_dtype), ks, vs, kp, vp)
 
 
 def _require(t: torch.Tensor, name: str) -> None:
@@ -129,7 +148,7 @@ def _require(t: torch.Tensor, name: str) -> None:
 
 
 def pa_reshape_and_cache(key, value, slot_mapping, k_cache, v_cache, cache_dtype=None,
-                         k_scale: float = 1.0, v_scale: float = 1.0, device_error=None,
+                         k_scale=1.0, v_scale=1.0, device_error=None,
                          stream=None) -> None:
     """Write rows ``key/value [T, kv_heads, head_dim]`` into the caches."""
     for t, n in ((key, "key"), (value, "value"), (slot_mapping, "slot_mapping"),
@@ -156,7 +175,7 @@ def pa_decode_workspace_size(num_seqs: int, num_q_heads: int, num_kv_heads: int,
 
 
 def pa_decode(out, q, k_cache, v_cache, block_tables, seq_lens, max_seq_len: int,
-              scale: float, cache_dtype=None, k_scale: float = 1.0, v_scale: float = 1.0,
+              scale: float, cache_dtype=None, k_scale=1.0, v_scale=1.0,
               partition_size: int = 0, workspace=None, device_error=None,
               stream=None) -> torch.Tensor:
     """Paged decode attention; writes ``out [S, Hq, head_dim]`` (q's dtype)."""
@@ -185,7 +204,7 @@ def pa_decode(out, q, k_cache, v_cache, block_tables, seq_lens, max_seq_len: int
 
 def pa_decode_static_scratch(out, q, k_cache, v_cache, block_tables, seq_lens,
                              max_seq_len: int, scale: float, cache_dtype=None,
-                             k_scale: float = 1.0, v_scale: float = 1.0,
+                             k_scale=1.0, v_scale=1.0,
                              partition_size: int = 0, device_error=None,
                              stream=None) -> torch.Tensor:
     """``pa_decode`` for callers that cannot allocate device memory.

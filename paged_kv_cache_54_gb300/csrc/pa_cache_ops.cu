@@ -8,13 +8,22 @@
 namespace pa {
 namespace {
 
+// INT8 code of an already-divided value: nearest integer, ties to even,
+// saturated to [-128, 127]; NaN stores 0.
+__device__ __forceinline__ uint32_t int8_code(float y) {
+  if (y != y) return 0u;
+  y = fminf(fmaxf(y, -128.f), 127.f);
+  return static_cast<uint32_t>(__float2int_rn(y)) & 0xFFu;
+}
+
 // Token t, head h, destination chunk c (16 bytes of the cache row).
 template <int SRC, int DST>
 __global__ void __launch_bounds__(256) reshape_and_cache_kernel(
     const uint8_t *__restrict__ key, const uint8_t *__restrict__ value,
     const int64_t *__restrict__ slots, int num_tokens, int kv_heads, int head_dim,
     int block_size, long long num_slots, uint8_t *__restrict__ k_cache,
-    uint8_t *__restrict__ v_cache, float k_scale, float v_scale, int *err) {
+    uint8_t *__restrict__ v_cache, float k_scale, float v_scale,
+    const float *__restrict__ k_head_scales, const float *__restrict__ v_head_scales, int *err) {
   constexpr int DE = elt_bytes(DST);
   constexpr int CE = 16 / DE;  // elements per destination chunk
   const int cpr = head_dim / CE;
@@ -41,11 +50,11 @@ __global__ void __launch_bounds__(256) reshape_and_cache_kernel(
       *reinterpret_cast<uint4 *>(v_cache + dst * 2) =
           __ldg(reinterpret_cast<const uint4 *>(value + src * 2));
     } else {
-      const __nv_fp8_interpretation_t interp = (DST == kE4M3) ? __NV_E4M3 : __NV_E5M2;
 #pragma unroll
       for (int which = 0; which < 2; ++which) {
         const uint8_t *in = (which == 0 ? key : value) + src * 2;
-        const float scale = which == 0 ? k_scale : v_scale;
+        const float *head_scales = which == 0 ? k_head_scales : v_head_scales;
+        const float scale = head_scales != nullptr ? __ldg(head_scales + h) : (which == 0 ? k_scale : v_scale);
         const uint4 a = __ldg(reinterpret_cast<const uint4 *>(in));
         const uint4 b = __ldg(reinterpret_cast<const uint4 *>(in + 16));
         const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
@@ -59,8 +68,13 @@ __global__ void __launch_bounds__(256) reshape_and_cache_kernel(
             // stored = value / scale, in IEEE float32 (division rounded to nearest)
             f.x = __fdiv_rn(f.x, scale);
             f.y = __fdiv_rn(f.y, scale);
-            const __nv_fp8x2_storage_t q = __nv_cvt_float2_to_fp8x2(f, __NV_SATFINITE, interp);
-            packed |= static_cast<uint32_t>(q) << (16 * half);
+            if constexpr (DST == kI8) {
+              packed |= (int8_code(f.x) | (int8_code(f.y) << 8)) << (16 * half);
+            } else {
+              const __nv_fp8_interpretation_t interp = (DST == kE4M3) ? __NV_E4M3 : __NV_E5M2;
+              const __nv_fp8x2_storage_t q = __nv_cvt_float2_to_fp8x2(f, __NV_SATFINITE, interp);
+              packed |= static_cast<uint32_t>(q) << (16 * half);
+            }
           }
           o[k] = packed;
         }
@@ -141,15 +155,18 @@ extern "C" pa_status pa_reshape_and_cache(const void *key, const void *value, in
   reshape_and_cache_kernel<SRC, DST><<<blocks, threads, 0, s>>>(k8, v8, slot_mapping, num_tokens, \
                                                                 H, D, bs, nslots, kc, vc,         \
                                                                 cache->k_scale, cache->v_scale,   \
-                                                                device_error)
+                                                                cache->k_head_scales,             \
+                                                                cache->v_head_scales, device_error)
   if (dst == PA_F16) {
     PA_LAUNCH_RC(kF16, kF16);
   } else if (dst == PA_BF16) {
     PA_LAUNCH_RC(kBF16, kBF16);
   } else if (dst == PA_FP8_E4M3) {
     if (src_dtype == PA_F16) PA_LAUNCH_RC(kF16, kE4M3); else PA_LAUNCH_RC(kBF16, kE4M3);
-  } else {
+  } else if (dst == PA_FP8_E5M2) {
     if (src_dtype == PA_F16) PA_LAUNCH_RC(kF16, kE5M2); else PA_LAUNCH_RC(kBF16, kE5M2);
+  } else {
+    if (src_dtype == PA_F16) PA_LAUNCH_RC(kF16, kI8); else PA_LAUNCH_RC(kBF16, kI8);
   }
 #undef PA_LAUNCH_RC
   const cudaError_t e = cudaGetLastError();

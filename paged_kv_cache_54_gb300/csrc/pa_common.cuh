@@ -11,7 +11,7 @@
 
 namespace pa {
 
-enum DType : int { kF16 = 0, kBF16 = 1, kE4M3 = 2, kE5M2 = 3 };
+enum DType : int { kF16 = 0, kBF16 = 1, kE4M3 = 2, kE5M2 = 3, kI8 = 4 };
 
 enum DevErr : int {
   kErrNone = 0,
@@ -26,8 +26,10 @@ enum DevErr : int {
 // Wait limit for every spin on an mbarrier: 2 s of %globaltimer.
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;
 
-__host__ __device__ constexpr int elt_bytes(int dt) { return (dt == kE4M3 || dt == kE5M2) ? 1 : 2; }
 __host__ __device__ constexpr bool is_fp8(int dt) { return dt == kE4M3 || dt == kE5M2; }
+// one-byte KV codes: FP8 or INT8, each stored as value / scale
+__host__ __device__ constexpr bool is_byte(int dt) { return is_fp8(dt) || dt == kI8; }
+__host__ __device__ constexpr int elt_bytes(int dt) { return is_byte(dt) ? 1 : 2; }
 
 __device__ __forceinline__ void record_error(int *err, int code) {
   if (err != nullptr) atomicCAS(err, 0, code);
@@ -47,35 +49,60 @@ __device__ __forceinline__ float2 half2_bits_to_float2(uint32_t w) {
   }
 }
 
-// two FP8 codes (low byte = first element) -> __half2 bits (exact)
-template <int DT>
-__device__ __forceinline__ uint32_t fp8x2_to_half2_bits(uint32_t two_codes) {
-  __half2_raw r = __nv_cvt_fp8x2_to_halfraw2(
-      static_cast<__nv_fp8x2_storage_t>(two_codes & 0xFFFFu),
-      DT == kE4M3 ? __NV_E4M3 : __NV_E5M2);
-  return static_cast<uint32_t>(r.x) | (static_cast<uint32_t>(r.y) << 16);
+// Four INT8 codes in one word -> two __half2 (codes 0,1 -> lo; 2,3 -> hi),
+// exact.  Flipping the sign bit turns code c into the unsigned u = c + 128;
+// the half with bit pattern 0x6400 | u is 1024 + u (exponent 10, so the ten
+// mantissa bits count units), and subtracting 1152 = 1024 + 128 leaves c.
+__device__ __forceinline__ void i8x4_to_half2x2(uint32_t w, uint32_t &lo, uint32_t &hi) {
+  const uint32_t u = w ^ 0x80808080u;
+  uint32_t a, b;
+  asm("prmt.b32 %0, %1, %2, 0x4140;" : "=r"(a) : "r"(u), "r"(0x64646464u));
+  asm("prmt.b32 %0, %1, %2, 0x4342;" : "=r"(b) : "r"(u), "r"(0x64646464u));
+  const __half2 bias = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));
+  const __half2 x = __hsub2(*reinterpret_cast<const __half2 *>(&a), bias);
+  const __half2 y = __hsub2(*reinterpret_cast<const __half2 *>(&b), bias);
+  lo = *reinterpret_cast<const uint32_t *>(&x);
+  hi = *reinterpret_cast<const uint32_t *>(&y);
 }
 
-// four FP8 codes in one word -> two __half2 (codes 0,1 -> lo; codes 2,3 -> hi),
-// exact: every e4m3 / e5m2 value is an fp16 value
+// two one-byte codes (low byte = first element) -> __half2 bits (exact:
+// every e4m3 / e5m2 value and every int8 is an fp16 value)
 template <int DT>
-__device__ __forceinline__ void fp8x4_to_half2x2(uint32_t w, uint32_t &lo, uint32_t &hi) {
+__device__ __forceinline__ uint32_t byte2_to_half2_bits(uint32_t two_codes) {
+  if constexpr (DT == kI8) {
+    uint32_t lo, hi;
+    i8x4_to_half2x2(two_codes, lo, hi);
+    return lo;
+  } else {
+    __half2_raw r = __nv_cvt_fp8x2_to_halfraw2(
+        static_cast<__nv_fp8x2_storage_t>(two_codes & 0xFFFFu),
+        DT == kE4M3 ? __NV_E4M3 : __NV_E5M2);
+    return static_cast<uint32_t>(r.x) | (static_cast<uint32_t>(r.y) << 16);
+  }
+}
+
+// four one-byte codes in one word -> two __half2 (codes 0,1 -> lo; codes
+// 2,3 -> hi), exact
+template <int DT>
+__device__ __forceinline__ void byte4_to_half2x2(uint32_t w, uint32_t &lo, uint32_t &hi) {
   if constexpr (DT == kE4M3) {
     asm("{\n\t.reg .b16 a, b;\n\tmov.b32 {a, b}, %2;\n\t"
         "cvt.rn.f16x2.e4m3x2 %0, a;\n\tcvt.rn.f16x2.e4m3x2 %1, b;\n\t}"
         : "=r"(lo), "=r"(hi)
         : "r"(w));
-  } else {
+  } else if constexpr (DT == kE5M2) {
     asm("{\n\t.reg .b16 a, b;\n\tmov.b32 {a, b}, %2;\n\t"
         "cvt.rn.f16x2.e5m2x2 %0, a;\n\tcvt.rn.f16x2.e5m2x2 %1, b;\n\t}"
         : "=r"(lo), "=r"(hi)
         : "r"(w));
+  } else {
+    i8x4_to_half2x2(w, lo, hi);
   }
 }
 
 template <int DT>
-__device__ __forceinline__ float2 fp8x2_to_float2(uint32_t two_codes) {
-  uint32_t h = fp8x2_to_half2_bits<DT>(two_codes);
+__device__ __forceinline__ float2 byte2_to_float2(uint32_t two_codes) {
+  uint32_t h = byte2_to_half2_bits<DT>(two_codes);
   return __half22float2(*reinterpret_cast<const __half2 *>(&h));
 }
 

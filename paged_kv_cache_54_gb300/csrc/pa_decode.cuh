@@ -554,8 +554,8 @@ struct SimtState {
         f[2 * k] = a.x;
         f[2 * k + 1] = a.y;
       } else {
-        const float2 a = fp8x2_to_float2<KV>(w);
-        const float2 b = fp8x2_to_float2<KV>(w >> 16);
+        const float2 a = byte2_to_float2<KV>(w);
+        const float2 b = byte2_to_float2<KV>(w >> 16);
         f[4 * k] = a.x;
         f[4 * k + 1] = a.y;
         f[4 * k + 2] = b.x;
@@ -577,7 +577,7 @@ struct SimtState {
     } else {
 #pragma unroll
       for (int e = 0; e < EPL; e += 2) {
-        const float2 a = fp8x2_to_float2<KV>(*reinterpret_cast<const uint16_t *>(src + e));
+        const float2 a = byte2_to_float2<KV>(*reinterpret_cast<const uint16_t *>(src + e));
         f[e] = a.x;
         f[e + 1] = a.y;
       }
@@ -714,7 +714,7 @@ __device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1
 template <int KV, int QT, int D, int G, int QM>
 struct MmaState {
   static constexpr bool SW = swizzled<KV, D, G>();
-  static constexpr bool KV8 = is_fp8(KV);
+  static constexpr bool KV8 = is_byte(KV);
   static constexpr int MT = KV8 ? kF16 : KV;  // mma input type
   static constexpr int ELT = elt_bytes(KV);
   static constexpr int ROWB = D * ELT;
@@ -815,7 +815,7 @@ struct MmaState {
     } else {
       const int e = 4 * kk;
       const uint32_t w = w32(ch[e / CE], (e % CE) / 4);
-      return fp8x2_to_half2_bits<KV>(r ? (w >> 16) : w);
+      return byte2_to_half2_bits<KV>(r ? (w >> 16) : w);
     }
   }
 
@@ -829,7 +829,7 @@ struct MmaState {
       const int byte = col & 3;
       const uint32_t a = ra[col / 4], b = rb[col / 4];
       const uint32_t two = prmt(a, b, static_cast<uint32_t>(byte | ((4 + byte) << 4)));
-      return fp8x2_to_half2_bits<KV>(two);
+      return byte2_to_half2_bits<KV>(two);
     }
   }
 
@@ -838,7 +838,7 @@ struct MmaState {
                                                  uint32_t &lo, uint32_t &hi) {
     const uint32_t b = col & 3;
     const uint32_t two = prmt(ra[col / 4], rb[col / 4], b | ((4 + b) << 4) | ((b + 1) << 8) | ((5 + b) << 12));
-    fp8x4_to_half2x2<KV>(two, lo, hi);
+    byte4_to_half2x2<KV>(two, lo, hi);
   }
 
   __device__ __forceinline__ void slice(const uint8_t *Kb, const uint8_t *Vb, int row0, int n, float v_scale) {
@@ -867,8 +867,8 @@ struct MmaState {
         a3 = k_reg(k1, kk, 1);
       } else {  // local elements 4kk..4kk+3 are one word of the row's chunk
         const int e = 4 * kk;
-        fp8x4_to_half2x2<KV>(w32(k0[e / CE], (e % CE) / 4), a0, a2);
-        fp8x4_to_half2x2<KV>(w32(k1[e / CE], (e % CE) / 4), a1, a3);
+        byte4_to_half2x2<KV>(w32(k0[e / CE], (e % CE) / 4), a0, a2);
+        byte4_to_half2x2<KV>(w32(k1[e / CE], (e % CE) / 4), a1, a3);
       }
       mma16816<MT>(sacc[kk & 3], a0, a1, a2, a3, qb[kk][0], qb[kk][1]);
     }
@@ -1089,12 +1089,20 @@ __device__ __forceinline__ bool run_item(const DecodeParams &p, SmemHeader &hdr,
                                          int &ncomb, StageInfo inf, const volatile int *abort) {
   const int lane = threadIdx.x & 31;
   const int ncols = inf.k * G;
+  // scales of the item's KV head: per tensor (folded in by the host) or per head
+  float qk_scale = p.qk_scale_log2, v_scale = p.v_scale;
+  if constexpr (is_byte(KV)) {
+    if (p.k_head_scale != nullptr) {
+      qk_scale *= __ldg(p.k_head_scale + inf.h);
+      v_scale = __ldg(p.v_head_scale + inf.h);
+    }
+  }
   State st;
-  st.start(stages + static_cast<size_t>(stage) * p.stage_bytes + p.q_off, p.qk_scale_log2, ncols);
+  st.start(stages + static_cast<size_t>(stage) * p.stage_bytes + p.q_off, qk_scale, ncols);
   while (true) {
     const uint8_t *sb = stages + static_cast<size_t>(stage) * p.stage_bytes;
     const int n = min(16, inf.ntok - 16 * cw);
-    if (n > 0) st.slice(sb + p.k_off, sb + p.v_off, 16 * cw, n, p.v_scale);
+    if (n > 0) st.slice(sb + p.k_off, sb + p.v_off, 16 * cw, n, v_scale);
     __syncwarp();
     if (lane == 0) mbar_arrive(&hdr.empty[stage]);
     const bool last = (inf.flags & kLast) != 0;
@@ -1110,7 +1118,7 @@ __device__ __forceinline__ bool run_item(const DecodeParams &p, SmemHeader &hdr,
   }
   // three consumer-wide barriers: states written, weights computed, scratch
   // read (so that the next item may overwrite it)
-  st.to_scratch(so, sm, sl, cw, p.v_scale, ncols);
+  st.to_scratch(so, sm, sl, cw, v_scale, ncols);
   mbar_arrive(&hdr.combine);
   if (!mbar_wait(&hdr.combine, (3 * ncomb) & 1, abort)) return false;
   bool ok = true;

@@ -68,7 +68,7 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 // [rows, 2, 128 B] when it is 256 bytes; the box is one (block, head) tile
 // of block_size rows, written to shared memory with the 128-byte swizzle.
 bool encode_cache_map(CUtensorMap *map, const void *cache, const pa_cache_desc *c) {
-  const int elt = (c->dtype == PA_FP8_E4M3 || c->dtype == PA_FP8_E5M2) ? 1 : 2;
+  const int elt = c->dtype >= PA_FP8_E4M3 ? 1 : 2;
   const int rowb = c->head_dim * elt;
   if (rowb < 128) return true;  // 64-byte rows use plain bulk copies
   PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
@@ -130,8 +130,8 @@ extern "C" pa_status pa_decode(void *out, const void *q, int32_t q_dtype, int32_
   if (G != 1 && G != 2 && G != 4 && G != 8) return PA_ERR_UNSUPPORTED;
   if (!supported_cache_shape(cache)) return PA_ERR_UNSUPPORTED;
   if (q_dtype != PA_F16 && q_dtype != PA_BF16) return PA_ERR_UNSUPPORTED;
-  const bool fp8 = cache->dtype == PA_FP8_E4M3 || cache->dtype == PA_FP8_E5M2;
-  if (!fp8 && q_dtype != cache->dtype) return PA_ERR_UNSUPPORTED;
+  const bool byte_codes = cache->dtype >= PA_FP8_E4M3;  // FP8 or INT8, with scales
+  if (!byte_codes && q_dtype != cache->dtype) return PA_ERR_UNSUPPORTED;
   if (partition_size != 0 &&
       (partition_size < kStageTok || partition_size > kMaxPartition ||
        partition_size % kStageTok || partition_size % cache->block_size))
@@ -165,8 +165,11 @@ extern "C" pa_status pa_decode(void *out, const void *q, int32_t q_dtype, int32_
   p.partition_size = w.partition;
   p.max_parts = w.max_parts;
   p.len_cap = static_cast<int>(cap > 0x7fffffff ? 0x7fffffff : cap);
-  p.qk_scale_log2 = scale * (fp8 ? cache->k_scale : 1.0f) * 1.4426950408889634f;
-  p.v_scale = fp8 ? cache->v_scale : 1.0f;
+  const bool per_head = byte_codes && cache->k_head_scales != nullptr;
+  p.qk_scale_log2 = scale * (byte_codes && !per_head ? cache->k_scale : 1.0f) * 1.4426950408889634f;
+  p.v_scale = byte_codes && !per_head ? cache->v_scale : 1.0f;
+  p.k_head_scale = per_head ? cache->k_head_scales : nullptr;
+  p.v_head_scale = per_head ? cache->v_head_scales : nullptr;
   p.work = reinterpret_cast<int *>(ws);
   p.items = reinterpret_cast<int4 *>(ws + w.pairs_off);
   p.plan_len = reinterpret_cast<int *>(ws + w.len_off);
@@ -187,6 +190,7 @@ extern "C" pa_status pa_decode(void *out, const void *q, int32_t q_dtype, int32_
     case PA_BF16: return dispatch_decode_bf16(q_dtype, cache->head_dim, G, p, dev, s);
     case PA_FP8_E4M3: return dispatch_decode_e4m3(q_dtype, cache->head_dim, G, p, dev, s);
     case PA_FP8_E5M2: return dispatch_decode_e5m2(q_dtype, cache->head_dim, G, p, dev, s);
+    case PA_INT8: return dispatch_decode_i8(q_dtype, cache->head_dim, G, p, dev, s);
   }
   return PA_ERR_UNSUPPORTED;
 }

@@ -69,8 +69,10 @@ struct DecodeParams {
   const int32_t *seq_lens;
   int num_seqs, num_q_heads, num_kv_heads, num_blocks, block_size, max_blocks;
   int partition_size, max_parts, len_cap;
-  float qk_scale_log2;  // softmax scale * k_scale * log2(e)
-  float v_scale;
+  float qk_scale_log2;  // softmax scale * log2(e) * k_scale (k_scale = 1 with per-head scales)
+  float v_scale;        // v_scale (1 with per-head scales)
+  const float *k_head_scale;  // [num_kv_heads] or null: per-head scales of a one-byte cache
+  const float *v_head_scale;
   int num_stages, stage_bytes, k_off, v_off, q_off, scratch_off, stages_off;
   int kmax;   // most sequences one item may batch
   int *work;  // [0] claim counter, [1] number of items
@@ -94,5 +96,7 @@ pa_status dispatch_decode_e4m3(int q_dtype, int head_dim, int group, DecodeParam
                                const DeviceInfo &dev, cudaStream_t stream);
 pa_status dispatch_decode_e5m2(int q_dtype, int head_dim, int group, DecodeParams p,
                                const DeviceInfo &dev, cudaStream_t stream);
+pa_status dispatch_decode_i8(int q_dtype, int head_dim, int group, DecodeParams p,
+                             const DeviceInfo &dev, cudaStream_t stream);
 
 }  // namespace pa

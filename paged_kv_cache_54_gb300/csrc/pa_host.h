@@ -27,10 +27,17 @@ inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 
 inline bool valid_cache_desc(const pa_cache_desc *c) {
   if (c == nullptr) return false;
   if (c->num_blocks <= 0 || c->kv_heads <= 0 || c->block_size <= 0 || c->head_dim <= 0) return false;
-  if (c->dtype < PA_F16 || c->dtype > PA_FP8_E5M2) return false;
+  if (c->dtype < PA_F16 || c->dtype > PA_INT8) return false;
   if (c->dtype >= PA_FP8_E4M3) {
     if (!(c->k_scale > 0.f) || !(c->v_scale > 0.f)) return false;
     if (c->k_scale > 3.0e38f || c->v_scale > 3.0e38f) return false;
+    if ((reinterpret_cast<uintptr_t>(c->k_head_scales) & 3u) ||
+        (reinterpret_cast<uintptr_t>(c->v_head_scales) & 3u))
+      return false;
+    // one pointer without the other would leave a tensor without scales
+    if ((c->k_head_scales == nullptr) != (c->v_head_scales == nullptr)) return false;
+  } else if (c->k_head_scales != nullptr || c->v_head_scales != nullptr) {
+    return false;  // 16-bit caches have no scales
   }
   return true;
 }

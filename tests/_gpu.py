@@ -4,13 +4,15 @@ import numpy as np
 import torch
 
 import paged_kv_cache_54_gb300 as pa
+import workloads as W
 from oracle import attention as A
 from oracle import fp8 as F
-from oracle.cache import NAN_CODE, PagedKVCache, bits_to_f64
+from oracle import int8 as I8
+from oracle.cache import NAN_CODE, PagedKVCache, bits_to_f64, head_scale
 
 DEV = "cuda:0"
 TOL = {"f16": 2e-3, "bf16": 1e-2}
-FP8_TOL = 1e-2
+FP8_TOL = 1e-2    # one-byte caches (FP8, INT8) against the oracle on the dequantised values
 
 
 def bits(t):
@@ -22,7 +24,7 @@ def bits(t):
 
 def new_caches(w):
     shape = (w.num_blocks, w.Hkv, w.bs, w.d)
-    if w.cache_dtype in ("e4m3", "e5m2"):
+    if w.cache_dtype in W.BYTE_DTYPES:
         kc = torch.full(shape, NAN_CODE[w.cache_dtype], dtype=torch.uint8, device=DEV)
         vc = torch.full(shape, NAN_CODE[w.cache_dtype], dtype=torch.uint8, device=DEV)
     else:
@@ -30,6 +32,14 @@ def new_caches(w):
         kc = torch.full(shape, float("nan"), dtype=dt, device=DEV)
         vc = torch.full(shape, float("nan"), dtype=dt, device=DEV)
     return kc, vc
+
+
+def scale_arg(scale):
+    """A workload's scale as the binding takes it: a number, or a float32
+    device tensor of one scale per KV head."""
+    if np.ndim(scale) == 0:
+        return float(scale)
+    return torch.tensor(scale, dtype=torch.float32, device=DEV)
 
 
 class GpuRun:
@@ -45,7 +55,8 @@ class GpuRun:
         self.new_slots = torch.from_numpy(w.new_slots).to(DEV)
         self.pairs = torch.from_numpy(w.cow_pairs).to(DEV)
         self.out = torch.empty_like(w.q)
-        self.kw = dict(cache_dtype=w.cache_dtype, k_scale=w.k_scale, v_scale=w.v_scale)
+        self.kw = dict(cache_dtype=w.cache_dtype, k_scale=scale_arg(w.k_scale),
+                       v_scale=scale_arg(w.v_scale))
         self.ws = torch.empty(max(256, pa.pa_decode_workspace_size(
             w.S, w.Hq, w.Hkv, w.d, w.max_seq_len, self.P)), dtype=torch.uint8, device=DEV)
 
@@ -84,6 +95,22 @@ def oracle_cache(w):
     return c
 
 
+def encode_rows(w, raw, which):
+    """Oracle storage codes of source rows [n, Hkv, d] (16-bit patterns) for
+    the K (which="k") or V cache: each head with its own scale."""
+    if w.cache_dtype not in W.BYTE_DTYPES:
+        return raw
+    scales = w.k_scale if which == "k" else w.v_scale
+    out = np.empty(raw.shape, dtype=np.uint8)
+    for h in range(raw.shape[1]):
+        sc = head_scale(scales, h)
+        if w.cache_dtype == "int8":
+            out[:, h] = I8.quantize_bits16(raw[:, h], w.src_dtype, sc)
+        else:
+            out[:, h] = F.quantize_bits16(raw[:, h], w.src_dtype, sc, w.cache_dtype)
+    return out
+
+
 def q_values(w):
     return bits_to_f64(bits(w.q), w.q_dtype)
 
@@ -99,14 +126,17 @@ def logical_kv(w, s, h):
     ctx_idx = [i for k, i in rows if k == "ctx"]
     new_idx = [i for k, i in rows if k == "new"]
     out = []
-    for src_ctx, src_new, scale in ((w.ctx_k, w.new_k, w.k_scale), (w.ctx_v, w.new_v, w.v_scale)):
+    for src_ctx, src_new, scales in ((w.ctx_k, w.new_k, w.k_scale), (w.ctx_v, w.new_v, w.v_scale)):
+        scale = head_scale(scales, h)
         parts = []
         if ctx_idx:
             parts.append(bits(src_ctx[torch.tensor(ctx_idx, device=src_ctx.device), h]))
         if new_idx:
             parts.append(bits(src_new[torch.tensor(new_idx, device=src_new.device), h]))
         raw = np.concatenate(parts) if parts else np.zeros((0, w.d), np.uint16)
-        if w.cache_dtype in ("e4m3", "e5m2"):
+        if w.cache_dtype == "int8":
+            vals = I8.decode(I8.quantize_bits16(raw, w.src_dtype, scale)) * scale
+        elif w.cache_dtype in ("e4m3", "e5m2"):
             vals = F.decode(F.quantize_bits16(raw, w.src_dtype, scale, w.cache_dtype),
                             w.cache_dtype) * scale
         else:
@@ -134,4 +164,4 @@ def ulp(x, dtype):
 
 
 def tolerance(w):
-    return FP8_TOL if w.cache_dtype in ("e4m3", "e5m2") else TOL[w.q_dtype]
+    return FP8_TOL if w.cache_dtype in W.BYTE_DTYPES else TOL[w.q_dtype]

@@ -55,3 +55,30 @@ def test_partition_size_choice_is_deterministic():
     a = pa.pa_decode_workspace_size(64, 32, 32, 128, 4096)
     b = pa.pa_decode_workspace_size(64, 32, 32, 128, 4096)
     assert a == b > 0
+
+
+def test_scale_descriptions_are_validated_on_the_host():
+    import paged_kv_cache_54_gb300 as pa
+    lib = pa.load_library()
+
+    def rc(desc):   # zero tokens: only the description is checked
+        return lib.pa_reshape_and_cache(16, 16, 0, 8, 0, 16, 16, ctypes.byref(desc), None, None)
+
+    assert rc(pa.PaCacheDesc(16, 2, 16, 64, pa.PA_INT8, 0.05, 0.05)) == 0
+    assert rc(pa.PaCacheDesc(16, 2, 16, 64, pa.PA_INT8, 0.05, 0.05, 4096, 8192)) == 0
+    assert rc(pa.PaCacheDesc(16, 2, 16, 64, 5, 1.0, 1.0)) == 1          # unknown dtype
+    assert rc(pa.PaCacheDesc(16, 2, 16, 64, pa.PA_INT8, 0.0, 1.0)) == 1  # scale must be > 0
+    assert rc(pa.PaCacheDesc(16, 2, 16, 64, pa.PA_INT8, 1.0, 1.0, 4096, None)) == 1  # K without V
+    assert rc(pa.PaCacheDesc(16, 2, 16, 64, pa.PA_FP8_E4M3, 1.0, 1.0, 4098, 8192)) == 1  # misaligned
+    assert rc(pa.PaCacheDesc(16, 2, 16, 64, pa.PA_F16, 1.0, 1.0, 4096, 8192)) == 1  # 16-bit: no scales
+
+
+def test_binding_marshals_per_head_scales():
+    import torch
+    import paged_kv_cache_54_gb300 as pa
+    kc = torch.zeros((4, 2, 16, 64), dtype=torch.uint8)
+    d = pa.cache_desc(kc, "int8", 0.25, 0.5)
+    assert (d.dtype, d.k_scale, d.v_scale, d.k_head_scales, d.v_head_scales) == (4, 0.25, 0.5, None, None)
+    with pytest.raises(ValueError):   # per-head scales must live on the device
+        pa.cache_desc(kc, "int8", torch.ones(2), torch.ones(2))
+    assert pa.cache_desc(torch.zeros((4, 2, 16, 64), dtype=torch.int8)).dtype == pa.PA_INT8

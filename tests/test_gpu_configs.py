@@ -1,4 +1,4 @@
-"""The five named workloads at full size, in the launch configuration the
+"""The named workloads at full size, in the launch configuration the
 benchmark times: sampled outputs against the oracle (computed one by one
 from the logical sequences), sampled cache slots bit-exact, invariants on
 every output."""
@@ -7,7 +7,6 @@ import pytest
 import torch
 
 import workloads as W
-from oracle import fp8 as F
 from tests import _gpu as G
 
 pytestmark = pytest.mark.gpu
@@ -23,9 +22,9 @@ def _sample_rows(w, n, seed):
     return sorted(rows)
 
 
-@pytest.mark.parametrize("name", W.CONFIG_ORDER)
+@pytest.mark.parametrize("name", W.ALL_CONFIGS)
 def test_named_config(name):
-    w = W.make_workload(name, W.CONFIG_ORDER.index(name) + 1, device=G.DEV)
+    w = W.make_workload(name, W.config_seed(name), device=G.DEV)
     run = G.GpuRun(w).setup()
     run.step()
     torch.cuda.synchronize()
@@ -55,10 +54,8 @@ def test_named_config(name):
         ksrc = w.ctx_k if src == "ctx" else w.new_k
         vsrc = w.ctx_v if src == "ctx" else w.new_v
         sel = torch.from_numpy(idx).to(G.DEV)
-        kb, vb = G.bits(ksrc[sel]), G.bits(vsrc[sel])
-        if w.cache_dtype in ("e4m3", "e5m2"):
-            kb = F.quantize_bits16(kb, w.src_dtype, w.k_scale, w.cache_dtype)
-            vb = F.quantize_bits16(vb, w.src_dtype, w.v_scale, w.cache_dtype)
+        kb = G.encode_rows(w, G.bits(ksrc[sel]), "k")
+        vb = G.encode_rows(w, G.bits(vsrc[sel]), "v")
         for j, t in enumerate(idx):
             slot = int(slots[t])
             blk, off = divmod(slot, w.bs)

@@ -1,5 +1,6 @@
 """pa_decode against the float64 oracle on small seeded cases (GPU)."""
 import itertools
+import zlib
 
 import numpy as np
 import pytest
@@ -11,7 +12,12 @@ from tests import _gpu as G
 pytestmark = pytest.mark.gpu
 
 DTYPES = [("f16", "f16"), ("bf16", "bf16"), ("e4m3", "bf16"), ("e4m3", "f16"),
-          ("e5m2", "f16"), ("e5m2", "bf16")]
+          ("e5m2", "f16"), ("e5m2", "bf16"), ("int8", "bf16"), ("int8", "f16")]
+
+
+def _seed(*key):
+    """A seed fixed by the test's parameters (str hashes vary between runs)."""
+    return zlib.crc32(repr(key).encode()) % 1000
 
 
 def _check(w, got, ref, extra_ulp=True):
@@ -37,10 +43,11 @@ def test_decode_matches_oracle(cache_dtype, q_dtype, d, bs, group):
     Hkv = 2
     P = 128
     lens = _lens(bs, P)
-    fp8 = cache_dtype in ("e4m3", "e5m2")
-    w = W.random_case(hash((cache_dtype, q_dtype, d, bs, group)) % 1000, len(lens), Hkv * group,
+    scales = {"e4m3": (0.5, 1.5), "e5m2": (0.5, 1.5), "int8": (0.03, 0.045)}
+    ks, vs = scales.get(cache_dtype, (1.0, 1.0))
+    w = W.random_case(_seed(cache_dtype, q_dtype, d, bs, group), len(lens), Hkv * group,
                       Hkv, d, bs, cache_dtype, q_dtype, lens, device=G.DEV,
-                      k_scale=0.5 if fp8 else 1.0, v_scale=1.5 if fp8 else 1.0)
+                      k_scale=ks, v_scale=vs)
     run = G.GpuRun(w, partition_size=P).setup()
     run.step()
     torch.cuda.synchronize()
@@ -50,8 +57,30 @@ def test_decode_matches_oracle(cache_dtype, q_dtype, d, bs, group):
     assert torch.all(run.out[0] == 0)          # length 0 gives zeros
 
 
+@pytest.mark.parametrize("cache_dtype,q_dtype", [("e4m3", "bf16"), ("e5m2", "f16"),
+                                                 ("int8", "bf16"), ("int8", "f16")])
+@pytest.mark.parametrize("group", [1, 2, 8])
+@pytest.mark.parametrize("d", [64, 128])
+def test_decode_per_head_scales(cache_dtype, q_dtype, group, d):
+    Hkv = 4
+    base = 0.03 if cache_dtype == "int8" else 0.5
+    ks = tuple(base * f for f in (1.0, 0.37, 2.9, 1.61))
+    vs = tuple(base * f for f in (0.8, 3.3, 0.51, 1.0))
+    lens = [1, 17, 64, 200, 513, 1100]
+    w = W.random_case(_seed("per-head", cache_dtype, q_dtype, group, d), len(lens),
+                      Hkv * group, Hkv, d, 16, cache_dtype, q_dtype, lens, device=G.DEV,
+                      k_scale=ks, v_scale=vs, partition_size=256)
+    run = G.GpuRun(w).setup()
+    run.step()
+    torch.cuda.synchronize()
+    assert int(run.err.item()) == 0
+    ref = G.oracle_decode(w, G.oracle_cache(w))
+    _check(w, run.out, ref)
+
+
 @pytest.mark.parametrize("cache_dtype,q_dtype,group", [("f16", "f16", 1), ("bf16", "bf16", 2),
-                                                       ("e4m3", "bf16", 8), ("f16", "f16", 4)])
+                                                       ("e4m3", "bf16", 8), ("f16", "f16", 4),
+                                                       ("int8", "bf16", 8), ("int8", "f16", 1)])
 def test_partition_size_does_not_change_the_result(cache_dtype, q_dtype, group):
     lens = [1, 100, 511, 512, 513, 1500, 2049]
     w = W.random_case(9, len(lens), 2 * group, 2, 128, 16, cache_dtype, q_dtype, lens,
@@ -98,9 +127,10 @@ def test_repeated_calls_are_deterministic():
     assert torch.equal(a, run.out)
 
 
-def test_large_query_values_with_fp8_cache():
+@pytest.mark.parametrize("cache_dtype", ["e4m3", "int8"])
+def test_large_query_values_with_byte_cache(cache_dtype):
     lens = [50, 300]
-    w = W.random_case(8, 2, 8, 1, 128, 16, "e4m3", "bf16", lens, device=G.DEV)
+    w = W.random_case(8, 2, 8, 1, 128, 16, cache_dtype, "bf16", lens, device=G.DEV)
     # entries beyond fp16's range (the fp16 tensor-core path rescales q by a
     # power of two); the softmax scale shrinks by the same factor so that the
     # scores, and the conditioning of the problem, stay as before
@@ -132,7 +162,7 @@ def test_bad_block_id_and_length_are_reported():
     assert int(run.err.item()) == 3
 
 
-SHARED_DTYPES = [("f16", "f16"), ("bf16", "bf16"), ("e4m3", "bf16")]
+SHARED_DTYPES = [("f16", "f16"), ("bf16", "bf16"), ("e4m3", "bf16"), ("int8", "f16")]
 
 
 @pytest.mark.parametrize("cache_dtype,q_dtype", SHARED_DTYPES)

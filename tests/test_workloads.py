@@ -34,7 +34,7 @@ def test_qwen3_shape_matches_page_size():
     assert per_tok * g["seq_len"] == g["bytes_per_seq_mib"] * 2 ** 20
 
 
-@pytest.mark.parametrize("name", W.CONFIG_ORDER)
+@pytest.mark.parametrize("name", W.ALL_CONFIGS)
 def test_structure_is_valid(name):
     st = W.build_structure(name, 1)
     bs, nb = st["cfg"]["bs"], st["num_blocks"]

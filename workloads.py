@@ -94,6 +94,12 @@ CONFIGS: Dict[str, dict] = {
 }
 CONFIG_ORDER = ["tiny", "llama2-7b", "qwen3-prefix", "opt13b-beam", "gqa-fp8"]
 EXTRA_CONFIGS = ["gqa-int8"]
+ALL_CONFIGS = CONFIG_ORDER + EXTRA_CONFIGS
+
+
+def config_seed(name: str) -> int:
+    """Default seed of a named workload (its position, from 1)."""
+    return ALL_CONFIGS.index(name) + 1
 BYTE_DTYPES = ("e4m3", "e5m2", "int8")
 
 
