@@ -20,6 +20,13 @@ codes for e4m3 / e5m2 / int8.  Values are recovered with :func:`values`.
 * ``copy_blocks``: the copy step of copy-on-write ([P4] §3.3): every element
   of block ``src`` (all heads, all token slots) is copied to block ``dst``,
   in K and in V.
+* ``swap_blocks``: swapping a preempted request's blocks out to CPU memory
+  and back ([P1] §5.1–5.2: on preemption the KV cache is copied to CPU
+  memory instead of being dropped; [P4] §3.5: inactive blocks go to the
+  CPU swap space; [P3] §7.2: reusable blocks are offloaded to CPU memory).
+  A second pool of the same block shape stands for the CPU memory; each
+  (src, dst) pair copies one whole block from one pool to the other, bit
+  for bit.
 """
 
 from __future__ import annotations
@@ -136,6 +143,26 @@ class PagedKVCache:
         for src, dst in pairs:
             self.k[int(dst)] = self.k[int(src)]
             self.v[int(dst)] = self.v[int(src)]
+
+    def swap_blocks(self, other: "PagedKVCache", pairs, direction: str) -> None:
+        """Whole-block moves between this pool and ``other`` (same kv_heads,
+        block_size, head_dim and dtype; any number of blocks).
+
+        direction "out": block src of this pool -> block dst of ``other``;
+        direction "in":  block src of ``other`` -> block dst of this pool.
+        """
+        if (other.kv_heads, other.block_size, other.head_dim, other.dtype) != \
+                (self.kv_heads, self.block_size, self.head_dim, self.dtype):
+            raise ValueError("pools differ in block shape")
+        if direction == "out":
+            src, dst = self, other
+        elif direction == "in":
+            src, dst = other, self
+        else:
+            raise ValueError(direction)
+        for s, d in pairs:
+            dst.k[int(d)] = src.k[int(s)]
+            dst.v[int(d)] = src.v[int(s)]
 
     def k_values(self) -> np.ndarray:
         return values(self.k, self.dtype, self.k_scale)

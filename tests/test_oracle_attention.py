@@ -282,3 +282,34 @@ def test_planted_offset_error_in_gather_is_caught(monkeypatch):
     with pytest.raises(AssertionError):
         _run_sdpa_pin()
     monkeypatch.setattr(A, "gather", orig)
+
+
+def test_swap_out_and_in_round_trip():
+    """Blocks swapped out to a second pool and back into other device blocks
+    hold the same codes; decoding through the remapped tables gives the same
+    result; every block no pair names is untouched."""
+    w = W.random_case(12, 3, 4, 2, 16, 8, "e4m3", "bf16", [13, 30, 7], k_scale=0.5)
+    c = _fill(w)
+    before_k, before_v = c.k.copy(), c.v.copy()
+    host = PagedKVCache(10, w.Hkv, w.bs, w.d, w.cache_dtype, fill_nan=False)
+    seq1 = [int(b) for b in w.block_tables[1, :-(-30 // w.bs)]]
+    out_pairs = [(b, i) for i, b in enumerate(seq1)]
+    c.swap_blocks(host, out_pairs, "out")
+    for b, i in out_pairs:
+        assert (host.k[i] == c.k[b]).all() and (host.v[i] == c.v[b]).all()
+    assert (host.k[len(seq1):] == 0).all()
+    used = {int(b) for s in range(w.S) for b in w.block_tables[s, :-(-int(w.seq_lens[s]) // w.bs)]}
+    free = [b for b in range(w.num_blocks) if b not in used][:len(seq1)]
+    c.swap_blocks(host, [(i, f) for i, f in enumerate(free)], "in")
+    for (b, i), f in zip(out_pairs, free):
+        assert (c.k[f] == before_k[b]).all() and (c.v[f] == before_v[b]).all()
+    untouched = [b for b in range(w.num_blocks) if b not in free]
+    assert (c.k[untouched] == before_k[untouched]).all()
+    tables = w.block_tables.copy()
+    tables[1, :len(free)] = free
+    q = _qvals(w)
+    a = A.paged_decode(q, before_k, before_v, "e4m3", w.block_tables, w.seq_lens, w.scale, 0.5)
+    b = A.paged_decode(q, c.k, c.v, "e4m3", tables, w.seq_lens, w.scale, 0.5)
+    np.testing.assert_array_equal(a, b)
+    with pytest.raises(ValueError):
+        c.swap_blocks(PagedKVCache(4, w.Hkv, 16, w.d, w.cache_dtype), [(0, 0)], "out")
