@@ -53,6 +53,10 @@ def parse():
     ap.add_argument("--config", default=DEFAULT_CONFIG, choices=W.ALL_CONFIGS)
     ap.add_argument("--seed", type=int, default=None)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--op", default="step", choices=["step", "swap"],
+                    help="step: the decode step (default); swap: pa_swap_blocks of "
+                         "preempted sequences' blocks out to pinned host memory and back")
+    ap.add_argument("--swap-seqs", type=int, default=16)
     return ap.parse_args()
 
 
@@ -420,11 +424,197 @@ def run_reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
+# ---------------------------------------------------------------------------
+# block swap between the device caches and page-locked host memory
+# ---------------------------------------------------------------------------
+SWAP_METRIC = "KV block swap device<->host GB/s (pa_swap_blocks, out + in)"
+
+
+def _swap_pairs(w, n_seqs):
+    """Swap-out pairs (device block, host slot) of the first n_seqs sequences'
+    blocks, and swap-in pairs (host slot, free device block)."""
+    seqs = range(min(n_seqs, w.S))
+    blocks = [int(b) for s in seqs for b in w.block_tables[s, :-(-int(w.seq_lens[s]) // w.bs)]]
+    used = {int(b) for s in range(w.S) for b in w.block_tables[s, :-(-int(w.seq_lens[s]) // w.bs)]}
+    free = [b for b in range(w.num_blocks) if b not in used]
+    n = min(len(blocks), len(free))
+    out_pairs = np.array([[b, i] for i, b in enumerate(blocks[:n])], dtype=np.int64)
+    in_pairs = np.array([[i, f] for i, f in enumerate(free[:n])], dtype=np.int64)
+    return out_pairs, in_pairs
+
+
+def run_swap(args, rank, world, local):
+    import torch
+    import paged_kv_cache_54_gb300 as pa
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device(f"cuda:{local}"))
+    torch.cuda.set_device(local)
+    dev = f"cuda:{local}"
+    seed = args.seed if args.seed is not None else W.config_seed(args.config)
+    w = W.make_workload(args.config, seed, values=False)
+    out_np, in_np = _swap_pairs(w, args.swap_seqs)
+    n = len(out_np)
+    elt = w.elt_bytes()
+    shape = (w.num_blocks, w.Hkv, w.bs, w.d)
+    cdt = torch.uint8 if elt == 1 else torch.int16
+    gen = torch.Generator(device=dev).manual_seed(seed)
+    kc = torch.randint(0, 255, shape, generator=gen, device=dev, dtype=torch.int32).to(cdt)
+    vc = torch.randint(0, 255, shape, generator=gen, device=dev, dtype=torch.int32).to(cdt)
+    hk = torch.empty((n,) + shape[1:], dtype=cdt).pin_memory()
+    hv = torch.empty((n,) + shape[1:], dtype=cdt).pin_memory()
+    out_pairs = torch.from_numpy(out_np).to(dev)
+    in_pairs = torch.from_numpy(in_np).to(dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    kw = dict(cache_dtype=w.cache_dtype, device_error=err)
+    block_bytes = w.Hkv * w.bs * w.d * elt
+    moved = 2 * n * block_bytes                       # K and V, per direction
+    stream = torch.cuda.current_stream()
+
+    def swap_step(evs=None):
+        if evs:
+            evs[0].record(stream)
+        pa.pa_swap_blocks(kc, vc, hk, hv, out_pairs, "out", **kw)
+        if evs:
+            evs[1].record(stream)
+        pa.pa_swap_blocks(kc, vc, hk, hv, in_pairs, "in", **kw)
+        if evs:
+            evs[2].record(stream)
+
+    sampler = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
+    for _ in range(args.warmup):
+        swap_step()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    K = args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    if sampler:
+        sampler.mark_start()
+    torch.cuda.synchronize()
+    for i in range(K):
+        swap_step(evs[i])
+    torch.cuda.synchronize()
+    if sampler:
+        sampler.mark_end()
+    t_out = statistics.mean(e[0].elapsed_time(e[1]) for e in evs) / 1e3
+    t_in = statistics.mean(e[1].elapsed_time(e[2]) for e in evs) / 1e3
+    elapsed = evs[0][0].elapsed_time(evs[-1][2]) / 1e3
+    if world > 1:
+        t = torch.tensor([elapsed], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed = float(t.item())
+    # the link's copy-engine rate for the same bytes: one contiguous pinned
+    # copy per direction (the denominator of the roofline)
+    flat_d = torch.empty(moved, dtype=torch.uint8, device=dev)
+    flat_h = torch.empty(moved, dtype=torch.uint8).pin_memory()
+
+    def ce_time(dst, src, reps=10):
+        for _ in range(2):
+            dst.copy_(src, non_blocking=True)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(reps):
+            dst.copy_(src, non_blocking=True)
+        b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / 1e3 / reps
+
+    ce_d2h = ce_time(flat_h, flat_d)
+    ce_h2d = ce_time(flat_d, flat_h)
+    # end to end through the public call: the pairs are uploaded from pinned
+    # host memory each step, the error flag read back
+    hp_out, hp_in = out_pairs.cpu().pin_memory(), in_pairs.cpu().pin_memory()
+    err_host = torch.empty(1, dtype=torch.int32).pin_memory()
+
+    def e2e_step():
+        out_pairs.copy_(hp_out, non_blocking=True)
+        in_pairs.copy_(hp_in, non_blocking=True)
+        swap_step()
+        err_host.copy_(err, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    KE = max(5, K // 4)
+    e0.record(stream)
+    for _ in range(KE):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_t = e0.elapsed_time(e1) / 1e3 / KE
+    clocks = sampler.finish() if sampler else None
+    derr = int(err.item())
+    if world > 1:
+        dist.destroy_process_group()
+    if rank != 0:
+        return
+    step_t = elapsed / K
+    achieved = 2 * moved / (t_out + t_in) / 1e9
+    peak = 2 * moved / (ce_d2h + ce_h2d) / 1e9 if ce_d2h > 0 and ce_h2d > 0 else None
+    line = {
+        "metric": SWAP_METRIC, "value": round(world * 2 * moved / step_t / 1e9, 2), "unit": "GB/s",
+        "n_gpus": world, "steps": K, "warmup": args.warmup, "ms_per_step": round(step_t * 1e3, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u8",
+        "data": "synthetic (random cache bytes; block ids of the workload's first sequences)",
+        "config": {
+            "workload": f"swap of {min(args.swap_seqs, w.S)} sequences of {args.config} "
+                        f"({n} blocks of {block_bytes // 1024} KiB per K or V) out to pinned host "
+                        f"memory and back into free device blocks",
+            "blocks": n, "bytes_per_direction": moved, "block_bytes": block_bytes,
+            "l2": "inputs larger than L2 (%.0f MB per direction vs 129 MB L2)" % (moved / 1e6),
+            "parallelism": f"replicas x{world}",
+        },
+        "gpu_launches": 2 * K,
+        "device_error": derr,
+        "swap_out_gbs": round(moved / t_out / 1e9, 2),
+        "swap_in_gbs": round(moved / t_in / 1e9, 2),
+        "roofline": {
+            "kernel": "swap_blocks_kernel (out + in, CUDA events)", "bound": "c2c",
+            "achieved": round(achieved, 2), "peak": None if peak is None else round(peak, 2),
+            "unit": "GB/s", "frac": None if peak is None else round(achieved / peak, 4),
+            "peak_kind": "measured in this run: one contiguous pinned copy-engine transfer of "
+                         "the same bytes per direction (no host-link figure in the driver's peaks)",
+            "copy_engine_d2h_gbs": round(moved / ce_d2h / 1e9, 2),
+            "copy_engine_h2d_gbs": round(moved / ce_h2d / 1e9, 2),
+            "traffic": None,
+        },
+        "e2e": {"value": round(2 * moved / e2e_t / 1e9, 2), "unit": "GB/s",
+                "h2d_bytes_per_step": int(2 * n * 16), "d2h_bytes_per_step": 4,
+                "ms_per_step": round(e2e_t * 1e3, 4)},
+        "clocks": clocks,
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = swap_cpu_baseline(w, out_np)
+    print(json.dumps(line), flush=True)
+
+
+def swap_cpu_baseline(w, out_np, budget_s: float = 5.0):
+    """The oracle's pool-to-pool block moves on the host cores (a bounded
+    sample: the first 64 swap-out pairs)."""
+    from oracle.cache import PagedKVCache
+    pairs = out_np[:64]
+    nb = int(pairs[:, 0].max()) + 1
+    dev = PagedKVCache(nb, w.Hkv, w.bs, w.d, w.cache_dtype, fill_nan=False)
+    host = PagedKVCache(len(pairs), w.Hkv, w.bs, w.d, w.cache_dtype, fill_nan=False)
+    t0 = time.perf_counter()
+    reps = 0
+    while time.perf_counter() - t0 < budget_s:
+        dev.swap_blocks(host, pairs, "out")
+        reps += 1
+    dt = (time.perf_counter() - t0) / reps
+    nbytes = 2 * len(pairs) * dev.k[0].nbytes
+    return {"value": round(nbytes / dt / 1e9, 3), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"{len(pairs)} block pairs swapped out by the NumPy oracle, {reps} passes"}
+
+
 def main():
     args = parse()
     rank, world, local = dist_env()
     if args.impl == "reference":
         run_reference(args, rank, world)
+    elif args.op == "swap":
+        run_swap(args, rank, world, local)
     else:
         run_ours(args, rank, world, local)
 

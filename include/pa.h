@@ -8,7 +8,9 @@
  *                         or INT8 with a scale per tensor or per KV head);
  *   pa_decode             single-query decode attention over the paged cache,
  *                         reached through per-sequence block tables;
- *   pa_copy_blocks        whole-block copies, the copy step of copy-on-write.
+ *   pa_copy_blocks        whole-block copies, the copy step of copy-on-write;
+ *   pa_swap_blocks        whole-block moves between the device caches and a
+ *                         pool in host memory (swap-out / swap-in).
  *
  * Pages that state the problem (cited by title and section):
  *   [P1] "【性能飞跃】从 OOM 到丝滑推理:深度工程化 RAG 架构下的内存管理艺术"
@@ -240,6 +242,48 @@ PA_API pa_status pa_decode_static_scratch(
 PA_API pa_status pa_copy_blocks(void *k_cache, void *v_cache, const pa_cache_desc *cache,
                          const int64_t *block_mapping, int32_t num_pairs,
                          int *device_error, pa_stream_t stream);
+
+typedef enum {
+  PA_SWAP_OUT = 0, /* device cache block src -> second-pool block dst */
+  PA_SWAP_IN = 1   /* second-pool block src -> device cache block dst */
+} pa_swap_direction;
+
+/*
+ * pa_swap_blocks — move whole blocks between the device caches and a second
+ * pool of the same block shape, normally in CPU memory: the swap-out of a
+ * preempted request and its swap-in ([P1] §5.1–§5.2: the KV cache is copied
+ * to CPU memory instead of being dropped; [P4] §3.5: inactive blocks go to
+ * the CPU swap space; [P3] §7.2: reusable blocks are offloaded to CPU
+ * memory).  One launch moves every pair, so small blocks cost no more
+ * launches or copy commands than large ones ([P1] §5.2 names the per-block
+ * copy count as what makes swapping slow for small blocks).
+ *
+ *   k_cache/v_cache  device caches described by *cache.
+ *   host_k/host_v    the second pool, [host_num_blocks, kv_heads, block_size,
+ *                    head_dim] of cache->dtype in the caches' layout.  It
+ *                    must be memory the current device can address:
+ *                    page-locked host memory (cudaHostAlloc / cudaMallocHost,
+ *                    or registered with cudaHostRegister) or memory of the
+ *                    current device, 16-byte aligned.  Any other memory
+ *                    returns PA_ERR_UNSUPPORTED (checked with
+ *                    cudaPointerGetAttributes before any launch).  The
+ *                    caller guarantees that it holds host_num_blocks blocks.
+ *   block_mapping    device int64 [num_pairs, 2]: (src, dst).  PA_SWAP_OUT:
+ *                    src is a device block, dst a second-pool block;
+ *                    PA_SWAP_IN: src is a second-pool block, dst a device
+ *                    block.
+ *   direction        pa_swap_direction.
+ * For each pair, block dst of the destination pool (K and V) becomes a
+ * bit-exact copy of block src of the source pool.  Destinations must be
+ * distinct.  A pair with an id out of its pool's range is skipped and
+ * reported as device error 5.  The host pool is read or written by the
+ * kernel directly (over NVLink-C2C on a Grace system), so it must stay
+ * allocated and page-locked until the stream has passed the call.
+ */
+PA_API pa_status pa_swap_blocks(void *k_cache, void *v_cache, const pa_cache_desc *cache,
+                                void *host_k, void *host_v, int64_t host_num_blocks,
+                                const int64_t *block_mapping, int32_t num_pairs,
+                                int32_t direction, int *device_error, pa_stream_t stream);
 
 /* Static description of a status code. */
 PA_API const char *pa_status_string(pa_status status);

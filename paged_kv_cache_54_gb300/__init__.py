@@ -7,6 +7,8 @@ functions carry the C ABI's names:
     pa_reshape_and_cache   write new tokens' K/V into the paged caches
     pa_decode              paged single-query decode attention
     pa_copy_blocks         whole-block copies (copy-on-write)
+    pa_swap_blocks         whole-block moves between the device caches and
+                           a pool in page-locked host memory
     pa_decode_workspace_size
 
 PyTorch supplies the device memory and the stream; there is no CPU or
@@ -33,8 +35,9 @@ if hasattr(torch, "float8_e5m2"):
     _TORCH_CODES[torch.float8_e5m2] = PA_FP8_E5M2
 
 EXPORTED = ("pa_reshape_and_cache", "pa_decode_workspace_size", "pa_decode",
-            "pa_decode_static_scratch", "pa_copy_blocks", "pa_status_string",
-            "pa_last_cuda_error")
+            "pa_decode_static_scratch", "pa_copy_blocks", "pa_swap_blocks",
+            "pa_status_string", "pa_last_cuda_error")
+PA_SWAP_OUT, PA_SWAP_IN = 0, 1
 STATIC_SCRATCH_BYTES = 16 << 20   # PA_DECODE_STATIC_SCRATCH_BYTES
 
 
@@ -77,6 +80,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.pa_decode_static_scratch.restype = ctypes.c_int
     lib.pa_copy_blocks.argtypes = [vp, vp, ctypes.POINTER(PaCacheDesc), vp, i32, vp, vp]
     lib.pa_copy_blocks.restype = ctypes.c_int
+    lib.pa_swap_blocks.argtypes = [vp, vp, ctypes.POINTER(PaCacheDesc), vp, vp, ctypes.c_int64,
+                                   vp, i32, i32, vp, vp]
+    lib.pa_swap_blocks.restype = ctypes.c_int
     lib.pa_status_string.argtypes = [ctypes.c_int]
     lib.pa_status_string.restype = ctypes.c_char_p
     lib.pa_last_cuda_error.argtypes = []
@@ -245,3 +251,36 @@ def pa_copy_blocks(k_cache, v_cache, block_mapping, cache_dtype=None, device_err
                               block_mapping.data_ptr(), block_mapping.shape[0],
                               _ptr(device_error), _stream(stream)),
            "pa_copy_blocks")
+
+
+def pa_swap_blocks(k_cache, v_cache, host_k, host_v, block_mapping, direction: str,
+                   cache_dtype=None, device_error=None, stream=None) -> None:
+    """Whole-block moves between the device caches and a second pool.
+
+    ``host_k`` / ``host_v``: ``[host_blocks, kv_heads, block_size, head_dim]``
+    in page-locked CPU memory (``pin_memory()``) or on the caches' device.
+    ``direction`` "out": for each (src, dst) row of ``block_mapping [n, 2]``
+    device block src -> host block dst; "in": host block src -> device
+    block dst.
+    """
+    for t, n in ((k_cache, "k_cache"), (v_cache, "v_cache"), (block_mapping, "block_mapping")):
+        _require(t, n)
+    for t, n in ((host_k, "host_k"), (host_v, "host_v")):
+        if not t.is_contiguous() or not (t.is_cuda or t.is_pinned()):
+            raise ValueError(f"{n} must be contiguous, in page-locked host memory or on the device")
+        if t.shape[1:] != k_cache.shape[1:] or t.element_size() != k_cache.element_size():
+            raise ValueError(f"{n} must have the caches' block shape and element size")
+    if host_k.shape != host_v.shape:
+        raise ValueError("host_k and host_v must have one shape")
+    if block_mapping.dtype != torch.int64:
+        raise ValueError("block_mapping must be int64")
+    codes = {"out": PA_SWAP_OUT, "in": PA_SWAP_IN}
+    if direction not in codes:
+        raise ValueError('direction must be "out" or "in"')
+    desc = cache_desc(k_cache, cache_dtype)
+    lib = load_library()
+    _check(lib.pa_swap_blocks(k_cache.data_ptr(), v_cache.data_ptr(), ctypes.byref(desc),
+                              host_k.data_ptr(), host_v.data_ptr(), host_k.shape[0],
+                              block_mapping.data_ptr(), block_mapping.shape[0], codes[direction],
+                              _ptr(device_error), _stream(stream)),
+           "pa_swap_blocks")

@@ -110,6 +110,67 @@ __global__ void __launch_bounds__(256) copy_blocks_kernel(uint8_t *__restrict__ 
   }
 }
 
+// Whole-block moves between two pools of one block shape (the device caches
+// and a pool in host memory, either way).  Thread t of CTA b handles four
+// 16-byte vectors kUnroll * blockDim apart per round, issuing the four loads
+// before the four stores so that enough reads are in flight to cover the
+// latency of a host-memory link.  (pair, K|V, vector) is the flat index.
+constexpr int kSwapUnroll = 4;
+
+__global__ void __launch_bounds__(256) swap_blocks_kernel(
+    const uint8_t *__restrict__ src_k, const uint8_t *__restrict__ src_v, uint8_t *__restrict__ dst_k,
+    uint8_t *__restrict__ dst_v, const int64_t *__restrict__ mapping, int num_pairs, long long block_bytes,
+    long long src_blocks, long long dst_blocks, int *err) {
+  const long long vecs = block_bytes / 16;
+  const long long total = static_cast<long long>(num_pairs) * 2 * vecs;
+  const long long step = static_cast<long long>(gridDim.x) * blockDim.x * kSwapUnroll;
+  for (long long base = static_cast<long long>(blockIdx.x) * blockDim.x * kSwapUnroll + threadIdx.x; base < total;
+       base += step) {
+    uint4 x[kSwapUnroll];
+    uint8_t *to[kSwapUnroll];
+#pragma unroll
+    for (int u = 0; u < kSwapUnroll; ++u) {
+      to[u] = nullptr;
+      const long long i = base + static_cast<long long>(u) * blockDim.x;
+      if (i >= total) continue;
+      const long long pair = i / (2 * vecs);
+      const long long r = i - pair * 2 * vecs;
+      const int which = r >= vecs;
+      const long long v = r - which * vecs;
+      const long long s = __ldg(mapping + 2 * pair);
+      const long long d = __ldg(mapping + 2 * pair + 1);
+      if (s < 0 || s >= src_blocks || d < 0 || d >= dst_blocks) {
+        if (v == 0 && which == 0) record_error(err, kErrCopyIndex);
+        continue;
+      }
+      x[u] = *reinterpret_cast<const uint4 *>((which ? src_v : src_k) + s * block_bytes + v * 16);
+      to[u] = (which ? dst_v : dst_k) + d * block_bytes + v * 16;
+    }
+#pragma unroll
+    for (int u = 0; u < kSwapUnroll; ++u)
+      if (to[u] != nullptr) *reinterpret_cast<uint4 *>(to[u]) = x[u];
+  }
+}
+
+// Device address of memory the current device can address: its own memory
+// (returned as is) or page-locked host memory (its mapped device address).
+bool device_view(void *p, int device, uint8_t **out) {
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();  // clear the error the query recorded
+    return false;
+  }
+  if ((a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged) && a.device == device) {
+    *out = static_cast<uint8_t *>(p);
+    return true;
+  }
+  if (a.type == cudaMemoryTypeHost && a.devicePointer != nullptr) {
+    *out = static_cast<uint8_t *>(a.devicePointer);
+    return true;
+  }
+  return false;
+}
+
 int grid_for(long long work_items, int threads) {
   DeviceInfo info;
   int sms = current_device_info(&info) ? info.sm_count : 148;
@@ -191,5 +252,36 @@ extern "C" pa_status pa_copy_blocks(void *k_cache, void *v_cache, const pa_cache
       static_cast<uint8_t *>(k_cache), static_cast<uint8_t *>(v_cache), block_mapping, num_pairs,
       block_bytes, cache->num_blocks, device_error);
   const cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? PA_OK : cuda_fail(e);
+}
+
+extern "C" pa_status pa_swap_blocks(void *k_cache, void *v_cache, const pa_cache_desc *cache, void *host_k,
+                                    void *host_v, int64_t host_num_blocks, const int64_t *block_mapping,
+                                    int32_t num_pairs, int32_t direction, int *device_error,
+                                    pa_stream_t stream) {
+  if (!valid_cache_desc(cache) || num_pairs < 0 || host_num_blocks < 0) return PA_ERR_INVALID;
+  if (direction != PA_SWAP_OUT && direction != PA_SWAP_IN) return PA_ERR_INVALID;
+  if (num_pairs == 0) return PA_OK;
+  if (!k_cache || !v_cache || !host_k || !host_v || !block_mapping) return PA_ERR_INVALID;
+  if (!aligned16(k_cache) || !aligned16(v_cache) || !aligned16(host_k) || !aligned16(host_v) ||
+      (reinterpret_cast<uintptr_t>(block_mapping) & 7u))
+    return PA_ERR_INVALID;
+  if (!supported_cache_shape(cache)) return PA_ERR_UNSUPPORTED;
+  int device = 0;
+  cudaError_t e = cudaGetDevice(&device);
+  if (e != cudaSuccess) return cuda_fail(e);
+  uint8_t *hk = nullptr, *hv = nullptr;
+  if (!device_view(host_k, device, &hk) || !device_view(host_v, device, &hv)) return PA_ERR_UNSUPPORTED;
+  const long long block_bytes = static_cast<long long>(cache->kv_heads) * cache->block_size *
+                                cache->head_dim * elt_bytes(cache->dtype);
+  const long long work = static_cast<long long>(num_pairs) * 2 * (block_bytes / 16);
+  const int threads = 256;
+  const int blocks = grid_for((work + kSwapUnroll - 1) / kSwapUnroll, threads);
+  uint8_t *dk = static_cast<uint8_t *>(k_cache), *dv = static_cast<uint8_t *>(v_cache);
+  const bool out = direction == PA_SWAP_OUT;
+  swap_blocks_kernel<<<blocks, threads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+      out ? dk : hk, out ? dv : hv, out ? hk : dk, out ? hv : dv, block_mapping, num_pairs, block_bytes,
+      out ? cache->num_blocks : host_num_blocks, out ? host_num_blocks : cache->num_blocks, device_error);
+  e = cudaGetLastError();
   return e == cudaSuccess ? PA_OK : cuda_fail(e);
 }
