@@ -19,6 +19,8 @@ int8        Symmetric int8 KV codes (round half to even, saturate), the
 cache       Host paged KV cache: the cache write through a slot mapping and
             the whole-block copy used by copy-on-write.
 attention   Single-query decode attention over the paged cache in float64.
+prefix_cache  Content-keyed full blocks with reference counts and a
+            least-recently-freed free list (prefix caching).
 
 Pages cited (by title and section):
   [P1] "【性能飞跃】从 OOM 到丝滑推理:深度工程化 RAG 架构下的内存管理艺术"
@@ -31,4 +33,4 @@ Every function here is pinned by ``-m "not gpu"`` tests in ``tests/`` to
 values the pages print, closed forms, library routines or brute force.
 """
 
-from . import allocator, attention, cache, fp8, int8  # noqa: F401
+from . import allocator, attention, cache, fp8, int8, prefix_cache  # noqa: F401
