@@ -53,9 +53,10 @@ def parse():
     ap.add_argument("--config", default=DEFAULT_CONFIG, choices=W.ALL_CONFIGS)
     ap.add_argument("--seed", type=int, default=None)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--op", default="step", choices=["step", "swap"],
+    ap.add_argument("--op", default="step", choices=["step", "swap", "prefix-cache"],
                     help="step: the decode step (default); swap: pa_swap_blocks of "
-                         "preempted sequences' blocks out to pinned host memory and back")
+                         "preempted sequences' blocks out to pinned host memory and back; "
+                         "prefix-cache: the host prefix cache building shared-prefix tables")
     ap.add_argument("--swap-seqs", type=int, default=16)
     return ap.parse_args()
 
@@ -608,11 +609,79 @@ def swap_cpu_baseline(w, out_np, budget_s: float = 5.0):
             "sample": f"{len(pairs)} block pairs swapped out by the NumPy oracle, {reps} passes"}
 
 
+# ---------------------------------------------------------------------------
+# the host prefix cache (native C++ behind the C ABI)
+# ---------------------------------------------------------------------------
+PREFIX_METRIC = "prefix cache: prompt tokens looked up and placed per second (host, native)"
+
+
+def _prefix_requests(seed, n=256, prompt_len=1024, lo=16, hi=512):
+    rng = np.random.default_rng(seed)
+    prompt = rng.integers(0, 32000, prompt_len).astype(np.int32)
+    return [np.concatenate([prompt, rng.integers(0, 32000, int(rng.integers(lo, hi + 1)))
+                            .astype(np.int32)]) for _ in range(n)]
+
+
+def _prefix_pass(c, reqs):
+    for s, t in enumerate(reqs):
+        c.add_sequence(s, t)
+    for s in range(len(reqs)):
+        c.free_sequence(s)
+
+
+def run_prefix_cache(args, rank, world):
+    """A step: 256 requests sharing one 1024-token prompt (the shared-prefix
+    decode workload's structure) are admitted, then all finish; the first
+    step computes the prompt, every later one hits it in the kept blocks."""
+    if rank != 0:
+        return
+    import paged_kv_cache_54_gb300 as pa
+    seed = args.seed if args.seed is not None else 3
+    reqs = _prefix_requests(seed)
+    nb = 64 + sum(-(-(len(t) - 1024) // 16) for t in reqs) + 64
+    c = pa.PrefixCache(nb, 16)
+    for _ in range(max(3, args.warmup)):
+        _prefix_pass(c, reqs)
+    K = min(args.steps, 200)
+    t0 = time.perf_counter()
+    for _ in range(K):
+        _prefix_pass(c, reqs)
+    dt = (time.perf_counter() - t0) / K
+    st = c.stats()
+    ntok = int(sum(len(t) for t in reqs))
+    line = {
+        "metric": PREFIX_METRIC, "value": round(ntok / dt, 1), "unit": "tokens/s", "n_gpus": world,
+        "steps": K, "warmup": max(3, args.warmup), "ms_per_step": round(dt * 1e3, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int32",
+        "data": "synthetic (seeded token ids)",
+        "config": {"workload": f"256 requests = one 1024-token prompt + U[16,512] own tokens, "
+                               f"block size 16, {nb} blocks; admit all, then free all",
+                   "tokens_per_step": ntok, "hit_rate": round(st["hit_tokens"] / st["queried_tokens"], 4)},
+        "gpu_launches": 0,
+        "roofline": None,
+        "note": "host code: no GPU kernel runs in this operation",
+    }
+    if not args.no_cpu_baseline:
+        from oracle.prefix_cache import PrefixCache
+        o = PrefixCache(nb, 16)
+        _prefix_pass(o, reqs)
+        t0, reps = time.perf_counter(), 0
+        while time.perf_counter() - t0 < 5.0:
+            _prefix_pass(o, reqs)
+            reps += 1
+        odt = (time.perf_counter() - t0) / reps
+        line["cpu_baseline"] = {"value": round(ntok / odt, 1), "unit": "tokens/s", "cores": 1,
+                                "kind": "oracle", "sample": f"the same step in the Python oracle, {reps} passes"}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse()
     rank, world, local = dist_env()
     if args.impl == "reference":
         run_reference(args, rank, world)
+    elif args.op == "prefix-cache":
+        run_prefix_cache(args, rank, world)
     elif args.op == "swap":
         run_swap(args, rank, world, local)
     else:

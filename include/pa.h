@@ -12,6 +12,13 @@
  *   pa_swap_blocks        whole-block moves between the device caches and a
  *                         pool in host memory (swap-out / swap-in).
  *
+ * and one host-side structure that hands out the blocks:
+ *
+ *   pa_prefix_cache_*     the block pool with prefix caching: full blocks
+ *                         keyed by their content and everything before it,
+ *                         shared through reference counts, kept after their
+ *                         last user until needed again.
+ *
  * Pages that state the problem (cited by title and section):
  *   [P1] "【性能飞跃】从 OOM 到丝滑推理:深度工程化 RAG 架构下的内存管理艺术"
  *        §2.1 (logical blocks mapped to scattered physical blocks through a
@@ -77,7 +84,8 @@ typedef enum {
   PA_ERR_INVALID = 1,      /* null pointer, negative size, misalignment, ... */
   PA_ERR_UNSUPPORTED = 2,  /* valid but outside the supported set below */
   PA_ERR_CUDA = 3,         /* a CUDA runtime call or launch failed */
-  PA_ERR_DEVICE_CHECK = 4  /* for callers that map a nonzero *device_error */
+  PA_ERR_DEVICE_CHECK = 4, /* for callers that map a nonzero *device_error */
+  PA_ERR_OUT_OF_BLOCKS = 5 /* the block pool cannot supply the request */
 } pa_status;
 
 typedef enum {
@@ -284,6 +292,89 @@ PA_API pa_status pa_swap_blocks(void *k_cache, void *v_cache, const pa_cache_des
                                 void *host_k, void *host_v, int64_t host_num_blocks,
                                 const int64_t *block_mapping, int32_t num_pairs,
                                 int32_t direction, int *device_error, pa_stream_t stream);
+
+/*
+ * Prefix cache (host) — the block pool behind the block tables, with
+ * prefix caching ([P3] §4.2–§4.3; [P1] §3.2).
+ *
+ * - A full block's key covers its token ids and everything before it: the
+ *   64-bit FNV-1a hash of the parent block's key (8 bytes little-endian, 0
+ *   for the first block) followed by the block's token ids (4 bytes each,
+ *   little-endian).  A hit also requires the stored parent key and token
+ *   ids to equal the request's.
+ * - pa_prefix_cache_add_sequence maps the longest run of cached full blocks
+ *   from the start of the prompt into the new table (reference count + 1)
+ *   and takes fresh blocks for the rest; only the part that missed needs
+ *   its KV computed and written.  Fresh full blocks are keyed at once (the
+ *   caller writes their KV before any later request attends to them); the
+ *   last, partial block stays private until decoding fills it.
+ * - pa_prefix_cache_free_sequence decrements the sequence's blocks, last
+ *   block first; a block at zero joins the back of the free list and keeps
+ *   its content and key until it is taken again.
+ * - Fresh blocks are taken from the front of the free list (least recently
+ *   freed first; initially the pool order), which evicts a kept key.
+ * - A request the free list cannot supply returns PA_ERR_OUT_OF_BLOCKS and
+ *   changes nothing.
+ * Ownership: the handle owns its memory (host only; no CUDA calls).  Calls
+ * on one handle must not overlap (no internal lock).  Block ids are
+ * 0..num_blocks-1, the physical blocks of the caches; slot = block *
+ * block_size + offset as everywhere in this header.
+ */
+typedef struct pa_prefix_cache pa_prefix_cache;
+
+typedef struct {
+  int64_t free_blocks;         /* blocks on the free list */
+  int64_t cached_free_blocks;  /* of which still keyed (hittable) */
+  int64_t used_blocks;         /* blocks with a nonzero reference count */
+  int64_t cached_blocks;       /* keyed blocks, used or free */
+  int64_t queried_tokens;      /* prompt tokens passed to add_sequence */
+  int64_t hit_tokens;          /* of which found cached */
+  int64_t evictions;           /* keyed free blocks taken for new content */
+} pa_prefix_cache_stats;
+
+/* pool_order: host int32 [num_blocks], a permutation giving the initial free
+ * order, or NULL for 0..num_blocks-1.  Returns NULL on invalid arguments
+ * (or out of host memory). */
+PA_API pa_prefix_cache *pa_prefix_cache_create(int32_t num_blocks, int32_t block_size,
+                                               const int32_t *pool_order);
+PA_API void pa_prefix_cache_destroy(pa_prefix_cache *cache);
+
+/* New sequence seq_id (must not exist) with its prompt tokens (host int32
+ * [num_tokens]); *num_cached_tokens (nullable) = prompt tokens found
+ * cached, a multiple of block_size. */
+PA_API pa_status pa_prefix_cache_add_sequence(pa_prefix_cache *cache, int64_t seq_id,
+                                              const int32_t *tokens, int32_t num_tokens,
+                                              int32_t *num_cached_tokens);
+
+/* One decoded token: takes a block when the last one is full; *slot
+ * (nullable) = the token's flat slot, for pa_reshape_and_cache. */
+PA_API pa_status pa_prefix_cache_append_token(pa_prefix_cache *cache, int64_t seq_id,
+                                              int32_t token, int64_t *slot);
+
+PA_API pa_status pa_prefix_cache_free_sequence(pa_prefix_cache *cache, int64_t seq_id);
+
+/* Block table of one sequence: returns its length (or -1 for an unknown
+ * sequence) and copies up to `capacity` entries to `table` (nullable);
+ * *num_tokens (nullable) = the sequence's length in tokens. */
+PA_API int32_t pa_prefix_cache_block_table(const pa_prefix_cache *cache, int64_t seq_id,
+                                           int32_t *table, int32_t capacity, int32_t *num_tokens);
+
+/* Block tables of several sequences as the host int32 [num_seqs, width]
+ * array pa_decode reads (rows zero-padded), and their lengths (host int32
+ * [num_seqs], nullable).  PA_ERR_INVALID if a sequence is unknown or has
+ * more than `width` blocks (nothing is written then). */
+PA_API pa_status pa_prefix_cache_block_tables(const pa_prefix_cache *cache, const int64_t *seq_ids,
+                                              int32_t num_seqs, int32_t *tables, int32_t width,
+                                              int32_t *seq_lens);
+
+PA_API pa_status pa_prefix_cache_get_stats(const pa_prefix_cache *cache, pa_prefix_cache_stats *out);
+
+/* The free list front to back: returns its length and copies up to
+ * `capacity` block ids (out nullable). */
+PA_API int32_t pa_prefix_cache_free_order(const pa_prefix_cache *cache, int32_t *out, int32_t capacity);
+
+/* Reference count of a block (-1 for an id out of range). */
+PA_API int32_t pa_prefix_cache_ref_count(const pa_prefix_cache *cache, int32_t block);
 
 /* Static description of a status code. */
 PA_API const char *pa_status_string(pa_status status);

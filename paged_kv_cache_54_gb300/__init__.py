@@ -10,6 +10,8 @@ functions carry the C ABI's names:
     pa_swap_blocks         whole-block moves between the device caches and
                            a pool in page-locked host memory
     pa_decode_workspace_size
+    PrefixCache            the host block pool with prefix caching
+                           (pa_prefix_cache_*)
 
 PyTorch supplies the device memory and the stream; there is no CPU or
 PyTorch fallback: if ``libpa.so`` is missing, every call raises.
@@ -36,7 +38,12 @@ if hasattr(torch, "float8_e5m2"):
 
 EXPORTED = ("pa_reshape_and_cache", "pa_decode_workspace_size", "pa_decode",
             "pa_decode_static_scratch", "pa_copy_blocks", "pa_swap_blocks",
-            "pa_status_string", "pa_last_cuda_error")
+            "pa_status_string", "pa_last_cuda_error",
+            "pa_prefix_cache_create", "pa_prefix_cache_destroy", "pa_prefix_cache_add_sequence",
+            "pa_prefix_cache_append_token", "pa_prefix_cache_free_sequence",
+            "pa_prefix_cache_block_table", "pa_prefix_cache_block_tables",
+            "pa_prefix_cache_get_stats", "pa_prefix_cache_free_order", "pa_prefix_cache_ref_count")
+PA_ERR_OUT_OF_BLOCKS = 5
 PA_SWAP_OUT, PA_SWAP_IN = 0, 1
 STATIC_SCRATCH_BYTES = 16 << 20   # PA_DECODE_STATIC_SCRATCH_BYTES
 
@@ -51,6 +58,16 @@ class PaCacheDesc(ctypes.Structure):
 
 class PaError(RuntimeError):
     pass
+
+
+class OutOfBlocks(PaError):
+    pass
+
+
+class PaPrefixCacheStats(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int64) for n in (
+        "free_blocks", "cached_free_blocks", "used_blocks", "cached_blocks",
+        "queried_tokens", "hit_tokens", "evictions")]
 
 
 _lib = None
@@ -83,6 +100,26 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.pa_swap_blocks.argtypes = [vp, vp, ctypes.POINTER(PaCacheDesc), vp, vp, ctypes.c_int64,
                                    vp, i32, i32, vp, vp]
     lib.pa_swap_blocks.restype = ctypes.c_int
+    i64, i32p = ctypes.c_int64, ctypes.POINTER(ctypes.c_int32)
+    lib.pa_prefix_cache_create.argtypes = [i32, i32, vp]
+    lib.pa_prefix_cache_create.restype = vp
+    lib.pa_prefix_cache_destroy.argtypes = [vp]
+    lib.pa_prefix_cache_destroy.restype = None
+    lib.pa_prefix_cache_add_sequence.argtypes = [vp, i64, vp, i32, i32p]
+    lib.pa_prefix_cache_append_token.argtypes = [vp, i64, i32, ctypes.POINTER(ctypes.c_int64)]
+    lib.pa_prefix_cache_free_sequence.argtypes = [vp, i64]
+    lib.pa_prefix_cache_block_table.argtypes = [vp, i64, vp, i32, i32p]
+    lib.pa_prefix_cache_block_table.restype = i32
+    lib.pa_prefix_cache_block_tables.argtypes = [vp, vp, i32, vp, i32, vp]
+    lib.pa_prefix_cache_get_stats.argtypes = [vp, ctypes.POINTER(PaPrefixCacheStats)]
+    lib.pa_prefix_cache_free_order.argtypes = [vp, vp, i32]
+    lib.pa_prefix_cache_free_order.restype = i32
+    lib.pa_prefix_cache_ref_count.argtypes = [vp, i32]
+    lib.pa_prefix_cache_ref_count.restype = i32
+    for name in ("pa_prefix_cache_add_sequence", "pa_prefix_cache_append_token",
+                 "pa_prefix_cache_free_sequence", "pa_prefix_cache_block_tables",
+                 "pa_prefix_cache_get_stats"):
+        getattr(lib, name).restype = ctypes.c_int
     lib.pa_status_string.argtypes = [ctypes.c_int]
     lib.pa_status_string.restype = ctypes.c_char_p
     lib.pa_last_cuda_error.argtypes = []
@@ -102,7 +139,8 @@ def _check(status: int, what: str) -> None:
         msg = lib.pa_status_string(status).decode()
         if status == 3:
             msg += ": " + lib.pa_last_cuda_error().decode()
-        raise PaError(f"{what} failed: {msg} (status {status})")
+        cls = OutOfBlocks if status == PA_ERR_OUT_OF_BLOCKS else PaError
+        raise cls(f"{what} failed: {msg} (status {status})")
 
 
 def _ptr(t) -> int | None:
@@ -284,3 +322,83 @@ def pa_swap_blocks(k_cache, v_cache, host_k, host_v, block_mapping, direction: s
                               block_mapping.data_ptr(), block_mapping.shape[0], codes[direction],
                               _ptr(device_error), _stream(stream)),
            "pa_swap_blocks")
+
+
+class PrefixCache:
+    """The host block pool with prefix caching (``pa_prefix_cache_*``).
+
+    Sequences are named by integer ids; token ids are int32.  Raises
+    ``OutOfBlocks`` when the free list cannot supply a request (nothing is
+    changed then)."""
+
+    def __init__(self, num_blocks: int, block_size: int, pool_order=None):
+        import numpy as np
+        self._lib = load_library()
+        self.num_blocks, self.block_size = int(num_blocks), int(block_size)
+        order = None
+        if pool_order is not None:
+            self._order = np.ascontiguousarray(pool_order, dtype=np.int32)
+            order = self._order.ctypes.data
+        self._h = self._lib.pa_prefix_cache_create(self.num_blocks, self.block_size, order)
+        if not self._h:
+            raise ValueError("invalid prefix cache arguments")
+
+    def close(self) -> None:
+        if getattr(self, "_h", None):
+            self._lib.pa_prefix_cache_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        self.close()
+
+    def add_sequence(self, seq: int, tokens) -> int:
+        import numpy as np
+        t = np.ascontiguousarray(tokens, dtype=np.int32)
+        n = ctypes.c_int32(0)
+        _check(self._lib.pa_prefix_cache_add_sequence(self._h, int(seq), t.ctypes.data, t.size,
+                                                      ctypes.byref(n)), "add_sequence")
+        return n.value
+
+    def append_token(self, seq: int, token: int) -> int:
+        slot = ctypes.c_int64(0)
+        _check(self._lib.pa_prefix_cache_append_token(self._h, int(seq), int(token),
+                                                      ctypes.byref(slot)), "append_token")
+        return slot.value
+
+    def free_sequence(self, seq: int) -> None:
+        _check(self._lib.pa_prefix_cache_free_sequence(self._h, int(seq)), "free_sequence")
+
+    def table(self, seq: int):
+        import numpy as np
+        n = self._lib.pa_prefix_cache_block_table(self._h, int(seq), None, 0, None)
+        if n < 0:
+            raise KeyError(seq)
+        out = np.zeros(max(n, 1), dtype=np.int32)
+        self._lib.pa_prefix_cache_block_table(self._h, int(seq), out.ctypes.data, n, None)
+        return out[:n].tolist()
+
+    def block_tables(self, seqs, width: int):
+        """(int32 [len(seqs), width] tables, int32 [len(seqs)] lengths)."""
+        import numpy as np
+        ids = np.ascontiguousarray(seqs, dtype=np.int64)
+        tables = np.zeros((len(ids), width), dtype=np.int32)
+        lens = np.zeros(len(ids), dtype=np.int32)
+        _check(self._lib.pa_prefix_cache_block_tables(self._h, ids.ctypes.data, len(ids),
+                                                      tables.ctypes.data, width, lens.ctypes.data),
+               "block_tables")
+        return tables, lens
+
+    def stats(self) -> dict:
+        st = PaPrefixCacheStats()
+        _check(self._lib.pa_prefix_cache_get_stats(self._h, ctypes.byref(st)), "get_stats")
+        return {n: getattr(st, n) for n, _ in PaPrefixCacheStats._fields_}
+
+    def free_order(self):
+        import numpy as np
+        n = self._lib.pa_prefix_cache_free_order(self._h, None, 0)
+        out = np.zeros(max(n, 1), dtype=np.int32)
+        self._lib.pa_prefix_cache_free_order(self._h, out.ctypes.data, n)
+        return out[:n].tolist()
+
+    def ref_count(self, block: int) -> int:
+        return int(self._lib.pa_prefix_cache_ref_count(self._h, int(block)))

@@ -21,7 +21,7 @@ CFLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE
           "-Xcompiler", "-fvisibility=hidden"]
 SOURCES = ["pa_host.cu", "pa_cache_ops.cu", "pa_decode_api.cu", "pa_decode_f16.cu",
            "pa_decode_bf16.cu", "pa_decode_e4m3.cu", "pa_decode_e5m2.cu", "pa_decode_i8.cu",
-           "pa_decode_static.cu"]
+           "pa_decode_static.cu", "pa_prefix_cache.cpp"]
 
 
 def _nvcc() -> str:
@@ -46,10 +46,10 @@ def build(verbose: bool = False, force: bool = False) -> str:
     jobs = []
     for s in SOURCES:
         src = os.path.join(CSRC, s)
-        obj = os.path.join(BUILD, s.replace(".cu", ".o"))
+        obj = os.path.join(BUILD, os.path.splitext(s)[0] + ".o")
         if force or _needs_rebuild(obj, src):
             jobs.append([nvcc, *ARCH, *CFLAGS, "-c", src, "-o", obj])
-    objs = [os.path.join(BUILD, s.replace(".cu", ".o")) for s in SOURCES]
+    objs = [os.path.join(BUILD, os.path.splitext(s)[0] + ".o") for s in SOURCES]
 
     def run(cmd):
         r = subprocess.run(cmd, capture_output=True, text=True)

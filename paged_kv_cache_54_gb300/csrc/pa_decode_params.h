@@ -25,7 +25,7 @@ constexpr int kCtasPerSm = PA_DECODE_CTAS_PER_SM;  // resident decode CTAs per S
 // sub-partitions and a warp takes all its registers from one of them, so the
 // sub-partition holding the most warps, ceil(warps / 4), sets the limit
 // (registers are allocated in units of 8 per thread).
-constexpr int regs_for_ctas(int ctas) {
+__host__ __device__ constexpr int regs_for_ctas(int ctas) {
   return (16384 / (((ctas * (kThreads / 32) + 3) / 4) * 32)) / 8 * 8 > 255
              ? 255
              : (16384 / (((ctas * (kThreads / 32) + 3) / 4) * 32)) / 8 * 8;

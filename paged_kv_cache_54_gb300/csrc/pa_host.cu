@@ -52,6 +52,7 @@ extern "C" const char *pa_status_string(pa_status status) {
     case PA_ERR_UNSUPPORTED: return "unsupported configuration";
     case PA_ERR_CUDA: return "CUDA error";
     case PA_ERR_DEVICE_CHECK: return "device-side check failed";
+    case PA_ERR_OUT_OF_BLOCKS: return "out of blocks";
   }
   return "unknown status";
 }
