@@ -76,3 +76,44 @@ def paged_decode(q: np.ndarray, k_codes: np.ndarray, v_codes: np.ndarray,
             V = gather(v_codes, dtype, head_scale(v_scale, h), block_tables[s], L, h, bs)
             out[s, heads] = attend(q[s, heads], K, V, scale)
     return out
+
+
+def paged_prefill(q: np.ndarray, q_lens, k_codes: np.ndarray, v_codes: np.ndarray,
+                  dtype: str, block_tables, seq_lens, scale: float,
+                  k_scale=1.0, v_scale=1.0) -> np.ndarray:
+    """Causal attention of several new tokens per sequence over the paged cache.
+
+    [P3] §4.2: after a prefix hit only the part that missed is computed.
+    Sequence s holds L_s = seq_lens[s] tokens in the cache, of which the
+    last n_s = q_lens[s] are new; new token j sits at position
+    p = L_s - n_s + j and attends to the tokens at positions 0..p (itself
+    included), read through the block table like the decode's:
+
+        o[j, hq] = sum_{i <= p} softmax_i(scale * <q[j, hq], k_i>) * v_i
+
+    q: [sum_s n_s, Hq, d] float64, the sequences' new tokens one after the
+    other.  Returns float64 [sum_s n_s, Hq, d].
+    """
+    T, Hq, d = q.shape
+    Hkv, bs = k_codes.shape[1], k_codes.shape[2]
+    if Hq % Hkv:
+        raise ValueError("query heads must be a multiple of KV heads")
+    G = Hq // Hkv
+    q_lens = [int(n) for n in q_lens]
+    if sum(q_lens) != T:
+        raise ValueError("q rows must equal the sum of q_lens")
+    out = np.zeros((T, Hq, d))
+    row = 0
+    for s, n in enumerate(q_lens):
+        L = int(seq_lens[s])
+        if n > L:
+            raise ValueError("more new tokens than the sequence holds")
+        for h in range(Hkv):
+            K = gather(k_codes, dtype, head_scale(k_scale, h), block_tables[s], L, h, bs)
+            V = gather(v_codes, dtype, head_scale(v_scale, h), block_tables[s], L, h, bs)
+            for j in range(n):
+                p = L - n + j
+                heads = [h * G + g for g in range(G)]
+                out[row + j, heads] = attend(q[row + j, heads], K[:p + 1], V[:p + 1], scale)
+        row += n
+    return out

@@ -313,3 +313,79 @@ def test_swap_out_and_in_round_trip():
     np.testing.assert_array_equal(a, b)
     with pytest.raises(ValueError):
         c.swap_blocks(PagedKVCache(4, w.Hkv, 16, w.d, w.cache_dtype), [(0, 0)], "out")
+
+
+def _prefill_case(seed, lens, q_lens, Hq=4, Hkv=2, d=16, bs=4, dtype="f16"):
+    w = W.random_case(seed, len(lens), Hq, Hkv, d, bs, dtype, dtype, lens)
+    c = _fill(w)
+    rng = np.random.default_rng(seed)
+    q = rng.standard_normal((sum(q_lens), Hq, d))
+    return w, c, q
+
+
+def test_prefill_whole_sequence_equals_causal_sdpa():
+    lens = [9, 23, 1]
+    w, c, q = _prefill_case(40, lens, lens)
+    out = A.paged_prefill(q, lens, c.k, c.v, "f16", w.block_tables, w.seq_lens, w.scale)
+    row = 0
+    for s, L in enumerate(lens):
+        K = torch.from_numpy(np.stack([_logical(w, s, "k")[:, h] for h in range(w.Hkv)]))
+        V = torch.from_numpy(np.stack([_logical(w, s, "v")[:, h] for h in range(w.Hkv)]))
+        Kq, Vq = K.repeat_interleave(w.G, 0), V.repeat_interleave(w.G, 0)
+        Q = torch.from_numpy(q[row:row + L]).transpose(0, 1)          # [Hq, L, d]
+        mask = torch.ones(L, L, dtype=torch.bool).tril()
+        ref = torch.nn.functional.scaled_dot_product_attention(Q, Kq, Vq, attn_mask=mask,
+                                                               scale=w.scale)
+        np.testing.assert_allclose(out[row:row + L], ref.transpose(0, 1).numpy(), rtol=1e-12,
+                                   atol=1e-14)
+        row += L
+
+
+def test_prefill_last_row_is_the_decode():
+    lens, q_lens = [30, 17, 5], [7, 17, 1]
+    w, c, q = _prefill_case(41, lens, q_lens, Hq=8, Hkv=2)
+    out = A.paged_prefill(q, q_lens, c.k, c.v, "f16", w.block_tables, w.seq_lens, w.scale)
+    last = np.cumsum(q_lens) - 1
+    dec = A.paged_decode(q[last], c.k, c.v, "f16", w.block_tables, w.seq_lens, w.scale)
+    np.testing.assert_allclose(out[last], dec, rtol=1e-13, atol=1e-15)
+
+
+def test_prefill_of_the_missed_suffix_equals_the_full_prefill():
+    """[P3] §4.2: with the prefix cached, computing only the new tokens gives
+    the rows a prefill of the whole sequence gives them."""
+    lens = [26, 40]
+    w, c, q_full = _prefill_case(42, lens, lens)
+    full = A.paged_prefill(q_full, lens, c.k, c.v, "f16", w.block_tables, w.seq_lens, w.scale)
+    cached = [16, 36]
+    q_lens = [L - k for L, k in zip(lens, cached)]
+    sel = np.concatenate([np.arange(k, L) + off for k, L, off in
+                          zip(cached, lens, np.cumsum([0] + lens[:-1]))])
+    part = A.paged_prefill(q_full[sel], q_lens, c.k, c.v, "f16", w.block_tables, w.seq_lens,
+                           w.scale)
+    np.testing.assert_allclose(part, full[sel], rtol=1e-13, atol=1e-15)
+
+
+def test_prefill_brute_force_tiny():
+    lens, q_lens = [6, 3], [4, 3]
+    w, c, q = _prefill_case(43, lens, q_lens, Hq=2, Hkv=1, d=3, bs=2)
+    out = A.paged_prefill(q, q_lens, c.k, c.v, "f16", w.block_tables, w.seq_lens, w.scale)
+    row = 0
+    for s, (L, n) in enumerate(zip(lens, q_lens)):
+        K, V = _logical(w, s, "k")[:, 0], _logical(w, s, "v")[:, 0]
+        for j in range(n):
+            p = L - n + j
+            for hq in range(2):
+                sc = [w.scale * sum(q[row + j, hq, e] * K[i, e] for e in range(3)) for i in range(p + 1)]
+                mx = max(sc)
+                ws = [math.exp(x - mx) for x in sc]
+                ref = [sum(ws[i] * V[i, e] for i in range(p + 1)) / sum(ws) for e in range(3)]
+                np.testing.assert_allclose(out[row + j, hq], ref, rtol=1e-12)
+        row += n
+
+
+def test_planted_off_by_one_causal_mask_fails(monkeypatch):
+    real = A.attend
+    monkeypatch.setattr(A, "attend", lambda q, K, V, scale: real(q, K[:-1] if len(K) > 1 else K,
+                                                                 V[:-1] if len(V) > 1 else V, scale))
+    with pytest.raises(AssertionError):
+        test_prefill_whole_sequence_equals_causal_sdpa()
