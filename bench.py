@@ -53,10 +53,12 @@ def parse():
     ap.add_argument("--config", default=DEFAULT_CONFIG, choices=W.ALL_CONFIGS)
     ap.add_argument("--seed", type=int, default=None)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--op", default="step", choices=["step", "swap", "prefix-cache"],
+    ap.add_argument("--op", default="step", choices=["step", "swap", "prefix-cache", "prefill"],
                     help="step: the decode step (default); swap: pa_swap_blocks of "
                          "preempted sequences' blocks out to pinned host memory and back; "
-                         "prefix-cache: the host prefix cache building shared-prefix tables")
+                         "prefix-cache: the host prefix cache building shared-prefix tables; "
+                         "prefill: causal prefill of each sequence's tokens after the shared "
+                         "prefix (qwen3-prefix)")
     ap.add_argument("--swap-seqs", type=int, default=16)
     return ap.parse_args()
 
@@ -675,11 +677,189 @@ def run_prefix_cache(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
+# ---------------------------------------------------------------------------
+# causal prefill of the part a prefix hit did not cover
+# ---------------------------------------------------------------------------
+PREFILL_METRIC = "paged causal prefill after a prefix hit: TFLOP/s (QK^T + PV) and new tokens/s"
+
+
+def prefill_flops(w, q_lens):
+    """Algorithmic flops: each new token j of sequence s (position p) does
+    2*d multiply-adds per key for QK^T and for PV over p + 1 keys, per
+    query head."""
+    total = 0
+    for s, n in enumerate(q_lens):
+        L = int(w.seq_lens[s])
+        keys = sum(range(L - n + 1, L + 1))          # sum over j of (p_j + 1)
+        total += 4 * w.d * w.Hq * keys
+    return total
+
+
+def run_prefill(args, rank, world, local):
+    import torch
+    import paged_kv_cache_54_gb300 as pa
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device(f"cuda:{local}"))
+    torch.cuda.set_device(local)
+    dev = f"cuda:{local}"
+    config = "qwen3-prefix"
+    seed = args.seed if args.seed is not None else W.config_seed(config)
+    w = W.make_workload(config, seed, device=dev)
+    prefix = W.CONFIGS[config]["prefix"]
+    q_lens = [int(L) - prefix for L in w.seq_lens]
+    T = sum(q_lens)
+    shape = (w.num_blocks, w.Hkv, w.bs, w.d)
+    kc = torch.zeros(shape, dtype=torch.bfloat16, device=dev)
+    vc = torch.zeros(shape, dtype=torch.bfloat16, device=dev)
+    # the cached prefix is written once (it was computed by an earlier
+    # request); each step writes the new tokens' K/V and prefills them
+    pa.pa_reshape_and_cache(w.ctx_k[:prefix].contiguous(), w.ctx_v[:prefix].contiguous(),
+                            torch.from_numpy(w.ctx_slots[:prefix]).to(dev), kc, vc)
+    gen = torch.Generator(device=dev).manual_seed(seed)
+    k_new = torch.randn((T, w.Hkv, w.d), generator=gen, device=dev).bfloat16()
+    v_new = torch.randn((T, w.Hkv, w.d), generator=gen, device=dev).bfloat16()
+    q = torch.randn((T, w.Hq, w.d), generator=gen, device=dev).bfloat16()
+    slots_np = np.concatenate([
+        [int(w.block_tables[s, p // w.bs]) * w.bs + p % w.bs for p in range(prefix, int(w.seq_lens[s]))]
+        for s in range(w.S)]).astype(np.int64)
+    slots = torch.from_numpy(slots_np).to(dev)
+    cu = torch.tensor(np.concatenate([[0], np.cumsum(q_lens)]), dtype=torch.int32, device=dev)
+    bt = torch.from_numpy(w.block_tables).to(dev)
+    sl = torch.from_numpy(w.seq_lens).to(dev)
+    out = torch.empty_like(q)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream()
+    maxq = max(q_lens)
+
+    def step(evs=None):
+        pa.pa_reshape_and_cache(k_new, v_new, slots, kc, vc, device_error=err)
+        if evs:
+            evs[0].record(stream)
+        pa.pa_prefill(out, q, cu, kc, vc, bt, sl, maxq, w.scale, device_error=err)
+        if evs:
+            evs[1].record(stream)
+
+    sampler = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    K = args.steps
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if sampler:
+        sampler.mark_start()
+    torch.cuda.synchronize()
+    t0.record(stream)
+    for i in range(K):
+        step(evs[i])
+    t1.record(stream)
+    torch.cuda.synchronize()
+    if sampler:
+        sampler.mark_end()
+    elapsed = t0.elapsed_time(t1) / 1e3
+    pf = statistics.mean(a.elapsed_time(b) for a, b in evs) / 1e3
+    if world > 1:
+        t = torch.tensor([elapsed], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed = float(t.item())
+    # end to end: q and the new K/V from pinned host memory, the output back
+    hq_, hk_, hv_ = q.cpu().pin_memory(), k_new.cpu().pin_memory(), v_new.cpu().pin_memory()
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+
+    def e2e_step():
+        q.copy_(hq_, non_blocking=True)
+        k_new.copy_(hk_, non_blocking=True)
+        v_new.copy_(hv_, non_blocking=True)
+        step()
+        out_h.copy_(out, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    KE = max(5, K // 4)
+    e0.record(stream)
+    for _ in range(KE):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_t = e0.elapsed_time(e1) / 1e3 / KE
+    clocks = sampler.finish() if sampler else None
+    derr = int(err.item())
+    if world > 1:
+        dist.destroy_process_group()
+    if rank != 0:
+        return
+    flops = prefill_flops(w, q_lens)
+    peaks, kind = measured_peaks()
+    peak = peaks.get("bf16_tflops")
+    achieved = flops / pf / 1e12
+    step_t = elapsed / K
+    line = {
+        "metric": PREFILL_METRIC, "value": round(world * flops / step_t / 1e12, 2), "unit": "TFLOP/s",
+        "n_gpus": world, "steps": K, "warmup": args.warmup, "ms_per_step": round(step_t * 1e3, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) q/K/V; the shared-prefix workload's tables and lengths)",
+        "config": {"workload": f"{config}: {w.S} seqs, cached prefix {prefix} tokens, new tokens "
+                               f"{min(q_lens)}..{max(q_lens)} (total {T}), {w.Hq}q/{w.Hkv}kv heads, "
+                               f"d {w.d}, bs {w.bs}, bf16",
+                   "new_tokens_per_step": T, "flops_per_step": flops,
+                   "l2": "K/V of the suffixes %.0f MB + the shared prefix; outputs %.0f MB"
+                         % (T * w.Hkv * w.d * 4 / 1e6, T * w.Hq * w.d * 2 / 1e6),
+                   "parallelism": f"replicas x{world}"},
+        "new_tokens_per_s": round(world * T / step_t, 1),
+        "gpu_launches": 2 * K,
+        "device_error": derr,
+        "roofline": {"kernel": "prefill_kernel (CUDA events)", "bound": "tensor",
+                     "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
+                     "frac": round(achieved / peak, 4) if peak else None,
+                     "peak_kind": f"{kind} dense bf16 (cuBLAS, burst)",
+                     "traffic": None, "avg_launch_ms": round(pf * 1e3, 4),
+                     "algorithmic_flops_per_launch": flops},
+        "e2e": {"value": round(flops / e2e_t / 1e12, 2), "unit": "TFLOP/s",
+                "h2d_bytes_per_step": int(q.numel() * 2 + k_new.numel() * 4),
+                "d2h_bytes_per_step": int(out.numel() * 2), "ms_per_step": round(e2e_t * 1e3, 4)},
+        "clocks": clocks,
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = prefill_cpu_baseline(w, q_lens, prefix)
+    print(json.dumps(line), flush=True)
+
+
+def prefill_cpu_baseline(w, q_lens, prefix, budget_s: float = 10.0):
+    """The oracle's prefill on a bounded sample: the first sequence's first
+    16 new tokens, all query heads."""
+    import torch
+    from oracle import attention as A
+    from oracle.cache import PagedKVCache
+    sub = W.subset(w, [0], 1)
+    n = min(16, q_lens[0])
+    L = prefix + n
+    c = PagedKVCache(sub.num_blocks, sub.Hkv, sub.bs, sub.d, sub.cache_dtype, fill_nan=False)
+    rng = np.random.default_rng(0)
+    c.k[:] = rng.integers(0, 1 << 15, c.k.shape, dtype=np.uint16) & 0x3BFF
+    c.v[:] = rng.integers(0, 1 << 15, c.v.shape, dtype=np.uint16) & 0x3BFF
+    q = rng.standard_normal((n, w.Hq, w.d))
+    t0, reps = time.perf_counter(), 0
+    while time.perf_counter() - t0 < budget_s:
+        A.paged_prefill(q, [n], c.k, c.v, sub.cache_dtype, sub.block_tables, np.array([L]), w.scale)
+        reps += 1
+    dt = (time.perf_counter() - t0) / reps
+    flops = 4 * w.d * w.Hq * sum(range(L - n + 1, L + 1))
+    return {"value": round(flops / dt / 1e12, 6), "unit": "TFLOP/s", "cores": _cores(), "kind": "oracle",
+            "sample": f"{n} new tokens after a {prefix}-token prefix, all {w.Hq} query heads, "
+                      f"float64 NumPy oracle, {reps} passes"}
+
+
 def main():
     args = parse()
     rank, world, local = dist_env()
     if args.impl == "reference":
         run_reference(args, rank, world)
+    elif args.op == "prefill":
+        run_prefill(args, rank, world, local)
     elif args.op == "prefix-cache":
         run_prefix_cache(args, rank, world)
     elif args.op == "swap":

@@ -8,6 +8,9 @@
  *                         or INT8 with a scale per tensor or per KV head);
  *   pa_decode             single-query decode attention over the paged cache,
  *                         reached through per-sequence block tables;
+ *   pa_prefill            causal attention of several new tokens per sequence
+ *                         over the paged cache (the part of a prompt a
+ *                         prefix-cache hit did not cover);
  *   pa_copy_blocks        whole-block copies, the copy step of copy-on-write;
  *   pa_swap_blocks        whole-block moves between the device caches and a
  *                         pool in host memory (swap-out / swap-in).
@@ -200,6 +203,42 @@ PA_API pa_status pa_decode(void *out, const void *q, int32_t q_dtype,
                     int32_t max_seq_len, float scale, int32_t partition_size,
                     void *workspace, size_t workspace_bytes, int *device_error,
                     pa_stream_t stream);
+
+/*
+ * pa_prefill — causal attention of each sequence's new tokens over all of
+ * its tokens in the paged cache ([P3] §4.2: after a prefix hit only the part
+ * that missed is computed; their K and V are written with
+ * pa_reshape_and_cache first).
+ *
+ * Sequence s holds L_s = seq_lens[s] tokens, of which the last
+ * n_s = cu_q_lens[s + 1] - cu_q_lens[s] are new.  New token j of sequence s
+ * sits at position p = L_s - n_s + j; for each query head hq, with KV head
+ * h = hq / G as in pa_decode:
+ *   out[cu_q_lens[s] + j, hq, :] =
+ *       sum_{i <= p} softmax_i(scale * <q[cu_q_lens[s] + j, hq, :], k_i>) v_i
+ * with token i read from block block_tables[s, i / block_size] at offset
+ * i % block_size.
+ *
+ *   out, q         device [cu_q_lens[num_seqs], num_q_heads, head_dim] of
+ *                  q_dtype, which must equal the cache dtype (16-bit caches
+ *                  only: PA_F16 or PA_BF16).
+ *   cu_q_lens      device int32 [num_seqs + 1], non-decreasing, from 0.
+ *   max_q_len      host upper bound of n_s, used to size the grid.
+ *   block_tables, max_blocks_per_seq, seq_lens  as in pa_decode; each
+ *                  n_s <= L_s <= max_blocks_per_seq * block_size.
+ * Device checks: a length that breaks these bounds (or n_s > max_q_len)
+ * skips the sequence and reports error 3; a block id out of range reads
+ * block 0 instead and reports error 1; a stalled pipeline reports error 4.
+ * Supported set: num_q_heads / kv_heads in {1, 2, 4, 8}; block_size and
+ * head_dim as in pa_cache_desc; num_seqs and kv_heads <= 65535.  Needs no
+ * workspace and allocates nothing.
+ */
+PA_API pa_status pa_prefill(void *out, const void *q, int32_t q_dtype, const int32_t *cu_q_lens,
+                            int32_t num_seqs, int32_t num_q_heads, int32_t max_q_len,
+                            const void *k_cache, const void *v_cache, const pa_cache_desc *cache,
+                            const int32_t *block_tables, int32_t max_blocks_per_seq,
+                            const int32_t *seq_lens, float scale, int *device_error,
+                            pa_stream_t stream);
 
 /*
  * pa_decode_static_scratch — pa_decode for callers that cannot allocate.

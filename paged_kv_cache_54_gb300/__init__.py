@@ -6,6 +6,8 @@ functions carry the C ABI's names:
 
     pa_reshape_and_cache   write new tokens' K/V into the paged caches
     pa_decode              paged single-query decode attention
+    pa_prefill             paged causal attention of several new tokens per
+                           sequence (the part a prefix hit did not cover)
     pa_copy_blocks         whole-block copies (copy-on-write)
     pa_swap_blocks         whole-block moves between the device caches and
                            a pool in page-locked host memory
@@ -36,7 +38,7 @@ if hasattr(torch, "float8_e4m3fn"):
 if hasattr(torch, "float8_e5m2"):
     _TORCH_CODES[torch.float8_e5m2] = PA_FP8_E5M2
 
-EXPORTED = ("pa_reshape_and_cache", "pa_decode_workspace_size", "pa_decode",
+EXPORTED = ("pa_reshape_and_cache", "pa_decode_workspace_size", "pa_decode", "pa_prefill",
             "pa_decode_static_scratch", "pa_copy_blocks", "pa_swap_blocks",
             "pa_status_string", "pa_last_cuda_error",
             "pa_prefix_cache_create", "pa_prefix_cache_destroy", "pa_prefix_cache_add_sequence",
@@ -97,6 +99,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.pa_decode_static_scratch.restype = ctypes.c_int
     lib.pa_copy_blocks.argtypes = [vp, vp, ctypes.POINTER(PaCacheDesc), vp, i32, vp, vp]
     lib.pa_copy_blocks.restype = ctypes.c_int
+    lib.pa_prefill.argtypes = [vp, vp, i32, vp, i32, i32, i32, vp, vp, ctypes.POINTER(PaCacheDesc),
+                               vp, i32, vp, ctypes.c_float, vp, vp]
+    lib.pa_prefill.restype = ctypes.c_int
     lib.pa_swap_blocks.argtypes = [vp, vp, ctypes.POINTER(PaCacheDesc), vp, vp, ctypes.c_int64,
                                    vp, i32, i32, vp, vp]
     lib.pa_swap_blocks.restype = ctypes.c_int
@@ -243,6 +248,31 @@ def pa_decode(out, q, k_cache, v_cache, block_tables, seq_lens, max_seq_len: int
                          partition_size, workspace.data_ptr(), workspace.numel(),
                          _ptr(device_error), _stream(stream)),
            "pa_decode")
+    return out
+
+
+def pa_prefill(out, q, cu_q_lens, k_cache, v_cache, block_tables, seq_lens, max_q_len: int,
+               scale: float, device_error=None, stream=None) -> torch.Tensor:
+    """Causal attention of the new tokens ``q [T, Hq, head_dim]`` (sequence
+    s's are rows cu_q_lens[s]..cu_q_lens[s+1]-1, its last tokens) over the
+    paged cache; writes ``out`` like ``q``."""
+    for t, n in ((out, "out"), (q, "q"), (cu_q_lens, "cu_q_lens"), (k_cache, "k_cache"),
+                 (v_cache, "v_cache"), (block_tables, "block_tables"), (seq_lens, "seq_lens")):
+        _require(t, n)
+    if cu_q_lens.dtype != torch.int32 or block_tables.dtype != torch.int32 or \
+            seq_lens.dtype != torch.int32:
+        raise ValueError("cu_q_lens, block_tables and seq_lens must be int32")
+    desc = cache_desc(k_cache)
+    qcode = _TORCH_CODES.get(q.dtype)
+    if out.dtype != q.dtype or out.shape != q.shape or q.dim() != 3:
+        raise ValueError("q/out must be [T, Hq, head_dim] of one dtype")
+    lib = load_library()
+    _check(lib.pa_prefill(out.data_ptr(), q.data_ptr(), -1 if qcode is None else qcode,
+                          cu_q_lens.data_ptr(), cu_q_lens.numel() - 1, q.shape[1], int(max_q_len),
+                          k_cache.data_ptr(), v_cache.data_ptr(), ctypes.byref(desc),
+                          block_tables.data_ptr(), block_tables.shape[1], seq_lens.data_ptr(),
+                          scale, _ptr(device_error), _stream(stream)),
+           "pa_prefill")
     return out
 
 

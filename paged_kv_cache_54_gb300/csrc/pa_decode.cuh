@@ -675,24 +675,6 @@ struct SimtState {
 // ----------------------------------------------------------------------------
 // consumer state: tensor-core mma.sync (several queries share the K/V tile)
 // ----------------------------------------------------------------------------
-template <int MT>
-__device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                         uint32_t b0, uint32_t b1) {
-  if constexpr (MT == kF16) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-        "{%0,%1,%2,%3};"
-        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-  } else {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-        "{%0,%1,%2,%3};"
-        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-  }
-}
-
 // Fragment layout of m16n8k16 (lane = 4*gq + tq):
 //   A regs: (row gq, cols 2tq..+1), (row gq+8, same), (row gq, cols 2tq+8..+9), (row gq+8, same)
 //   B regs: (rows 2tq..+1, col gq), (rows 2tq+8..+9, col gq)

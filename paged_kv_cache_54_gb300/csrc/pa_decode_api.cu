@@ -49,20 +49,6 @@ bool layout_for(int num_seqs, int num_q_heads, int kv_heads, int head_dim, int m
   return true;
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void *f = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
-  });
-  return fn;
-}
-
 // Tiled view of a cache as rows of head_dim elements, one row per (block,
 // head, token slot): 2-D [rows, 128 B] when a row is 128 bytes, 3-D
 // [rows, 2, 128 B] when it is 256 bytes; the box is one (block, head) tile

@@ -1,6 +1,8 @@
 // Host-side helpers shared by the libpa entry points.
 #pragma once
 
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -21,6 +23,10 @@ bool current_device_info(DeviceInfo *out);
 // Record the text of a failed CUDA call for pa_last_cuda_error() and return
 // PA_ERR_CUDA.
 pa_status cuda_fail(cudaError_t err);
+
+// cuTensorMapEncodeTiled from the driver (looked up once through the
+// runtime, so the library needs no link to libcuda); null if unavailable.
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
 
 inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 

@@ -1,0 +1,150 @@
+"""pa_prefill against the float64 oracle (GPU): small seeded cases over the
+supported shapes with ragged new-token counts, the shared-prefix workload at
+full size on sampled rows, and the device checks."""
+import zlib
+
+import numpy as np
+import pytest
+import torch
+
+import paged_kv_cache_54_gb300 as pa
+import workloads as W
+from oracle import attention as A
+from tests import _gpu as G
+
+pytestmark = pytest.mark.gpu
+
+# (L_s, n_s): whole prompts, suffixes after a cached prefix, single tokens,
+# lengths around the 64-key stage and the query tiles
+CASES = [(1, 1), (17, 17), (100, 37), (64, 64), (65, 1), (300, 129), (700, 5), (129, 128),
+         (250, 250), (33, 9)]
+
+
+def _seed(*key):
+    return zlib.crc32(repr(key).encode()) % 1000
+
+
+def _run(w, q, q_lens, err=None):
+    cu = torch.tensor(np.concatenate([[0], np.cumsum(q_lens)]), dtype=torch.int32, device=G.DEV)
+    out = torch.empty_like(q)
+    run = G.GpuRun(w).setup()
+    run.step()
+    err = run.err if err is None else err
+    pa.pa_prefill(out, q, cu, run.kc, run.vc, run.bt, run.sl, max(q_lens), w.scale, device_error=err)
+    torch.cuda.synchronize()
+    return out, run
+
+
+def _check(w, got, ref):
+    tol = G.TOL[w.q_dtype]
+    got = got.float().cpu().numpy().astype(np.float64)
+    bound = np.maximum(tol, G.ulp(ref, w.q_dtype))
+    err = np.abs(got - ref)
+    assert not (err > bound).any(), (f"max |err| {err.max():.3e} at "
+                                     f"{np.argwhere(err > bound)[:5].tolist()}")
+    return float(err.max())
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("bs", [8, 16, 32])
+@pytest.mark.parametrize("group", [1, 2, 4, 8])
+def test_prefill_matches_oracle(dtype, d, bs, group):
+    Hkv = 2
+    lens = [L for L, _ in CASES]
+    q_lens = [n for _, n in CASES]
+    w = W.random_case(_seed(dtype, d, bs, group), len(lens), Hkv * group, Hkv, d, bs, dtype, dtype,
+                      lens, device=G.DEV)
+    gen = torch.Generator(device=G.DEV).manual_seed(_seed("q", dtype, d, bs, group))
+    q = torch.randn((sum(q_lens), Hkv * group, d), generator=gen, device=G.DEV).to(w.q.dtype)
+    out, run = _run(w, q, q_lens)
+    assert int(run.err.item()) == 0
+    c = G.oracle_cache(w)
+    ref = A.paged_prefill(G.bits_to_f64(G.bits(q), dtype), q_lens, c.k, c.v, dtype,
+                          w.block_tables, w.seq_lens, w.scale)
+    _check(w, out, ref)
+
+
+def test_prefill_last_rows_agree_with_decode():
+    lens = [300, 77, 1024]
+    q_lens = [40, 77, 3]
+    w = W.random_case(8, len(lens), 8, 2, 128, 16, "bf16", "bf16", lens, device=G.DEV)
+    gen = torch.Generator(device=G.DEV).manual_seed(9)
+    q = torch.randn((sum(q_lens), 8, 128), generator=gen, device=G.DEV).bfloat16()
+    out, run = _run(w, q, q_lens)
+    last = np.cumsum(q_lens) - 1
+    dec = torch.empty((len(lens), 8, 128), dtype=torch.bfloat16, device=G.DEV)
+    pa.pa_decode(dec, q[torch.from_numpy(last).to(G.DEV)].contiguous(), run.kc, run.vc, run.bt,
+                 run.sl, max(lens), w.scale)
+    torch.cuda.synchronize()
+    diff = (out[torch.from_numpy(last).to(G.DEV)].float() - dec.float()).abs().max().item()
+    assert diff <= 2e-2
+
+
+def test_shared_prefix_suffix_prefill_full_size():
+    """The shared-prefix workload (256 sequences, one 1024-token prefix):
+    prefill each sequence's own tokens after the cached prefix; sampled rows
+    against the oracle computed one row at a time."""
+    w = W.make_workload("qwen3-prefix", W.config_seed("qwen3-prefix"), device=G.DEV)
+    q_lens = [int(L) - 1024 for L in w.seq_lens]
+    gen = torch.Generator(device=G.DEV).manual_seed(31)
+    q = torch.randn((sum(q_lens), w.Hq, w.d), generator=gen, device=G.DEV).bfloat16()
+    out, run = _run(w, q, q_lens)
+    assert int(run.err.item()) == 0
+    got = out.float().cpu().numpy()
+    qv = G.bits_to_f64(G.bits(q), "bf16")
+    rng = np.random.default_rng(4)
+    starts = np.concatenate([[0], np.cumsum(q_lens)])
+    worst = 0.0
+    for _ in range(24):
+        s = int(rng.integers(w.S))
+        j = int(rng.integers(q_lens[s]))
+        hq = int(rng.integers(w.Hq))
+        p = int(w.seq_lens[s]) - q_lens[s] + j
+        K, V = G.logical_kv(w, s, hq // w.G)
+        ref = A.attend(qv[starts[s] + j, hq], K[:p + 1], V[:p + 1], w.scale)[0]
+        e = float(np.abs(got[starts[s] + j, hq] - ref).max())
+        worst = max(worst, e)
+        assert e <= G.TOL["bf16"], (s, j, hq, e)
+    print(f"sampled rows, max |err| {worst:.2e}")
+
+
+def test_bad_lengths_and_blocks_are_reported():
+    lens = [40, 50]
+    w = W.random_case(3, 2, 2, 2, 64, 16, "f16", "f16", lens, device=G.DEV)
+    q = torch.randn((60, 2, 64), device=G.DEV).half()
+    # n_s > L_s for the second sequence: skipped, error 3
+    cu = torch.tensor([0, 10, 60], dtype=torch.int32, device=G.DEV)
+    run = G.GpuRun(w).setup()
+    run.step()
+    torch.cuda.synchronize()
+    out = torch.zeros_like(q)
+    pa.pa_prefill(out, q, cu, run.kc, run.vc, run.bt,
+                  torch.tensor([40, 45], dtype=torch.int32, device=G.DEV), 50, w.scale,
+                  device_error=run.err)
+    torch.cuda.synchronize()
+    assert int(run.err.item()) == 3
+    assert torch.all(out[10:] == 0) and torch.isfinite(out[:10].float()).all()
+    # a block id past the pool: error 1
+    err = torch.zeros(1, dtype=torch.int32, device=G.DEV)
+    bt = run.bt.clone()
+    bt[0, 1] = w.num_blocks + 5
+    pa.pa_prefill(out[:20], q[:20].contiguous(), torch.tensor([0, 10, 20], dtype=torch.int32, device=G.DEV),
+                  run.kc, run.vc, bt, run.sl, 10, w.scale, device_error=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 1
+
+
+def test_unsupported_inputs_are_refused_on_the_host():
+    kc = torch.zeros((4, 2, 16, 64), dtype=torch.uint8, device=G.DEV)
+    q = torch.zeros((3, 2, 64), dtype=torch.float16, device=G.DEV)
+    cu = torch.tensor([0, 3], dtype=torch.int32, device=G.DEV)
+    bt = torch.zeros((1, 4), dtype=torch.int32, device=G.DEV)
+    sl = torch.tensor([3], dtype=torch.int32, device=G.DEV)
+    lib = pa.load_library()
+    desc = pa.cache_desc(kc, "e4m3")
+    import ctypes
+    st = lib.pa_prefill(q.data_ptr(), q.data_ptr(), 0, cu.data_ptr(), 1, 2, 3, kc.data_ptr(),
+                        kc.data_ptr(), ctypes.byref(desc), bt.data_ptr(), 4, sl.data_ptr(), 0.125,
+                        None, None)
+    assert st == 2   # one-byte caches: unsupported in prefill
