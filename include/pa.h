@@ -219,9 +219,9 @@ PA_API pa_status pa_decode(void *out, const void *q, int32_t q_dtype,
  * with token i read from block block_tables[s, i / block_size] at offset
  * i % block_size.
  *
- *   out, q         device [cu_q_lens[num_seqs], num_q_heads, head_dim] of
- *                  q_dtype, which must equal the cache dtype (16-bit caches
- *                  only: PA_F16 or PA_BF16).
+ *   out, q         device [num_q_tokens, num_q_heads, head_dim] of q_dtype,
+ *                  which must equal the cache dtype (16-bit caches only:
+ *                  PA_F16 or PA_BF16); num_q_tokens = cu_q_lens[num_seqs].
  *   cu_q_lens      device int32 [num_seqs + 1], non-decreasing, from 0.
  *   max_q_len      host upper bound of n_s, used to size the grid.
  *   block_tables, max_blocks_per_seq, seq_lens  as in pa_decode; each
@@ -233,8 +233,9 @@ PA_API pa_status pa_decode(void *out, const void *q, int32_t q_dtype,
  * head_dim as in pa_cache_desc; num_seqs and kv_heads <= 65535.  Needs no
  * workspace and allocates nothing.
  */
-PA_API pa_status pa_prefill(void *out, const void *q, int32_t q_dtype, const int32_t *cu_q_lens,
-                            int32_t num_seqs, int32_t num_q_heads, int32_t max_q_len,
+PA_API pa_status pa_prefill(void *out, const void *q, int32_t q_dtype, int32_t num_q_tokens,
+                            const int32_t *cu_q_lens, int32_t num_seqs, int32_t num_q_heads,
+                            int32_t max_q_len,
                             const void *k_cache, const void *v_cache, const pa_cache_desc *cache,
                             const int32_t *block_tables, int32_t max_blocks_per_seq,
                             const int32_t *seq_lens, float scale, int *device_error,

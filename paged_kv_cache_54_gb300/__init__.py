@@ -99,7 +99,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.pa_decode_static_scratch.restype = ctypes.c_int
     lib.pa_copy_blocks.argtypes = [vp, vp, ctypes.POINTER(PaCacheDesc), vp, i32, vp, vp]
     lib.pa_copy_blocks.restype = ctypes.c_int
-    lib.pa_prefill.argtypes = [vp, vp, i32, vp, i32, i32, i32, vp, vp, ctypes.POINTER(PaCacheDesc),
+    lib.pa_prefill.argtypes = [vp, vp, i32, i32, vp, i32, i32, i32, vp, vp, ctypes.POINTER(PaCacheDesc),
                                vp, i32, vp, ctypes.c_float, vp, vp]
     lib.pa_prefill.restype = ctypes.c_int
     lib.pa_swap_blocks.argtypes = [vp, vp, ctypes.POINTER(PaCacheDesc), vp, vp, ctypes.c_int64,
@@ -267,7 +267,7 @@ def pa_prefill(out, q, cu_q_lens, k_cache, v_cache, block_tables, seq_lens, max_
     if out.dtype != q.dtype or out.shape != q.shape or q.dim() != 3:
         raise ValueError("q/out must be [T, Hq, head_dim] of one dtype")
     lib = load_library()
-    _check(lib.pa_prefill(out.data_ptr(), q.data_ptr(), -1 if qcode is None else qcode,
+    _check(lib.pa_prefill(out.data_ptr(), q.data_ptr(), -1 if qcode is None else qcode, q.shape[0],
                           cu_q_lens.data_ptr(), cu_q_lens.numel() - 1, q.shape[1], int(max_q_len),
                           k_cache.data_ptr(), v_cache.data_ptr(), ctypes.byref(desc),
                           block_tables.data_ptr(), block_tables.shape[1], seq_lens.data_ptr(),

@@ -1,19 +1,32 @@
-// Paged causal prefill: attention of each sequence's new tokens (the part a
-// prefix-cache hit did not cover) over all of its tokens in the paged cache.
+// Paged causal prefill on the 5th-generation tensor cores: attention of each
+// sequence's new tokens (the part a prefix-cache hit did not cover) over all
+// of its tokens in the paged cache.
 //
-// One CTA = one KV head h, one tile of 64 query rows of one sequence; a row
-// is a (new token, query head of h's group) pair, token-major, so a tile
-// holds 64 / G new tokens.  Warp w of the four consumer warps owns rows
-// 16w..16w+15 as the M dimension of m16n8k16 tensor-core products:
-//   S = Q K^T   (N = 64 keys of the stage, K = head_dim)
-//   O += P V    (N = head_dim,            K = the stage's 64 keys)
-// with an online softmax in base 2 between them and the causal mask (key
-// position <= the row's position).  The fifth warp stages the K and V tiles
-// of 64 keys with tiled TMA, one box per (block, 128-byte half of a row),
-// written with the 128-byte swizzle; Q, K (both operands read row-wise) and
-// V (read transposed) come out of the swizzled tiles with ldmatrix without
-// bank conflicts.  P never leaves registers: the accumulator fragment of S
-// is the A-operand fragment of P V.
+// One CTA = one KV head h and 256 query rows of one sequence, as two tiles
+// of 128; a row is a (new token, query head of h's group) pair, token-major,
+// so a CTA holds 256 / G new tokens.  Every K/V stage staged in shared memory
+// serves both tiles.  Each tile is the M = 128 dimension of tcgen05.mma, and
+// its row r lives in tensor-memory lane r (columns 256 * tile + ...):
+//   S = Q K^T   M 128, N = 64 keys of a stage, K = head_dim   (S in TMEM)
+//   O += P V    M 128, N = head_dim,  K = the stage's 64 keys  (O in TMEM)
+// Warps:
+//   0..7  softmax, one warpgroup per tile: thread r of a warpgroup owns row
+//         r.  It reads its S row from TMEM, applies the causal mask (key
+//         position <= the row's position) and an online softmax in base 2,
+//         writes P (16-bit) to shared memory as the K-major A operand of P V,
+//         and rescales its O row in TMEM when the row maximum has grown by
+//         more than 2^8 (lazy rescaling: P entries stay below 256).
+//   8     TMA: Q once (one 4-D box per tile and 128-byte half of a row),
+//         then K and V in stages of 64 keys, one box per (block, half), all
+//         with the 128-byte swizzle; block-table entries are fetched one
+//         stage ahead by the warp's lanes.
+//   9     MMA: one thread issues the products.  Both tiles' S of the next
+//         stage are issued before waiting for this stage's P, so the tensor
+//         cores work on them while the softmax warps work on P; S is
+//         double-buffered in TMEM for that.  tcgen05.commit signals
+//         completions on mbarriers.
+// TMEM: all 512 columns (per tile S: 2 x 64, O: head_dim); one CTA per SM,
+// four K/V stages in flight.
 #include <limits.h>
 #include <math.h>
 
@@ -23,18 +36,24 @@
 namespace pa {
 namespace {
 
-constexpr int kPfWarps = 4;                  // consumer warps
-constexpr int kPfRows = 16 * kPfWarps;       // query rows per CTA
-constexpr int kPfKeys = 64;                  // keys per pipeline stage
-constexpr int kPfStages = 3;
-constexpr int kPfThreads = 32 * (kPfWarps + 1);
-constexpr int kPfHalf = kPfKeys * 128;       // one 128-byte column half of a 64-key tile
+constexpr int kPfTileRows = 128;     // rows per tile (M)
+constexpr int kPfTiles = 2;          // tiles per CTA
+constexpr int kPfRows = kPfTileRows * kPfTiles;
+constexpr int kPfKeys = 64;          // keys per pipeline stage
+constexpr int kPfTmaWarp = 8;
+constexpr int kPfMmaWarp = 9;
+constexpr int kPfThreads = 32 * 10;
+constexpr int kPfHalf = kPfKeys * 128;  // one 128-byte column half of a 64-key stage
+constexpr int kPfStages = 4;
+constexpr uint32_t kPfTmemCols = 512;
+constexpr uint32_t kPfTileCols = 256;  // TMEM columns per tile
+constexpr float kPfLazy = 8.f;  // rescale O only when the row maximum grows by more (base 2)
 
 struct PrefillParams {
-  CUtensorMap tmap_k;  // [rows, head_dim] 16-bit view of each cache, box {64, block_size}
+  CUtensorMap tmap_q;  // [T, Hkv, G, head_dim] view of q, box {64, G, 1, 128/G}
+  CUtensorMap tmap_k;  // [rows, head_dim] view of each cache, box {64, block_size}
   CUtensorMap tmap_v;
   void *out;
-  const uint8_t *q;
   const int32_t *cu_q;
   const int32_t *block_tables;
   const int32_t *seq_lens;
@@ -43,273 +62,354 @@ struct PrefillParams {
   int *err;
 };
 
-struct PfHeader {
-  uint64_t full[kPfStages];
-  uint64_t empty[kPfStages];
-  int abort;
-};
-
 template <int D>
 struct PfLayout {
   static constexpr int NH = D / 64;  // 128-byte halves of a 16-bit row
   static constexpr int Q_OFF = 1024;
-  static constexpr int Q_HALF = kPfRows * 128;
-  static constexpr int STAGE_OFF = Q_OFF + NH * Q_HALF;
+  static constexpr int Q_HALF = kPfTileRows * 128;
+  static constexpr int Q_TILE = NH * Q_HALF;
+  static constexpr int P_OFF = Q_OFF + kPfTiles * Q_TILE;
+  static constexpr int P_TILE = kPfTileRows * 128;
+  static constexpr int STAGE_OFF = P_OFF + kPfTiles * P_TILE;
   static constexpr int STAGE_BYTES = 2 * NH * kPfHalf;  // K halves, then V halves
   static constexpr int SMEM = STAGE_OFF + kPfStages * STAGE_BYTES;
 };
 
-// chunk c (16 bytes) of row r in a region of 128-byte rows written with the
-// 128-byte swizzle (region 1024-byte aligned)
+struct PfHeader {
+  uint64_t kv_full[kPfStages];
+  uint64_t kv_empty[kPfStages];
+  uint64_t s_full[kPfTiles][2];
+  uint64_t p_full[kPfTiles];
+  uint64_t pv_done[kPfTiles];
+  uint64_t q_full;
+  uint64_t fin;
+  uint32_t tmem_base;
+  int abort;
+};
+
+// chunk c (16 bytes) of row r in a region of 128-byte rows with the 128-byte
+// swizzle (region 1024-byte aligned)
 __device__ __forceinline__ uint32_t swz128(int r, int c) {
   return static_cast<uint32_t>(r * 128 + ((c ^ (r & 7)) << 4));
 }
 
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 template <int DT, int D, int G>
-__global__ void __launch_bounds__(kPfThreads, 2) prefill_kernel(const __grid_constant__ PrefillParams p) {
+__global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_constant__ PrefillParams p) {
   using Lay = PfLayout<D>;
   constexpr int NH = Lay::NH;
-  constexpr int QT = kPfRows / G;  // new tokens per CTA
+  constexpr int NS = kPfStages;
+  constexpr int QT = kPfTileRows / G;  // new tokens per tile
+  constexpr int QC = kPfRows / G;      // new tokens per CTA
   constexpr int KSTEPS = D / 16;
-  constexpr int NTD = D / 8;  // n-tiles of the output
+  constexpr int AB = DT == kF16 ? 0 : 1;
+  constexpr uint32_t IDESC_QK = umma_idesc_f16(AB, kPfTileRows, kPfKeys, false);
+  constexpr uint32_t IDESC_PV = umma_idesc_f16(AB, kPfTileRows, D, true);
   extern __shared__ __align__(1024) uint8_t smem[];
   PfHeader &hdr = *reinterpret_cast<PfHeader *>(smem);
-  const int tile = gridDim.x - 1 - blockIdx.x;  // the longest (last) tiles start first
+  const int cta = gridDim.x - 1 - blockIdx.x;  // the longest (last) token ranges start first
   const int s = blockIdx.y, h = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   const int q0 = __ldg(p.cu_q + s);
   const int n = __ldg(p.cu_q + s + 1) - q0;
   const int L = __ldg(p.seq_lens + s);
-  if (n < 0 || L < n || L > p.max_blocks * p.block_size || n > static_cast<int>(gridDim.x) * QT) {
+  if (n < 0 || L < n || L > p.max_blocks * p.block_size || n > static_cast<int>(gridDim.x) * QC) {
     if (threadIdx.x == 0 && blockIdx.x == 0) record_error(p.err, kErrSeqLen);
     return;
   }
-  if (tile * QT >= n) return;
+  if (cta * QC >= n) return;
   if ((smem_addr(smem) & 1023u) != 0) {  // the swizzle needs 1024-byte atoms
     if (threadIdx.x == 0) record_error(p.err, kErrSmemAlign);
     return;
   }
-  const int pos0 = L - n;                        // position of new token 0
-  const int kv_end = pos0 + min(n, (tile + 1) * QT);  // keys 0..kv_end-1 are needed
-  const int n_tiles = (kv_end + kPfKeys - 1) / kPfKeys;
+  const int tiles = cta * QC + QT < n ? 2 : 1;          // the second tile may hold no new token
+  const int pos0 = L - n;                               // position of new token 0
+  const int kv_end = pos0 + min(n, (cta + 1) * QC);     // keys 0..kv_end-1 are needed
+  const int n_stages = (kv_end + kPfKeys - 1) / kPfKeys;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kPfStages; ++i) {
-      mbar_init(&hdr.full[i], 1);
-      mbar_init(&hdr.empty[i], kPfWarps);
+    for (int i = 0; i < NS; ++i) {
+      mbar_init(&hdr.kv_full[i], 1);
+      mbar_init(&hdr.kv_empty[i], 1);
     }
+    for (int t = 0; t < kPfTiles; ++t) {
+      mbar_init(&hdr.s_full[t][0], 1);
+      mbar_init(&hdr.s_full[t][1], 1);
+      mbar_init(&hdr.p_full[t], kPfTileRows);
+      mbar_init(&hdr.pv_done[t], 1);
+    }
+    mbar_init(&hdr.q_full, 1);
+    mbar_init(&hdr.fin, 1);
     hdr.abort = 0;
     fence_mbar_init();
   }
+  if (warp == kPfMmaWarp) tc_alloc(&hdr.tmem_base, kPfTmemCols);
+  tc_fence_before_sync();
   __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = hdr.tmem_base;
   uint8_t *qs = smem + Lay::Q_OFF;
+  uint8_t *ps = smem + Lay::P_OFF;
   uint8_t *stages = smem + Lay::STAGE_OFF;
+  volatile int *abort = &hdr.abort;
 
-  // ---------------------------------------------------------------- producer
-  if (warp == kPfWarps) {
-    if (lane != 0) return;
+  if (warp == kPfTmaWarp) {
+    // ------------------------------------------------------------ TMA
+    // The whole warp runs the loop: lane j fetches block-table entry j of the
+    // next stage while lane 0 issues this stage's copies.
+    if (lane == 0) {
+      mbar_arrive_expect_tx(&hdr.q_full, tiles * NH * kPfTileRows * 128u);
+      for (int t = 0; t < tiles; ++t)
+#pragma unroll
+        for (int hf = 0; hf < NH; ++hf)
+          tma_load_4d(qs + t * Lay::Q_TILE + hf * Lay::Q_HALF, &p.tmap_q, hf * 64, 0, h, q0 + cta * QC + t * QT,
+                      &hdr.q_full);
+    }
     const int bs = p.block_size;
-    const int bpt = kPfKeys / bs;  // blocks per stage
+    const int bpt = kPfKeys / bs;  // blocks per stage (<= 8)
+    const int32_t *table = p.block_tables + static_cast<size_t>(s) * p.max_blocks;
+    auto stage_blocks = [&](int i) { return min(bpt, (kv_end - i * kPfKeys + bs - 1) / bs); };
+    int next = lane < stage_blocks(0) ? __ldg(table + lane) : 0;
     int issued = 0;
     bool ok = true;
-    for (int i = 0; i < n_tiles; ++i) {
-      const int st = i % kPfStages;
-      if (i >= kPfStages && !mbar_wait(&hdr.empty[st], ((i / kPfStages) - 1) & 1, &hdr.abort)) {
+    for (int i = 0; i < n_stages; ++i) {
+      const int st = i % NS;
+      const int nblk = stage_blocks(i);
+      int phys = next;
+      if (i + 1 < n_stages && lane < stage_blocks(i + 1)) next = __ldg(table + (i + 1) * bpt + lane);
+      if (lane < nblk && (phys < 0 || phys >= p.num_blocks)) {
+        record_error(p.err, kErrBlockIndex);
+        phys = 0;  // read a valid block; the result is void and flagged
+      }
+      bool waited = true;
+      if (lane == 0 && i >= NS) waited = mbar_wait(&hdr.kv_empty[st], ((i / NS) - 1) & 1, abort);
+      if (!__shfl_sync(0xffffffffu, waited, 0)) {
         ok = false;
         break;
       }
-      const int k0 = i * kPfKeys;
-      const int nblk = min(bpt, (kv_end - k0 + bs - 1) / bs);
-      mbar_arrive_expect_tx(&hdr.full[st], 2u * NH * static_cast<uint32_t>(nblk * bs) * 128u);
       uint8_t *kb = stages + st * Lay::STAGE_BYTES;
       uint8_t *vb = kb + NH * kPfHalf;
-      const int32_t *row = p.block_tables + static_cast<size_t>(s) * p.max_blocks + k0 / bs;
+      if (lane == 0) mbar_arrive_expect_tx(&hdr.kv_full[st], 2u * NH * static_cast<uint32_t>(nblk * bs) * 128u);
       for (int j = 0; j < nblk; ++j) {
-        int phys = __ldg(row + j);
-        if (phys < 0 || phys >= p.num_blocks) {
-          record_error(p.err, kErrBlockIndex);
-          phys = 0;  // read a valid block; the result is void and flagged
-        }
-        const int r0 = (phys * p.num_kv_heads + h) * bs;
+        const int pj = __shfl_sync(0xffffffffu, phys, j);
+        if (lane == 0) {
+          const int r0 = (pj * p.num_kv_heads + h) * bs;
 #pragma unroll
-        for (int hf = 0; hf < NH; ++hf) {
-          tma_load_2d(kb + hf * kPfHalf + j * bs * 128, &p.tmap_k, hf * 64, r0, &hdr.full[st]);
-          tma_load_2d(vb + hf * kPfHalf + j * bs * 128, &p.tmap_v, hf * 64, r0, &hdr.full[st]);
+          for (int hf = 0; hf < NH; ++hf) {
+            tma_load_2d(kb + hf * kPfHalf + j * bs * 128, &p.tmap_k, hf * 64, r0, &hdr.kv_full[st]);
+            tma_load_2d(vb + hf * kPfHalf + j * bs * 128, &p.tmap_v, hf * 64, r0, &hdr.kv_full[st]);
+          }
         }
       }
       issued = i + 1;
     }
+    if (lane == 0) {
+      if (!ok) {
+        record_error(p.err, kErrTimeout);
+        *abort = 1;
+        // wait, within the limit, for the copies still in flight
+        for (int j = max(0, issued - NS); j < issued; ++j)
+          mbar_wait(&hdr.kv_full[j % NS], (j / NS) & 1, nullptr);
+      }
+      mbar_wait(&hdr.q_full, 0, nullptr);
+    }
+  } else if (warp == kPfMmaWarp) {
+    // ------------------------------------------------------------ MMA
+    if (lane == 0) {
+      bool ok = mbar_wait(&hdr.q_full, 0, abort);
+      const uint32_t qaddr = smem_addr(qs), paddr = smem_addr(ps), saddr = smem_addr(stages);
+      auto issue_qk = [&](int i) -> bool {
+        const int st = i % NS;
+        if (!mbar_wait(&hdr.kv_full[st], (i / NS) & 1, abort)) return false;
+        tc_fence_after_sync();
+        const uint32_t kb = saddr + st * Lay::STAGE_BYTES;
+        for (int t = 0; t < tiles; ++t) {
+          const uint32_t d = tmem + t * kPfTileCols + (i & 1) * kPfKeys;
+          const uint32_t qt = qaddr + t * Lay::Q_TILE;
+#pragma unroll
+          for (int kk = 0; kk < KSTEPS; ++kk) {
+            const uint32_t off = (kk % 4) * 32;  // 16 elements = 32 bytes into the swizzled row
+            const uint64_t a = umma_desc_sw128(qt + (kk / 4) * Lay::Q_HALF + off, 16, 1024);
+            const uint64_t b = umma_desc_sw128(kb + (kk / 4) * kPfHalf + off, 16, 1024);
+            tc_mma_f16(d, a, b, IDESC_QK, kk > 0);
+          }
+          tc_commit(&hdr.s_full[t][i & 1]);
+        }
+        return true;
+      };
+      if (ok) ok = issue_qk(0);
+      for (int i = 0; i < n_stages && ok; ++i) {
+        if (i + 1 < n_stages && !issue_qk(i + 1)) {
+          ok = false;
+          break;
+        }
+        const uint32_t vb = saddr + (i % NS) * Lay::STAGE_BYTES + NH * kPfHalf;
+        for (int t = 0; t < tiles; ++t) {
+          if (!mbar_wait(&hdr.p_full[t], i & 1, abort)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+          const uint32_t pt = paddr + t * Lay::P_TILE;
+#pragma unroll
+          for (int kk = 0; kk < kPfKeys / 16; ++kk) {
+            const uint64_t a = umma_desc_sw128(pt + kk * 32, 16, 1024);
+            const uint64_t b = umma_desc_sw128(vb + kk * 2048, kPfHalf, 1024);
+            tc_mma_f16(tmem + t * kPfTileCols + 2 * kPfKeys, a, b, IDESC_PV, (i > 0 || kk > 0) ? 1u : 0u);
+          }
+          tc_commit(&hdr.pv_done[t]);
+        }
+        if (!ok) break;
+        tc_commit(&hdr.kv_empty[i % NS]);
+      }
+      if (!ok) {
+        record_error(p.err, kErrTimeout);
+        *abort = 1;
+      }
+      // every product issued has completed before the memory is released
+      tc_commit(&hdr.fin);
+      mbar_wait(&hdr.fin, 0, nullptr);
+    }
+  } else if (warp / 4 < tiles) {
+    // ------------------------------------------------------------ softmax
+    const int t = warp / 4;                  // tile
+    const int r = threadIdx.x & 127;         // row = TMEM lane
+    const int tok = cta * QC + t * QT + r / G;
+    const int pos = pos0 + min(tok, n - 1);  // rows past the new tokens take the last one's (not stored)
+    const uint32_t trow = tmem + t * kPfTileCols + (static_cast<uint32_t>(32 * (warp & 3)) << 16);
+    uint8_t *pt = ps + t * Lay::P_TILE;
+    float m = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int i = 0; i < n_stages; ++i) {
+      if (!__all_sync(0xffffffffu, mbar_wait(&hdr.s_full[t][i & 1], (i >> 1) & 1, abort))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after_sync();
+      const int k0 = i * kPfKeys;
+      float sv[kPfKeys];
+      {
+        uint32_t raw[32];
+        tc_ld32(trow + (i & 1) * kPfKeys, raw);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) sv[j] = __uint_as_float(raw[j]);
+        tc_ld32(trow + (i & 1) * kPfKeys + 32, raw);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) sv[32 + j] = __uint_as_float(raw[j]);
+      }
+      float mx0 = -INFINITY, mx1 = -INFINITY;  // two chains for the maximum
+#pragma unroll
+      for (int j = 0; j < kPfKeys; j += 2) {
+        sv[j] = (k0 + j <= pos) ? sv[j] * p.qk_scale_log2 : -INFINITY;
+        sv[j + 1] = (k0 + j + 1 <= pos) ? sv[j + 1] * p.qk_scale_log2 : -INFINITY;
+        mx0 = fmaxf(mx0, sv[j]);
+        mx1 = fmaxf(mx1, sv[j + 1]);
+      }
+      const float mx = fmaxf(mx0, mx1);
+      // the previous P V must be done before P and O are touched again
+      if (i > 0 && !__all_sync(0xffffffffu, mbar_wait(&hdr.pv_done[t], (i - 1) & 1, abort))) {
+        ok = false;
+        break;
+      }
+      const bool grow = mx > m + kPfLazy;
+      if (__any_sync(0xffffffffu, grow && i > 0)) {  // tcgen05.ld / st are warp-wide
+        tc_fence_after_sync();
+        const float alpha = grow ? fast_exp2(m - mx) : 1.f;
+#pragma unroll
+        for (int c = 0; c < D; c += 32) {
+          uint32_t ov[32];
+          tc_ld32(trow + 2 * kPfKeys + c, ov);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) ov[j] = __float_as_uint(__uint_as_float(ov[j]) * alpha);
+          tc_st32(trow + 2 * kPfKeys + c, ov);
+        }
+      }
+      if (grow) {
+        l *= fast_exp2(m - mx);  // 0 while m is -inf (l is 0 then)
+        m = mx;
+      }
+      const float base = m == -INFINITY ? 0.f : m;
+      uint32_t pw[kPfKeys / 2];
+      float l0 = 0.f, l1 = 0.f;
+#pragma unroll
+      for (int j = 0; j < kPfKeys; j += 2) {
+        const float a = fast_exp2(sv[j] - base), b = fast_exp2(sv[j + 1] - base);
+        l0 += a;
+        l1 += b;
+        pw[j / 2] = pack2_rn<DT>(a, b);
+      }
+      l += l0 + l1;
+#pragma unroll
+      for (int c = 0; c < 8; ++c)
+        *reinterpret_cast<uint4 *>(pt + swz128(r, c)) = make_uint4(pw[4 * c], pw[4 * c + 1], pw[4 * c + 2],
+                                                                    pw[4 * c + 3]);
+      if (t == 0 && k0 + kPfKeys > kv_end) {
+        // keys past kv_end hold stale (possibly NaN) values: zero their V rows,
+        // since 0 * NaN would reach O (tile 0's P V is issued first)
+        if (!__all_sync(0xffffffffu, mbar_wait(&hdr.kv_full[i % NS], (i / NS) & 1, abort))) {
+          ok = false;
+          break;
+        }
+        uint8_t *vb = stages + (i % NS) * Lay::STAGE_BYTES + NH * kPfHalf;
+        const int z0 = kv_end - k0;
+        for (int idx = r; idx < (kPfKeys - z0) * 8 * NH; idx += kPfTileRows) {
+          const int hf = idx / ((kPfKeys - z0) * 8), rem = idx % ((kPfKeys - z0) * 8);
+          *reinterpret_cast<uint4 *>(vb + hf * kPfHalf + (z0 + rem / 8) * 128 + (rem % 8) * 16) =
+              make_uint4(0u, 0u, 0u, 0u);
+        }
+      }
+      fence_proxy_async_smem();  // P (and zeroed V rows) visible to the tensor cores
+      tc_fence_before_sync();    // O stores ordered before the arrive
+      mbar_arrive(&hdr.p_full[t]);
+    }
     if (!ok) {
       record_error(p.err, kErrTimeout);
-      hdr.abort = 1;
-      // wait, within the limit, for the copies still in flight
-      for (int j = max(0, issued - kPfStages); j < issued; ++j)
-        mbar_wait(&hdr.full[j % kPfStages], (j / kPfStages) & 1, nullptr);
-    }
-    return;
-  }
-
-  // ---------------------------------------------------------------- consumers
-  const int gq = lane >> 2, tq = lane & 3;
-  // Q rows of the tile into shared memory (zeros past the new tokens)
-  for (int idx = threadIdx.x; idx < kPfRows * (D / 8); idx += kPfWarps * 32) {
-    const int r = idx / (D / 8), c = idx % (D / 8);
-    const int t = tile * QT + r / G;
-    const int hq = h * G + r % G;
-    uint4 v = make_uint4(0u, 0u, 0u, 0u);
-    if (t < n)
-      v = __ldg(reinterpret_cast<const uint4 *>(
-          p.q + ((static_cast<size_t>(q0 + t) * p.num_q_heads + hq) * D + c * 8) * 2));
-    *reinterpret_cast<uint4 *>(qs + (c / 8) * Lay::Q_HALF + swz128(r, c % 8)) = v;
-  }
-  named_bar_sync(1, kPfWarps * 32);
-  uint32_t qa[KSTEPS][4];
+      *abort = 1;
+    } else if (__all_sync(0xffffffffu, mbar_wait(&hdr.pv_done[t], (n_stages - 1) & 1, abort))) {
+      tc_fence_after_sync();
+      const float inv = 1.f / l;
+      const bool store = tok < n;
+      uint8_t *row = static_cast<uint8_t *>(p.out) +
+                     (static_cast<size_t>(q0 + min(tok, n - 1)) * p.num_q_heads + h * G + r % G) * D * 2;
 #pragma unroll
-  for (int kk = 0; kk < KSTEPS; ++kk) {
-    const int r = 16 * warp + (lane & 7) + ((lane >> 3) & 1) * 8;
-    const int c = 2 * kk + (lane >> 4);
-    ldsm_x4(smem_addr(qs + (c / 8) * Lay::Q_HALF + swz128(r, c % 8)), qa[kk][0], qa[kk][1], qa[kk][2],
-            qa[kk][3]);
-  }
-  // positions of the lane's two rows (rows past the new tokens take the last
-  // one's, and are not stored)
-  const int ra = 16 * warp + gq, rb = ra + 8;
-  const int ta = tile * QT + ra / G, tb = tile * QT + rb / G;
-  const int pa_ = pos0 + min(ta, n - 1), pb_ = pos0 + min(tb, n - 1);
-  const int pmax = pos0 + min(tile * QT + (16 * warp + 15) / G, n - 1);
-
-  float o[NTD][4];
+      for (int c = 0; c < D; c += 32) {
+        uint32_t ov[32];
+        tc_ld32(trow + 2 * kPfKeys + c, ov);
+        if (store) {
 #pragma unroll
-  for (int j = 0; j < NTD; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
-  float ma = -INFINITY, mb = -INFINITY, la = 0.f, lb = 0.f;
-  const volatile int *abort = &hdr.abort;
-  bool ok = true;
-  for (int i = 0; i < n_tiles; ++i) {
-    const int st = i % kPfStages;
-    if (!mbar_wait(&hdr.full[st], (i / kPfStages) & 1, abort)) {
-      ok = false;
-      break;
-    }
-    const int k0 = i * kPfKeys;
-    if (k0 <= pmax) {  // else every key of the stage is past all the warp's rows
-      const uint8_t *kb = stages + st * Lay::STAGE_BYTES;
-      const uint8_t *vb = kb + NH * kPfHalf;
-      // ---- S = Q K^T ----
-      float sc[8][4];
-#pragma unroll
-      for (int j = 0; j < 8; ++j) sc[j][0] = sc[j][1] = sc[j][2] = sc[j][3] = 0.f;
-#pragma unroll
-      for (int kk = 0; kk < KSTEPS; ++kk) {
-        const int c = 2 * kk + ((lane >> 3) & 1);
-#pragma unroll
-        for (int jp = 0; jp < 4; ++jp) {
-          const int key = 16 * jp + (lane & 7) + (lane >> 4) * 8;
-          uint32_t b0, b1, b2, b3;
-          ldsm_x4(smem_addr(kb + (c / 8) * kPfHalf + swz128(key, c % 8)), b0, b1, b2, b3);
-          mma16816<DT>(sc[2 * jp], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], b0, b1);
-          mma16816<DT>(sc[2 * jp + 1], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], b2, b3);
-        }
-      }
-      // ---- scale, causal mask, online softmax (rows ra: regs 0,1; rb: regs 2,3) ----
-      float xa = -INFINITY, xb = -INFINITY;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int key = k0 + 8 * j + 2 * tq + e;
-          sc[j][e] = key <= pa_ ? sc[j][e] * p.qk_scale_log2 : -INFINITY;
-          sc[j][2 + e] = key <= pb_ ? sc[j][2 + e] * p.qk_scale_log2 : -INFINITY;
-          xa = fmaxf(xa, sc[j][e]);
-          xb = fmaxf(xb, sc[j][2 + e]);
-        }
-      }
-      xa = fmaxf(xa, __shfl_xor_sync(0xffffffffu, xa, 1));
-      xa = fmaxf(xa, __shfl_xor_sync(0xffffffffu, xa, 2));
-      xb = fmaxf(xb, __shfl_xor_sync(0xffffffffu, xb, 1));
-      xb = fmaxf(xb, __shfl_xor_sync(0xffffffffu, xb, 2));
-      const float na = fmaxf(ma, xa), nb = fmaxf(mb, xb);
-      const float ba = na == -INFINITY ? 0.f : na, bb = nb == -INFINITY ? 0.f : nb;
-      const float aa = exp2f(ma - ba), ab = exp2f(mb - bb);
-      ma = na;
-      mb = nb;
-      la *= aa;
-      lb *= ab;
-#pragma unroll
-      for (int j = 0; j < NTD; ++j) {
-        o[j][0] *= aa;
-        o[j][1] *= aa;
-        o[j][2] *= ab;
-        o[j][3] *= ab;
-      }
-      uint32_t pf[4][4];  // P as the A operand, k-step kk2 = keys 16kk2..16kk2+15
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const float p0 = exp2f(sc[j][0] - ba), p1 = exp2f(sc[j][1] - ba);
-        const float p2 = exp2f(sc[j][2] - bb), p3 = exp2f(sc[j][3] - bb);
-        la += p0 + p1;
-        lb += p2 + p3;
-        pf[j >> 1][(j & 1) * 2] = pack2_rn<DT>(p0, p1);
-        pf[j >> 1][(j & 1) * 2 + 1] = pack2_rn<DT>(p2, p3);
-      }
-      // ---- O += P V ----
-      const bool tail = k0 + kPfKeys > kv_end;  // keys >= kv_end hold stale data: zero their V
-#pragma unroll
-      for (int kk2 = 0; kk2 < 4; ++kk2) {
-        const int key = 16 * kk2 + (lane & 7) + ((lane >> 3) & 1) * 8;
-#pragma unroll
-        for (int ndp = 0; ndp < NTD / 2; ++ndp) {
-          const int c = 2 * ndp + (lane >> 4);
-          uint32_t b0, b1, b2, b3;
-          ldsm_x4_trans(smem_addr(vb + (c / 8) * kPfHalf + swz128(key, c % 8)), b0, b1, b2, b3);
-          if (tail) {
-            const int ka = k0 + 16 * kk2 + 2 * tq, kb2 = ka + 8;
-            const uint32_t ma0 = (ka < kv_end ? 0x0000FFFFu : 0u) | (ka + 1 < kv_end ? 0xFFFF0000u : 0u);
-            const uint32_t mb0 = (kb2 < kv_end ? 0x0000FFFFu : 0u) | (kb2 + 1 < kv_end ? 0xFFFF0000u : 0u);
-            b0 &= ma0;
-            b2 &= ma0;
-            b1 &= mb0;
-            b3 &= mb0;
+          for (int j = 0; j < 32; j += 8) {
+            uint4 v;
+            v.x = pack2_rn<DT>(__uint_as_float(ov[j]) * inv, __uint_as_float(ov[j + 1]) * inv);
+            v.y = pack2_rn<DT>(__uint_as_float(ov[j + 2]) * inv, __uint_as_float(ov[j + 3]) * inv);
+            v.z = pack2_rn<DT>(__uint_as_float(ov[j + 4]) * inv, __uint_as_float(ov[j + 5]) * inv);
+            v.w = pack2_rn<DT>(__uint_as_float(ov[j + 6]) * inv, __uint_as_float(ov[j + 7]) * inv);
+            *reinterpret_cast<uint4 *>(row + (c + j) * 2) = v;
           }
-          mma16816<DT>(o[2 * ndp], pf[kk2][0], pf[kk2][1], pf[kk2][2], pf[kk2][3], b0, b1);
-          mma16816<DT>(o[2 * ndp + 1], pf[kk2][0], pf[kk2][1], pf[kk2][2], pf[kk2][3], b2, b3);
         }
       }
-    }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&hdr.empty[st]);
-  }
-  if (!ok) {
-    if (lane == 0) {
+    } else {
       record_error(p.err, kErrTimeout);
-      hdr.abort = 1;
+      *abort = 1;
     }
-    return;
   }
-  // ---- normalise and store ----
-  la += __shfl_xor_sync(0xffffffffu, la, 1);
-  la += __shfl_xor_sync(0xffffffffu, la, 2);
-  lb += __shfl_xor_sync(0xffffffffu, lb, 1);
-  lb += __shfl_xor_sync(0xffffffffu, lb, 2);
-  const float ia = 1.f / la, ib = 1.f / lb;
-  uint8_t *out = static_cast<uint8_t *>(p.out);
-  if (ta < n) {
-    uint8_t *row = out + (static_cast<size_t>(q0 + ta) * p.num_q_heads + h * G + ra % G) * D * 2;
-#pragma unroll
-    for (int j = 0; j < NTD; ++j)
-      *reinterpret_cast<uint32_t *>(row + (8 * j + 2 * tq) * 2) = pack2_rn<DT>(o[j][0] * ia, o[j][1] * ia);
-  }
-  if (tb < n) {
-    uint8_t *row = out + (static_cast<size_t>(q0 + tb) * p.num_q_heads + h * G + rb % G) * D * 2;
-#pragma unroll
-    for (int j = 0; j < NTD; ++j)
-      *reinterpret_cast<uint32_t *>(row + (8 * j + 2 * tq) * 2) = pack2_rn<DT>(o[j][2] * ib, o[j][3] * ib);
+  // ------------------------------------------------------------ teardown
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == kPfMmaWarp) {
+    tc_fence_after_sync();
+    tc_dealloc(tmem, kPfTmemCols);
   }
 }
 
 template <int DT, int D, int G>
 pa_status launch_prefill(const PrefillParams &p, int num_seqs, int max_q_len, cudaStream_t stream) {
-  constexpr int QT = kPfRows / G;
+  constexpr int QC = kPfRows / G;
   static bool configured[64];  // per device: dynamic shared memory already allowed
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -320,7 +420,7 @@ pa_status launch_prefill(const PrefillParams &p, int num_seqs, int max_q_len, cu
     if (e != cudaSuccess) return cuda_fail(e);
     if (dev >= 0 && dev < 64) configured[dev] = true;
   }
-  const dim3 grid((max_q_len + QT - 1) / QT, num_seqs, p.num_kv_heads);
+  const dim3 grid((max_q_len + QC - 1) / QC, num_seqs, p.num_kv_heads);
   prefill_kernel<DT, D, G><<<grid, kPfThreads, PfLayout<D>::SMEM, stream>>>(p);
   e = cudaGetLastError();
   return e == cudaSuccess ? PA_OK : cuda_fail(e);
@@ -339,7 +439,7 @@ pa_status by_group(int G, const PrefillParams &p, int num_seqs, int max_q_len, c
 
 // [rows, head_dim] view of a 16-bit cache, box {64 elements, block_size rows}
 // (one 128-byte half of one (block, head) tile), 128-byte swizzle.
-bool encode_prefill_map(CUtensorMap *map, const void *cache, const pa_cache_desc *c) {
+bool encode_cache_view(CUtensorMap *map, const void *cache, const pa_cache_desc *c) {
   PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
   if (enc == nullptr) return false;
   const cuuint64_t rows = static_cast<cuuint64_t>(c->num_blocks) * c->kv_heads * c->block_size;
@@ -352,20 +452,38 @@ bool encode_prefill_map(CUtensorMap *map, const void *cache, const pa_cache_desc
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// [T, Hkv, G, head_dim] view of q, box {64 elements, G, 1, 128 / G}: one
+// 128-byte half of the 128 (token, head) rows of a tile, token-major; rows
+// past T read as zeros.
+bool encode_q_view(CUtensorMap *map, const void *q, int num_tokens, int kv_heads, int G, int head_dim) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (enc == nullptr) return false;
+  const cuuint64_t row = static_cast<cuuint64_t>(head_dim) * 2;
+  const cuuint64_t dims[4] = {static_cast<cuuint64_t>(head_dim), static_cast<cuuint64_t>(G),
+                              static_cast<cuuint64_t>(kv_heads), static_cast<cuuint64_t>(num_tokens)};
+  const cuuint64_t strides[3] = {row, row * G, row * G * kv_heads};
+  const cuuint32_t box[4] = {64, static_cast<cuuint32_t>(G), 1, static_cast<cuuint32_t>(kPfTileRows / G)};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 4, const_cast<void *>(q), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace
 }  // namespace pa
 
 using namespace pa;
 
-extern "C" pa_status pa_prefill(void *out, const void *q, int32_t q_dtype, const int32_t *cu_q_lens,
-                                int32_t num_seqs, int32_t num_q_heads, int32_t max_q_len, const void *k_cache,
-                                const void *v_cache, const pa_cache_desc *cache, const int32_t *block_tables,
+extern "C" pa_status pa_prefill(void *out, const void *q, int32_t q_dtype, int32_t num_q_tokens,
+                                const int32_t *cu_q_lens, int32_t num_seqs, int32_t num_q_heads,
+                                int32_t max_q_len, const void *k_cache, const void *v_cache,
+                                const pa_cache_desc *cache, const int32_t *block_tables,
                                 int32_t max_blocks_per_seq, const int32_t *seq_lens, float scale,
                                 int *device_error, pa_stream_t stream) {
-  if (!valid_cache_desc(cache) || num_seqs < 0 || num_q_heads <= 0 || max_q_len < 0 ||
+  if (!valid_cache_desc(cache) || num_seqs < 0 || num_q_heads <= 0 || max_q_len < 0 || num_q_tokens < 0 ||
       max_blocks_per_seq <= 0 || !isfinite(scale))
     return PA_ERR_INVALID;
-  if (num_seqs == 0 || max_q_len == 0) return PA_OK;
+  if (num_seqs == 0 || max_q_len == 0 || num_q_tokens == 0) return PA_OK;
   if (!out || !q || !cu_q_lens || !k_cache || !v_cache || !block_tables || !seq_lens) return PA_ERR_INVALID;
   if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) ||
       (reinterpret_cast<uintptr_t>(cu_q_lens) & 3u) || (reinterpret_cast<uintptr_t>(block_tables) & 3u) ||
@@ -383,10 +501,10 @@ extern "C" pa_status pa_prefill(void *out, const void *q, int32_t q_dtype, const
     return PA_ERR_UNSUPPORTED;  // TMA row coordinates are 32-bit
 
   PrefillParams p{};
-  if (!encode_prefill_map(&p.tmap_k, k_cache, cache) || !encode_prefill_map(&p.tmap_v, v_cache, cache))
+  if (!encode_q_view(&p.tmap_q, q, num_q_tokens, cache->kv_heads, G, cache->head_dim) ||
+      !encode_cache_view(&p.tmap_k, k_cache, cache) || !encode_cache_view(&p.tmap_v, v_cache, cache))
     return cuda_fail(cudaErrorInvalidValue);
   p.out = out;
-  p.q = static_cast<const uint8_t *>(q);
   p.cu_q = cu_q_lens;
   p.block_tables = block_tables;
   p.seq_lens = seq_lens;

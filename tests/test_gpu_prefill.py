@@ -144,7 +144,7 @@ def test_unsupported_inputs_are_refused_on_the_host():
     lib = pa.load_library()
     desc = pa.cache_desc(kc, "e4m3")
     import ctypes
-    st = lib.pa_prefill(q.data_ptr(), q.data_ptr(), 0, cu.data_ptr(), 1, 2, 3, kc.data_ptr(),
+    st = lib.pa_prefill(q.data_ptr(), q.data_ptr(), 0, 3, cu.data_ptr(), 1, 2, 3, kc.data_ptr(),
                         kc.data_ptr(), ctypes.byref(desc), bt.data_ptr(), 4, sl.data_ptr(), 0.125,
                         None, None)
     assert st == 2   # one-byte caches: unsupported in prefill
