@@ -148,6 +148,24 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(inside)}
 
 
+def max_over_ranks(value: float, world: int, device) -> float:
+    """The largest of the ranks' values (every rank gets it): the job's time
+    is its slowest rank's.  Uses the process group already initialised."""
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(units_per_rank: float, world: int, seconds: float) -> float:
+    """Whole-job throughput with the same work on every rank (weak scaling):
+    all ranks' units over the slowest rank's time."""
+    return world * units_per_rank / seconds
+
+
 def workload_bytes(w):
     kv = w.kv_unique_bytes()
     qo = 2 * w.S * w.Hq * w.d * 2
@@ -236,10 +254,7 @@ def run_ours(args, rank, world, local):
     elapsed = t0.elapsed_time(t1) / 1e3
     dec_ms = [a.elapsed_time(b) for a, b in ev]
     dec_avg = statistics.mean(dec_ms) / 1e3
-    if world > 1:
-        t = torch.tensor([elapsed], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed = float(t.item())
+    elapsed = max_over_ranks(elapsed, world, dev)
     derr = int(err.item())
 
     # end to end through the C ABI with host buffers (pinned), copies inside
@@ -295,7 +310,7 @@ def run_ours(args, rank, world, local):
     traffic = recorded_traffic(args.config)
     line = {
         "metric": METRIC,
-        "value": round(world * kv_bytes / step_t / 1e9, 2),
+        "value": round(job_rate(kv_bytes, world, step_t) / 1e9, 2),
         "unit": "GB/s",
         "n_gpus": world,
         "steps": K,
@@ -503,10 +518,7 @@ def run_swap(args, rank, world, local):
     t_out = statistics.mean(e[0].elapsed_time(e[1]) for e in evs) / 1e3
     t_in = statistics.mean(e[1].elapsed_time(e[2]) for e in evs) / 1e3
     elapsed = evs[0][0].elapsed_time(evs[-1][2]) / 1e3
-    if world > 1:
-        t = torch.tensor([elapsed], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed = float(t.item())
+    elapsed = max_over_ranks(elapsed, world, dev)
     # the link's copy-engine rate for the same bytes: one contiguous pinned
     # copy per direction (the denominator of the roofline)
     flat_d = torch.empty(moved, dtype=torch.uint8, device=dev)
@@ -556,7 +568,7 @@ def run_swap(args, rank, world, local):
     achieved = 2 * moved / (t_out + t_in) / 1e9
     peak = 2 * moved / (ce_d2h + ce_h2d) / 1e9 if ce_d2h > 0 and ce_h2d > 0 else None
     line = {
-        "metric": SWAP_METRIC, "value": round(world * 2 * moved / step_t / 1e9, 2), "unit": "GB/s",
+        "metric": SWAP_METRIC, "value": round(job_rate(2 * moved, world, step_t) / 1e9, 2), "unit": "GB/s",
         "n_gpus": world, "steps": K, "warmup": args.warmup, "ms_per_step": round(step_t * 1e3, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u8",
         "data": "synthetic (random cache bytes; block ids of the workload's first sequences)",
@@ -761,10 +773,7 @@ def run_prefill(args, rank, world, local):
         sampler.mark_end()
     elapsed = t0.elapsed_time(t1) / 1e3
     pf = statistics.mean(a.elapsed_time(b) for a, b in evs) / 1e3
-    if world > 1:
-        t = torch.tensor([elapsed], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed = float(t.item())
+    elapsed = max_over_ranks(elapsed, world, dev)
     # end to end: q and the new K/V from pinned host memory, the output back
     hq_, hk_, hv_ = q.cpu().pin_memory(), k_new.cpu().pin_memory(), v_new.cpu().pin_memory()
     out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
@@ -798,7 +807,7 @@ def run_prefill(args, rank, world, local):
     achieved = flops / pf / 1e12
     step_t = elapsed / K
     line = {
-        "metric": PREFILL_METRIC, "value": round(world * flops / step_t / 1e12, 2), "unit": "TFLOP/s",
+        "metric": PREFILL_METRIC, "value": round(job_rate(flops, world, step_t) / 1e12, 2), "unit": "TFLOP/s",
         "n_gpus": world, "steps": K, "warmup": args.warmup, "ms_per_step": round(step_t * 1e3, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded N(0,1) q/K/V; the shared-prefix workload's tables and lengths)",

@@ -416,6 +416,18 @@ PA_API int32_t pa_prefix_cache_free_order(const pa_prefix_cache *cache, int32_t 
 /* Reference count of a block (-1 for an id out of range). */
 PA_API int32_t pa_prefix_cache_ref_count(const pa_prefix_cache *cache, int32_t block);
 
+/*
+ * pa_selftest_wait_timeout — exercise the failure path every pipeline wait
+ * of this library shares, without faulting the GPU.
+ *
+ * Launches one CTA that waits, with the same bounded wait the kernels use,
+ * on an mbarrier phase that nothing completes.  After the wait's time limit
+ * (2 s) the kernel writes device error 4 to *device_error (device int,
+ * required) and returns normally: the context stays usable.  Asynchronous
+ * on `stream`; allocates nothing.
+ */
+PA_API pa_status pa_selftest_wait_timeout(int *device_error, pa_stream_t stream);
+
 /* Static description of a status code. */
 PA_API const char *pa_status_string(pa_status status);
 

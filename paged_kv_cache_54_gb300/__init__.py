@@ -40,7 +40,7 @@ if hasattr(torch, "float8_e5m2"):
 
 EXPORTED = ("pa_reshape_and_cache", "pa_decode_workspace_size", "pa_decode", "pa_prefill",
             "pa_decode_static_scratch", "pa_copy_blocks", "pa_swap_blocks",
-            "pa_status_string", "pa_last_cuda_error",
+            "pa_status_string", "pa_last_cuda_error", "pa_selftest_wait_timeout",
             "pa_prefix_cache_create", "pa_prefix_cache_destroy", "pa_prefix_cache_add_sequence",
             "pa_prefix_cache_append_token", "pa_prefix_cache_free_sequence",
             "pa_prefix_cache_block_table", "pa_prefix_cache_block_tables",
@@ -125,6 +125,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
                  "pa_prefix_cache_free_sequence", "pa_prefix_cache_block_tables",
                  "pa_prefix_cache_get_stats"):
         getattr(lib, name).restype = ctypes.c_int
+    lib.pa_selftest_wait_timeout.argtypes = [vp, vp]
+    lib.pa_selftest_wait_timeout.restype = ctypes.c_int
     lib.pa_status_string.argtypes = [ctypes.c_int]
     lib.pa_status_string.restype = ctypes.c_char_p
     lib.pa_last_cuda_error.argtypes = []
@@ -304,6 +306,14 @@ def pa_decode_static_scratch(out, q, k_cache, v_cache, block_tables, seq_lens,
         block_tables.shape[1], seq_lens.data_ptr(), max_seq_len, scale, partition_size,
         _ptr(device_error), _stream(stream)), "pa_decode_static_scratch")
     return out
+
+
+def pa_selftest_wait_timeout(device_error, stream=None) -> None:
+    """Run the bounded-wait failure path once: after about 2 s the kernel
+    writes device error 4 to ``device_error`` (a CUDA int32 tensor)."""
+    _require(device_error, "device_error")
+    _check(load_library().pa_selftest_wait_timeout(device_error.data_ptr(), _stream(stream)),
+           "pa_selftest_wait_timeout")
 
 
 def pa_copy_blocks(k_cache, v_cache, block_mapping, cache_dtype=None, device_error=None,

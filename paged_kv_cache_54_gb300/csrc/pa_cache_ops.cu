@@ -171,6 +171,18 @@ bool device_view(void *p, int device, uint8_t **out) {
   return false;
 }
 
+// An mbarrier that expects one arrival which never comes: the bounded wait
+// gives up after its time limit and the kernel reports a timeout.
+__global__ void selftest_wait_kernel(int *err) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0 && !mbar_wait(&bar, 0, nullptr)) record_error(err, kErrTimeout);
+}
+
 int grid_for(long long work_items, int threads) {
   DeviceInfo info;
   int sms = current_device_info(&info) ? info.sm_count : 148;
@@ -283,5 +295,12 @@ extern "C" pa_status pa_swap_blocks(void *k_cache, void *v_cache, const pa_cache
       out ? dk : hk, out ? dv : hv, out ? hk : dk, out ? hv : dv, block_mapping, num_pairs, block_bytes,
       out ? cache->num_blocks : host_num_blocks, out ? host_num_blocks : cache->num_blocks, device_error);
   e = cudaGetLastError();
+  return e == cudaSuccess ? PA_OK : cuda_fail(e);
+}
+
+extern "C" pa_status pa_selftest_wait_timeout(int *device_error, pa_stream_t stream) {
+  if (device_error == nullptr) return PA_ERR_INVALID;
+  selftest_wait_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(device_error);
+  const cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? PA_OK : cuda_fail(e);
 }
