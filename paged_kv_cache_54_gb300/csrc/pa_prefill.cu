@@ -20,11 +20,15 @@
 //         then K and V in stages of 64 keys, one box per (block, half), all
 //         with the 128-byte swizzle; block-table entries are fetched one
 //         stage ahead by the warp's lanes.
-//   9     MMA: one thread issues the products.  Both tiles' S of the next
-//         stage are issued before waiting for this stage's P, so the tensor
-//         cores work on them while the softmax warps work on P; S is
-//         double-buffered in TMEM for that.  tcgen05.commit signals
-//         completions on mbarriers.
+//   9,10  MMA, one warp per tile (one thread of each issues): the tile's S of
+//         the next stage is issued before waiting for this stage's P, so the
+//         tensor cores work on it while the softmax warps work on P (S is
+//         double-buffered in TMEM for that).  A thread issues a product
+//         about every 30 ns, so one issuing thread for both tiles would hold
+//         one tile's P V behind the other tile's S; with one per tile, each
+//         answers its own tile's P at once.  tcgen05.commit signals
+//         completions on mbarriers; a K/V stage is free once both tiles'
+//         P V have completed.
 // TMEM: all 512 columns (per tile S: 2 x 64, O: head_dim); one CTA per SM,
 // four K/V stages in flight.
 #include <limits.h>
@@ -41,8 +45,8 @@ constexpr int kPfTiles = 2;          // tiles per CTA
 constexpr int kPfRows = kPfTileRows * kPfTiles;
 constexpr int kPfKeys = 64;          // keys per pipeline stage
 constexpr int kPfTmaWarp = 8;
-constexpr int kPfMmaWarp = 9;
-constexpr int kPfThreads = 32 * 10;
+constexpr int kPfMmaWarp = 9;  // and 10: one issuing warp per tile
+constexpr int kPfThreads = 32 * 11;
 constexpr int kPfHalf = kPfKeys * 128;  // one 128-byte column half of a 64-key stage
 constexpr int kPfStages = 4;
 constexpr uint32_t kPfTmemCols = 512;
@@ -82,7 +86,7 @@ struct PfHeader {
   uint64_t p_full[kPfTiles];
   uint64_t pv_done[kPfTiles];
   uint64_t q_full;
-  uint64_t fin;
+  uint64_t fin[kPfTiles];
   uint32_t tmem_base;
   int abort;
 };
@@ -136,7 +140,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
   if (threadIdx.x == 0) {
     for (int i = 0; i < NS; ++i) {
       mbar_init(&hdr.kv_full[i], 1);
-      mbar_init(&hdr.kv_empty[i], 1);
+      mbar_init(&hdr.kv_empty[i], tiles);  // each tile's MMA warp frees the stage
     }
     for (int t = 0; t < kPfTiles; ++t) {
       mbar_init(&hdr.s_full[t][0], 1);
@@ -145,7 +149,8 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
       mbar_init(&hdr.pv_done[t], 1);
     }
     mbar_init(&hdr.q_full, 1);
-    mbar_init(&hdr.fin, 1);
+    mbar_init(&hdr.fin[0], 1);
+    mbar_init(&hdr.fin[1], 1);
     hdr.abort = 0;
     fence_mbar_init();
   }
@@ -219,28 +224,27 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
       }
       mbar_wait(&hdr.q_full, 0, nullptr);
     }
-  } else if (warp == kPfMmaWarp) {
-    // ------------------------------------------------------------ MMA
-    if (lane == 0) {
+  } else if (warp >= kPfMmaWarp) {
+    // ------------------------------------------------------------ MMA (tile t)
+    const int t = warp - kPfMmaWarp;
+    if (lane == 0 && t < tiles) {
       bool ok = mbar_wait(&hdr.q_full, 0, abort);
-      const uint32_t qaddr = smem_addr(qs), paddr = smem_addr(ps), saddr = smem_addr(stages);
+      const uint32_t qt = smem_addr(qs) + t * Lay::Q_TILE, pt = smem_addr(ps) + t * Lay::P_TILE;
+      const uint32_t saddr = smem_addr(stages);
+      const uint32_t tt = tmem + t * kPfTileCols;
       auto issue_qk = [&](int i) -> bool {
         const int st = i % NS;
         if (!mbar_wait(&hdr.kv_full[st], (i / NS) & 1, abort)) return false;
         tc_fence_after_sync();
         const uint32_t kb = saddr + st * Lay::STAGE_BYTES;
-        for (int t = 0; t < tiles; ++t) {
-          const uint32_t d = tmem + t * kPfTileCols + (i & 1) * kPfKeys;
-          const uint32_t qt = qaddr + t * Lay::Q_TILE;
 #pragma unroll
-          for (int kk = 0; kk < KSTEPS; ++kk) {
-            const uint32_t off = (kk % 4) * 32;  // 16 elements = 32 bytes into the swizzled row
-            const uint64_t a = umma_desc_sw128(qt + (kk / 4) * Lay::Q_HALF + off, 16, 1024);
-            const uint64_t b = umma_desc_sw128(kb + (kk / 4) * kPfHalf + off, 16, 1024);
-            tc_mma_f16(d, a, b, IDESC_QK, kk > 0);
-          }
-          tc_commit(&hdr.s_full[t][i & 1]);
+        for (int kk = 0; kk < KSTEPS; ++kk) {
+          const uint32_t off = (kk % 4) * 32;  // 16 elements = 32 bytes into the swizzled row
+          const uint64_t a = umma_desc_sw128(qt + (kk / 4) * Lay::Q_HALF + off, 16, 1024);
+          const uint64_t b = umma_desc_sw128(kb + (kk / 4) * kPfHalf + off, 16, 1024);
+          tc_mma_f16(tt + (i & 1) * kPfKeys, a, b, IDESC_QK, kk > 0);
         }
+        tc_commit(&hdr.s_full[t][i & 1]);
         return true;
       };
       if (ok) ok = issue_qk(0);
@@ -249,32 +253,28 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
           ok = false;
           break;
         }
-        const uint32_t vb = saddr + (i % NS) * Lay::STAGE_BYTES + NH * kPfHalf;
-        for (int t = 0; t < tiles; ++t) {
-          if (!mbar_wait(&hdr.p_full[t], i & 1, abort)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after_sync();
-          const uint32_t pt = paddr + t * Lay::P_TILE;
-#pragma unroll
-          for (int kk = 0; kk < kPfKeys / 16; ++kk) {
-            const uint64_t a = umma_desc_sw128(pt + kk * 32, 16, 1024);
-            const uint64_t b = umma_desc_sw128(vb + kk * 2048, kPfHalf, 1024);
-            tc_mma_f16(tmem + t * kPfTileCols + 2 * kPfKeys, a, b, IDESC_PV, (i > 0 || kk > 0) ? 1u : 0u);
-          }
-          tc_commit(&hdr.pv_done[t]);
+        if (!mbar_wait(&hdr.p_full[t], i & 1, abort)) {
+          ok = false;
+          break;
         }
-        if (!ok) break;
+        tc_fence_after_sync();
+        const uint32_t vb = saddr + (i % NS) * Lay::STAGE_BYTES + NH * kPfHalf;
+#pragma unroll
+        for (int kk = 0; kk < kPfKeys / 16; ++kk) {
+          const uint64_t a = umma_desc_sw128(pt + kk * 32, 16, 1024);
+          const uint64_t b = umma_desc_sw128(vb + kk * 2048, kPfHalf, 1024);
+          tc_mma_f16(tt + 2 * kPfKeys, a, b, IDESC_PV, (i > 0 || kk > 0) ? 1u : 0u);
+        }
+        tc_commit(&hdr.pv_done[t]);
         tc_commit(&hdr.kv_empty[i % NS]);
       }
       if (!ok) {
         record_error(p.err, kErrTimeout);
         *abort = 1;
       }
-      // every product issued has completed before the memory is released
-      tc_commit(&hdr.fin);
-      mbar_wait(&hdr.fin, 0, nullptr);
+      // every product this thread issued has completed before the memory is released
+      tc_commit(&hdr.fin[t]);
+      mbar_wait(&hdr.fin[t], 0, nullptr);
     }
   } else if (warp / 4 < tiles) {
     // ------------------------------------------------------------ softmax
@@ -349,9 +349,10 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
       for (int c = 0; c < 8; ++c)
         *reinterpret_cast<uint4 *>(pt + swz128(r, c)) = make_uint4(pw[4 * c], pw[4 * c + 1], pw[4 * c + 2],
                                                                     pw[4 * c + 3]);
-      if (t == 0 && k0 + kPfKeys > kv_end) {
+      if (k0 + kPfKeys > kv_end) {
         // keys past kv_end hold stale (possibly NaN) values: zero their V rows,
-        // since 0 * NaN would reach O (tile 0's P V is issued first)
+        // since 0 * NaN would reach O.  Each tile does it before its own P V
+        // (the tiles' products are issued independently); both write zeros.
         if (!__all_sync(0xffffffffu, mbar_wait(&hdr.kv_full[i % NS], (i / NS) & 1, abort))) {
           ok = false;
           break;
