@@ -236,13 +236,16 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
         const int st = i % NS;
         if (!mbar_wait(&hdr.kv_full[st], (i / NS) & 1, abort)) return false;
         tc_fence_after_sync();
-        const uint32_t kb = saddr + st * Lay::STAGE_BYTES;
+        // descriptors of the first k-step; a k-step advances the start
+        // address field (16-byte units) by 32 bytes, a row half by a region
+        const uint64_t a0 = umma_desc_sw128(qt, 16, 1024);
+        const uint64_t b0 = umma_desc_sw128(saddr + st * Lay::STAGE_BYTES, 16, 1024);
+        const uint32_t d = tt + (i & 1) * kPfKeys;
 #pragma unroll
         for (int kk = 0; kk < KSTEPS; ++kk) {
           const uint32_t off = (kk % 4) * 32;  // 16 elements = 32 bytes into the swizzled row
-          const uint64_t a = umma_desc_sw128(qt + (kk / 4) * Lay::Q_HALF + off, 16, 1024);
-          const uint64_t b = umma_desc_sw128(kb + (kk / 4) * kPfHalf + off, 16, 1024);
-          tc_mma_f16(tt + (i & 1) * kPfKeys, a, b, IDESC_QK, kk > 0);
+          tc_mma_f16(d, a0 + (((kk / 4) * Lay::Q_HALF + off) >> 4), b0 + (((kk / 4) * kPfHalf + off) >> 4),
+                     IDESC_QK, kk > 0);
         }
         tc_commit(&hdr.s_full[t][i & 1]);
         return true;
@@ -258,13 +261,11 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
           break;
         }
         tc_fence_after_sync();
-        const uint32_t vb = saddr + (i % NS) * Lay::STAGE_BYTES + NH * kPfHalf;
+        const uint64_t a0 = umma_desc_sw128(pt, 16, 1024);
+        const uint64_t b0 = umma_desc_sw128(saddr + (i % NS) * Lay::STAGE_BYTES + NH * kPfHalf, kPfHalf, 1024);
 #pragma unroll
-        for (int kk = 0; kk < kPfKeys / 16; ++kk) {
-          const uint64_t a = umma_desc_sw128(pt + kk * 32, 16, 1024);
-          const uint64_t b = umma_desc_sw128(vb + kk * 2048, kPfHalf, 1024);
-          tc_mma_f16(tt + 2 * kPfKeys, a, b, IDESC_PV, (i > 0 || kk > 0) ? 1u : 0u);
-        }
+        for (int kk = 0; kk < kPfKeys / 16; ++kk)  // 16 keys: 32 bytes of P rows, 2048 bytes of V rows
+          tc_mma_f16(tt + 2 * kPfKeys, a0 + kk * 2, b0 + kk * 128, IDESC_PV, (i > 0 || kk > 0) ? 1u : 0u);
         tc_commit(&hdr.pv_done[t]);
         tc_commit(&hdr.kv_empty[i % NS]);
       }
