@@ -18,8 +18,9 @@
 //         more than 2^8 (lazy rescaling: P entries stay below 256).
 //   8     TMA: Q once (one 4-D box per tile and 128-byte half of a row),
 //         then K and V in stages of 64 keys, one box per (block, half), all
-//         with the 128-byte swizzle; block-table entries are fetched one
-//         stage ahead by the warp's lanes.
+//         with the 128-byte swizzle.  Lane j fetches block-table entry j one
+//         stage ahead and issues block j's boxes, so a stage's copies go out
+//         from several threads at once.
 //   9,10  MMA, one warp per tile (one thread of each issues): the tile's S of
 //         the next stage is issued before waiting for this stage's P, so the
 //         tensor cores work on it while the softmax warps work on P (S is
@@ -201,15 +202,13 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
       uint8_t *kb = stages + st * Lay::STAGE_BYTES;
       uint8_t *vb = kb + NH * kPfHalf;
       if (lane == 0) mbar_arrive_expect_tx(&hdr.kv_full[st], 2u * NH * static_cast<uint32_t>(nblk * bs) * 128u);
-      for (int j = 0; j < nblk; ++j) {
-        const int pj = __shfl_sync(0xffffffffu, phys, j);
-        if (lane == 0) {
-          const int r0 = (pj * p.num_kv_heads + h) * bs;
+      __syncwarp();
+      if (lane < nblk) {  // lane j issues block j's boxes: the lanes' copies go out together
+        const int r0 = (phys * p.num_kv_heads + h) * bs;
 #pragma unroll
-          for (int hf = 0; hf < NH; ++hf) {
-            tma_load_2d(kb + hf * kPfHalf + j * bs * 128, &p.tmap_k, hf * 64, r0, &hdr.kv_full[st]);
-            tma_load_2d(vb + hf * kPfHalf + j * bs * 128, &p.tmap_v, hf * 64, r0, &hdr.kv_full[st]);
-          }
+        for (int hf = 0; hf < NH; ++hf) {
+          tma_load_2d(kb + hf * kPfHalf + lane * bs * 128, &p.tmap_k, hf * 64, r0, &hdr.kv_full[st]);
+          tma_load_2d(vb + hf * kPfHalf + lane * bs * 128, &p.tmap_v, hf * 64, r0, &hdr.kv_full[st]);
         }
       }
       issued = i + 1;
