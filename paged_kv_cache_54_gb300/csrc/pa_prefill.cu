@@ -13,9 +13,11 @@
 //   0..7  softmax, one warpgroup per tile: thread r of a warpgroup owns row
 //         r.  It reads its S row from TMEM, applies the causal mask (key
 //         position <= the row's position) and an online softmax in base 2,
-//         writes P (16-bit) to shared memory as the K-major A operand of P V,
-//         and rescales its O row in TMEM when the row maximum has grown by
-//         more than 2^8 (lazy rescaling: P entries stay below 256).
+//         writes P (16-bit pairs) back over the S buffer it just read, where
+//         P V takes it as a tensor-memory A operand, and rescales its O row in
+//         TMEM only when the row maximum has grown by more than 2^8 (lazy
+//         rescaling: P entries stay below 256).  P has a buffer per stage
+//         parity, so the next stage's softmax does not wait for this P V.
 //   8     TMA: Q once (one 4-D box per tile and 128-byte half of a row),
 //         then K and V in stages of 64 keys, one box per (block, half), all
 //         with the 128-byte swizzle.  Lane j fetches block-table entry j one
@@ -30,8 +32,8 @@
 //         answers its own tile's P at once.  tcgen05.commit signals
 //         completions on mbarriers; a K/V stage is free once both tiles'
 //         P V have completed.
-// TMEM: all 512 columns (per tile S: 2 x 64, O: head_dim); one CTA per SM,
-// four K/V stages in flight.
+// TMEM: all 512 columns (per tile S / P: 2 x 64, O: head_dim); one CTA per
+// SM, five K/V stages in flight.
 #include <limits.h>
 #include <math.h>
 
@@ -49,7 +51,7 @@ constexpr int kPfTmaWarp = 8;
 constexpr int kPfMmaWarp = 9;  // and 10: one issuing warp per tile
 constexpr int kPfThreads = 32 * 11;
 constexpr int kPfHalf = kPfKeys * 128;  // one 128-byte column half of a 64-key stage
-constexpr int kPfStages = 4;
+constexpr int kPfStages = 5;
 constexpr uint32_t kPfTmemCols = 512;
 constexpr uint32_t kPfTileCols = 256;  // TMEM columns per tile
 constexpr float kPfLazy = 8.f;  // rescale O only when the row maximum grows by more (base 2)
@@ -73,9 +75,7 @@ struct PfLayout {
   static constexpr int Q_OFF = 1024;
   static constexpr int Q_HALF = kPfTileRows * 128;
   static constexpr int Q_TILE = NH * Q_HALF;
-  static constexpr int P_OFF = Q_OFF + kPfTiles * Q_TILE;
-  static constexpr int P_TILE = kPfTileRows * 128;
-  static constexpr int STAGE_OFF = P_OFF + kPfTiles * P_TILE;
+  static constexpr int STAGE_OFF = Q_OFF + kPfTiles * Q_TILE;
   static constexpr int STAGE_BYTES = 2 * NH * kPfHalf;  // K halves, then V halves
   static constexpr int SMEM = STAGE_OFF + kPfStages * STAGE_BYTES;
 };
@@ -84,19 +84,14 @@ struct PfHeader {
   uint64_t kv_full[kPfStages];
   uint64_t kv_empty[kPfStages];
   uint64_t s_full[kPfTiles][2];
-  uint64_t p_full[kPfTiles];
+  uint64_t p_full[kPfTiles][2];  // by stage parity: the softmax may run a stage ahead
   uint64_t pv_done[kPfTiles];
+  uint64_t o_ready[kPfTiles];    // once: the tile's last P V has completed
   uint64_t q_full;
   uint64_t fin[kPfTiles];
   uint32_t tmem_base;
   int abort;
 };
-
-// chunk c (16 bytes) of row r in a region of 128-byte rows with the 128-byte
-// swizzle (region 1024-byte aligned)
-__device__ __forceinline__ uint32_t swz128(int r, int c) {
-  return static_cast<uint32_t>(r * 128 + ((c ^ (r & 7)) << 4));
-}
 
 __device__ __forceinline__ float fast_exp2(float x) {
   float y;
@@ -146,8 +141,10 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
     for (int t = 0; t < kPfTiles; ++t) {
       mbar_init(&hdr.s_full[t][0], 1);
       mbar_init(&hdr.s_full[t][1], 1);
-      mbar_init(&hdr.p_full[t], kPfTileRows);
+      mbar_init(&hdr.p_full[t][0], kPfTileRows);
+      mbar_init(&hdr.p_full[t][1], kPfTileRows);
       mbar_init(&hdr.pv_done[t], 1);
+      mbar_init(&hdr.o_ready[t], 1);
     }
     mbar_init(&hdr.q_full, 1);
     mbar_init(&hdr.fin[0], 1);
@@ -161,7 +158,6 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
   tc_fence_after_sync();
   const uint32_t tmem = hdr.tmem_base;
   uint8_t *qs = smem + Lay::Q_OFF;
-  uint8_t *ps = smem + Lay::P_OFF;
   uint8_t *stages = smem + Lay::STAGE_OFF;
   volatile int *abort = &hdr.abort;
 
@@ -228,7 +224,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
     const int t = warp - kPfMmaWarp;
     if (lane == 0 && t < tiles) {
       bool ok = mbar_wait(&hdr.q_full, 0, abort);
-      const uint32_t qt = smem_addr(qs) + t * Lay::Q_TILE, pt = smem_addr(ps) + t * Lay::P_TILE;
+      const uint32_t qt = smem_addr(qs) + t * Lay::Q_TILE;
       const uint32_t saddr = smem_addr(stages);
       const uint32_t tt = tmem + t * kPfTileCols;
       auto issue_qk = [&](int i) -> bool {
@@ -255,17 +251,18 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
           ok = false;
           break;
         }
-        if (!mbar_wait(&hdr.p_full[t], i & 1, abort)) {
+        if (!mbar_wait(&hdr.p_full[t][i & 1], (i >> 1) & 1, abort)) {
           ok = false;
           break;
         }
         tc_fence_after_sync();
-        const uint64_t a0 = umma_desc_sw128(pt, 16, 1024);
         const uint64_t b0 = umma_desc_sw128(saddr + (i % NS) * Lay::STAGE_BYTES + NH * kPfHalf, kPfHalf, 1024);
 #pragma unroll
-        for (int kk = 0; kk < kPfKeys / 16; ++kk)  // 16 keys: 32 bytes of P rows, 2048 bytes of V rows
-          tc_mma_f16(tt + 2 * kPfKeys, a0 + kk * 2, b0 + kk * 128, IDESC_PV, (i > 0 || kk > 0) ? 1u : 0u);
+        for (int kk = 0; kk < kPfKeys / 16; ++kk)  // 16 keys: 8 columns of P, 2048 bytes of V rows
+          tc_mma_f16_ta(tt + 2 * kPfKeys, tt + (i & 1) * kPfKeys + kk * 8, b0 + kk * 128, IDESC_PV,
+                        (i > 0 || kk > 0) ? 1u : 0u);
         tc_commit(&hdr.pv_done[t]);
+        if (i + 1 == n_stages) tc_commit(&hdr.o_ready[t]);
         tc_commit(&hdr.kv_empty[i % NS]);
       }
       if (!ok) {
@@ -283,7 +280,6 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
     const int tok = cta * QC + t * QT + r / G;
     const int pos = pos0 + min(tok, n - 1);  // rows past the new tokens take the last one's (not stored)
     const uint32_t trow = tmem + t * kPfTileCols + (static_cast<uint32_t>(32 * (warp & 3)) << 16);
-    uint8_t *pt = ps + t * Lay::P_TILE;
     float m = -INFINITY, l = 0.f;
     bool ok = true;
     for (int i = 0; i < n_stages; ++i) {
@@ -312,13 +308,16 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
         mx1 = fmaxf(mx1, sv[j + 1]);
       }
       const float mx = fmaxf(mx0, mx1);
-      // the previous P V must be done before P and O are touched again
-      if (i > 0 && !__all_sync(0xffffffffu, mbar_wait(&hdr.pv_done[t], (i - 1) & 1, abort))) {
-        ok = false;
-        break;
-      }
       const bool grow = mx > m + kPfLazy;
       if (__any_sync(0xffffffffu, grow && i > 0)) {  // tcgen05.ld / st are warp-wide
+        // O holds the previous P V: wait for it, then rescale.  S of this
+        // stage was issued after the P V before the previous one, and the
+        // tensor pipe completes in order, so pv_done is at most one phase
+        // behind here and the parity wait is exact.
+        if (!__all_sync(0xffffffffu, mbar_wait(&hdr.pv_done[t], (i - 1) & 1, abort))) {
+          ok = false;
+          break;
+        }
         tc_fence_after_sync();
         const float alpha = grow ? fast_exp2(m - mx) : 1.f;
 #pragma unroll
@@ -345,10 +344,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
         pw[j / 2] = pack2_rn<DT>(a, b);
       }
       l += l0 + l1;
-#pragma unroll
-      for (int c = 0; c < 8; ++c)
-        *reinterpret_cast<uint4 *>(pt + swz128(r, c)) = make_uint4(pw[4 * c], pw[4 * c + 1], pw[4 * c + 2],
-                                                                    pw[4 * c + 3]);
+      tc_st32(trow + (i & 1) * kPfKeys, pw);  // P over the S buffer just read
       if (k0 + kPfKeys > kv_end) {
         // keys past kv_end hold stale (possibly NaN) values: zero their V rows,
         // since 0 * NaN would reach O.  Each tile does it before its own P V
@@ -364,15 +360,18 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
           *reinterpret_cast<uint4 *>(vb + hf * kPfHalf + (z0 + rem / 8) * 128 + (rem % 8) * 16) =
               make_uint4(0u, 0u, 0u, 0u);
         }
+        fence_proxy_async_smem();  // the zeroed V rows visible to the tensor cores
       }
-      fence_proxy_async_smem();  // P (and zeroed V rows) visible to the tensor cores
-      tc_fence_before_sync();    // O stores ordered before the arrive
-      mbar_arrive(&hdr.p_full[t]);
+      tc_fence_before_sync();  // P and O stores ordered before the arrive
+      mbar_arrive(&hdr.p_full[t][i & 1]);
     }
     if (!ok) {
       record_error(p.err, kErrTimeout);
       *abort = 1;
-    } else if (__all_sync(0xffffffffu, mbar_wait(&hdr.pv_done[t], (n_stages - 1) & 1, abort))) {
+    } else if (__all_sync(0xffffffffu, mbar_wait(&hdr.o_ready[t], 0, abort))) {
+      // (pv_done cannot serve here: the softmax does not wait for every P V,
+      // so the last two may both be pending and a parity wait would take the
+      // older phase for the newer)
       tc_fence_after_sync();
       const float inv = 1.f / l;
       const bool store = tok < n;
