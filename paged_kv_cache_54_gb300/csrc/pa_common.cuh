@@ -244,23 +244,6 @@ __device__ __forceinline__ void tma_load_2d(void *smem_dst, const CUtensorMap *m
       : "memory");
 }
 
-// ldmatrix: four 8x8 matrices of 16-bit elements; lane l gives the address
-// of row l % 8 of matrix l / 8, and receives row l / 4, columns 2(l % 4) and
-// 2(l % 4) + 1 of each matrix (of its transpose with .trans).
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(addr)
-               : "memory");
-}
-__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2,
-                                              uint32_t &r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(addr)
-               : "memory");
-}
-
 // D += A * B on the legacy tensor-core path, m16n8k16, fp32 accumulators;
 // A and B both fp16 (MT == kF16) or both bf16.
 template <int MT>
@@ -390,9 +373,6 @@ __device__ __forceinline__ void tma_load_4d(void *smem_dst, const CUtensorMap *m
       : "memory");
 }
 
-__device__ __forceinline__ void named_bar_sync(int id, int threads) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
-}
 
 // Programmatic dependent launch: a kernel launched with programmatic stream
 // serialization may start before the previous kernel in the stream ends;
