@@ -99,6 +99,32 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// Two fp32 lanes in one 64-bit register pair, for the packed f32x2 arithmetic.
+__device__ __forceinline__ uint64_t f2(float x, float y) {
+  uint64_t d;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "f"(x), "f"(y));
+  return d;
+}
+__device__ __forceinline__ void f2_split(uint64_t v, float &x, float &y) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(x), "=f"(y) : "l"(v));
+}
+__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {  // a * b + c, both lanes
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t fadd2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
 template <int DT, int D, int G>
 __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_constant__ PrefillParams p) {
   using Lay = PfLayout<D>;
@@ -299,15 +325,34 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
 #pragma unroll
         for (int j = 0; j < 32; ++j) sv[32 + j] = __uint_as_float(raw[j]);
       }
-      float mx0 = -INFINITY, mx1 = -INFINITY;  // two chains for the maximum
+      // Most stages lie wholly at or before every row of the warp: no mask,
+      // and with a positive scale the maximum is taken on the raw scores and
+      // the scale folded into the exponent's one fma.  Otherwise the scores
+      // are scaled, then masked (key position > row position: -inf).
+      const float c = p.qk_scale_log2;
+      const bool plain = c > 0.f && __all_sync(0xffffffffu, k0 + kPfKeys - 1 <= pos);
+      float mx, cm;
+      if (plain) {
+        float a = sv[0], b = sv[32];  // two chains of 3-input maxima
 #pragma unroll
-      for (int j = 0; j < kPfKeys; j += 2) {
-        sv[j] = (k0 + j <= pos) ? sv[j] * p.qk_scale_log2 : -INFINITY;
-        sv[j + 1] = (k0 + j + 1 <= pos) ? sv[j + 1] * p.qk_scale_log2 : -INFINITY;
-        mx0 = fmaxf(mx0, sv[j]);
-        mx1 = fmaxf(mx1, sv[j + 1]);
+        for (int j = 1; j < 31; j += 2) {
+          a = fmax3(a, sv[j], sv[j + 1]);
+          b = fmax3(b, sv[32 + j], sv[33 + j]);
+        }
+        mx = fmax3(a, b, fmaxf(sv[31], sv[63])) * c;
+        cm = c;
+      } else {
+        float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+        for (int j = 0; j < kPfKeys; j += 2) {
+          sv[j] = (k0 + j <= pos) ? sv[j] * c : -INFINITY;
+          sv[j + 1] = (k0 + j + 1 <= pos) ? sv[j + 1] * c : -INFINITY;
+          mx0 = fmaxf(mx0, sv[j]);
+          mx1 = fmaxf(mx1, sv[j + 1]);
+        }
+        mx = fmaxf(mx0, mx1);
+        cm = 1.f;
       }
-      const float mx = fmaxf(mx0, mx1);
       const bool grow = mx > m + kPfLazy;
       if (__any_sync(0xffffffffu, grow && i > 0)) {  // tcgen05.ld / st are warp-wide
         // O holds the previous P V: wait for it, then rescale.  S of this
@@ -334,16 +379,27 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
         m = mx;
       }
       const float base = m == -INFINITY ? 0.f : m;
+      // p = 2^(s * cm - base), two lanes per fma and per add of the row sum
+      const uint64_t cm2 = f2(cm, cm), nb2 = f2(-base, -base);
+      uint64_t sum0 = f2(0.f, 0.f), sum1 = sum0;
       uint32_t pw[kPfKeys / 2];
-      float l0 = 0.f, l1 = 0.f;
 #pragma unroll
       for (int j = 0; j < kPfKeys; j += 2) {
-        const float a = fast_exp2(sv[j] - base), b = fast_exp2(sv[j + 1] - base);
-        l0 += a;
-        l1 += b;
+        float x, y;
+        f2_split(ffma2(f2(sv[j], sv[j + 1]), cm2, nb2), x, y);
+        const float a = fast_exp2(x), b = fast_exp2(y);
         pw[j / 2] = pack2_rn<DT>(a, b);
+        if ((j & 2) == 0)
+          sum0 = fadd2(sum0, f2(a, b));
+        else
+          sum1 = fadd2(sum1, f2(a, b));
       }
-      l += l0 + l1;
+      {
+        float l0, l1, l2, l3;
+        f2_split(sum0, l0, l1);
+        f2_split(sum1, l2, l3);
+        l += (l0 + l1) + (l2 + l3);
+      }
       tc_st32(trow + (i & 1) * kPfKeys, pw);  // P over the S buffer just read
       if (k0 + kPfKeys > kv_end) {
         // keys past kv_end hold stale (possibly NaN) values: zero their V rows,

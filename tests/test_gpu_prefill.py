@@ -16,8 +16,10 @@ pytestmark = pytest.mark.gpu
 
 # (L_s, n_s): whole prompts, suffixes after a cached prefix, single tokens,
 # lengths around the 64-key stage and the query tiles
+# (520 new tokens: three query ranges of 256 rows even at group size 1, the
+# last with one tile)
 CASES = [(1, 1), (17, 17), (100, 37), (64, 64), (65, 1), (300, 129), (700, 5), (129, 128),
-         (250, 250), (33, 9)]
+         (250, 250), (33, 9), (600, 520)]
 
 
 def _seed(*key):
