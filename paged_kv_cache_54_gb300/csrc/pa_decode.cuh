@@ -1005,7 +1005,7 @@ struct MmaState {
 template <int QT, int D, int G, int QM>
 __device__ __forceinline__ void combine_item(const DecodeParams &p, const StageInfo &inf, int ncols,
                                              const float *so, float *sm, const float *sl, uint64_t *bar,
-                                             int ncomb, const volatile int *abort, bool &ok) {
+                                             uint32_t parity, const volatile int *abort, bool &ok) {
   const int ct = threadIdx.x - 32;
   const int P = p.partition_size;
   // 1) per column j: weights w_c = exp2(m_c - M) / sum_c exp2(m_c - M) l_c,
@@ -1033,7 +1033,7 @@ __device__ __forceinline__ void combine_item(const DecodeParams &p, const StageI
     }
   }
   mbar_arrive(bar);
-  if (!mbar_wait(bar, (3 * ncomb + 1) & 1, abort)) {
+  if (!mbar_wait(bar, parity, abort)) {
     ok = false;
     return;
   }
@@ -1066,9 +1066,8 @@ __device__ __forceinline__ void combine_item(const DecodeParams &p, const StageI
 // one work item, from its first (already waited) stage to its combine
 // ----------------------------------------------------------------------------
 template <int KV, int QT, int D, int G, int QM, class State>
-__device__ __forceinline__ bool run_item(const DecodeParams &p, SmemHeader &hdr, uint8_t *stages, float *so,
-                                         float *sm, float *sl, int cw, int &stage, uint32_t &phase,
-                                         int &ncomb, StageInfo inf, const volatile int *abort) {
+__device__ __forceinline__ bool run_item(const DecodeParams &p, SmemHeader &hdr, uint8_t *stages, int cw,
+                                         int &stage, uint32_t &phase, StageInfo inf, const volatile int *abort) {
   const int lane = threadIdx.x & 31;
   const int ncols = inf.k * G;
   // scales of the item's KV head: per tensor (folded in by the host) or per head
@@ -1086,29 +1085,41 @@ __device__ __forceinline__ bool run_item(const DecodeParams &p, SmemHeader &hdr,
     const int n = min(16, inf.ntok - 16 * cw);
     if (n > 0) st.slice(sb + p.k_off, sb + p.v_off, 16 * cw, n, v_scale);
     __syncwarp();
+    if (inf.flags & kLast) break;  // the last stage is kept: it becomes the combine scratch
     if (lane == 0) mbar_arrive(&hdr.empty[stage]);
-    const bool last = (inf.flags & kLast) != 0;
     if (++stage == p.num_stages) {
       stage = 0;
       phase ^= 1u;
     }
-    if (last) break;
     if (!mbar_wait(&hdr.full[stage], phase, abort)) return false;
     const StageInfo nxt = hdr.info[stage];
     inf.ntok = nxt.ntok;
     inf.flags = nxt.flags;
   }
-  // three consumer-wide barriers: states written, weights computed, scratch
-  // read (so that the next item may overwrite it)
+  // The four warps' states meet in the item's last stage buffer, once all
+  // of them are done reading it.  Four consumer-wide barriers an item (so
+  // the combine barrier's phase parity is the barrier's index mod 2): the
+  // stage read, the states written, the weights computed, the scratch read;
+  // then the stage goes back to the producer.
+  float *so = reinterpret_cast<float *>(stages + static_cast<size_t>(stage) * p.stage_bytes);
+  float *sm = so + kConsumerWarps * QM * D;
+  float *sl = sm + kConsumerWarps * QM;
+  mbar_arrive(&hdr.combine);
+  if (!mbar_wait(&hdr.combine, 0, abort)) return false;
   st.to_scratch(so, sm, sl, cw, v_scale, ncols);
   mbar_arrive(&hdr.combine);
-  if (!mbar_wait(&hdr.combine, (3 * ncomb) & 1, abort)) return false;
+  if (!mbar_wait(&hdr.combine, 1, abort)) return false;
   bool ok = true;
-  combine_item<QT, D, G, QM>(p, inf, ncols, so, sm, sl, &hdr.combine, ncomb, abort, ok);
+  combine_item<QT, D, G, QM>(p, inf, ncols, so, sm, sl, &hdr.combine, 0, abort, ok);
   if (!ok) return false;
   mbar_arrive(&hdr.combine);
-  if (!mbar_wait(&hdr.combine, (3 * ncomb + 2) & 1, abort)) return false;
-  ++ncomb;
+  if (!mbar_wait(&hdr.combine, 1, abort)) return false;
+  __syncwarp();
+  if (lane == 0) mbar_arrive(&hdr.empty[stage]);
+  if (++stage == p.num_stages) {
+    stage = 0;
+    phase ^= 1u;
+  }
   return true;
 }
 
@@ -1120,6 +1131,8 @@ __device__ __forceinline__ bool run_item(const DecodeParams &p, SmemHeader &hdr,
 template <int KV, int QT, int D, int G, bool MMA>
 __device__ __forceinline__ void decode_body(const DecodeParams &p) {
   constexpr int QM = query_capacity(G);
+  static_assert(kConsumerWarps * (QM * D + 2 * QM) * 4 <= 2 * kStageTok * D * elt_bytes(KV) + QM * D * 2,
+                "the combine scratch must fit in one pipeline stage");
   extern __shared__ __align__(128) uint8_t smem[];
   SmemHeader &hdr = *reinterpret_cast<SmemHeader *>(smem);
   const int warp = threadIdx.x >> 5;
@@ -1148,11 +1161,8 @@ __device__ __forceinline__ void decode_body(const DecodeParams &p) {
   const int lane = threadIdx.x & 31;
   const volatile int *abort = &hdr.abort;
   uint8_t *stages = smem + p.stages_off;
-  float *so = reinterpret_cast<float *>(smem + p.scratch_off);
-  float *sm = so + kConsumerWarps * QM * D;
-  float *sl = sm + kConsumerWarps * QM;
   using Mma = MmaState<KV, QT, D, G, QM>;
-  int stage = 0, ncomb = 0;
+  int stage = 0;
   uint32_t phase = 0;
   bool failed = false;
   while (true) {
@@ -1164,13 +1174,13 @@ __device__ __forceinline__ void decode_body(const DecodeParams &p) {
     if (inf.flags & kEnd) break;
     bool ok;
     if constexpr (MMA) {
-      ok = run_item<KV, QT, D, G, QM, Mma>(p, hdr, stages, so, sm, sl, cw, stage, phase, ncomb, inf, abort);
+      ok = run_item<KV, QT, D, G, QM, Mma>(p, hdr, stages, cw, stage, phase, inf, abort);
     } else {
       using Simt = SimtState<KV, QT, D, G, QM>;
       if (QM > G && inf.k > 1)
-        ok = run_item<KV, QT, D, G, QM, Mma>(p, hdr, stages, so, sm, sl, cw, stage, phase, ncomb, inf, abort);
+        ok = run_item<KV, QT, D, G, QM, Mma>(p, hdr, stages, cw, stage, phase, inf, abort);
       else
-        ok = run_item<KV, QT, D, G, QM, Simt>(p, hdr, stages, so, sm, sl, cw, stage, phase, ncomb, inf, abort);
+        ok = run_item<KV, QT, D, G, QM, Simt>(p, hdr, stages, cw, stage, phase, inf, abort);
     }
     if (!ok) {
       failed = true;
@@ -1185,23 +1195,21 @@ __device__ __forceinline__ void decode_body(const DecodeParams &p) {
 
 // Shared-memory plan of one decode instantiation.
 struct DecodeSmemPlan {
-  int stage_bytes, k_off, v_off, q_off, scratch_off, stages_off, num_stages, total;
+  int stage_bytes, k_off, v_off, q_off, stages_off, num_stages, total;
 };
 
 template <int KV, int D, int G>
 __host__ __device__ constexpr DecodeSmemPlan plan_smem(int max_smem) {
   constexpr int ROWB = D * elt_bytes(KV);
   constexpr int QM = query_capacity(G);
-  DecodeSmemPlan s{0, 0, 0, 0, 0, 0, 0, 0};
+  DecodeSmemPlan s{0, 0, 0, 0, 0, 0, 0};
   s.k_off = 0;
   s.v_off = kStageTok * ROWB;
   s.q_off = 2 * kStageTok * ROWB;
   // stages and their K / V regions start on 1024-byte boundaries (the
   // swizzle atom of the tensor copies)
   s.stage_bytes = (s.q_off + QM * D * 2 + 1023) / 1024 * 1024;
-  s.scratch_off = (static_cast<int>(sizeof(SmemHeader)) + 127) / 128 * 128;
-  const int scratch = kConsumerWarps * (QM * D + 2 * QM) * 4;
-  s.stages_off = (s.scratch_off + scratch + 1023) / 1024 * 1024;
+  s.stages_off = (static_cast<int>(sizeof(SmemHeader)) + 1023) / 1024 * 1024;
   int ns = (max_smem - s.stages_off) / s.stage_bytes;
   if (ns > kMaxStages) ns = kMaxStages;
   s.num_stages = ns;
@@ -1260,7 +1268,6 @@ pa_status launch_decode(DecodeParams p, const DeviceInfo &dev, cudaStream_t stre
   p.k_off = sp.k_off;
   p.v_off = sp.v_off;
   p.q_off = sp.q_off;
-  p.scratch_off = sp.scratch_off;
   p.stages_off = sp.stages_off;
   p.kmax = query_capacity(G) / G;
   void (*kern)(DecodeParams);

@@ -73,7 +73,7 @@ struct DecodeParams {
   float v_scale;        // v_scale (1 with per-head scales)
   const float *k_head_scale;  // [num_kv_heads] or null: per-head scales of a one-byte cache
   const float *v_head_scale;
-  int num_stages, stage_bytes, k_off, v_off, q_off, scratch_off, stages_off;
+  int num_stages, stage_bytes, k_off, v_off, q_off, stages_off;
   int kmax;   // most sequences one item may batch
   int *work;  // [0] claim counter, [1] number of items
   int4 *items;  // (first sequence, partition, sequences, 0)
