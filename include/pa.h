@@ -217,11 +217,12 @@ PA_API pa_status pa_decode(void *out, const void *q, int32_t q_dtype,
  *   out[cu_q_lens[s] + j, hq, :] =
  *       sum_{i <= p} softmax_i(scale * <q[cu_q_lens[s] + j, hq, :], k_i>) v_i
  * with token i read from block block_tables[s, i / block_size] at offset
- * i % block_size.
+ * i % block_size, and one-byte codes dequantised with the cache's scales as
+ * in pa_decode.
  *
- *   out, q         device [num_q_tokens, num_q_heads, head_dim] of q_dtype,
- *                  which must equal the cache dtype (16-bit caches only:
- *                  PA_F16 or PA_BF16); num_q_tokens = cu_q_lens[num_seqs].
+ *   out, q         device [num_q_tokens, num_q_heads, head_dim] of q_dtype:
+ *                  the cache dtype for 16-bit caches, PA_F16 or PA_BF16 for
+ *                  one-byte ones; num_q_tokens = cu_q_lens[num_seqs].
  *   cu_q_lens      device int32 [num_seqs + 1], non-decreasing, from 0.
  *   max_q_len      host upper bound of n_s, used to size the grid.
  *   block_tables, max_blocks_per_seq, seq_lens  as in pa_decode; each
@@ -231,7 +232,9 @@ PA_API pa_status pa_decode(void *out, const void *q, int32_t q_dtype,
  * block 0 instead and reports error 1; a stalled pipeline reports error 4.
  * Supported set: num_q_heads / kv_heads in {1, 2, 4, 8}; block_size and
  * head_dim as in pa_cache_desc; num_seqs and kv_heads <= 65535.  Needs no
- * workspace and allocates nothing.
+ * workspace and allocates nothing.  With a one-byte cache the products run
+ * on fp16 operands: a bf16 q is rounded to fp16 after scaling each 128-row
+ * query tile by a power of two that brings its largest |q| within 2^15.
  */
 PA_API pa_status pa_prefill(void *out, const void *q, int32_t q_dtype, int32_t num_q_tokens,
                             const int32_t *cu_q_lens, int32_t num_seqs, int32_t num_q_heads,

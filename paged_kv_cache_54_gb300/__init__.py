@@ -254,17 +254,19 @@ def pa_decode(out, q, k_cache, v_cache, block_tables, seq_lens, max_seq_len: int
 
 
 def pa_prefill(out, q, cu_q_lens, k_cache, v_cache, block_tables, seq_lens, max_q_len: int,
-               scale: float, device_error=None, stream=None) -> torch.Tensor:
+               scale: float, cache_dtype=None, k_scale=1.0, v_scale=1.0, device_error=None,
+               stream=None) -> torch.Tensor:
     """Causal attention of the new tokens ``q [T, Hq, head_dim]`` (sequence
     s's are rows cu_q_lens[s]..cu_q_lens[s+1]-1, its last tokens) over the
-    paged cache; writes ``out`` like ``q``."""
+    paged cache; writes ``out`` like ``q``.  One-byte caches take their
+    ``cache_dtype`` and scales as in ``pa_decode``."""
     for t, n in ((out, "out"), (q, "q"), (cu_q_lens, "cu_q_lens"), (k_cache, "k_cache"),
                  (v_cache, "v_cache"), (block_tables, "block_tables"), (seq_lens, "seq_lens")):
         _require(t, n)
     if cu_q_lens.dtype != torch.int32 or block_tables.dtype != torch.int32 or \
             seq_lens.dtype != torch.int32:
         raise ValueError("cu_q_lens, block_tables and seq_lens must be int32")
-    desc = cache_desc(k_cache)
+    desc = cache_desc(k_cache, cache_dtype, k_scale, v_scale)
     qcode = _TORCH_CODES.get(q.dtype)
     if out.dtype != q.dtype or out.shape != q.shape or q.dim() != 3:
         raise ValueError("q/out must be [T, Hq, head_dim] of one dtype")

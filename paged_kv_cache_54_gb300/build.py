@@ -21,7 +21,8 @@ CFLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE
           "-Xcompiler", "-fvisibility=hidden"]
 SOURCES = ["pa_host.cu", "pa_cache_ops.cu", "pa_decode_api.cu", "pa_decode_f16.cu",
            "pa_decode_bf16.cu", "pa_decode_e4m3.cu", "pa_decode_e5m2.cu", "pa_decode_i8.cu",
-           "pa_decode_static.cu", "pa_prefill.cu", "pa_prefix_cache.cpp"]
+           "pa_decode_static.cu", "pa_prefill.cu", "pa_prefill_e4m3.cu", "pa_prefill_e5m2.cu",
+           "pa_prefill_i8.cu", "pa_prefix_cache.cpp"]
 
 
 def _nvcc() -> str:

@@ -1,497 +1,13 @@
-// Paged causal prefill on the 5th-generation tensor cores: attention of each
-// sequence's new tokens (the part a prefix-cache hit did not cover) over all
-// of its tokens in the paged cache.
-//
-// One CTA = one KV head h and 256 query rows of one sequence, as two tiles
-// of 128; a row is a (new token, query head of h's group) pair, token-major,
-// so a CTA holds 256 / G new tokens.  Every K/V stage staged in shared memory
-// serves both tiles.  Each tile is the M = 128 dimension of tcgen05.mma, and
-// its row r lives in tensor-memory lane r (columns 256 * tile + ...):
-//   S = Q K^T   M 128, N = 64 keys of a stage, K = head_dim   (S in TMEM)
-//   O += P V    M 128, N = head_dim,  K = the stage's 64 keys  (O in TMEM)
-// Warps:
-//   0..7  softmax, one warpgroup per tile: thread r of a warpgroup owns row
-//         r.  It reads its S row from TMEM, applies the causal mask (key
-//         position <= the row's position) and an online softmax in base 2,
-//         writes P (16-bit pairs) back over the S buffer it just read, where
-//         P V takes it as a tensor-memory A operand, and rescales its O row in
-//         TMEM only when the row maximum has grown by more than 2^8 (lazy
-//         rescaling: P entries stay below 256).  P has a buffer per stage
-//         parity, so the next stage's softmax does not wait for this P V.
-//   8     TMA: Q once (one 4-D box per tile and 128-byte half of a row),
-//         then K and V in stages of 64 keys, one box per (block, half), all
-//         with the 128-byte swizzle.  Lane j fetches block-table entry j one
-//         stage ahead and issues block j's boxes, so a stage's copies go out
-//         from several threads at once.
-//   9,10  MMA, one warp per tile (one thread of each issues): the tile's S of
-//         the next stage is issued before waiting for this stage's P, so the
-//         tensor cores work on it while the softmax warps work on P (S is
-//         double-buffered in TMEM for that).  A thread issues a product
-//         about every 30 ns, so one issuing thread for both tiles would hold
-//         one tile's P V behind the other tile's S; with one per tile, each
-//         answers its own tile's P at once.  tcgen05.commit signals
-//         completions on mbarriers; a K/V stage is free once both tiles'
-//         P V have completed.
-// TMEM: all 512 columns (per tile S / P: 2 x 64, O: head_dim); one CTA per
-// SM, five K/V stages in flight.
+// pa_prefill: the C entry point, the tensor-map views it builds, and the
+// instantiations for 16-bit caches (the kernel is in pa_prefill.cuh; the
+// one-byte cache types have a translation unit each).
 #include <limits.h>
 #include <math.h>
 
-#include "pa_common.cuh"
-#include "pa_host.h"
+#include "pa_prefill.cuh"
 
 namespace pa {
 namespace {
-
-constexpr int kPfTileRows = 128;     // rows per tile (M)
-constexpr int kPfTiles = 2;          // tiles per CTA
-constexpr int kPfRows = kPfTileRows * kPfTiles;
-constexpr int kPfKeys = 64;          // keys per pipeline stage
-constexpr int kPfTmaWarp = 8;
-constexpr int kPfMmaWarp = 9;  // and 10: one issuing warp per tile
-constexpr int kPfThreads = 32 * 11;
-constexpr int kPfHalf = kPfKeys * 128;  // one 128-byte column half of a 64-key stage
-constexpr int kPfStages = 5;
-constexpr uint32_t kPfTmemCols = 512;
-constexpr uint32_t kPfTileCols = 256;  // TMEM columns per tile
-constexpr float kPfLazy = 8.f;  // rescale O only when the row maximum grows by more (base 2)
-
-struct PrefillParams {
-  CUtensorMap tmap_q;  // [T, Hkv, G, head_dim] view of q, box {64, G, 1, 128/G}
-  CUtensorMap tmap_k;  // [rows, head_dim] view of each cache, box {64, block_size}
-  CUtensorMap tmap_v;
-  void *out;
-  const int32_t *cu_q;
-  const int32_t *block_tables;
-  const int32_t *seq_lens;
-  int num_q_heads, num_kv_heads, num_blocks, block_size, max_blocks;
-  float qk_scale_log2;  // softmax scale * log2(e)
-  int *err;
-};
-
-template <int D>
-struct PfLayout {
-  static constexpr int NH = D / 64;  // 128-byte halves of a 16-bit row
-  static constexpr int Q_OFF = 1024;
-  static constexpr int Q_HALF = kPfTileRows * 128;
-  static constexpr int Q_TILE = NH * Q_HALF;
-  static constexpr int STAGE_OFF = Q_OFF + kPfTiles * Q_TILE;
-  static constexpr int STAGE_BYTES = 2 * NH * kPfHalf;  // K halves, then V halves
-  static constexpr int SMEM = STAGE_OFF + kPfStages * STAGE_BYTES;
-};
-
-struct PfHeader {
-  uint64_t kv_full[kPfStages];
-  uint64_t kv_empty[kPfStages];
-  uint64_t s_full[kPfTiles][2];
-  uint64_t p_full[kPfTiles][2];  // by stage parity: the softmax may run a stage ahead
-  uint64_t pv_done[kPfTiles];
-  uint64_t o_ready[kPfTiles];    // once: the tile's last P V has completed
-  uint64_t q_full;
-  uint64_t fin[kPfTiles];
-  uint32_t tmem_base;
-  int abort;
-};
-
-__device__ __forceinline__ float fast_exp2(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
-
-__device__ __forceinline__ float fmax3(float a, float b, float c) {
-  float d;
-  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
-  return d;
-}
-
-// Two fp32 lanes in one 64-bit register pair, for the packed f32x2 arithmetic.
-__device__ __forceinline__ uint64_t f2(float x, float y) {
-  uint64_t d;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "f"(x), "f"(y));
-  return d;
-}
-__device__ __forceinline__ void f2_split(uint64_t v, float &x, float &y) {
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(x), "=f"(y) : "l"(v));
-}
-__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {  // a * b + c, both lanes
-  uint64_t d;
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
-  return d;
-}
-__device__ __forceinline__ uint64_t fadd2(uint64_t a, uint64_t b) {
-  uint64_t d;
-  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-  return d;
-}
-
-template <int DT, int D, int G>
-__global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_constant__ PrefillParams p) {
-  using Lay = PfLayout<D>;
-  constexpr int NH = Lay::NH;
-  constexpr int NS = kPfStages;
-  constexpr int QT = kPfTileRows / G;  // new tokens per tile
-  constexpr int QC = kPfRows / G;      // new tokens per CTA
-  constexpr int KSTEPS = D / 16;
-  constexpr int AB = DT == kF16 ? 0 : 1;
-  constexpr uint32_t IDESC_QK = umma_idesc_f16(AB, kPfTileRows, kPfKeys, false);
-  constexpr uint32_t IDESC_PV = umma_idesc_f16(AB, kPfTileRows, D, true);
-  extern __shared__ __align__(1024) uint8_t smem[];
-  PfHeader &hdr = *reinterpret_cast<PfHeader *>(smem);
-  const int cta = gridDim.x - 1 - blockIdx.x;  // the longest (last) token ranges start first
-  const int s = blockIdx.y, h = blockIdx.z;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-
-  const int q0 = __ldg(p.cu_q + s);
-  const int n = __ldg(p.cu_q + s + 1) - q0;
-  const int L = __ldg(p.seq_lens + s);
-  if (n < 0 || L < n || L > p.max_blocks * p.block_size || n > static_cast<int>(gridDim.x) * QC) {
-    if (threadIdx.x == 0 && blockIdx.x == 0) record_error(p.err, kErrSeqLen);
-    return;
-  }
-  if (cta * QC >= n) return;
-  if ((smem_addr(smem) & 1023u) != 0) {  // the swizzle needs 1024-byte atoms
-    if (threadIdx.x == 0) record_error(p.err, kErrSmemAlign);
-    return;
-  }
-  const int tiles = cta * QC + QT < n ? 2 : 1;          // the second tile may hold no new token
-  const int pos0 = L - n;                               // position of new token 0
-  const int kv_end = pos0 + min(n, (cta + 1) * QC);     // keys 0..kv_end-1 are needed
-  const int n_stages = (kv_end + kPfKeys - 1) / kPfKeys;
-
-  if (threadIdx.x == 0) {
-    for (int i = 0; i < NS; ++i) {
-      mbar_init(&hdr.kv_full[i], 1);
-      mbar_init(&hdr.kv_empty[i], tiles);  // each tile's MMA warp frees the stage
-    }
-    for (int t = 0; t < kPfTiles; ++t) {
-      mbar_init(&hdr.s_full[t][0], 1);
-      mbar_init(&hdr.s_full[t][1], 1);
-      mbar_init(&hdr.p_full[t][0], kPfTileRows);
-      mbar_init(&hdr.p_full[t][1], kPfTileRows);
-      mbar_init(&hdr.pv_done[t], 1);
-      mbar_init(&hdr.o_ready[t], 1);
-    }
-    mbar_init(&hdr.q_full, 1);
-    mbar_init(&hdr.fin[0], 1);
-    mbar_init(&hdr.fin[1], 1);
-    hdr.abort = 0;
-    fence_mbar_init();
-  }
-  if (warp == kPfMmaWarp) tc_alloc(&hdr.tmem_base, kPfTmemCols);
-  tc_fence_before_sync();
-  __syncthreads();
-  tc_fence_after_sync();
-  const uint32_t tmem = hdr.tmem_base;
-  uint8_t *qs = smem + Lay::Q_OFF;
-  uint8_t *stages = smem + Lay::STAGE_OFF;
-  volatile int *abort = &hdr.abort;
-
-  if (warp == kPfTmaWarp) {
-    // ------------------------------------------------------------ TMA
-    // The whole warp runs the loop: lane j fetches block-table entry j of the
-    // next stage while lane 0 issues this stage's copies.
-    if (lane == 0) {
-      mbar_arrive_expect_tx(&hdr.q_full, tiles * NH * kPfTileRows * 128u);
-      for (int t = 0; t < tiles; ++t)
-#pragma unroll
-        for (int hf = 0; hf < NH; ++hf)
-          tma_load_4d(qs + t * Lay::Q_TILE + hf * Lay::Q_HALF, &p.tmap_q, hf * 64, 0, h, q0 + cta * QC + t * QT,
-                      &hdr.q_full);
-    }
-    const int bs = p.block_size;
-    const int bpt = kPfKeys / bs;  // blocks per stage (<= 8)
-    const int32_t *table = p.block_tables + static_cast<size_t>(s) * p.max_blocks;
-    auto stage_blocks = [&](int i) { return min(bpt, (kv_end - i * kPfKeys + bs - 1) / bs); };
-    int next = lane < stage_blocks(0) ? __ldg(table + lane) : 0;
-    int issued = 0;
-    bool ok = true;
-    for (int i = 0; i < n_stages; ++i) {
-      const int st = i % NS;
-      const int nblk = stage_blocks(i);
-      int phys = next;
-      if (i + 1 < n_stages && lane < stage_blocks(i + 1)) next = __ldg(table + (i + 1) * bpt + lane);
-      if (lane < nblk && (phys < 0 || phys >= p.num_blocks)) {
-        record_error(p.err, kErrBlockIndex);
-        phys = 0;  // read a valid block; the result is void and flagged
-      }
-      bool waited = true;
-      if (lane == 0 && i >= NS) waited = mbar_wait(&hdr.kv_empty[st], ((i / NS) - 1) & 1, abort);
-      if (!__shfl_sync(0xffffffffu, waited, 0)) {
-        ok = false;
-        break;
-      }
-      uint8_t *kb = stages + st * Lay::STAGE_BYTES;
-      uint8_t *vb = kb + NH * kPfHalf;
-      if (lane == 0) mbar_arrive_expect_tx(&hdr.kv_full[st], 2u * NH * static_cast<uint32_t>(nblk * bs) * 128u);
-      __syncwarp();
-      if (lane < nblk) {  // lane j issues block j's boxes: the lanes' copies go out together
-        const int r0 = (phys * p.num_kv_heads + h) * bs;
-#pragma unroll
-        for (int hf = 0; hf < NH; ++hf) {
-          tma_load_2d(kb + hf * kPfHalf + lane * bs * 128, &p.tmap_k, hf * 64, r0, &hdr.kv_full[st]);
-          tma_load_2d(vb + hf * kPfHalf + lane * bs * 128, &p.tmap_v, hf * 64, r0, &hdr.kv_full[st]);
-        }
-      }
-      issued = i + 1;
-    }
-    if (lane == 0) {
-      if (!ok) {
-        record_error(p.err, kErrTimeout);
-        *abort = 1;
-        // wait, within the limit, for the copies still in flight
-        for (int j = max(0, issued - NS); j < issued; ++j)
-          mbar_wait(&hdr.kv_full[j % NS], (j / NS) & 1, nullptr);
-      }
-      mbar_wait(&hdr.q_full, 0, nullptr);
-    }
-  } else if (warp >= kPfMmaWarp) {
-    // ------------------------------------------------------------ MMA (tile t)
-    const int t = warp - kPfMmaWarp;
-    if (lane == 0 && t < tiles) {
-      bool ok = mbar_wait(&hdr.q_full, 0, abort);
-      const uint32_t qt = smem_addr(qs) + t * Lay::Q_TILE;
-      const uint32_t saddr = smem_addr(stages);
-      const uint32_t tt = tmem + t * kPfTileCols;
-      auto issue_qk = [&](int i) -> bool {
-        const int st = i % NS;
-        if (!mbar_wait(&hdr.kv_full[st], (i / NS) & 1, abort)) return false;
-        tc_fence_after_sync();
-        // descriptors of the first k-step; a k-step advances the start
-        // address field (16-byte units) by 32 bytes, a row half by a region
-        const uint64_t a0 = umma_desc_sw128(qt, 16, 1024);
-        const uint64_t b0 = umma_desc_sw128(saddr + st * Lay::STAGE_BYTES, 16, 1024);
-        const uint32_t d = tt + (i & 1) * kPfKeys;
-#pragma unroll
-        for (int kk = 0; kk < KSTEPS; ++kk) {
-          const uint32_t off = (kk % 4) * 32;  // 16 elements = 32 bytes into the swizzled row
-          tc_mma_f16(d, a0 + (((kk / 4) * Lay::Q_HALF + off) >> 4), b0 + (((kk / 4) * kPfHalf + off) >> 4),
-                     IDESC_QK, kk > 0);
-        }
-        tc_commit(&hdr.s_full[t][i & 1]);
-        return true;
-      };
-      if (ok) ok = issue_qk(0);
-      for (int i = 0; i < n_stages && ok; ++i) {
-        if (i + 1 < n_stages && !issue_qk(i + 1)) {
-          ok = false;
-          break;
-        }
-        if (!mbar_wait(&hdr.p_full[t][i & 1], (i >> 1) & 1, abort)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after_sync();
-        const uint64_t b0 = umma_desc_sw128(saddr + (i % NS) * Lay::STAGE_BYTES + NH * kPfHalf, kPfHalf, 1024);
-#pragma unroll
-        for (int kk = 0; kk < kPfKeys / 16; ++kk)  // 16 keys: 8 columns of P, 2048 bytes of V rows
-          tc_mma_f16_ta(tt + 2 * kPfKeys, tt + (i & 1) * kPfKeys + kk * 8, b0 + kk * 128, IDESC_PV,
-                        (i > 0 || kk > 0) ? 1u : 0u);
-        tc_commit(&hdr.pv_done[t]);
-        if (i + 1 == n_stages) tc_commit(&hdr.o_ready[t]);
-        tc_commit(&hdr.kv_empty[i % NS]);
-      }
-      if (!ok) {
-        record_error(p.err, kErrTimeout);
-        *abort = 1;
-      }
-      // every product this thread issued has completed before the memory is released
-      tc_commit(&hdr.fin[t]);
-      mbar_wait(&hdr.fin[t], 0, nullptr);
-    }
-  } else if (warp / 4 < tiles) {
-    // ------------------------------------------------------------ softmax
-    const int t = warp / 4;                  // tile
-    const int r = threadIdx.x & 127;         // row = TMEM lane
-    const int tok = cta * QC + t * QT + r / G;
-    const int pos = pos0 + min(tok, n - 1);  // rows past the new tokens take the last one's (not stored)
-    const uint32_t trow = tmem + t * kPfTileCols + (static_cast<uint32_t>(32 * (warp & 3)) << 16);
-    float m = -INFINITY, l = 0.f;
-    bool ok = true;
-    for (int i = 0; i < n_stages; ++i) {
-      if (!__all_sync(0xffffffffu, mbar_wait(&hdr.s_full[t][i & 1], (i >> 1) & 1, abort))) {
-        ok = false;
-        break;
-      }
-      tc_fence_after_sync();
-      const int k0 = i * kPfKeys;
-      float sv[kPfKeys];
-      {
-        uint32_t raw[32];
-        tc_ld32(trow + (i & 1) * kPfKeys, raw);
-#pragma unroll
-        for (int j = 0; j < 32; ++j) sv[j] = __uint_as_float(raw[j]);
-        tc_ld32(trow + (i & 1) * kPfKeys + 32, raw);
-#pragma unroll
-        for (int j = 0; j < 32; ++j) sv[32 + j] = __uint_as_float(raw[j]);
-      }
-      // Most stages lie wholly at or before every row of the warp: no mask,
-      // and with a positive scale the maximum is taken on the raw scores and
-      // the scale folded into the exponent's one fma.  Otherwise the scores
-      // are scaled, then masked (key position > row position: -inf).
-      const float c = p.qk_scale_log2;
-      const bool plain = c > 0.f && __all_sync(0xffffffffu, k0 + kPfKeys - 1 <= pos);
-      float mx, cm;
-      if (plain) {
-        float a = sv[0], b = sv[32];  // two chains of 3-input maxima
-#pragma unroll
-        for (int j = 1; j < 31; j += 2) {
-          a = fmax3(a, sv[j], sv[j + 1]);
-          b = fmax3(b, sv[32 + j], sv[33 + j]);
-        }
-        mx = fmax3(a, b, fmaxf(sv[31], sv[63])) * c;
-        cm = c;
-      } else {
-        float mx0 = -INFINITY, mx1 = -INFINITY;
-#pragma unroll
-        for (int j = 0; j < kPfKeys; j += 2) {
-          sv[j] = (k0 + j <= pos) ? sv[j] * c : -INFINITY;
-          sv[j + 1] = (k0 + j + 1 <= pos) ? sv[j + 1] * c : -INFINITY;
-          mx0 = fmaxf(mx0, sv[j]);
-          mx1 = fmaxf(mx1, sv[j + 1]);
-        }
-        mx = fmaxf(mx0, mx1);
-        cm = 1.f;
-      }
-      const bool grow = mx > m + kPfLazy;
-      if (__any_sync(0xffffffffu, grow && i > 0)) {  // tcgen05.ld / st are warp-wide
-        // O holds the previous P V: wait for it, then rescale.  S of this
-        // stage was issued after the P V before the previous one, and the
-        // tensor pipe completes in order, so pv_done is at most one phase
-        // behind here and the parity wait is exact.
-        if (!__all_sync(0xffffffffu, mbar_wait(&hdr.pv_done[t], (i - 1) & 1, abort))) {
-          ok = false;
-          break;
-        }
-        tc_fence_after_sync();
-        const float alpha = grow ? fast_exp2(m - mx) : 1.f;
-#pragma unroll
-        for (int c = 0; c < D; c += 32) {
-          uint32_t ov[32];
-          tc_ld32(trow + 2 * kPfKeys + c, ov);
-#pragma unroll
-          for (int j = 0; j < 32; ++j) ov[j] = __float_as_uint(__uint_as_float(ov[j]) * alpha);
-          tc_st32(trow + 2 * kPfKeys + c, ov);
-        }
-      }
-      if (grow) {
-        l *= fast_exp2(m - mx);  // 0 while m is -inf (l is 0 then)
-        m = mx;
-      }
-      const float base = m == -INFINITY ? 0.f : m;
-      // p = 2^(s * cm - base), two lanes per fma and per add of the row sum
-      const uint64_t cm2 = f2(cm, cm), nb2 = f2(-base, -base);
-      uint64_t sum0 = f2(0.f, 0.f), sum1 = sum0;
-      uint32_t pw[kPfKeys / 2];
-#pragma unroll
-      for (int j = 0; j < kPfKeys; j += 2) {
-        float x, y;
-        f2_split(ffma2(f2(sv[j], sv[j + 1]), cm2, nb2), x, y);
-        const float a = fast_exp2(x), b = fast_exp2(y);
-        pw[j / 2] = pack2_rn<DT>(a, b);
-        if ((j & 2) == 0)
-          sum0 = fadd2(sum0, f2(a, b));
-        else
-          sum1 = fadd2(sum1, f2(a, b));
-      }
-      {
-        float l0, l1, l2, l3;
-        f2_split(sum0, l0, l1);
-        f2_split(sum1, l2, l3);
-        l += (l0 + l1) + (l2 + l3);
-      }
-      tc_st32(trow + (i & 1) * kPfKeys, pw);  // P over the S buffer just read
-      if (k0 + kPfKeys > kv_end) {
-        // keys past kv_end hold stale (possibly NaN) values: zero their V rows,
-        // since 0 * NaN would reach O.  Each tile does it before its own P V
-        // (the tiles' products are issued independently); both write zeros.
-        if (!__all_sync(0xffffffffu, mbar_wait(&hdr.kv_full[i % NS], (i / NS) & 1, abort))) {
-          ok = false;
-          break;
-        }
-        uint8_t *vb = stages + (i % NS) * Lay::STAGE_BYTES + NH * kPfHalf;
-        const int z0 = kv_end - k0;
-        for (int idx = r; idx < (kPfKeys - z0) * 8 * NH; idx += kPfTileRows) {
-          const int hf = idx / ((kPfKeys - z0) * 8), rem = idx % ((kPfKeys - z0) * 8);
-          *reinterpret_cast<uint4 *>(vb + hf * kPfHalf + (z0 + rem / 8) * 128 + (rem % 8) * 16) =
-              make_uint4(0u, 0u, 0u, 0u);
-        }
-        fence_proxy_async_smem();  // the zeroed V rows visible to the tensor cores
-      }
-      tc_fence_before_sync();  // P and O stores ordered before the arrive
-      mbar_arrive(&hdr.p_full[t][i & 1]);
-    }
-    if (!ok) {
-      record_error(p.err, kErrTimeout);
-      *abort = 1;
-    } else if (__all_sync(0xffffffffu, mbar_wait(&hdr.o_ready[t], 0, abort))) {
-      // (pv_done cannot serve here: the softmax does not wait for every P V,
-      // so the last two may both be pending and a parity wait would take the
-      // older phase for the newer)
-      tc_fence_after_sync();
-      const float inv = 1.f / l;
-      const bool store = tok < n;
-      uint8_t *row = static_cast<uint8_t *>(p.out) +
-                     (static_cast<size_t>(q0 + min(tok, n - 1)) * p.num_q_heads + h * G + r % G) * D * 2;
-#pragma unroll
-      for (int c = 0; c < D; c += 32) {
-        uint32_t ov[32];
-        tc_ld32(trow + 2 * kPfKeys + c, ov);
-        if (store) {
-#pragma unroll
-          for (int j = 0; j < 32; j += 8) {
-            uint4 v;
-            v.x = pack2_rn<DT>(__uint_as_float(ov[j]) * inv, __uint_as_float(ov[j + 1]) * inv);
-            v.y = pack2_rn<DT>(__uint_as_float(ov[j + 2]) * inv, __uint_as_float(ov[j + 3]) * inv);
-            v.z = pack2_rn<DT>(__uint_as_float(ov[j + 4]) * inv, __uint_as_float(ov[j + 5]) * inv);
-            v.w = pack2_rn<DT>(__uint_as_float(ov[j + 6]) * inv, __uint_as_float(ov[j + 7]) * inv);
-            *reinterpret_cast<uint4 *>(row + (c + j) * 2) = v;
-          }
-        }
-      }
-    } else {
-      record_error(p.err, kErrTimeout);
-      *abort = 1;
-    }
-  }
-  // ------------------------------------------------------------ teardown
-  tc_fence_before_sync();
-  __syncthreads();
-  if (warp == kPfMmaWarp) {
-    tc_fence_after_sync();
-    tc_dealloc(tmem, kPfTmemCols);
-  }
-}
-
-template <int DT, int D, int G>
-pa_status launch_prefill(const PrefillParams &p, int num_seqs, int max_q_len, cudaStream_t stream) {
-  constexpr int QC = kPfRows / G;
-  static bool configured[64];  // per device: dynamic shared memory already allowed
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return cuda_fail(e);
-  if (dev < 0 || dev >= 64 || !configured[dev]) {
-    e = cudaFuncSetAttribute(prefill_kernel<DT, D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             PfLayout<D>::SMEM);
-    if (e != cudaSuccess) return cuda_fail(e);
-    if (dev >= 0 && dev < 64) configured[dev] = true;
-  }
-  const dim3 grid((max_q_len + QC - 1) / QC, num_seqs, p.num_kv_heads);
-  prefill_kernel<DT, D, G><<<grid, kPfThreads, PfLayout<D>::SMEM, stream>>>(p);
-  e = cudaGetLastError();
-  return e == cudaSuccess ? PA_OK : cuda_fail(e);
-}
-
-template <int DT, int D>
-pa_status by_group(int G, const PrefillParams &p, int num_seqs, int max_q_len, cudaStream_t stream) {
-  switch (G) {
-    case 1: return launch_prefill<DT, D, 1>(p, num_seqs, max_q_len, stream);
-    case 2: return launch_prefill<DT, D, 2>(p, num_seqs, max_q_len, stream);
-    case 4: return launch_prefill<DT, D, 4>(p, num_seqs, max_q_len, stream);
-    case 8: return launch_prefill<DT, D, 8>(p, num_seqs, max_q_len, stream);
-  }
-  return PA_ERR_UNSUPPORTED;
-}
 
 // [rows, head_dim] view of a 16-bit cache, box {64 elements, block_size rows}
 // (one 128-byte half of one (block, head) tile), 128-byte swizzle.
@@ -549,8 +65,9 @@ extern "C" pa_status pa_prefill(void *out, const void *q, int32_t q_dtype, int32
   const int G = num_q_heads / cache->kv_heads;
   if (G != 1 && G != 2 && G != 4 && G != 8) return PA_ERR_UNSUPPORTED;
   if (!supported_cache_shape(cache)) return PA_ERR_UNSUPPORTED;
-  if (cache->dtype != PA_F16 && cache->dtype != PA_BF16) return PA_ERR_UNSUPPORTED;  // 16-bit caches only
-  if (q_dtype != cache->dtype) return PA_ERR_UNSUPPORTED;
+  const bool byte_codes = cache->dtype >= PA_FP8_E4M3;  // FP8 or INT8, with scales
+  if (byte_codes ? (q_dtype != PA_F16 && q_dtype != PA_BF16) : q_dtype != cache->dtype)
+    return PA_ERR_UNSUPPORTED;
   if (num_seqs > 65535 || cache->kv_heads > 65535) return PA_ERR_UNSUPPORTED;      // grid limits
   if (static_cast<long long>(cache->num_blocks) * cache->kv_heads * cache->block_size > INT_MAX ||
       static_cast<long long>(max_blocks_per_seq) * cache->block_size > INT_MAX)
@@ -558,8 +75,10 @@ extern "C" pa_status pa_prefill(void *out, const void *q, int32_t q_dtype, int32
 
   PrefillParams p{};
   if (!encode_q_view(&p.tmap_q, q, num_q_tokens, cache->kv_heads, G, cache->head_dim) ||
-      !encode_cache_view(&p.tmap_k, k_cache, cache) || !encode_cache_view(&p.tmap_v, v_cache, cache))
+      (!byte_codes && (!encode_cache_view(&p.tmap_k, k_cache, cache) || !encode_cache_view(&p.tmap_v, v_cache, cache))))
     return cuda_fail(cudaErrorInvalidValue);
+  p.k_cache = static_cast<const uint8_t *>(k_cache);
+  p.v_cache = static_cast<const uint8_t *>(v_cache);
   p.out = out;
   p.cu_q = cu_q_lens;
   p.block_tables = block_tables;
@@ -569,12 +88,20 @@ extern "C" pa_status pa_prefill(void *out, const void *q, int32_t q_dtype, int32
   p.num_blocks = cache->num_blocks;
   p.block_size = cache->block_size;
   p.max_blocks = max_blocks_per_seq;
-  p.qk_scale_log2 = scale * 1.4426950408889634f;
+  const bool per_head = byte_codes && cache->k_head_scales != nullptr;
+  p.qk_scale_log2 = scale * (byte_codes && !per_head ? cache->k_scale : 1.0f) * 1.4426950408889634f;
+  p.v_scale = byte_codes && !per_head ? cache->v_scale : 1.0f;
+  p.k_head_scale = per_head ? cache->k_head_scales : nullptr;
+  p.v_head_scale = per_head ? cache->v_head_scales : nullptr;
   p.err = device_error;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (cache->dtype == PA_F16)
-    return cache->head_dim == 64 ? by_group<kF16, 64>(G, p, num_seqs, max_q_len, s)
-                                 : by_group<kF16, 128>(G, p, num_seqs, max_q_len, s);
-  return cache->head_dim == 64 ? by_group<kBF16, 64>(G, p, num_seqs, max_q_len, s)
-                               : by_group<kBF16, 128>(G, p, num_seqs, max_q_len, s);
+  const int D = cache->head_dim;
+  switch (cache->dtype) {
+    case PA_F16: return dispatch_prefill<kF16>(q_dtype, D, G, p, num_seqs, max_q_len, s);
+    case PA_BF16: return dispatch_prefill<kBF16>(q_dtype, D, G, p, num_seqs, max_q_len, s);
+    case PA_FP8_E4M3: return dispatch_prefill_e4m3(q_dtype, D, G, p, num_seqs, max_q_len, s);
+    case PA_FP8_E5M2: return dispatch_prefill_e5m2(q_dtype, D, G, p, num_seqs, max_q_len, s);
+    case PA_INT8: return dispatch_prefill_i8(q_dtype, D, G, p, num_seqs, max_q_len, s);
+  }
+  return PA_ERR_UNSUPPORTED;
 }

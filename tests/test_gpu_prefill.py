@@ -32,13 +32,14 @@ def _run(w, q, q_lens, err=None):
     run = G.GpuRun(w).setup()
     run.step()
     err = run.err if err is None else err
-    pa.pa_prefill(out, q, cu, run.kc, run.vc, run.bt, run.sl, max(q_lens), w.scale, device_error=err)
+    pa.pa_prefill(out, q, cu, run.kc, run.vc, run.bt, run.sl, max(q_lens), w.scale, device_error=err,
+                  **run.kw)
     torch.cuda.synchronize()
     return out, run
 
 
 def _check(w, got, ref):
-    tol = G.TOL[w.q_dtype]
+    tol = G.tolerance(w)
     got = got.float().cpu().numpy().astype(np.float64)
     bound = np.maximum(tol, G.ulp(ref, w.q_dtype))
     err = np.abs(got - ref)
@@ -64,6 +65,51 @@ def test_prefill_matches_oracle(dtype, d, bs, group):
     c = G.oracle_cache(w)
     ref = A.paged_prefill(G.bits_to_f64(G.bits(q), dtype), q_lens, c.k, c.v, dtype,
                           w.block_tables, w.seq_lens, w.scale)
+    _check(w, out, ref)
+
+
+BYTE_CASES = [("e4m3", "bf16"), ("e5m2", "f16"), ("int8", "bf16"), ("int8", "f16"), ("e4m3", "f16")]
+
+
+@pytest.mark.parametrize("cache_dtype,q_dtype", BYTE_CASES)
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("group", [1, 2, 8])
+@pytest.mark.parametrize("per_head", [False, True])
+def test_prefill_byte_cache_matches_oracle(cache_dtype, q_dtype, d, group, per_head):
+    """FP8 and INT8 caches: codes widened to fp16 for the products, a bf16 q
+    rewritten as fp16, the K scale in the scores and the V scale in the
+    output; against the oracle on the dequantised values."""
+    Hkv = 2
+    lens = [L for L, _ in CASES]
+    q_lens = [n for _, n in CASES]
+    ks, vs = ((0.03, 0.07), (0.05, 0.02)) if per_head else (0.04, 0.06)
+    if cache_dtype != "int8" and not per_head:
+        ks, vs = 1.0, 0.5
+    w = W.random_case(_seed(cache_dtype, q_dtype, d, group, per_head), len(lens), Hkv * group, Hkv, d, 16,
+                      cache_dtype, q_dtype, lens, device=G.DEV, k_scale=ks, v_scale=vs)
+    gen = torch.Generator(device=G.DEV).manual_seed(_seed("qb", cache_dtype, d, group))
+    q = torch.randn((sum(q_lens), Hkv * group, d), generator=gen, device=G.DEV).to(w.q.dtype)
+    out, run = _run(w, q, q_lens)
+    assert int(run.err.item()) == 0
+    c = G.oracle_cache(w)
+    ref = A.paged_prefill(G.bits_to_f64(G.bits(q), q_dtype), q_lens, c.k, c.v, cache_dtype,
+                          w.block_tables, w.seq_lens, w.scale, w.k_scale, w.v_scale)
+    _check(w, out, ref)
+
+
+def test_prefill_byte_cache_large_bf16_queries():
+    """bf16 q beyond fp16's range: the query tile is scaled by a power of two
+    before it is rounded to fp16, and the factor undone on the scores."""
+    lens, q_lens = [300, 90], [200, 90]
+    w = W.random_case(4, 2, 4, 2, 128, 16, "e4m3", "bf16", lens, device=G.DEV, k_scale=0.02, v_scale=1.0)
+    gen = torch.Generator(device=G.DEV).manual_seed(12)
+    q = (torch.randn((sum(q_lens), 4, 128), generator=gen, device=G.DEV) * 2e5).bfloat16()
+    out, run = _run(w, q, q_lens)
+    assert int(run.err.item()) == 0
+    c = G.oracle_cache(w)
+    ref = A.paged_prefill(G.bits_to_f64(G.bits(q), "bf16"), q_lens, c.k, c.v, "e4m3",
+                          w.block_tables, w.seq_lens, w.scale, w.k_scale, w.v_scale)
+    assert np.isfinite(out.float().cpu().numpy()).all()
     _check(w, out, ref)
 
 
@@ -138,15 +184,19 @@ def test_bad_lengths_and_blocks_are_reported():
 
 
 def test_unsupported_inputs_are_refused_on_the_host():
-    kc = torch.zeros((4, 2, 16, 64), dtype=torch.uint8, device=G.DEV)
+    import ctypes
+    kc = torch.zeros((4, 2, 16, 64), dtype=torch.float16, device=G.DEV)
     q = torch.zeros((3, 2, 64), dtype=torch.float16, device=G.DEV)
     cu = torch.tensor([0, 3], dtype=torch.int32, device=G.DEV)
     bt = torch.zeros((1, 4), dtype=torch.int32, device=G.DEV)
     sl = torch.tensor([3], dtype=torch.int32, device=G.DEV)
     lib = pa.load_library()
-    desc = pa.cache_desc(kc, "e4m3")
-    import ctypes
-    st = lib.pa_prefill(q.data_ptr(), q.data_ptr(), 0, 3, cu.data_ptr(), 1, 2, 3, kc.data_ptr(),
-                        kc.data_ptr(), ctypes.byref(desc), bt.data_ptr(), 4, sl.data_ptr(), 0.125,
-                        None, None)
-    assert st == 2   # one-byte caches: unsupported in prefill
+
+    def call(desc, q_dtype, heads=2):
+        return lib.pa_prefill(q.data_ptr(), q.data_ptr(), q_dtype, 3, cu.data_ptr(), 1, heads, 3,
+                              kc.data_ptr(), kc.data_ptr(), ctypes.byref(desc), bt.data_ptr(), 4,
+                              sl.data_ptr(), 0.125, None, None)
+    assert call(pa.cache_desc(kc, "f16"), pa.PA_BF16) == 2    # a 16-bit cache takes its own q dtype
+    assert call(pa.cache_desc(kc, "f16"), pa.PA_F16, heads=6) == 2   # group size 3
+    kb = kc.view(torch.uint8)[..., :64]
+    assert call(pa.cache_desc(kb.contiguous(), "e4m3"), 7) == 2      # q neither fp16 nor bf16
