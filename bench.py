@@ -60,6 +60,9 @@ def parse():
                          "prefill: causal prefill of each sequence's tokens after the shared "
                          "prefix (qwen3-prefix)")
     ap.add_argument("--swap-seqs", type=int, default=16)
+    ap.add_argument("--prefill-cache", default="bf16", choices=["bf16", "e4m3", "e5m2", "int8"],
+                    help="cache type of the prefill bench (one-byte caches: codes of N(0,1) K/V "
+                         "with scale 1, or 1/32 for int8)")
     return ap.parse_args()
 
 
@@ -722,12 +725,16 @@ def run_prefill(args, rank, world, local):
     q_lens = [int(L) - prefix for L in w.seq_lens]
     T = sum(q_lens)
     shape = (w.num_blocks, w.Hkv, w.bs, w.d)
-    kc = torch.zeros(shape, dtype=torch.bfloat16, device=dev)
-    vc = torch.zeros(shape, dtype=torch.bfloat16, device=dev)
+    cdt = args.prefill_cache
+    byte = cdt != "bf16"
+    kc = torch.zeros(shape, dtype=torch.uint8 if byte else torch.bfloat16, device=dev)
+    vc = torch.zeros_like(kc)
+    kw = dict(cache_dtype=cdt, k_scale=1 / 32 if cdt == "int8" else 1.0,
+              v_scale=1 / 32 if cdt == "int8" else 1.0)
     # the cached prefix is written once (it was computed by an earlier
     # request); each step writes the new tokens' K/V and prefills them
     pa.pa_reshape_and_cache(w.ctx_k[:prefix].contiguous(), w.ctx_v[:prefix].contiguous(),
-                            torch.from_numpy(w.ctx_slots[:prefix]).to(dev), kc, vc)
+                            torch.from_numpy(w.ctx_slots[:prefix]).to(dev), kc, vc, **kw)
     gen = torch.Generator(device=dev).manual_seed(seed)
     k_new = torch.randn((T, w.Hkv, w.d), generator=gen, device=dev).bfloat16()
     v_new = torch.randn((T, w.Hkv, w.d), generator=gen, device=dev).bfloat16()
@@ -745,10 +752,10 @@ def run_prefill(args, rank, world, local):
     maxq = max(q_lens)
 
     def step(evs=None):
-        pa.pa_reshape_and_cache(k_new, v_new, slots, kc, vc, device_error=err)
+        pa.pa_reshape_and_cache(k_new, v_new, slots, kc, vc, device_error=err, **kw)
         if evs:
             evs[0].record(stream)
-        pa.pa_prefill(out, q, cu, kc, vc, bt, sl, maxq, w.scale, device_error=err)
+        pa.pa_prefill(out, q, cu, kc, vc, bt, sl, maxq, w.scale, device_error=err, **kw)
         if evs:
             evs[1].record(stream)
 
@@ -809,14 +816,15 @@ def run_prefill(args, rank, world, local):
     line = {
         "metric": PREFILL_METRIC, "value": round(job_rate(flops, world, step_t) / 1e12, 2), "unit": "TFLOP/s",
         "n_gpus": world, "steps": K, "warmup": args.warmup, "ms_per_step": round(step_t * 1e3, 4),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f16" if byte else "bf16",
         "data": "synthetic (seeded N(0,1) q/K/V; the shared-prefix workload's tables and lengths)",
         "config": {"workload": f"{config}: {w.S} seqs, cached prefix {prefix} tokens, new tokens "
                                f"{min(q_lens)}..{max(q_lens)} (total {T}), {w.Hq}q/{w.Hkv}kv heads, "
-                               f"d {w.d}, bs {w.bs}, bf16",
+                               f"d {w.d}, bs {w.bs}, q bf16, cache {cdt}",
                    "new_tokens_per_step": T, "flops_per_step": flops,
                    "l2": "K/V of the suffixes %.0f MB + the shared prefix; outputs %.0f MB"
-                         % (T * w.Hkv * w.d * 4 / 1e6, T * w.Hq * w.d * 2 / 1e6),
+                         % (T * w.Hkv * w.d * (2 if byte else 4) / 1e6, T * w.Hq * w.d * 2 / 1e6),
                    "parallelism": f"replicas x{world}"},
         "new_tokens_per_s": round(world * T / step_t, 1),
         "gpu_launches": 2 * K,
@@ -833,27 +841,32 @@ def run_prefill(args, rank, world, local):
         "clocks": clocks,
     }
     if not args.no_cpu_baseline:
-        line["cpu_baseline"] = prefill_cpu_baseline(w, q_lens, prefix)
+        line["cpu_baseline"] = prefill_cpu_baseline(w, q_lens, prefix, cdt)
     print(json.dumps(line), flush=True)
 
 
-def prefill_cpu_baseline(w, q_lens, prefix, budget_s: float = 10.0):
+def prefill_cpu_baseline(w, q_lens, prefix, cache_dtype="bf16", budget_s: float = 10.0):
     """The oracle's prefill on a bounded sample: the first sequence's first
-    16 new tokens, all query heads."""
+    16 new tokens, all query heads, over random finite codes of the cache
+    type."""
     import torch
     from oracle import attention as A
     from oracle.cache import PagedKVCache
     sub = W.subset(w, [0], 1)
     n = min(16, q_lens[0])
     L = prefix + n
-    c = PagedKVCache(sub.num_blocks, sub.Hkv, sub.bs, sub.d, sub.cache_dtype, fill_nan=False)
+    c = PagedKVCache(sub.num_blocks, sub.Hkv, sub.bs, sub.d, cache_dtype, fill_nan=False)
     rng = np.random.default_rng(0)
-    c.k[:] = rng.integers(0, 1 << 15, c.k.shape, dtype=np.uint16) & 0x3BFF
-    c.v[:] = rng.integers(0, 1 << 15, c.v.shape, dtype=np.uint16) & 0x3BFF
+    if cache_dtype == "bf16":
+        c.k[:] = rng.integers(0, 1 << 15, c.k.shape, dtype=np.uint16) & 0x3BFF
+        c.v[:] = rng.integers(0, 1 << 15, c.v.shape, dtype=np.uint16) & 0x3BFF
+    else:  # finite codes (no FP8 NaN or infinity)
+        c.k[:] = rng.integers(0, 256, c.k.shape, dtype=np.uint8) & 0xF6
+        c.v[:] = rng.integers(0, 256, c.v.shape, dtype=np.uint8) & 0xF6
     q = rng.standard_normal((n, w.Hq, w.d))
     t0, reps = time.perf_counter(), 0
     while time.perf_counter() - t0 < budget_s:
-        A.paged_prefill(q, [n], c.k, c.v, sub.cache_dtype, sub.block_tables, np.array([L]), w.scale)
+        A.paged_prefill(q, [n], c.k, c.v, cache_dtype, sub.block_tables, np.array([L]), w.scale)
         reps += 1
     dt = (time.perf_counter() - t0) / reps
     flops = 4 * w.d * w.Hq * sum(range(L - n + 1, L + 1))

@@ -39,7 +39,8 @@
 // One-byte caches (FP8 e4m3 / e5m2, INT8): the products take fp16 operands.
 // The TMA warp copies each (block, head) tile of codes whole (one bulk copy
 // per block for K and for V) into a ring of four code slots, widens them
-// exactly to fp16 into three 16-bit stages of the layout above, and marks
+// exactly to fp16 (a warpgroup of four widening warps, one on each SM
+// sub-partition) into three 16-bit stages of the layout above, and marks
 // the stage full.  A bf16 query tile is rewritten in place as fp16 by its
 // softmax warps, times a power of two that brings its largest entry within
 // fp16's range; the factor, and the K scale, go into the score scale, the
@@ -78,7 +79,11 @@ constexpr int kPfRows = kPfTileRows * kPfTiles;
 constexpr int kPfKeys = 64;          // keys per pipeline stage
 constexpr int kPfTmaWarp = 8;
 constexpr int kPfMmaWarp = 9;  // and 10: one issuing warp per tile
-constexpr int kPfThreads = 32 * 11;
+constexpr int kPfConvWarp0 = 12;  // one-byte caches: warps 12..15 widen the codes
+constexpr int kPfConvWarps = 4;
+// threads: softmax 8 warps, TMA, 2 MMA (one-byte caches: + an idle warp
+// that completes the third warpgroup, + the widening warpgroup)
+__host__ __device__ constexpr int pf_threads(bool kv8) { return 32 * (kv8 ? 16 : 11); }
 constexpr int kPfHalf = kPfKeys * 128;  // one 128-byte column half of a 64-key stage
 constexpr int kPfStages = 5;      // 16-bit K/V stages (three with one-byte caches)
 constexpr int kPfCodeSlots = 4;   // one-byte caches: stages of codes in flight
@@ -113,11 +118,52 @@ struct PfHeader {
   uint64_t q_full;
   uint64_t fin[kPfTiles];
   uint64_t code_full[kPfCodeSlots];  // one-byte caches: a stage's codes have landed
+  uint64_t code_empty[kPfCodeSlots]; // and the slot has been widened
   uint64_t q_ready[kPfTiles];        // a bf16 query tile has been rewritten as fp16
   float qmax[kPfTiles][4];           // its warps' largest |q|
   uint32_t tmem_base;
   int abort;
 };
+
+// Widen the codes of a slot (K then V, the first `keys` keys of each) into a
+// 16-bit stage: 8 codes make one 16-byte chunk, and chunk c of key row k of
+// half hf lands at chunk c ^ (k mod 8).  The work is 2 keys / KPI warp
+// iterations of 32 chunks, lane = (key, half, chunk); this warp takes
+// iterations part, part + parts, ...  keys is a multiple of 8.
+template <int KVT, int D>
+__device__ __forceinline__ void widen_codes(const uint8_t *slot, uint8_t *stage, int keys, int lane, int part,
+                                            int parts) {
+  constexpr int NH = D / 64;
+  constexpr int KPI = 32 / (NH * 8);
+  const int kr = lane / (NH * 8), hf = (lane >> 3) % NH, c = lane & 7;
+  const int per = keys / KPI;  // iterations per tensor
+  const uint8_t *src = slot + hf * 64 + c * 8;
+  uint8_t *dst = stage + hf * kPfHalf;
+  // the loads of a batch go before its stores: the compiler cannot tell
+  // that the stores do not alias them
+  constexpr int B = 4;
+  for (int it0 = part; it0 < 2 * per; it0 += B * parts) {
+    uint2 w[B];
+    int off[B];
+#pragma unroll
+    for (int u = 0; u < B; ++u) {
+      const int it = it0 + u * parts;
+      const int tv = it >= per;
+      const int k = (it - tv * per) * KPI + kr;
+      off[u] = it < 2 * per ? tv * NH * kPfHalf + k * 128 + ((c ^ (k & 7)) << 4) : -1;
+      w[u] = it < 2 * per ? *reinterpret_cast<const uint2 *>(src + tv * kPfKeys * D + k * D) : make_uint2(0u, 0u);
+    }
+#pragma unroll
+    for (int u = 0; u < B; ++u) {
+      if (off[u] >= 0) {
+        uint4 o;
+        byte4_to_half2x2<KVT>(w[u].x, o.x, o.y);
+        byte4_to_half2x2<KVT>(w[u].y, o.z, o.w);
+        *reinterpret_cast<uint4 *>(dst + off[u]) = o;
+      }
+    }
+  }
+}
 
 __device__ __forceinline__ void named_bar_sync(int id, int threads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
@@ -157,7 +203,7 @@ __device__ __forceinline__ uint64_t fadd2(uint64_t a, uint64_t b) {
 
 // DT: the type of q and out; KVT: the cache's (DT itself for 16-bit caches)
 template <int DT, int KVT, int D, int G>
-__global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_constant__ PrefillParams p) {
+__global__ void __launch_bounds__(pf_threads(is_byte(KVT)), 1) prefill_kernel(const __grid_constant__ PrefillParams p) {
   constexpr bool KV8 = is_byte(KVT);
   constexpr int MT = KV8 ? kF16 : DT;          // the products' operand type
   constexpr bool QCONV = KV8 && DT == kBF16;   // q is rewritten as fp16 first
@@ -196,10 +242,13 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < NS; ++i) {
-      mbar_init(&hdr.kv_full[i], 1);
+      mbar_init(&hdr.kv_full[i], KV8 ? kPfConvWarps : 1);  // one-byte caches: each widening warp
       mbar_init(&hdr.kv_empty[i], tiles);  // each tile's MMA warp frees the stage
     }
-    for (int c = 0; c < NC; ++c) mbar_init(&hdr.code_full[c], 1);
+    for (int c = 0; c < NC; ++c) {
+      mbar_init(&hdr.code_full[c], 1);
+      mbar_init(&hdr.code_empty[c], kPfConvWarps);
+    }
     for (int t = 0; t < kPfTiles; ++t) {
       mbar_init(&hdr.q_ready[t], 1);
       mbar_init(&hdr.s_full[t][0], 1);
@@ -225,49 +274,389 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
   uint8_t *codes = smem + Lay::CODE_OFF;
   volatile int *abort = &hdr.abort;
 
-  if (warp == kPfTmaWarp) {
-    // ------------------------------------------------------------ TMA
-    // The whole warp runs the loop: lane j fetches block-table entry j of the
-    // next stage while lane 0 issues this stage's copies.
-    if (lane == 0) {
-      mbar_arrive_expect_tx(&hdr.q_full, tiles * NH * kPfTileRows * 128u);
-      for (int t = 0; t < tiles; ++t)
-#pragma unroll
-        for (int hf = 0; hf < NH; ++hf)
-          tma_load_4d(qs + t * Lay::Q_TILE + hf * Lay::Q_HALF, &p.tmap_q, hf * 64, 0, h, q0 + cta * QC + t * QT,
-                      &hdr.q_full);
+  // Roles.  With one-byte caches the softmax warpgroups take 168 registers
+  // a thread and the other two (TMA, MMA, widening) 88: 256 x 168 +
+  // 256 x 88 = 512 x 128, the registers the block is launched with.
+  if (warp < 4 * kPfTiles) {
+    if constexpr (KV8) asm volatile("setmaxnreg.inc.sync.aligned.u32 168;" ::: "memory");
+    if (warp / 4 < tiles) {
+      // ------------------------------------------------------------ softmax
+      const int t = warp / 4;                  // tile
+      const int r = threadIdx.x & 127;         // row = TMEM lane
+      const int tok = cta * QC + t * QT + r / G;
+      const int pos = pos0 + min(tok, n - 1);  // rows past the new tokens take the last one's (not stored)
+      const uint32_t trow = tmem + t * kPfTileCols + (static_cast<uint32_t>(32 * (warp & 3)) << 16);
+      float m = -INFINITY, l = 0.f;
+      bool ok = true;
+      // score scale (base 2) and output scale; one-byte caches fold in their
+      // K and V scales, and a rewritten q its power-of-two factor
+      float c = p.qk_scale_log2, vsc = 1.f;
+      if constexpr (KV8) {
+        vsc = p.v_scale;
+        if (p.k_head_scale != nullptr) {
+          c *= __ldg(p.k_head_scale + h);
+          vsc = __ldg(p.v_head_scale + h);
+        }
+      }
+      if constexpr (QCONV) {
+        // the tile's q (bf16, swizzled in place; a pure elementwise rewrite
+        // keeps the layout): scale by 2^e so that max |q| <= 2^15, round to fp16
+        ok = __all_sync(0xffffffffu, mbar_wait(&hdr.q_full, 0, abort));
+        uint4 *qt = reinterpret_cast<uint4 *>(qs + t * Lay::Q_TILE);
+        constexpr int CH = Lay::Q_TILE / 16 / kPfTileRows;  // 16-byte chunks per thread
+        float amax = 0.f;
+        if (ok) {
+  #pragma unroll
+          for (int j = 0; j < CH; ++j) {
+            const uint4 v = qt[j * kPfTileRows + r];
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  #pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const float2 x = half2_bits_to_float2<kBF16>(w[u]);
+              amax = fmaxf(amax, fmaxf(fabsf(x.x), fabsf(x.y)));
+            }
+          }
+        }
+  #pragma unroll
+        for (int o2 = 1; o2 < 32; o2 <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o2));
+        if (lane == 0) hdr.qmax[t][warp & 3] = amax;
+        named_bar_sync(1 + t, kPfTileRows);
+        amax = fmaxf(fmaxf(hdr.qmax[t][0], hdr.qmax[t][1]), fmaxf(hdr.qmax[t][2], hdr.qmax[t][3]));
+        float f = 1.f;
+        if (amax > 16384.f && amax <= 3.0e38f) {
+          int ex;
+          frexpf(amax, &ex);
+          f = ldexpf(1.f, 14 - ex);
+        }
+        if (ok) {
+  #pragma unroll
+          for (int j = 0; j < CH; ++j) {
+            uint4 v = qt[j * kPfTileRows + r];
+            uint32_t *w = reinterpret_cast<uint32_t *>(&v);
+  #pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const float2 x = half2_bits_to_float2<kBF16>(w[u]);
+              w[u] = pack2_rn<kF16>(x.x * f, x.y * f);
+            }
+            qt[j * kPfTileRows + r] = v;
+          }
+        }
+        fence_proxy_async_smem();  // the rewritten q visible to the tensor cores
+        named_bar_sync(1 + t, kPfTileRows);
+        if (r == 0) mbar_arrive(&hdr.q_ready[t]);
+        c /= f;
+      }
+      for (int i = 0; i < n_stages && ok; ++i) {
+        if (!__all_sync(0xffffffffu, mbar_wait(&hdr.s_full[t][i & 1], (i >> 1) & 1, abort))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+        const int k0 = i * kPfKeys;
+        float sv[kPfKeys];
+        {
+          uint32_t raw[32];
+          tc_ld32(trow + (i & 1) * kPfKeys, raw);
+  #pragma unroll
+          for (int j = 0; j < 32; ++j) sv[j] = __uint_as_float(raw[j]);
+          tc_ld32(trow + (i & 1) * kPfKeys + 32, raw);
+  #pragma unroll
+          for (int j = 0; j < 32; ++j) sv[32 + j] = __uint_as_float(raw[j]);
+        }
+        // Most stages lie wholly at or before every row of the warp: no mask,
+        // and with a positive scale the maximum is taken on the raw scores and
+        // the scale folded into the exponent's one fma.  Otherwise the scores
+        // are scaled, then masked (key position > row position: -inf).
+        const bool plain = c > 0.f && __all_sync(0xffffffffu, k0 + kPfKeys - 1 <= pos);
+        float mx, cm;
+        if (plain) {
+          float a = sv[0], b = sv[32];  // two chains of 3-input maxima
+  #pragma unroll
+          for (int j = 1; j < 31; j += 2) {
+            a = fmax3(a, sv[j], sv[j + 1]);
+            b = fmax3(b, sv[32 + j], sv[33 + j]);
+          }
+          mx = fmax3(a, b, fmaxf(sv[31], sv[63])) * c;
+          cm = c;
+        } else {
+          float mx0 = -INFINITY, mx1 = -INFINITY;
+  #pragma unroll
+          for (int j = 0; j < kPfKeys; j += 2) {
+            sv[j] = (k0 + j <= pos) ? sv[j] * c : -INFINITY;
+            sv[j + 1] = (k0 + j + 1 <= pos) ? sv[j + 1] * c : -INFINITY;
+            mx0 = fmaxf(mx0, sv[j]);
+            mx1 = fmaxf(mx1, sv[j + 1]);
+          }
+          mx = fmaxf(mx0, mx1);
+          cm = 1.f;
+        }
+        const bool grow = mx > m + kPfLazy;
+        if (__any_sync(0xffffffffu, grow && i > 0)) {  // tcgen05.ld / st are warp-wide
+          // O holds the previous P V: wait for it, then rescale.  S of this
+          // stage was issued after the P V before the previous one, and the
+          // tensor pipe completes in order, so pv_done is at most one phase
+          // behind here and the parity wait is exact.
+          if (!__all_sync(0xffffffffu, mbar_wait(&hdr.pv_done[t], (i - 1) & 1, abort))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+          const float alpha = grow ? fast_exp2(m - mx) : 1.f;
+  #pragma unroll
+          for (int c = 0; c < D; c += 32) {
+            uint32_t ov[32];
+            tc_ld32(trow + 2 * kPfKeys + c, ov);
+  #pragma unroll
+            for (int j = 0; j < 32; ++j) ov[j] = __float_as_uint(__uint_as_float(ov[j]) * alpha);
+            tc_st32(trow + 2 * kPfKeys + c, ov);
+          }
+        }
+        if (grow) {
+          l *= fast_exp2(m - mx);  // 0 while m is -inf (l is 0 then)
+          m = mx;
+        }
+        const float base = m == -INFINITY ? 0.f : m;
+        // p = 2^(s * cm - base), two lanes per fma and per add of the row sum
+        const uint64_t cm2 = f2(cm, cm), nb2 = f2(-base, -base);
+        uint64_t sum0 = f2(0.f, 0.f), sum1 = sum0;
+        uint32_t pw[kPfKeys / 2];
+  #pragma unroll
+        for (int j = 0; j < kPfKeys; j += 2) {
+          float x, y;
+          f2_split(ffma2(f2(sv[j], sv[j + 1]), cm2, nb2), x, y);
+          const float a = fast_exp2(x), b = fast_exp2(y);
+          pw[j / 2] = pack2_rn<MT>(a, b);
+          if ((j & 2) == 0)
+            sum0 = fadd2(sum0, f2(a, b));
+          else
+            sum1 = fadd2(sum1, f2(a, b));
+        }
+        {
+          float l0, l1, l2, l3;
+          f2_split(sum0, l0, l1);
+          f2_split(sum1, l2, l3);
+          l += (l0 + l1) + (l2 + l3);
+        }
+        tc_st32(trow + (i & 1) * kPfKeys, pw);  // P over the S buffer just read
+        if (k0 + kPfKeys > kv_end) {
+          // keys past kv_end hold stale (possibly NaN) values: zero their V rows,
+          // since 0 * NaN would reach O.  Each tile does it before its own P V
+          // (the tiles' products are issued independently); both write zeros.
+          if (!__all_sync(0xffffffffu, mbar_wait(&hdr.kv_full[i % NS], (i / NS) & 1, abort))) {
+            ok = false;
+            break;
+          }
+          uint8_t *vb = stages + (i % NS) * Lay::STAGE_BYTES + NH * kPfHalf;
+          const int z0 = kv_end - k0;
+          for (int idx = r; idx < (kPfKeys - z0) * 8 * NH; idx += kPfTileRows) {
+            const int hf = idx / ((kPfKeys - z0) * 8), rem = idx % ((kPfKeys - z0) * 8);
+            *reinterpret_cast<uint4 *>(vb + hf * kPfHalf + (z0 + rem / 8) * 128 + (rem % 8) * 16) =
+                make_uint4(0u, 0u, 0u, 0u);
+          }
+          fence_proxy_async_smem();  // the zeroed V rows visible to the tensor cores
+        }
+        tc_fence_before_sync();  // P and O stores ordered before the arrive
+        mbar_arrive(&hdr.p_full[t][i & 1]);
+      }
+      if (!ok) {
+        record_error(p.err, kErrTimeout);
+        *abort = 1;
+      } else if (__all_sync(0xffffffffu, mbar_wait(&hdr.o_ready[t], 0, abort))) {
+        // (pv_done cannot serve here: the softmax does not wait for every P V,
+        // so the last two may both be pending and a parity wait would take the
+        // older phase for the newer)
+        tc_fence_after_sync();
+        const float inv = vsc / l;
+        const bool store = tok < n;
+        uint8_t *row = static_cast<uint8_t *>(p.out) +
+                       (static_cast<size_t>(q0 + min(tok, n - 1)) * p.num_q_heads + h * G + r % G) * D * 2;
+  #pragma unroll
+        for (int c = 0; c < D; c += 32) {
+          uint32_t ov[32];
+          tc_ld32(trow + 2 * kPfKeys + c, ov);
+          if (store) {
+  #pragma unroll
+            for (int j = 0; j < 32; j += 8) {
+              uint4 v;
+              v.x = pack2_rn<DT>(__uint_as_float(ov[j]) * inv, __uint_as_float(ov[j + 1]) * inv);
+              v.y = pack2_rn<DT>(__uint_as_float(ov[j + 2]) * inv, __uint_as_float(ov[j + 3]) * inv);
+              v.z = pack2_rn<DT>(__uint_as_float(ov[j + 4]) * inv, __uint_as_float(ov[j + 5]) * inv);
+              v.w = pack2_rn<DT>(__uint_as_float(ov[j + 6]) * inv, __uint_as_float(ov[j + 7]) * inv);
+              *reinterpret_cast<uint4 *>(row + (c + j) * 2) = v;
+            }
+          }
+        }
+      } else {
+        record_error(p.err, kErrTimeout);
+        *abort = 1;
+      }
     }
-    const int bs = p.block_size;
-    const int bpt = kPfKeys / bs;  // blocks per stage (<= 8)
-    const int32_t *table = p.block_tables + static_cast<size_t>(s) * p.max_blocks;
-    auto stage_blocks = [&](int i) { return min(bpt, (kv_end - i * kPfKeys + bs - 1) / bs); };
-    int next = lane < stage_blocks(0) ? __ldg(table + lane) : 0;
-    int issued = 0;
-    bool ok = true;
-    if constexpr (KV8) {
-      // stage j's codes into slot j % NC: one bulk copy per block for K and
-      // for V, issued by lane (block); the table entries come a stage ahead
-      auto issue_codes = [&](int j) {
-        const int nblk = stage_blocks(j);
+  } else if (warp < 12) {
+    if constexpr (KV8) asm volatile("setmaxnreg.dec.sync.aligned.u32 88;" ::: "memory");
+    if (warp == kPfTmaWarp) {
+      // ------------------------------------------------------------ TMA
+      // The whole warp runs the loop: lane j fetches block-table entry j of the
+      // next stage while lane 0 issues this stage's copies.
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&hdr.q_full, tiles * NH * kPfTileRows * 128u);
+        for (int t = 0; t < tiles; ++t)
+  #pragma unroll
+          for (int hf = 0; hf < NH; ++hf)
+            tma_load_4d(qs + t * Lay::Q_TILE + hf * Lay::Q_HALF, &p.tmap_q, hf * 64, 0, h, q0 + cta * QC + t * QT,
+                        &hdr.q_full);
+      }
+      const int bs = p.block_size;
+      const int bpt = kPfKeys / bs;  // blocks per stage (<= 8)
+      const int32_t *table = p.block_tables + static_cast<size_t>(s) * p.max_blocks;
+      auto stage_blocks = [&](int i) { return min(bpt, (kv_end - i * kPfKeys + bs - 1) / bs); };
+      int next = lane < stage_blocks(0) ? __ldg(table + lane) : 0;
+      int issued = 0;
+      bool ok = true;
+      if constexpr (KV8) {
+        // stage j's codes into slot j % NC: one bulk copy per block for K and
+        // for V, issued by lane (block); the table entries come a stage ahead
+        auto issue_codes = [&](int j) {
+          const int nblk = stage_blocks(j);
+          int phys = next;
+          if (j + 1 < n_stages && lane < stage_blocks(j + 1)) next = __ldg(table + (j + 1) * bpt + lane);
+          if (lane < nblk && (phys < 0 || phys >= p.num_blocks)) {
+            record_error(p.err, kErrBlockIndex);
+            phys = 0;  // read a valid block; the result is void and flagged
+          }
+          uint8_t *cb = codes + (j % NC) * Lay::CODE_BYTES;
+          const uint32_t tile = static_cast<uint32_t>(bs) * D;
+          if (lane == 0) mbar_arrive_expect_tx(&hdr.code_full[j % NC], 2u * nblk * tile);
+          __syncwarp();
+          if (lane < nblk) {
+            const size_t off = (static_cast<size_t>(phys) * p.num_kv_heads + h) * tile;
+            bulk_g2s(cb + lane * tile, p.k_cache + off, tile, &hdr.code_full[j % NC]);
+            bulk_g2s(cb + kPfKeys * D + lane * tile, p.v_cache + off, tile, &hdr.code_full[j % NC]);
+          }
+        };
+        // a slot is refilled once the widening warps are done with it
+        for (int j = 0; j < n_stages && ok; ++j) {
+          bool freed = true;
+          if (lane == 0 && j >= NC) freed = mbar_wait(&hdr.code_empty[j % NC], ((j / NC) - 1) & 1, abort);
+          if (!__shfl_sync(0xffffffffu, freed, 0)) {
+            ok = false;
+            break;
+          }
+          issue_codes(j);
+          issued = j + 1;
+        }
+        if (lane == 0 && !ok) {
+          record_error(p.err, kErrTimeout);
+          *abort = 1;
+          // wait, within the limit, for the copies still in flight
+          for (int j = max(0, issued - NC); j < issued; ++j) mbar_wait(&hdr.code_full[j % NC], (j / NC) & 1, nullptr);
+        }
+        if (lane == 0) mbar_wait(&hdr.q_full, 0, nullptr);
+      } else {
+      for (int i = 0; i < n_stages; ++i) {
+        const int st = i % NS;
+        const int nblk = stage_blocks(i);
         int phys = next;
-        if (j + 1 < n_stages && lane < stage_blocks(j + 1)) next = __ldg(table + (j + 1) * bpt + lane);
+        if (i + 1 < n_stages && lane < stage_blocks(i + 1)) next = __ldg(table + (i + 1) * bpt + lane);
         if (lane < nblk && (phys < 0 || phys >= p.num_blocks)) {
           record_error(p.err, kErrBlockIndex);
           phys = 0;  // read a valid block; the result is void and flagged
         }
-        uint8_t *cb = codes + (j % NC) * Lay::CODE_BYTES;
-        const uint32_t tile = static_cast<uint32_t>(bs) * D;
-        if (lane == 0) mbar_arrive_expect_tx(&hdr.code_full[j % NC], 2u * nblk * tile);
-        __syncwarp();
-        if (lane < nblk) {
-          const size_t off = (static_cast<size_t>(phys) * p.num_kv_heads + h) * tile;
-          bulk_g2s(cb + lane * tile, p.k_cache + off, tile, &hdr.code_full[j % NC]);
-          bulk_g2s(cb + kPfKeys * D + lane * tile, p.v_cache + off, tile, &hdr.code_full[j % NC]);
+        bool waited = true;
+        if (lane == 0 && i >= NS) waited = mbar_wait(&hdr.kv_empty[st], ((i / NS) - 1) & 1, abort);
+        if (!__shfl_sync(0xffffffffu, waited, 0)) {
+          ok = false;
+          break;
         }
-      };
-      int done = 0;  // stages converted
+        uint8_t *kb = stages + st * Lay::STAGE_BYTES;
+        uint8_t *vb = kb + NH * kPfHalf;
+        if (lane == 0) mbar_arrive_expect_tx(&hdr.kv_full[st], 2u * NH * static_cast<uint32_t>(nblk * bs) * 128u);
+        __syncwarp();
+        if (lane < nblk) {  // lane j issues block j's boxes: the lanes' copies go out together
+          const int r0 = (phys * p.num_kv_heads + h) * bs;
+  #pragma unroll
+          for (int hf = 0; hf < NH; ++hf) {
+            tma_load_2d(kb + hf * kPfHalf + lane * bs * 128, &p.tmap_k, hf * 64, r0, &hdr.kv_full[st]);
+            tma_load_2d(vb + hf * kPfHalf + lane * bs * 128, &p.tmap_v, hf * 64, r0, &hdr.kv_full[st]);
+          }
+        }
+        issued = i + 1;
+      }
+      if (lane == 0) {
+        if (!ok) {
+          record_error(p.err, kErrTimeout);
+          *abort = 1;
+          // wait, within the limit, for the copies still in flight
+          for (int j = max(0, issued - NS); j < issued; ++j)
+            mbar_wait(&hdr.kv_full[j % NS], (j / NS) & 1, nullptr);
+        }
+        mbar_wait(&hdr.q_full, 0, nullptr);
+      }
+      }
+    } else if (warp == kPfMmaWarp || warp == kPfMmaWarp + 1) {
+      // ------------------------------------------------------------ MMA (tile t)
+      const int t = warp - kPfMmaWarp;
+      if (lane == 0 && t < tiles) {
+        bool ok = mbar_wait(QCONV ? &hdr.q_ready[t] : &hdr.q_full, 0, abort);
+        const uint32_t qt = smem_addr(qs) + t * Lay::Q_TILE;
+        const uint32_t saddr = smem_addr(stages);
+        const uint32_t tt = tmem + t * kPfTileCols;
+        auto issue_qk = [&](int i) -> bool {
+          const int st = i % NS;
+          if (!mbar_wait(&hdr.kv_full[st], (i / NS) & 1, abort)) return false;
+          tc_fence_after_sync();
+          // descriptors of the first k-step; a k-step advances the start
+          // address field (16-byte units) by 32 bytes, a row half by a region
+          const uint64_t a0 = umma_desc_sw128(qt, 16, 1024);
+          const uint64_t b0 = umma_desc_sw128(saddr + st * Lay::STAGE_BYTES, 16, 1024);
+          const uint32_t d = tt + (i & 1) * kPfKeys;
+  #pragma unroll
+          for (int kk = 0; kk < KSTEPS; ++kk) {
+            const uint32_t off = (kk % 4) * 32;  // 16 elements = 32 bytes into the swizzled row
+            tc_mma_f16(d, a0 + (((kk / 4) * Lay::Q_HALF + off) >> 4), b0 + (((kk / 4) * kPfHalf + off) >> 4),
+                       IDESC_QK, kk > 0);
+          }
+          tc_commit(&hdr.s_full[t][i & 1]);
+          return true;
+        };
+        if (ok) ok = issue_qk(0);
+        for (int i = 0; i < n_stages && ok; ++i) {
+          if (i + 1 < n_stages && !issue_qk(i + 1)) {
+            ok = false;
+            break;
+          }
+          if (!mbar_wait(&hdr.p_full[t][i & 1], (i >> 1) & 1, abort)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+          const uint64_t b0 = umma_desc_sw128(saddr + (i % NS) * Lay::STAGE_BYTES + NH * kPfHalf, kPfHalf, 1024);
+  #pragma unroll
+          for (int kk = 0; kk < kPfKeys / 16; ++kk)  // 16 keys: 8 columns of P, 2048 bytes of V rows
+            tc_mma_f16_ta(tt + 2 * kPfKeys, tt + (i & 1) * kPfKeys + kk * 8, b0 + kk * 128, IDESC_PV,
+                          (i > 0 || kk > 0) ? 1u : 0u);
+          tc_commit(&hdr.pv_done[t]);
+          if (i + 1 == n_stages) tc_commit(&hdr.o_ready[t]);
+          tc_commit(&hdr.kv_empty[i % NS]);
+        }
+        if (!ok) {
+          record_error(p.err, kErrTimeout);
+          *abort = 1;
+        }
+        // every product this thread issued has completed before the memory is released
+        tc_commit(&hdr.fin[t]);
+        mbar_wait(&hdr.fin[t], 0, nullptr);
+      }
+    }
+  } else {
+    if constexpr (KV8) {
+      asm volatile("setmaxnreg.dec.sync.aligned.u32 88;" ::: "memory");
+      // ------------------------------------------------------------ widening
+      // warp 12 + q widens warp-iterations q, q + 4, ... of every stage
+      const int q = warp - kPfConvWarp0;
+      const int bs = p.block_size;
+      const int bpt = kPfKeys / bs;
+      bool ok = true;
       for (int i = 0; i < n_stages; ++i) {
-        while (issued < n_stages && issued < i + NC) issue_codes(issued++);
         const int st = i % NS;
         if (!__all_sync(0xffffffffu, mbar_wait(&hdr.code_full[i % NC], (i / NC) & 1, abort))) {
           ok = false;
@@ -279,338 +668,22 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
           ok = false;
           break;
         }
-        // widen: 8 codes -> one 16-byte chunk of the swizzled 16-bit stage
-        // (chunk c of key row k of half hf at chunk c ^ (k mod 8))
-        const uint8_t *cb = codes + (i % NC) * Lay::CODE_BYTES;
-        uint8_t *sb = stages + st * Lay::STAGE_BYTES;
-        const int per = stage_blocks(i) * bs * NH * 8;  // chunks of K (and of V)
-        for (int idx = lane; idx < 2 * per; idx += 32) {
-          const int tv = idx >= per, r = idx - tv * per;
-          const int k = r / (NH * 8), hf = (r / 8) % NH, c = r % 8;
-          const uint2 w = *reinterpret_cast<const uint2 *>(cb + tv * kPfKeys * D + k * D + hf * 64 + c * 8);
-          uint4 o;
-          byte4_to_half2x2<KVT>(w.x, o.x, o.y);
-          byte4_to_half2x2<KVT>(w.y, o.z, o.w);
-          *reinterpret_cast<uint4 *>(sb + (tv * NH + hf) * kPfHalf + k * 128 + ((c ^ (k & 7)) << 4)) = o;
-        }
+        const int keys = min(bpt, (kv_end - i * kPfKeys + bs - 1) / bs) * bs;
+        widen_codes<KVT, D>(codes + (i % NC) * Lay::CODE_BYTES, stages + st * Lay::STAGE_BYTES, keys, lane, q,
+                            kPfConvWarps);
         // the 16-bit stage visible to the tensor cores, and the code slot's
         // reads ordered before the bulk copy that refills it
         fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&hdr.kv_full[st]);
-        done = i + 1;
-      }
-      if (lane == 0 && !ok) {
-        record_error(p.err, kErrTimeout);
-        *abort = 1;
-        for (int j = done; j < issued; ++j) mbar_wait(&hdr.code_full[j % NC], (j / NC) & 1, nullptr);
-      }
-      if (lane == 0) mbar_wait(&hdr.q_full, 0, nullptr);
-    } else {
-    for (int i = 0; i < n_stages; ++i) {
-      const int st = i % NS;
-      const int nblk = stage_blocks(i);
-      int phys = next;
-      if (i + 1 < n_stages && lane < stage_blocks(i + 1)) next = __ldg(table + (i + 1) * bpt + lane);
-      if (lane < nblk && (phys < 0 || phys >= p.num_blocks)) {
-        record_error(p.err, kErrBlockIndex);
-        phys = 0;  // read a valid block; the result is void and flagged
-      }
-      bool waited = true;
-      if (lane == 0 && i >= NS) waited = mbar_wait(&hdr.kv_empty[st], ((i / NS) - 1) & 1, abort);
-      if (!__shfl_sync(0xffffffffu, waited, 0)) {
-        ok = false;
-        break;
-      }
-      uint8_t *kb = stages + st * Lay::STAGE_BYTES;
-      uint8_t *vb = kb + NH * kPfHalf;
-      if (lane == 0) mbar_arrive_expect_tx(&hdr.kv_full[st], 2u * NH * static_cast<uint32_t>(nblk * bs) * 128u);
-      __syncwarp();
-      if (lane < nblk) {  // lane j issues block j's boxes: the lanes' copies go out together
-        const int r0 = (phys * p.num_kv_heads + h) * bs;
-#pragma unroll
-        for (int hf = 0; hf < NH; ++hf) {
-          tma_load_2d(kb + hf * kPfHalf + lane * bs * 128, &p.tmap_k, hf * 64, r0, &hdr.kv_full[st]);
-          tma_load_2d(vb + hf * kPfHalf + lane * bs * 128, &p.tmap_v, hf * 64, r0, &hdr.kv_full[st]);
+        if (lane == 0) {
+          mbar_arrive(&hdr.kv_full[st]);
+          mbar_arrive(&hdr.code_empty[i % NC]);
         }
       }
-      issued = i + 1;
-    }
-    if (lane == 0) {
-      if (!ok) {
-        record_error(p.err, kErrTimeout);
-        *abort = 1;
-        // wait, within the limit, for the copies still in flight
-        for (int j = max(0, issued - NS); j < issued; ++j)
-          mbar_wait(&hdr.kv_full[j % NS], (j / NS) & 1, nullptr);
-      }
-      mbar_wait(&hdr.q_full, 0, nullptr);
-    }
-    }
-  } else if (warp >= kPfMmaWarp) {
-    // ------------------------------------------------------------ MMA (tile t)
-    const int t = warp - kPfMmaWarp;
-    if (lane == 0 && t < tiles) {
-      bool ok = mbar_wait(QCONV ? &hdr.q_ready[t] : &hdr.q_full, 0, abort);
-      const uint32_t qt = smem_addr(qs) + t * Lay::Q_TILE;
-      const uint32_t saddr = smem_addr(stages);
-      const uint32_t tt = tmem + t * kPfTileCols;
-      auto issue_qk = [&](int i) -> bool {
-        const int st = i % NS;
-        if (!mbar_wait(&hdr.kv_full[st], (i / NS) & 1, abort)) return false;
-        tc_fence_after_sync();
-        // descriptors of the first k-step; a k-step advances the start
-        // address field (16-byte units) by 32 bytes, a row half by a region
-        const uint64_t a0 = umma_desc_sw128(qt, 16, 1024);
-        const uint64_t b0 = umma_desc_sw128(saddr + st * Lay::STAGE_BYTES, 16, 1024);
-        const uint32_t d = tt + (i & 1) * kPfKeys;
-#pragma unroll
-        for (int kk = 0; kk < KSTEPS; ++kk) {
-          const uint32_t off = (kk % 4) * 32;  // 16 elements = 32 bytes into the swizzled row
-          tc_mma_f16(d, a0 + (((kk / 4) * Lay::Q_HALF + off) >> 4), b0 + (((kk / 4) * kPfHalf + off) >> 4),
-                     IDESC_QK, kk > 0);
-        }
-        tc_commit(&hdr.s_full[t][i & 1]);
-        return true;
-      };
-      if (ok) ok = issue_qk(0);
-      for (int i = 0; i < n_stages && ok; ++i) {
-        if (i + 1 < n_stages && !issue_qk(i + 1)) {
-          ok = false;
-          break;
-        }
-        if (!mbar_wait(&hdr.p_full[t][i & 1], (i >> 1) & 1, abort)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after_sync();
-        const uint64_t b0 = umma_desc_sw128(saddr + (i % NS) * Lay::STAGE_BYTES + NH * kPfHalf, kPfHalf, 1024);
-#pragma unroll
-        for (int kk = 0; kk < kPfKeys / 16; ++kk)  // 16 keys: 8 columns of P, 2048 bytes of V rows
-          tc_mma_f16_ta(tt + 2 * kPfKeys, tt + (i & 1) * kPfKeys + kk * 8, b0 + kk * 128, IDESC_PV,
-                        (i > 0 || kk > 0) ? 1u : 0u);
-        tc_commit(&hdr.pv_done[t]);
-        if (i + 1 == n_stages) tc_commit(&hdr.o_ready[t]);
-        tc_commit(&hdr.kv_empty[i % NS]);
-      }
-      if (!ok) {
+      if (!ok && lane == 0) {
         record_error(p.err, kErrTimeout);
         *abort = 1;
       }
-      // every product this thread issued has completed before the memory is released
-      tc_commit(&hdr.fin[t]);
-      mbar_wait(&hdr.fin[t], 0, nullptr);
-    }
-  } else if (warp / 4 < tiles) {
-    // ------------------------------------------------------------ softmax
-    const int t = warp / 4;                  // tile
-    const int r = threadIdx.x & 127;         // row = TMEM lane
-    const int tok = cta * QC + t * QT + r / G;
-    const int pos = pos0 + min(tok, n - 1);  // rows past the new tokens take the last one's (not stored)
-    const uint32_t trow = tmem + t * kPfTileCols + (static_cast<uint32_t>(32 * (warp & 3)) << 16);
-    float m = -INFINITY, l = 0.f;
-    bool ok = true;
-    // score scale (base 2) and output scale; one-byte caches fold in their
-    // K and V scales, and a rewritten q its power-of-two factor
-    float c = p.qk_scale_log2, vsc = 1.f;
-    if constexpr (KV8) {
-      vsc = p.v_scale;
-      if (p.k_head_scale != nullptr) {
-        c *= __ldg(p.k_head_scale + h);
-        vsc = __ldg(p.v_head_scale + h);
-      }
-    }
-    if constexpr (QCONV) {
-      // the tile's q (bf16, swizzled in place; a pure elementwise rewrite
-      // keeps the layout): scale by 2^e so that max |q| <= 2^15, round to fp16
-      ok = __all_sync(0xffffffffu, mbar_wait(&hdr.q_full, 0, abort));
-      uint4 *qt = reinterpret_cast<uint4 *>(qs + t * Lay::Q_TILE);
-      constexpr int CH = Lay::Q_TILE / 16 / kPfTileRows;  // 16-byte chunks per thread
-      float amax = 0.f;
-      if (ok) {
-#pragma unroll
-        for (int j = 0; j < CH; ++j) {
-          const uint4 v = qt[j * kPfTileRows + r];
-          const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const float2 x = half2_bits_to_float2<kBF16>(w[u]);
-            amax = fmaxf(amax, fmaxf(fabsf(x.x), fabsf(x.y)));
-          }
-        }
-      }
-#pragma unroll
-      for (int o2 = 1; o2 < 32; o2 <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o2));
-      if (lane == 0) hdr.qmax[t][warp & 3] = amax;
-      named_bar_sync(1 + t, kPfTileRows);
-      amax = fmaxf(fmaxf(hdr.qmax[t][0], hdr.qmax[t][1]), fmaxf(hdr.qmax[t][2], hdr.qmax[t][3]));
-      float f = 1.f;
-      if (amax > 16384.f && amax <= 3.0e38f) {
-        int ex;
-        frexpf(amax, &ex);
-        f = ldexpf(1.f, 14 - ex);
-      }
-      if (ok) {
-#pragma unroll
-        for (int j = 0; j < CH; ++j) {
-          uint4 v = qt[j * kPfTileRows + r];
-          uint32_t *w = reinterpret_cast<uint32_t *>(&v);
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const float2 x = half2_bits_to_float2<kBF16>(w[u]);
-            w[u] = pack2_rn<kF16>(x.x * f, x.y * f);
-          }
-          qt[j * kPfTileRows + r] = v;
-        }
-      }
-      fence_proxy_async_smem();  // the rewritten q visible to the tensor cores
-      named_bar_sync(1 + t, kPfTileRows);
-      if (r == 0) mbar_arrive(&hdr.q_ready[t]);
-      c /= f;
-    }
-    for (int i = 0; i < n_stages && ok; ++i) {
-      if (!__all_sync(0xffffffffu, mbar_wait(&hdr.s_full[t][i & 1], (i >> 1) & 1, abort))) {
-        ok = false;
-        break;
-      }
-      tc_fence_after_sync();
-      const int k0 = i * kPfKeys;
-      float sv[kPfKeys];
-      {
-        uint32_t raw[32];
-        tc_ld32(trow + (i & 1) * kPfKeys, raw);
-#pragma unroll
-        for (int j = 0; j < 32; ++j) sv[j] = __uint_as_float(raw[j]);
-        tc_ld32(trow + (i & 1) * kPfKeys + 32, raw);
-#pragma unroll
-        for (int j = 0; j < 32; ++j) sv[32 + j] = __uint_as_float(raw[j]);
-      }
-      // Most stages lie wholly at or before every row of the warp: no mask,
-      // and with a positive scale the maximum is taken on the raw scores and
-      // the scale folded into the exponent's one fma.  Otherwise the scores
-      // are scaled, then masked (key position > row position: -inf).
-      const bool plain = c > 0.f && __all_sync(0xffffffffu, k0 + kPfKeys - 1 <= pos);
-      float mx, cm;
-      if (plain) {
-        float a = sv[0], b = sv[32];  // two chains of 3-input maxima
-#pragma unroll
-        for (int j = 1; j < 31; j += 2) {
-          a = fmax3(a, sv[j], sv[j + 1]);
-          b = fmax3(b, sv[32 + j], sv[33 + j]);
-        }
-        mx = fmax3(a, b, fmaxf(sv[31], sv[63])) * c;
-        cm = c;
-      } else {
-        float mx0 = -INFINITY, mx1 = -INFINITY;
-#pragma unroll
-        for (int j = 0; j < kPfKeys; j += 2) {
-          sv[j] = (k0 + j <= pos) ? sv[j] * c : -INFINITY;
-          sv[j + 1] = (k0 + j + 1 <= pos) ? sv[j + 1] * c : -INFINITY;
-          mx0 = fmaxf(mx0, sv[j]);
-          mx1 = fmaxf(mx1, sv[j + 1]);
-        }
-        mx = fmaxf(mx0, mx1);
-        cm = 1.f;
-      }
-      const bool grow = mx > m + kPfLazy;
-      if (__any_sync(0xffffffffu, grow && i > 0)) {  // tcgen05.ld / st are warp-wide
-        // O holds the previous P V: wait for it, then rescale.  S of this
-        // stage was issued after the P V before the previous one, and the
-        // tensor pipe completes in order, so pv_done is at most one phase
-        // behind here and the parity wait is exact.
-        if (!__all_sync(0xffffffffu, mbar_wait(&hdr.pv_done[t], (i - 1) & 1, abort))) {
-          ok = false;
-          break;
-        }
-        tc_fence_after_sync();
-        const float alpha = grow ? fast_exp2(m - mx) : 1.f;
-#pragma unroll
-        for (int c = 0; c < D; c += 32) {
-          uint32_t ov[32];
-          tc_ld32(trow + 2 * kPfKeys + c, ov);
-#pragma unroll
-          for (int j = 0; j < 32; ++j) ov[j] = __float_as_uint(__uint_as_float(ov[j]) * alpha);
-          tc_st32(trow + 2 * kPfKeys + c, ov);
-        }
-      }
-      if (grow) {
-        l *= fast_exp2(m - mx);  // 0 while m is -inf (l is 0 then)
-        m = mx;
-      }
-      const float base = m == -INFINITY ? 0.f : m;
-      // p = 2^(s * cm - base), two lanes per fma and per add of the row sum
-      const uint64_t cm2 = f2(cm, cm), nb2 = f2(-base, -base);
-      uint64_t sum0 = f2(0.f, 0.f), sum1 = sum0;
-      uint32_t pw[kPfKeys / 2];
-#pragma unroll
-      for (int j = 0; j < kPfKeys; j += 2) {
-        float x, y;
-        f2_split(ffma2(f2(sv[j], sv[j + 1]), cm2, nb2), x, y);
-        const float a = fast_exp2(x), b = fast_exp2(y);
-        pw[j / 2] = pack2_rn<MT>(a, b);
-        if ((j & 2) == 0)
-          sum0 = fadd2(sum0, f2(a, b));
-        else
-          sum1 = fadd2(sum1, f2(a, b));
-      }
-      {
-        float l0, l1, l2, l3;
-        f2_split(sum0, l0, l1);
-        f2_split(sum1, l2, l3);
-        l += (l0 + l1) + (l2 + l3);
-      }
-      tc_st32(trow + (i & 1) * kPfKeys, pw);  // P over the S buffer just read
-      if (k0 + kPfKeys > kv_end) {
-        // keys past kv_end hold stale (possibly NaN) values: zero their V rows,
-        // since 0 * NaN would reach O.  Each tile does it before its own P V
-        // (the tiles' products are issued independently); both write zeros.
-        if (!__all_sync(0xffffffffu, mbar_wait(&hdr.kv_full[i % NS], (i / NS) & 1, abort))) {
-          ok = false;
-          break;
-        }
-        uint8_t *vb = stages + (i % NS) * Lay::STAGE_BYTES + NH * kPfHalf;
-        const int z0 = kv_end - k0;
-        for (int idx = r; idx < (kPfKeys - z0) * 8 * NH; idx += kPfTileRows) {
-          const int hf = idx / ((kPfKeys - z0) * 8), rem = idx % ((kPfKeys - z0) * 8);
-          *reinterpret_cast<uint4 *>(vb + hf * kPfHalf + (z0 + rem / 8) * 128 + (rem % 8) * 16) =
-              make_uint4(0u, 0u, 0u, 0u);
-        }
-        fence_proxy_async_smem();  // the zeroed V rows visible to the tensor cores
-      }
-      tc_fence_before_sync();  // P and O stores ordered before the arrive
-      mbar_arrive(&hdr.p_full[t][i & 1]);
-    }
-    if (!ok) {
-      record_error(p.err, kErrTimeout);
-      *abort = 1;
-    } else if (__all_sync(0xffffffffu, mbar_wait(&hdr.o_ready[t], 0, abort))) {
-      // (pv_done cannot serve here: the softmax does not wait for every P V,
-      // so the last two may both be pending and a parity wait would take the
-      // older phase for the newer)
-      tc_fence_after_sync();
-      const float inv = vsc / l;
-      const bool store = tok < n;
-      uint8_t *row = static_cast<uint8_t *>(p.out) +
-                     (static_cast<size_t>(q0 + min(tok, n - 1)) * p.num_q_heads + h * G + r % G) * D * 2;
-#pragma unroll
-      for (int c = 0; c < D; c += 32) {
-        uint32_t ov[32];
-        tc_ld32(trow + 2 * kPfKeys + c, ov);
-        if (store) {
-#pragma unroll
-          for (int j = 0; j < 32; j += 8) {
-            uint4 v;
-            v.x = pack2_rn<DT>(__uint_as_float(ov[j]) * inv, __uint_as_float(ov[j + 1]) * inv);
-            v.y = pack2_rn<DT>(__uint_as_float(ov[j + 2]) * inv, __uint_as_float(ov[j + 3]) * inv);
-            v.z = pack2_rn<DT>(__uint_as_float(ov[j + 4]) * inv, __uint_as_float(ov[j + 5]) * inv);
-            v.w = pack2_rn<DT>(__uint_as_float(ov[j + 6]) * inv, __uint_as_float(ov[j + 7]) * inv);
-            *reinterpret_cast<uint4 *>(row + (c + j) * 2) = v;
-          }
-        }
-      }
-    } else {
-      record_error(p.err, kErrTimeout);
-      *abort = 1;
     }
   }
   // ------------------------------------------------------------ teardown
@@ -637,7 +710,7 @@ pa_status launch_prefill(const PrefillParams &p, int num_seqs, int max_q_len, cu
     if (dev >= 0 && dev < 64) configured[dev] = true;
   }
   const dim3 grid((max_q_len + QC - 1) / QC, num_seqs, p.num_kv_heads);
-  prefill_kernel<DT, KVT, D, G><<<grid, kPfThreads, Lay::SMEM, stream>>>(p);
+  prefill_kernel<DT, KVT, D, G><<<grid, pf_threads(is_byte(KVT)), Lay::SMEM, stream>>>(p);
   e = cudaGetLastError();
   return e == cudaSuccess ? PA_OK : cuda_fail(e);
 }
