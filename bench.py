@@ -259,6 +259,7 @@ def run_ours(args, rank, world, local):
     dec_avg = statistics.mean(dec_ms) / 1e3
     elapsed = max_over_ranks(elapsed, world, dev)
     derr = int(err.item())
+    graph_t = graph_step_time(step, K, stream)
 
     # end to end through the C ABI with host buffers (pinned), copies inside
     host = {
@@ -350,10 +351,42 @@ def run_ours(args, rank, world, local):
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                 "ms_per_step": round(e2e_t * 1e3, 4)},
         "clocks": clocks,
+        "graph": ({"ms_per_step": round(graph_t * 1e3, 4), "value": round(kv_bytes / graph_t / 1e9, 2),
+                   "unit": "GB/s", "note": "the same step captured once in a CUDA graph and replayed"}
+                  if isinstance(graph_t, float) else {"error": graph_t}),
     }
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args.config, seed, budget_s=12.0)
     print(json.dumps(line), flush=True)
+
+
+def graph_step_time(step, K: int, stream):
+    """Seconds per step when the step's launches are captured once in a CUDA
+    graph and replayed K times (no host launch work between kernels); the
+    error text if capture fails."""
+    import torch
+    try:
+        g = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream()
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            step()
+        stream.wait_stream(side)
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g):
+            step()
+        for _ in range(3):
+            g.replay()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(K):
+            g.replay()
+        b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / 1e3 / K
+    except RuntimeError as e:
+        return str(e).splitlines()[0][:200]
 
 
 def _auto_partition(w):

@@ -113,6 +113,40 @@ def test_prefill_byte_cache_large_bf16_queries():
     _check(w, out, ref)
 
 
+@pytest.mark.parametrize("cache_dtype,q_dtype", [("f16", "f16"), ("e4m3", "bf16")])
+def test_sequences_without_new_tokens(cache_dtype, q_dtype):
+    """cu_q_lens may repeat: sequences with no new token produce no rows and
+    leave the others' rows intact."""
+    lens = [40, 300, 17, 129, 64]
+    q_lens = [0, 120, 0, 129, 1]
+    w = W.random_case(21, len(lens), 4, 2, 128, 16, cache_dtype, q_dtype, lens, device=G.DEV)
+    gen = torch.Generator(device=G.DEV).manual_seed(22)
+    q = torch.randn((sum(q_lens), 4, 128), generator=gen, device=G.DEV).to(w.q.dtype)
+    out, run = _run(w, q, q_lens)
+    assert int(run.err.item()) == 0
+    c = G.oracle_cache(w)
+    ref = A.paged_prefill(G.bits_to_f64(G.bits(q), q_dtype), q_lens, c.k, c.v, cache_dtype,
+                          w.block_tables, w.seq_lens, w.scale, w.k_scale, w.v_scale)
+    _check(w, out, ref)
+
+
+def test_many_short_sequences():
+    """3000 sequences of 1-3 new tokens (a decode-sized prefill): a grid of
+    3000 sequences by 2 KV heads, most CTAs holding a few rows."""
+    rng = np.random.default_rng(8)
+    lens = rng.integers(3, 200, 3000).tolist()
+    q_lens = [int(min(L, n)) for L, n in zip(lens, rng.integers(1, 4, 3000))]
+    w = W.random_case(23, len(lens), 4, 2, 64, 16, "bf16", "bf16", lens, device=G.DEV)
+    gen = torch.Generator(device=G.DEV).manual_seed(24)
+    q = torch.randn((sum(q_lens), 4, 64), generator=gen, device=G.DEV).bfloat16()
+    out, run = _run(w, q, q_lens)
+    assert int(run.err.item()) == 0
+    c = G.oracle_cache(w)
+    ref = A.paged_prefill(G.bits_to_f64(G.bits(q), "bf16"), q_lens, c.k, c.v, "bf16",
+                          w.block_tables, w.seq_lens, w.scale)
+    _check(w, out, ref)
+
+
 def test_prefill_last_rows_agree_with_decode():
     lens = [300, 77, 1024]
     q_lens = [40, 77, 3]
