@@ -389,3 +389,29 @@ def test_planted_off_by_one_causal_mask_fails(monkeypatch):
                                                                  V[:-1] if len(V) > 1 else V, scale))
     with pytest.raises(AssertionError):
         test_prefill_whole_sequence_equals_causal_sdpa()
+
+
+def test_prefill_int8_per_head_scales_equal_dequantised_sdpa():
+    """Prefill over an INT8 cache with one scale per KV head ([P3] §6.3) is
+    causal attention over code x scale of the head: the codes are read here
+    as two's-complement bytes and gathered through the tables with NumPy,
+    and the attention is torch's."""
+    lens, q_lens = [21, 9], [13, 9]
+    ks, vs = (0.05, 0.11), (0.07, 0.03)
+    w = W.random_case(44, 2, 4, 2, 16, 4, "int8", "f16", lens, k_scale=ks, v_scale=vs)
+    c = _fill(w)
+    q = np.random.default_rng(44).standard_normal((sum(q_lens), 4, 16))
+    out = A.paged_prefill(q, q_lens, c.k, c.v, "int8", w.block_tables, w.seq_lens, w.scale, ks, vs)
+    kf, vf = c.k.view(np.int8).astype(np.float64), c.v.view(np.int8).astype(np.float64)
+    row = 0
+    for s, (L, n) in enumerate(zip(lens, q_lens)):
+        blocks = w.block_tables[s, :-(-L // w.bs)]
+        K = kf[blocks].transpose(1, 0, 2, 3).reshape(w.Hkv, -1, w.d)[:, :L] * np.array(ks)[:, None, None]
+        V = vf[blocks].transpose(1, 0, 2, 3).reshape(w.Hkv, -1, w.d)[:, :L] * np.array(vs)[:, None, None]
+        Kq = torch.from_numpy(K).repeat_interleave(w.G, 0)
+        Vq = torch.from_numpy(V).repeat_interleave(w.G, 0)
+        Q = torch.from_numpy(q[row:row + n]).transpose(0, 1)
+        mask = torch.arange(L)[None, :] <= torch.arange(L - n, L)[:, None]
+        ref = torch.nn.functional.scaled_dot_product_attention(Q, Kq, Vq, attn_mask=mask, scale=w.scale)
+        np.testing.assert_allclose(out[row:row + n], ref.transpose(0, 1).numpy(), rtol=1e-12, atol=1e-14)
+        row += n
