@@ -187,8 +187,20 @@ __global__ void __launch_bounds__(1024) plan_kernel(const __grid_constant__ Deco
   const int bpp = P / p.block_size;
   const int S = p.num_seqs;
   launch_dependents();  // the decode grid may become resident; it waits for us
-  int *len = S <= kPlanSmemSeqs ? s_len : p.plan_len;
-  int *off = S <= kPlanSmemSeqs ? s_off : p.plan_off;
+  const bool in_smem = S <= kPlanSmemSeqs;
+  int *len = in_smem ? s_len : p.plan_len;
+  int *off = in_smem ? s_off : p.plan_off;
+  // pair k = (s, q): found by a binary search of the offsets when they are
+  // in shared memory, else read from the pair list in the workspace
+  auto pair_at = [&](int k) -> int2 {
+    if (!in_smem) return p.plan_pairs[k];
+    int lo = 0, hi = S - 1;  // the last s with off[s] <= k
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (off[mid] <= k) lo = mid; else hi = mid - 1;
+    }
+    return make_int2(lo, k - off[lo]);
+  };
   // A) lengths, partition counts, and the (s, q) pair list in sequence order
   if (tid == 0) base = 0;
   __syncthreads();
@@ -206,7 +218,8 @@ __global__ void __launch_bounds__(1024) plan_kernel(const __grid_constant__ Deco
     if (s < S) {
       const int o = b + ex;
       off[s] = o;
-      for (int q = 0; q < nP; ++q) p.plan_pairs[o + q] = make_int2(s, q);
+      if (!in_smem)
+        for (int q = 0; q < nP; ++q) p.plan_pairs[o + q] = make_int2(s, q);
     }
     __syncthreads();     // ... before thread 0 advances it
     if (tid == 0) base = b + tot;
@@ -219,7 +232,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(const __grid_constant__ Deco
   // B) does pair (s, q) join the item of (s-1, q)?  One thread per pair.
   if (p.kmax > 1) {
     for (int k = tid; k < npairs; k += 1024) {
-      const int2 sq = p.plan_pairs[k];
+      const int2 sq = pair_at(k);
       bool jn = false;
       if (sq.x % p.kmax != 0) {
         const int need = (sq.y + 1) * P;
@@ -238,7 +251,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(const __grid_constant__ Deco
     int lead = 0, ksz = 1;
     int2 sq = make_int2(0, 0);
     if (k < npairs) {
-      sq = p.plan_pairs[k];
+      sq = pair_at(k);
       lead = (p.kmax > 1) ? (join[k] == 0) : 1;
       if (lead && p.kmax > 1) {
         for (int j = 1; j < p.kmax && sq.x + j < S; ++j) {
@@ -267,15 +280,17 @@ __global__ void __launch_bounds__(1024) plan_kernel(const __grid_constant__ Deco
 // ----------------------------------------------------------------------------
 template <int QT, int D>
 __global__ void __launch_bounds__(256) merge_kernel(const __grid_constant__ DecodeParams p) {
-  grid_dependency_wait();  // partials of the decode grid
   const int lane = threadIdx.x & 31;
   const long long gw = (blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x) >> 5;
   if (gw >= static_cast<long long>(p.num_seqs) * p.num_q_heads) return;
   const int s = static_cast<int>(gw / p.num_q_heads);
   const int hq = static_cast<int>(gw % p.num_q_heads);
+  // the lengths are an input (no kernel of this call writes them): read
+  // before waiting for the decode grid, whose partials come after
   const int L = min(max(__ldg(p.seq_lens + s), 0), p.len_cap);
   const int nP = max(1, (L + p.partition_size - 1) / p.partition_size);
   if (nP <= 1) return;
+  grid_dependency_wait();  // partials of the decode grid
   const size_t base = static_cast<size_t>(s) * p.max_parts * p.num_q_heads + hq;
   // pass 1: the largest partition maximum (lane q reads partition q, q + 32, ...)
   float M = -INFINITY;
