@@ -97,6 +97,26 @@ def test_prefill_byte_cache_matches_oracle(cache_dtype, q_dtype, d, group, per_h
     _check(w, out, ref)
 
 
+@pytest.mark.parametrize("cache_dtype,q_dtype", [("e4m3", "bf16"), ("int8", "f16")])
+@pytest.mark.parametrize("bs", [8, 32])
+def test_prefill_byte_cache_block_sizes(cache_dtype, q_dtype, bs):
+    """One-byte caches at block sizes 8 and 32: eight or two code tiles a
+    stage, whole blocks widened."""
+    Hkv, group = 2, 2
+    lens = [L for L, _ in CASES]
+    q_lens = [n for _, n in CASES]
+    w = W.random_case(_seed("bs", cache_dtype, bs), len(lens), Hkv * group, Hkv, 128, bs, cache_dtype,
+                      q_dtype, lens, device=G.DEV, k_scale=0.05, v_scale=0.04)
+    gen = torch.Generator(device=G.DEV).manual_seed(_seed("qbs", cache_dtype, bs))
+    q = torch.randn((sum(q_lens), Hkv * group, 128), generator=gen, device=G.DEV).to(w.q.dtype)
+    out, run = _run(w, q, q_lens)
+    assert int(run.err.item()) == 0
+    c = G.oracle_cache(w)
+    ref = A.paged_prefill(G.bits_to_f64(G.bits(q), q_dtype), q_lens, c.k, c.v, cache_dtype,
+                          w.block_tables, w.seq_lens, w.scale, w.k_scale, w.v_scale)
+    _check(w, out, ref)
+
+
 def test_prefill_byte_cache_large_bf16_queries():
     """bf16 q beyond fp16's range: the query tile is scaled by a power of two
     before it is rounded to fp16, and the factor undone on the scores."""
