@@ -325,15 +325,7 @@ def run_ours(args, rank, world, local):
         "vs_baseline": None,
         "dtype": w.cache_dtype,
         "data": "synthetic (seeded N(0,1) K/V/q, seeded lengths and shuffled block pool)",
-        "config": {
-            "workload": f"{args.config}: {_describe(w)}",
-            "num_seqs": w.S, "q_heads": w.Hq, "kv_heads": w.Hkv, "head_dim": w.d,
-            "block_size": w.bs, "cache_dtype": w.cache_dtype, "q_dtype": w.q_dtype,
-            "partition_size": P or _auto_partition(w),
-            "kv_bytes_per_step": kv_bytes, "seed": seed,
-            "l2": "inputs larger than L2 (KV working set %.2f GB vs 129 MB L2)" % (kv_bytes / 1e9),
-            "parallelism": f"replicas x{world}",
-        },
+        "config": decode_config(w, args.config, seed, world),
         "seq_layer_per_s": round(world * w.S / step_t, 1),
         "gpu_launches": launches_per_step * K,
         "device_error": derr,
@@ -358,6 +350,20 @@ def run_ours(args, rank, world, local):
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args.config, seed, budget_s=12.0)
     print(json.dumps(line), flush=True)
+
+
+def decode_config(w, config: str, seed: int, world: int) -> dict:
+    """The workload description of a decode bench line (both arms)."""
+    kv_bytes, _ = workload_bytes(w)
+    return {
+        "workload": f"{config}: {_describe(w)}",
+        "num_seqs": w.S, "q_heads": w.Hq, "kv_heads": w.Hkv, "head_dim": w.d,
+        "block_size": w.bs, "cache_dtype": w.cache_dtype, "q_dtype": w.q_dtype,
+        "partition_size": w.partition_size or _auto_partition(w),
+        "kv_bytes_per_step": kv_bytes, "seed": seed,
+        "l2": "inputs larger than L2 (KV working set %.2f GB vs 129 MB L2)" % (kv_bytes / 1e9),
+        "parallelism": f"replicas x{world}",
+    }
 
 
 def graph_step_time(step, K: int, stream):
@@ -470,7 +476,8 @@ def run_reference(args, rank, world):
         "impl": "reference", "metric": METRIC, "value": val, "unit": "GB/s", "n_gpus": world,
         "steps": steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": {"workload": f"{args.config} (bounded sample: 2 sequences)"},
+        "data": "synthetic", "config": decode_config(W.make_workload(args.config, seed, values=False), args.config,
+                                                   seed, world),
         "cpu_baseline": {"value": val, "unit": "GB/s", "cores": _cores(), "kind": "oracle",
                          "sample": f"first 2 sequences of {args.config}, all query heads"},
         "e2e": {"value": val, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
