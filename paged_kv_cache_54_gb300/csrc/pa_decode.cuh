@@ -53,12 +53,16 @@ constexpr float kLazyRescale = 8.0f;
 // chunk at byte offset `off` lands at off ^ (((off >> 7) & 7) << 4).  Every
 // shared-memory read of K or V goes through swz<SW>() on the offset relative
 // to the (1024-byte aligned) K or V region of the stage.
-// Used for the kernels whose items always run on the tensor-core path
-// (G >= 2): there the swizzle makes the fragment reads conflict-free.  The
-// G == 1 kernels keep the linear layout, on which the SIMT path's reads are
-// already conflict-free.
+// Every item on the tensor-core path is staged this way (rows of at least
+// 128 bytes): the swizzle makes its fragment reads conflict-free.  In the
+// G == 1 kernels the items with one query per tile (SIMT path) keep the
+// linear layout and 1-D bulk copies, on which their reads are already
+// conflict-free; the items batching sequences that share blocks (beams)
+// run on the tensor-core path and are staged swizzled, item by item.
+template <int KV, int D>
+__host__ __device__ constexpr bool tiled_rows() { return D * elt_bytes(KV) >= 128; }
 template <int KV, int D, int G>
-__host__ __device__ constexpr bool swizzled() { return D * elt_bytes(KV) >= 128 && G >= 2; }
+__host__ __device__ constexpr bool swizzled() { return tiled_rows<KV, D>() && G >= 2; }
 
 template <bool SW>
 __device__ __forceinline__ int swz(int off) {
@@ -457,7 +461,9 @@ __device__ __forceinline__ void producer_warp(const DecodeParams &p, uint8_t *sm
           record_error(p.err, kErrBlockIndex);
           b = 0;
         }
-        if constexpr (swizzled<KV, D, G>()) {
+        bool tiled = swizzled<KV, D, G>();
+        if constexpr (tiled_rows<KV, D>() && G == 1) tiled = kseq > 1;  // a shared item: tensor-core path
+        if (tiled) {
           // tile rows [row0, row0 + bs) of the [num_blocks * kv_heads * bs, d] view
           const int row0 = (b * p.num_kv_heads + h) * bs;
           tma_load_tile<(D * elt_bytes(KV) > 128)>(sb + p.k_off + lane * tile, &p.tmap_k, row0, &hdr.full[stage]);
@@ -710,7 +716,7 @@ struct SimtState {
 //   for 256-byte rows, where the V reads are 2-way.
 template <int KV, int QT, int D, int G, int QM>
 struct MmaState {
-  static constexpr bool SW = swizzled<KV, D, G>();
+  static constexpr bool SW = tiled_rows<KV, D>();  // always staged swizzled when rows allow
   static constexpr bool KV8 = is_byte(KV);
   static constexpr int MT = KV8 ? kF16 : KV;  // mma input type
   static constexpr int ELT = elt_bytes(KV);
@@ -1253,8 +1259,8 @@ __host__ __device__ constexpr int kernel_regs() {
 }
 
 // The tiled TMA reads the tensor maps from the kernel's parameter space, so
-// the swizzled kernels take their parameters as grid constants; the others
-// take them by value.
+// the kernels that may stage swizzled tiles (rows of 128 bytes or more) take
+// their parameters as grid constants; the others take them by value.
 template <int KV, int QT, int D, int G, bool MMA>
 __global__ void __maxnreg__((kernel_regs<KV, D, G>())) decode_kernel_tma(const __grid_constant__ DecodeParams p) {
   decode_body<KV, QT, D, G, MMA>(p);
@@ -1286,7 +1292,7 @@ pa_status launch_decode(DecodeParams p, const DeviceInfo &dev, cudaStream_t stre
   p.stages_off = sp.stages_off;
   p.kmax = query_capacity(G) / G;
   void (*kern)(DecodeParams);
-  if constexpr (swizzled<KV, D, G>()) {
+  if constexpr (tiled_rows<KV, D>()) {
     kern = decode_kernel_tma<KV, QT, D, G, MMA>;
   } else {
     kern = decode_kernel<KV, QT, D, G, MMA>;

@@ -166,8 +166,8 @@ extern "C" pa_status pa_decode(void *out, const void *q, int32_t q_dtype, int32_
   p.part_o = reinterpret_cast<float *>(ws + w.o_off);
   p.err = device_error;
 
-  if (G >= 2 && (!encode_cache_map(&p.tmap_k, k_cache, cache) ||
-                 !encode_cache_map(&p.tmap_v, v_cache, cache)))  // tiled views for the swizzled kernels
+  if (!encode_cache_map(&p.tmap_k, k_cache, cache) ||
+      !encode_cache_map(&p.tmap_v, v_cache, cache))  // tiled views for the swizzled (tensor-path) stages
     return cuda_fail(cudaErrorInvalidValue);
 
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
