@@ -13,7 +13,9 @@
 // Warps:
 //   0..7  softmax, one warpgroup per tile: thread r of a warpgroup owns row
 //         r.  It reads its S row from TMEM, applies the causal mask (key
-//         position <= the row's position) and an online softmax in base 2,
+//         position <= the row's position) on the stages that reach past
+//         some row of its warp, and an online softmax in base 2 (packed
+//         f32x2 arithmetic, the scale folded into the exponent's fma),
 //         writes P (16-bit pairs) back over the S buffer it just read, where
 //         P V takes it as a tensor-memory A operand, and rescales its O row in
 //         TMEM only when the row maximum has grown by more than 2^8 (lazy
@@ -38,13 +40,15 @@
 //
 // One-byte caches (FP8 e4m3 / e5m2, INT8): the products take fp16 operands.
 // The TMA warp copies each (block, head) tile of codes whole (one bulk copy
-// per block for K and for V) into a ring of four code slots, widens them
-// exactly to fp16 (a warpgroup of four widening warps, one on each SM
-// sub-partition) into three 16-bit stages of the layout above, and marks
-// the stage full.  A bf16 query tile is rewritten in place as fp16 by its
-// softmax warps, times a power of two that brings its largest entry within
-// fp16's range; the factor, and the K scale, go into the score scale, the
-// V scale into the output.
+// per block for K and for V) into a ring of four code slots; warps 12..15,
+// one on each SM sub-partition, widen the codes exactly to fp16 into three
+// 16-bit stages of the layout above and mark each stage full (warp 11 only
+// completes the third warpgroup).  The softmax warpgroups take 168
+// registers a thread and the others 88 (setmaxnreg), within the 512 x 128
+// the block is launched with.  A bf16 query tile is rewritten in place as
+// fp16 by its softmax warps, times a power of two that brings its largest
+// entry within fp16's range; the factor, and the K scale, go into the score
+// scale, the V scale into the output.
 #include <limits.h>
 #include <math.h>
 
