@@ -243,6 +243,21 @@ __global__ void __launch_bounds__(pf_threads(is_byte(KVT)), 1) prefill_kernel(co
   const int pos0 = L - n;                               // position of new token 0
   const int kv_end = pos0 + min(n, (cta + 1) * QC);     // keys 0..kv_end-1 are needed
   const int n_stages = (kv_end + kPfKeys - 1) / kPfKeys;
+  // The TMA warp starts the descriptor fetches and the first stage's table
+  // entries now, so that they overlap the set-up below.
+  const int32_t *table = p.block_tables + static_cast<size_t>(s) * p.max_blocks;
+  int first_entry = 0;
+  if (warp == kPfTmaWarp) {
+    if (lane == 0) {
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&p.tmap_q)) : "memory");
+      if constexpr (!KV8) {
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&p.tmap_k)) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&p.tmap_v)) : "memory");
+      }
+    }
+    const int nb0 = min(kPfKeys / p.block_size, (kv_end + p.block_size - 1) / p.block_size);
+    if (lane < nb0) first_entry = __ldg(table + lane);
+  }
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < NS; ++i) {
@@ -511,9 +526,8 @@ __global__ void __launch_bounds__(pf_threads(is_byte(KVT)), 1) prefill_kernel(co
       }
       const int bs = p.block_size;
       const int bpt = kPfKeys / bs;  // blocks per stage (<= 8)
-      const int32_t *table = p.block_tables + static_cast<size_t>(s) * p.max_blocks;
       auto stage_blocks = [&](int i) { return min(bpt, (kv_end - i * kPfKeys + bs - 1) / bs); };
-      int next = lane < stage_blocks(0) ? __ldg(table + lane) : 0;
+      int next = first_entry;  // the first stage's entries, fetched at the start
       int issued = 0;
       bool ok = true;
       if constexpr (KV8) {
