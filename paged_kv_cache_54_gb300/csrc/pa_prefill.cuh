@@ -226,6 +226,14 @@ __global__ void __launch_bounds__(pf_threads(is_byte(KVT)), 1) prefill_kernel(co
   const int cta = gridDim.x - 1 - blockIdx.x;  // the longest (last) token ranges start first
   const int s = blockIdx.y, h = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // the tensor-map descriptors are fetched while the lengths are read
+  if (warp == kPfTmaWarp && lane == 0) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&p.tmap_q)) : "memory");
+    if constexpr (!KV8) {
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&p.tmap_k)) : "memory");
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&p.tmap_v)) : "memory");
+    }
+  }
 
   const int q0 = __ldg(p.cu_q + s);
   const int n = __ldg(p.cu_q + s + 1) - q0;
@@ -243,18 +251,11 @@ __global__ void __launch_bounds__(pf_threads(is_byte(KVT)), 1) prefill_kernel(co
   const int pos0 = L - n;                               // position of new token 0
   const int kv_end = pos0 + min(n, (cta + 1) * QC);     // keys 0..kv_end-1 are needed
   const int n_stages = (kv_end + kPfKeys - 1) / kPfKeys;
-  // The TMA warp starts the descriptor fetches and the first stage's table
-  // entries now, so that they overlap the set-up below.
+  // the TMA warp reads the first stage's table entries now, so that they
+  // arrive during the set-up below
   const int32_t *table = p.block_tables + static_cast<size_t>(s) * p.max_blocks;
   int first_entry = 0;
   if (warp == kPfTmaWarp) {
-    if (lane == 0) {
-      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&p.tmap_q)) : "memory");
-      if constexpr (!KV8) {
-        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&p.tmap_k)) : "memory");
-        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&p.tmap_v)) : "memory");
-      }
-    }
     const int nb0 = min(kPfKeys / p.block_size, (kv_end + p.block_size - 1) / p.block_size);
     if (lane < nb0) first_entry = __ldg(table + lane);
   }
