@@ -9,17 +9,25 @@
 namespace pa {
 namespace {
 
-// [rows, head_dim] view of a 16-bit cache, box {64 elements, block_size rows}
-// (one 128-byte half of one (block, head) tile), 128-byte swizzle.
+// [row groups, half, row, 64 elements] view of a 16-bit cache: a row group
+// is 8 consecutive rows (token slots of one block and head), a half is a
+// 128-byte column half of a row.  The box {64, 8, head_dim / 64,
+// block_size / 8} is one whole (block, head) tile.  It lands group by group,
+// each group half by half, as 8-row x 128-byte atoms with the 128-byte
+// swizzle: the stage layout the prefill's tensor cores read.  The half
+// stride (128 bytes) is smaller than the row stride; each box line is still
+// 128 contiguous bytes.
 bool encode_cache_view(CUtensorMap *map, const void *cache, const pa_cache_desc *c) {
   PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
   if (enc == nullptr) return false;
-  const cuuint64_t rows = static_cast<cuuint64_t>(c->num_blocks) * c->kv_heads * c->block_size;
-  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(c->head_dim), rows};
-  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(c->head_dim) * 2};
-  const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(c->block_size)};
-  const cuuint32_t estr[2] = {1, 1};
-  return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void *>(cache), dims, strides, box, estr,
+  const cuuint64_t row = static_cast<cuuint64_t>(c->head_dim) * 2;
+  const cuuint64_t halves = static_cast<cuuint64_t>(c->head_dim / 64);
+  const cuuint64_t groups = static_cast<cuuint64_t>(c->num_blocks) * c->kv_heads * (c->block_size / 8);
+  const cuuint64_t dims[4] = {64, 8, halves, groups};
+  const cuuint64_t strides[3] = {row, 128, row * 8};
+  const cuuint32_t box[4] = {64, 8, static_cast<cuuint32_t>(halves), static_cast<cuuint32_t>(c->block_size / 8)};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 4, const_cast<void *>(cache), dims, strides, box, estr,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }

@@ -59,7 +59,7 @@ namespace pa {
 
 struct PrefillParams {
   CUtensorMap tmap_q;  // [T, Hkv, G, head_dim] view of q, box {64, G, 1, 128/G}
-  CUtensorMap tmap_k;  // [rows, head_dim] view of each 16-bit cache, box {64, block_size}
+  CUtensorMap tmap_k;  // 16-bit caches: [row group, half, row, 64] view, box = one (block, head) tile
   CUtensorMap tmap_v;
   const uint8_t *k_cache;  // one-byte caches: the codes
   const uint8_t *v_cache;
@@ -88,7 +88,19 @@ constexpr int kPfConvWarps = 4;
 // threads: softmax 8 warps, TMA, 2 MMA (one-byte caches: + an idle warp
 // that completes the third warpgroup, + the widening warpgroup)
 __host__ __device__ constexpr int pf_threads(bool kv8) { return 32 * (kv8 ? 16 : 11); }
-constexpr int kPfHalf = kPfKeys * 128;  // one 128-byte column half of a 64-key stage
+constexpr int kPfHalf = kPfKeys * 128;  // bytes of one 128-byte column half of a 64-key stage
+// A K or V stage holds its 64 keys as 8 groups of 8 rows.  Each group
+// is stored as its 128-byte row halves, one after the other, and each
+// half is an 8-row x 128-byte atom with the 128-byte swizzle.  A
+// (block, head) tile is a whole number of groups, so one tensor copy lands
+// it.  The tensor cores read K with the group stride as the 8-row stride
+// (and step to the next half by one atom), and read V with the atom as the
+// column-half stride and the group as the 8-key stride.
+constexpr int kPfAtom = 1024;
+template <int NH>
+__device__ __forceinline__ int kv_row_off(int key, int hf) {  // byte offset of (key, half) in a stage
+  return (key >> 3) * NH * kPfAtom + hf * kPfAtom + (key & 7) * 128;
+}
 constexpr int kPfStages = 5;      // 16-bit K/V stages (three with one-byte caches)
 constexpr int kPfCodeSlots = 4;   // one-byte caches: stages of codes in flight
 constexpr uint32_t kPfTmemCols = 512;
@@ -131,39 +143,43 @@ struct PfHeader {
 
 // Widen the codes of a slot (K then V, the first `keys` keys of each) into a
 // 16-bit stage: 8 codes make one 16-byte chunk, and chunk c of key row k of
-// half hf lands at chunk c ^ (k mod 8).  The work is 2 keys / KPI warp
-// iterations of 32 chunks, lane = (key, half, chunk); this warp takes
-// iterations part, part + parts, ...  keys is a multiple of 8.
-template <int KVT, int D>
-__device__ __forceinline__ void widen_codes(const uint8_t *slot, uint8_t *stage, int keys, int lane, int part,
-                                            int parts) {
+// half hf lands in that row of the stage's atom layout at chunk c ^ (k mod
+// 8).  A warp iteration converts 32 chunks, lane = (key, half, chunk), and
+// the PARTS widening warps take interleaved iterations.  A warp's
+// successive keys are then a multiple of 8 apart, so each lane keeps one
+// swizzle phase and steps its source and destination by constants.  keys
+// is a multiple of 8.
+template <int KVT, int D, int PARTS>
+__device__ __forceinline__ void widen_codes(const uint8_t *slot, uint8_t *stage, int keys, int lane, int part) {
   constexpr int NH = D / 64;
-  constexpr int KPI = 32 / (NH * 8);
+  constexpr int KPI = 32 / (NH * 8);     // keys per warp iteration
+  constexpr int KSTEP = PARTS * KPI;     // keys between one warp's iterations
+  static_assert(KSTEP % 8 == 0, "a lane's keys must keep their row in the atom");
+  constexpr int SRC_STEP = KSTEP * D;
+  constexpr int DST_STEP = KSTEP / 8 * NH * kPfAtom;
   const int kr = lane / (NH * 8), hf = (lane >> 3) % NH, c = lane & 7;
-  const int per = keys / KPI;  // iterations per tensor
-  const uint8_t *src = slot + hf * 64 + c * 8;
-  uint8_t *dst = stage + hf * kPfHalf;
-  // the loads of a batch go before its stores: the compiler cannot tell
-  // that the stores do not alias them
+  const int k0 = part * KPI + kr;
+  const int n = keys > k0 ? (keys - k0 + KSTEP - 1) / KSTEP : 0;  // this lane's keys of each tensor
   constexpr int B = 4;
-  for (int it0 = part; it0 < 2 * per; it0 += B * parts) {
-    uint2 w[B];
-    int off[B];
 #pragma unroll
-    for (int u = 0; u < B; ++u) {
-      const int it = it0 + u * parts;
-      const int tv = it >= per;
-      const int k = (it - tv * per) * KPI + kr;
-      off[u] = it < 2 * per ? tv * NH * kPfHalf + k * 128 + ((c ^ (k & 7)) << 4) : -1;
-      w[u] = it < 2 * per ? *reinterpret_cast<const uint2 *>(src + tv * kPfKeys * D + k * D) : make_uint2(0u, 0u);
-    }
+  for (int tv = 0; tv < 2; ++tv) {
+    const uint8_t *src = slot + tv * kPfKeys * D + k0 * D + hf * 64 + c * 8;
+    uint8_t *dst = stage + tv * NH * kPfHalf + kv_row_off<NH>(k0, hf) + ((c ^ (k0 & 7)) << 4);
+    // the loads of a batch go before its stores: the compiler cannot tell
+    // that the stores do not alias them
+    for (int m0 = 0; m0 < n; m0 += B) {
+      uint2 w[B];
 #pragma unroll
-    for (int u = 0; u < B; ++u) {
-      if (off[u] >= 0) {
-        uint4 o;
-        byte4_to_half2x2<KVT>(w[u].x, o.x, o.y);
-        byte4_to_half2x2<KVT>(w[u].y, o.z, o.w);
-        *reinterpret_cast<uint4 *>(dst + off[u]) = o;
+      for (int u = 0; u < B; ++u)
+        if (m0 + u < n) w[u] = *reinterpret_cast<const uint2 *>(src + (m0 + u) * SRC_STEP);
+#pragma unroll
+      for (int u = 0; u < B; ++u) {
+        if (m0 + u < n) {
+          uint4 o;
+          byte4_to_half2x2<KVT>(w[u].x, o.x, o.y);
+          byte4_to_half2x2<KVT>(w[u].y, o.z, o.w);
+          *reinterpret_cast<uint4 *>(dst + (m0 + u) * DST_STEP) = o;
+        }
       }
     }
   }
@@ -470,7 +486,7 @@ __global__ void __launch_bounds__(pf_threads(is_byte(KVT)), 1) prefill_kernel(co
           const int z0 = kv_end - k0;
           for (int idx = r; idx < (kPfKeys - z0) * 8 * NH; idx += kPfTileRows) {
             const int hf = idx / ((kPfKeys - z0) * 8), rem = idx % ((kPfKeys - z0) * 8);
-            *reinterpret_cast<uint4 *>(vb + hf * kPfHalf + (z0 + rem / 8) * 128 + (rem % 8) * 16) =
+            *reinterpret_cast<uint4 *>(vb + kv_row_off<NH>(z0 + rem / 8, hf) + (rem % 8) * 16) =
                 make_uint4(0u, 0u, 0u, 0u);
           }
           fence_proxy_async_smem();  // the zeroed V rows visible to the tensor cores
@@ -590,13 +606,10 @@ __global__ void __launch_bounds__(pf_threads(is_byte(KVT)), 1) prefill_kernel(co
         uint8_t *vb = kb + NH * kPfHalf;
         if (lane == 0) mbar_arrive_expect_tx(&hdr.kv_full[st], 2u * NH * static_cast<uint32_t>(nblk * bs) * 128u);
         __syncwarp();
-        if (lane < nblk) {  // lane j issues block j's boxes: the lanes' copies go out together
-          const int r0 = (phys * p.num_kv_heads + h) * bs;
-  #pragma unroll
-          for (int hf = 0; hf < NH; ++hf) {
-            tma_load_2d(kb + hf * kPfHalf + lane * bs * 128, &p.tmap_k, hf * 64, r0, &hdr.kv_full[st]);
-            tma_load_2d(vb + hf * kPfHalf + lane * bs * 128, &p.tmap_v, hf * 64, r0, &hdr.kv_full[st]);
-          }
+        if (lane < nblk) {  // lane j issues block j's tiles: the lanes' copies go out together
+          const int g0 = (phys * p.num_kv_heads + h) * (bs / 8);  // the tile's first row group
+          tma_load_4d(kb + lane * bs * NH * 128, &p.tmap_k, 0, 0, 0, g0, &hdr.kv_full[st]);
+          tma_load_4d(vb + lane * bs * NH * 128, &p.tmap_v, 0, 0, 0, g0, &hdr.kv_full[st]);
         }
         issued = i + 1;
       }
@@ -624,14 +637,15 @@ __global__ void __launch_bounds__(pf_threads(is_byte(KVT)), 1) prefill_kernel(co
           if (!mbar_wait(&hdr.kv_full[st], (i / NS) & 1, abort)) return false;
           tc_fence_after_sync();
           // descriptors of the first k-step; a k-step advances the start
-          // address field (16-byte units) by 32 bytes, a row half by a region
+          // address field (16-byte units) by 32 bytes, a row half by a
+          // region of q and by one atom of K
           const uint64_t a0 = umma_desc_sw128(qt, 16, 1024);
-          const uint64_t b0 = umma_desc_sw128(saddr + st * Lay::STAGE_BYTES, 16, 1024);
+          const uint64_t b0 = umma_desc_sw128(saddr + st * Lay::STAGE_BYTES, 16, NH * kPfAtom);
           const uint32_t d = tt + (i & 1) * kPfKeys;
   #pragma unroll
           for (int kk = 0; kk < KSTEPS; ++kk) {
             const uint32_t off = (kk % 4) * 32;  // 16 elements = 32 bytes into the swizzled row
-            tc_mma_f16(d, a0 + (((kk / 4) * Lay::Q_HALF + off) >> 4), b0 + (((kk / 4) * kPfHalf + off) >> 4),
+            tc_mma_f16(d, a0 + (((kk / 4) * Lay::Q_HALF + off) >> 4), b0 + (((kk / 4) * kPfAtom + off) >> 4),
                        IDESC_QK, kk > 0);
           }
           tc_commit(&hdr.s_full[t][i & 1]);
@@ -648,10 +662,11 @@ __global__ void __launch_bounds__(pf_threads(is_byte(KVT)), 1) prefill_kernel(co
             break;
           }
           tc_fence_after_sync();
-          const uint64_t b0 = umma_desc_sw128(saddr + (i % NS) * Lay::STAGE_BYTES + NH * kPfHalf, kPfHalf, 1024);
+          const uint64_t b0 =
+              umma_desc_sw128(saddr + (i % NS) * Lay::STAGE_BYTES + NH * kPfHalf, kPfAtom, NH * kPfAtom);
   #pragma unroll
-          for (int kk = 0; kk < kPfKeys / 16; ++kk)  // 16 keys: 8 columns of P, 2048 bytes of V rows
-            tc_mma_f16_ta(tt + 2 * kPfKeys, tt + (i & 1) * kPfKeys + kk * 8, b0 + kk * 128, IDESC_PV,
+          for (int kk = 0; kk < kPfKeys / 16; ++kk)  // 16 keys: 8 columns of P, two row groups of V
+            tc_mma_f16_ta(tt + 2 * kPfKeys, tt + (i & 1) * kPfKeys + kk * 8, b0 + kk * (2 * NH * kPfAtom >> 4), IDESC_PV,
                           (i > 0 || kk > 0) ? 1u : 0u);
           tc_commit(&hdr.pv_done[t]);
           if (i + 1 == n_stages) tc_commit(&hdr.o_ready[t]);
@@ -688,8 +703,8 @@ __global__ void __launch_bounds__(pf_threads(is_byte(KVT)), 1) prefill_kernel(co
           break;
         }
         const int keys = min(bpt, (kv_end - i * kPfKeys + bs - 1) / bs) * bs;
-        widen_codes<KVT, D>(codes + (i % NC) * Lay::CODE_BYTES, stages + st * Lay::STAGE_BYTES, keys, lane, q,
-                            kPfConvWarps);
+        widen_codes<KVT, D, kPfConvWarps>(codes + (i % NC) * Lay::CODE_BYTES, stages + st * Lay::STAGE_BYTES, keys,
+                                          lane, q);
         // the 16-bit stage visible to the tensor cores, and the code slot's
         // reads ordered before the bulk copy that refills it
         fence_proxy_async_smem();
