@@ -502,25 +502,39 @@ __global__ void __launch_bounds__(pf_threads(is_byte(KVT)), 1) prefill_kernel(co
         // so the last two may both be pending and a parity wait would take the
         // older phase for the newer)
         tc_fence_after_sync();
+        // O / l goes through this tile's q buffer (its products have all
+        // completed, so no product reads it any more): each thread writes
+        // its row, 16-byte chunk ch at ch ^ (row mod 8), then the tile's
+        // threads copy whole rows out, each warp instruction two rows of
+        // 16-bit outputs (rows past the sequence's new tokens are skipped).
         const float inv = vsc / l;
-        const bool store = tok < n;
-        uint8_t *row = static_cast<uint8_t *>(p.out) +
-                       (static_cast<size_t>(q0 + min(tok, n - 1)) * p.num_q_heads + h * G + r % G) * D * 2;
+        constexpr int RB = D * 2;      // bytes of an output row
+        constexpr int CPR = RB / 16;   // 16-byte chunks of a row
+        uint8_t *stg = qs + t * Lay::Q_TILE;
   #pragma unroll
         for (int c = 0; c < D; c += 32) {
           uint32_t ov[32];
           tc_ld32(trow + 2 * kPfKeys + c, ov);
-          if (store) {
   #pragma unroll
-            for (int j = 0; j < 32; j += 8) {
-              uint4 v;
-              v.x = pack2_rn<DT>(__uint_as_float(ov[j]) * inv, __uint_as_float(ov[j + 1]) * inv);
-              v.y = pack2_rn<DT>(__uint_as_float(ov[j + 2]) * inv, __uint_as_float(ov[j + 3]) * inv);
-              v.z = pack2_rn<DT>(__uint_as_float(ov[j + 4]) * inv, __uint_as_float(ov[j + 5]) * inv);
-              v.w = pack2_rn<DT>(__uint_as_float(ov[j + 6]) * inv, __uint_as_float(ov[j + 7]) * inv);
-              *reinterpret_cast<uint4 *>(row + (c + j) * 2) = v;
-            }
+          for (int j = 0; j < 32; j += 8) {
+            uint4 v;
+            v.x = pack2_rn<DT>(__uint_as_float(ov[j]) * inv, __uint_as_float(ov[j + 1]) * inv);
+            v.y = pack2_rn<DT>(__uint_as_float(ov[j + 2]) * inv, __uint_as_float(ov[j + 3]) * inv);
+            v.z = pack2_rn<DT>(__uint_as_float(ov[j + 4]) * inv, __uint_as_float(ov[j + 5]) * inv);
+            v.w = pack2_rn<DT>(__uint_as_float(ov[j + 6]) * inv, __uint_as_float(ov[j + 7]) * inv);
+            *reinterpret_cast<uint4 *>(stg + r * RB + ((((c + j) / 8) ^ (r & 7)) << 4)) = v;
           }
+        }
+        named_bar_sync(1 + t, kPfTileRows);
+        const int tok0 = cta * QC + t * QT;                          // the tile's first token
+        const int rows = min(kPfTileRows, (n - tok0) * G);           // rows with a new token
+        uint8_t *obase = static_cast<uint8_t *>(p.out) + (static_cast<size_t>(q0 + tok0) * p.num_q_heads + h * G) * RB;
+        const size_t tok_stride = static_cast<size_t>(p.num_q_heads) * RB;
+  #pragma unroll 4
+        for (int idx = r; idx < rows * CPR; idx += kPfTileRows) {
+          const int rr = idx / CPR, ch = idx % CPR;
+          const uint4 v = *reinterpret_cast<const uint4 *>(stg + rr * RB + ((ch ^ (rr & 7)) << 4));
+          *reinterpret_cast<uint4 *>(obase + (rr / G) * tok_stride + (rr % G) * RB + ch * 16) = v;
         }
       } else {
         record_error(p.err, kErrTimeout);
