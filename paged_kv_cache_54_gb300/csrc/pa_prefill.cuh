@@ -250,6 +250,14 @@ __global__ void __launch_bounds__(pf_threads(is_byte(KVT)), 1) prefill_kernel(co
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&p.tmap_v)) : "memory");
     }
   }
+  // and the TMA warp reads the sequence's first 64 block-table entries: a
+  // window of 32 (lane j: entry 32 w + j) in use and the next one
+  const int32_t *table = p.block_tables + static_cast<size_t>(s) * p.max_blocks;
+  int win = 0, win_next = 0;
+  if (warp == kPfTmaWarp) {
+    if (lane < p.max_blocks) win = __ldg(table + lane);
+    if (32 + lane < p.max_blocks) win_next = __ldg(table + 32 + lane);
+  }
 
   const int q0 = __ldg(p.cu_q + s);
   const int n = __ldg(p.cu_q + s + 1) - q0;
@@ -267,48 +275,99 @@ __global__ void __launch_bounds__(pf_threads(is_byte(KVT)), 1) prefill_kernel(co
   const int pos0 = L - n;                               // position of new token 0
   const int kv_end = pos0 + min(n, (cta + 1) * QC);     // keys 0..kv_end-1 are needed
   const int n_stages = (kv_end + kPfKeys - 1) / kPfKeys;
-  // the TMA warp reads the first stage's table entries now, so that they
-  // arrive during the set-up below
-  const int32_t *table = p.block_tables + static_cast<size_t>(s) * p.max_blocks;
-  int first_entry = 0;
+  uint8_t *qs = smem + Lay::Q_OFF;
+  uint8_t *stages = smem + Lay::STAGE_OFF;
+  uint8_t *codes = smem + Lay::CODE_OFF;
+  volatile int *abort = &hdr.abort;
+  const int bs = p.block_size;
+  const int bpt = kPfKeys / bs;  // blocks per stage (<= 8)
+  auto stage_blocks = [&](int i) { return min(bpt, (kv_end - i * kPfKeys + bs - 1) / bs); };
+  // The producer's copies of stage i, issued by the whole TMA warp in stage
+  // order: lane j copies block j of the stage, its table entry taken from
+  // the window, and the windows move on (the next one fetched) once a
+  // stage ends a window.
+  // 16-bit caches: each (block, head) tile of K and V by one tensor copy
+  // into stage i % NS.  One-byte caches: the codes of each block by one bulk
+  // copy into slot i % NC, widened by the widening warps.
+  auto issue_stage = [&](int i) {
+    const int nblk = stage_blocks(i);
+    const int e0 = i * bpt;  // the stage's first entry; bpt divides 32
+    int phys = __shfl_sync(0xffffffffu, win, (e0 & 31) + (lane & (bpt - 1)));
+    if (((e0 + bpt) & 31) == 0) {
+      win = win_next;
+      win_next = e0 + bpt + 32 + lane < p.max_blocks ? __ldg(table + e0 + bpt + 32 + lane) : 0;
+    }
+    if (lane < nblk && (phys < 0 || phys >= p.num_blocks)) {
+      record_error(p.err, kErrBlockIndex);
+      phys = 0;  // read a valid block; the result is void and flagged
+    }
+    if constexpr (KV8) {
+      uint8_t *cb = codes + (i % NC) * Lay::CODE_BYTES;
+      const uint32_t tile = static_cast<uint32_t>(bs) * D;
+      if (lane == 0) mbar_arrive_expect_tx(&hdr.code_full[i % NC], 2u * nblk * tile);
+      __syncwarp();
+      if (lane < nblk) {
+        const size_t off = (static_cast<size_t>(phys) * p.num_kv_heads + h) * tile;
+        bulk_g2s(cb + lane * tile, p.k_cache + off, tile, &hdr.code_full[i % NC]);
+        bulk_g2s(cb + kPfKeys * D + lane * tile, p.v_cache + off, tile, &hdr.code_full[i % NC]);
+      }
+    } else {
+      const int st = i % NS;
+      uint8_t *kb = stages + st * Lay::STAGE_BYTES;
+      uint8_t *vb = kb + NH * kPfHalf;
+      if (lane == 0) mbar_arrive_expect_tx(&hdr.kv_full[st], 2u * NH * static_cast<uint32_t>(nblk * bs) * 128u);
+      __syncwarp();
+      if (lane < nblk) {
+        const int g0 = (phys * p.num_kv_heads + h) * (bs / 8);  // the tile's first row group
+        tma_load_4d(kb + lane * bs * NH * 128, &p.tmap_k, 0, 0, 0, g0, &hdr.kv_full[st]);
+        tma_load_4d(vb + lane * bs * NH * 128, &p.tmap_v, 0, 0, 0, g0, &hdr.kv_full[st]);
+      }
+    }
+  };
+  // The TMA warp initialises the barriers and issues q and the first stage
+  // before the set-up barrier, so that those copies are in flight while
+  // tensor memory is allocated.  (The copy engine takes one copy about every
+  // 100 clocks, so issuing more here would only hold the barrier longer.)
+  const int pre = 1;
   if (warp == kPfTmaWarp) {
-    const int nb0 = min(kPfKeys / p.block_size, (kv_end + p.block_size - 1) / p.block_size);
-    if (lane < nb0) first_entry = __ldg(table + lane);
-  }
-
-  if (threadIdx.x == 0) {
-    for (int i = 0; i < NS; ++i) {
-      mbar_init(&hdr.kv_full[i], KV8 ? kPfConvWarps : 1);  // one-byte caches: each widening warp
-      mbar_init(&hdr.kv_empty[i], tiles);  // each tile's MMA warp frees the stage
+    if (lane == 0) {
+      for (int i = 0; i < NS; ++i) {
+        mbar_init(&hdr.kv_full[i], KV8 ? kPfConvWarps : 1);  // one-byte caches: each widening warp
+        mbar_init(&hdr.kv_empty[i], tiles);  // each tile's MMA warp frees the stage
+      }
+      for (int c = 0; c < NC; ++c) {
+        mbar_init(&hdr.code_full[c], 1);
+        mbar_init(&hdr.code_empty[c], kPfConvWarps);
+      }
+      for (int t = 0; t < kPfTiles; ++t) {
+        mbar_init(&hdr.q_ready[t], 1);
+        mbar_init(&hdr.s_full[t][0], 1);
+        mbar_init(&hdr.s_full[t][1], 1);
+        mbar_init(&hdr.p_full[t][0], kPfTileRows);
+        mbar_init(&hdr.p_full[t][1], kPfTileRows);
+        mbar_init(&hdr.pv_done[t], 1);
+        mbar_init(&hdr.o_ready[t], 1);
+      }
+      mbar_init(&hdr.q_full, 1);
+      mbar_init(&hdr.fin[0], 1);
+      mbar_init(&hdr.fin[1], 1);
+      hdr.abort = 0;
+      fence_mbar_init();
+      mbar_arrive_expect_tx(&hdr.q_full, tiles * NH * kPfTileRows * 128u);
+      for (int t = 0; t < tiles; ++t)
+  #pragma unroll
+        for (int hf = 0; hf < NH; ++hf)
+          tma_load_4d(qs + t * Lay::Q_TILE + hf * Lay::Q_HALF, &p.tmap_q, hf * 64, 0, h, q0 + cta * QC + t * QT,
+                      &hdr.q_full);
     }
-    for (int c = 0; c < NC; ++c) {
-      mbar_init(&hdr.code_full[c], 1);
-      mbar_init(&hdr.code_empty[c], kPfConvWarps);
-    }
-    for (int t = 0; t < kPfTiles; ++t) {
-      mbar_init(&hdr.q_ready[t], 1);
-      mbar_init(&hdr.s_full[t][0], 1);
-      mbar_init(&hdr.s_full[t][1], 1);
-      mbar_init(&hdr.p_full[t][0], kPfTileRows);
-      mbar_init(&hdr.p_full[t][1], kPfTileRows);
-      mbar_init(&hdr.pv_done[t], 1);
-      mbar_init(&hdr.o_ready[t], 1);
-    }
-    mbar_init(&hdr.q_full, 1);
-    mbar_init(&hdr.fin[0], 1);
-    mbar_init(&hdr.fin[1], 1);
-    hdr.abort = 0;
-    fence_mbar_init();
+    __syncwarp();
+    for (int i = 0; i < pre; ++i) issue_stage(i);
   }
   if (warp == kPfMmaWarp) tc_alloc(&hdr.tmem_base, kPfTmemCols);
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem = hdr.tmem_base;
-  uint8_t *qs = smem + Lay::Q_OFF;
-  uint8_t *stages = smem + Lay::STAGE_OFF;
-  uint8_t *codes = smem + Lay::CODE_OFF;
-  volatile int *abort = &hdr.abort;
 
   // Roles.  With one-byte caches the softmax warpgroups take 168 registers
   // a thread and the other two (TMA, MMA, widening) 88: 256 x 168 +
@@ -545,86 +604,20 @@ __global__ void __launch_bounds__(pf_threads(is_byte(KVT)), 1) prefill_kernel(co
     if constexpr (KV8) asm volatile("setmaxnreg.dec.sync.aligned.u32 88;" ::: "memory");
     if (warp == kPfTmaWarp) {
       // ------------------------------------------------------------ TMA
-      // The whole warp runs the loop: lane j fetches block-table entry j of the
-      // next stage while lane 0 issues this stage's copies.
-      if (lane == 0) {
-        mbar_arrive_expect_tx(&hdr.q_full, tiles * NH * kPfTileRows * 128u);
-        for (int t = 0; t < tiles; ++t)
-  #pragma unroll
-          for (int hf = 0; hf < NH; ++hf)
-            tma_load_4d(qs + t * Lay::Q_TILE + hf * Lay::Q_HALF, &p.tmap_q, hf * 64, 0, h, q0 + cta * QC + t * QT,
-                        &hdr.q_full);
-      }
-      const int bs = p.block_size;
-      const int bpt = kPfKeys / bs;  // blocks per stage (<= 8)
-      auto stage_blocks = [&](int i) { return min(bpt, (kv_end - i * kPfKeys + bs - 1) / bs); };
-      int next = first_entry;  // the first stage's entries, fetched at the start
-      int issued = 0;
+      // The rest of the stages, each once its slot has been freed (16-bit
+      // stages by both tiles' products, code slots by the widening warps).
+      const int slots = KV8 ? NC : NS;
+      int issued = pre;
       bool ok = true;
-      if constexpr (KV8) {
-        // stage j's codes into slot j % NC: one bulk copy per block for K and
-        // for V, issued by lane (block); the table entries come a stage ahead
-        auto issue_codes = [&](int j) {
-          const int nblk = stage_blocks(j);
-          int phys = next;
-          if (j + 1 < n_stages && lane < stage_blocks(j + 1)) next = __ldg(table + (j + 1) * bpt + lane);
-          if (lane < nblk && (phys < 0 || phys >= p.num_blocks)) {
-            record_error(p.err, kErrBlockIndex);
-            phys = 0;  // read a valid block; the result is void and flagged
-          }
-          uint8_t *cb = codes + (j % NC) * Lay::CODE_BYTES;
-          const uint32_t tile = static_cast<uint32_t>(bs) * D;
-          if (lane == 0) mbar_arrive_expect_tx(&hdr.code_full[j % NC], 2u * nblk * tile);
-          __syncwarp();
-          if (lane < nblk) {
-            const size_t off = (static_cast<size_t>(phys) * p.num_kv_heads + h) * tile;
-            bulk_g2s(cb + lane * tile, p.k_cache + off, tile, &hdr.code_full[j % NC]);
-            bulk_g2s(cb + kPfKeys * D + lane * tile, p.v_cache + off, tile, &hdr.code_full[j % NC]);
-          }
-        };
-        // a slot is refilled once the widening warps are done with it
-        for (int j = 0; j < n_stages && ok; ++j) {
-          bool freed = true;
-          if (lane == 0 && j >= NC) freed = mbar_wait(&hdr.code_empty[j % NC], ((j / NC) - 1) & 1, abort);
-          if (!__shfl_sync(0xffffffffu, freed, 0)) {
-            ok = false;
-            break;
-          }
-          issue_codes(j);
-          issued = j + 1;
-        }
-        if (lane == 0 && !ok) {
-          record_error(p.err, kErrTimeout);
-          *abort = 1;
-          // wait, within the limit, for the copies still in flight
-          for (int j = max(0, issued - NC); j < issued; ++j) mbar_wait(&hdr.code_full[j % NC], (j / NC) & 1, nullptr);
-        }
-        if (lane == 0) mbar_wait(&hdr.q_full, 0, nullptr);
-      } else {
-      for (int i = 0; i < n_stages; ++i) {
-        const int st = i % NS;
-        const int nblk = stage_blocks(i);
-        int phys = next;
-        if (i + 1 < n_stages && lane < stage_blocks(i + 1)) next = __ldg(table + (i + 1) * bpt + lane);
-        if (lane < nblk && (phys < 0 || phys >= p.num_blocks)) {
-          record_error(p.err, kErrBlockIndex);
-          phys = 0;  // read a valid block; the result is void and flagged
-        }
-        bool waited = true;
-        if (lane == 0 && i >= NS) waited = mbar_wait(&hdr.kv_empty[st], ((i / NS) - 1) & 1, abort);
-        if (!__shfl_sync(0xffffffffu, waited, 0)) {
+      for (int i = pre; i < n_stages; ++i) {
+        bool freed = true;
+        if (lane == 0 && i >= slots)
+          freed = mbar_wait(KV8 ? &hdr.code_empty[i % NC] : &hdr.kv_empty[i % NS], ((i / slots) - 1) & 1, abort);
+        if (!__shfl_sync(0xffffffffu, freed, 0)) {
           ok = false;
           break;
         }
-        uint8_t *kb = stages + st * Lay::STAGE_BYTES;
-        uint8_t *vb = kb + NH * kPfHalf;
-        if (lane == 0) mbar_arrive_expect_tx(&hdr.kv_full[st], 2u * NH * static_cast<uint32_t>(nblk * bs) * 128u);
-        __syncwarp();
-        if (lane < nblk) {  // lane j issues block j's tiles: the lanes' copies go out together
-          const int g0 = (phys * p.num_kv_heads + h) * (bs / 8);  // the tile's first row group
-          tma_load_4d(kb + lane * bs * NH * 128, &p.tmap_k, 0, 0, 0, g0, &hdr.kv_full[st]);
-          tma_load_4d(vb + lane * bs * NH * 128, &p.tmap_v, 0, 0, 0, g0, &hdr.kv_full[st]);
-        }
+        issue_stage(i);
         issued = i + 1;
       }
       if (lane == 0) {
@@ -632,11 +625,10 @@ __global__ void __launch_bounds__(pf_threads(is_byte(KVT)), 1) prefill_kernel(co
           record_error(p.err, kErrTimeout);
           *abort = 1;
           // wait, within the limit, for the copies still in flight
-          for (int j = max(0, issued - NS); j < issued; ++j)
-            mbar_wait(&hdr.kv_full[j % NS], (j / NS) & 1, nullptr);
+          for (int j = max(0, issued - slots); j < issued; ++j)
+            mbar_wait(KV8 ? &hdr.code_full[j % NC] : &hdr.kv_full[j % NS], (j / slots) & 1, nullptr);
         }
         mbar_wait(&hdr.q_full, 0, nullptr);
-      }
       }
     } else if (warp == kPfMmaWarp || warp == kPfMmaWarp + 1) {
       // ------------------------------------------------------------ MMA (tile t)
@@ -701,8 +693,6 @@ __global__ void __launch_bounds__(pf_threads(is_byte(KVT)), 1) prefill_kernel(co
       // ------------------------------------------------------------ widening
       // warp 12 + q widens warp-iterations q, q + 4, ... of every stage
       const int q = warp - kPfConvWarp0;
-      const int bs = p.block_size;
-      const int bpt = kPfKeys / bs;
       bool ok = true;
       for (int i = 0; i < n_stages; ++i) {
         const int st = i % NS;
