@@ -42,6 +42,9 @@ SMI_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.act
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "decode_traffic.txt")
 DECODE_SOURCES = [os.path.join(ROOT, "paged_kv_cache_54_gb300", "csrc", f)
                   for f in ("pa_decode.cuh", "pa_decode_params.h", "pa_common.cuh")]
+PREFILL_TRAFFIC_FILE = os.path.join(ROOT, "profiles", "prefill_traffic.txt")
+PREFILL_SOURCES = [os.path.join(ROOT, "paged_kv_cache_54_gb300", "csrc", f)
+                   for f in ("pa_prefill.cuh", "pa_prefill.cu", "pa_common.cuh")]
 
 
 def parse():
@@ -81,28 +84,28 @@ def measured_peaks():
         return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}, "fallback"
 
 
-def decode_source_hash() -> str:
+def source_hash(paths=DECODE_SOURCES) -> str:
     h = hashlib.sha256()
-    for p in DECODE_SOURCES:
+    for p in paths:
         with open(p, "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(config: str):
-    """DRAM bytes per decode launch from the committed ncu summary, if it was
-    taken on the current decode source; else None."""
+def recorded_traffic(key: str, path: str = TRAFFIC_FILE, sources=DECODE_SOURCES):
+    """DRAM bytes per launch of a kernel from a committed ncu summary, if it
+    was taken on the kernel's current source; else None."""
     try:
-        lines = open(TRAFFIC_FILE).read().splitlines()
+        lines = open(path).read().splitlines()
     except OSError:
         return None
     src, val = None, None
     for ln in lines:
         if ln.startswith("source_sha:"):
             src = ln.split(":", 1)[1].strip()
-        if ln.startswith(f"bytes_per_launch[{config}]:"):
+        if ln.startswith(f"bytes_per_launch[{key}]:"):
             val = float(ln.split(":", 1)[1].strip())
-    if src != decode_source_hash():
+    if src != source_hash(sources):
         return None
     return val
 
@@ -874,7 +877,8 @@ def run_prefill(args, rank, world, local):
                      "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
                      "frac": round(achieved / peak, 4) if peak else None,
                      "peak_kind": f"{kind} dense bf16 (cuBLAS, burst)",
-                     "traffic": None, "avg_launch_ms": round(pf * 1e3, 4),
+                     "traffic": recorded_traffic(cdt, PREFILL_TRAFFIC_FILE, PREFILL_SOURCES),
+                     "avg_launch_ms": round(pf * 1e3, 4),
                      "algorithmic_flops_per_launch": flops},
         "e2e": {"value": round(flops / e2e_t / 1e12, 2), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": int(q.numel() * 2 + k_new.numel() * 4),
