@@ -211,6 +211,40 @@ def test_shared_prefix_suffix_prefill_full_size():
     print(f"sampled rows, max |err| {worst:.2e}")
 
 
+@pytest.mark.parametrize("cache_dtype,k_scale,v_scale", [
+    ("e4m3", 1.0, 1.0),
+    ("int8", tuple(0.02 + 0.004 * h for h in range(8)), tuple(0.035 - 0.003 * h for h in range(8)))])
+def test_shared_prefix_suffix_prefill_full_size_one_byte(cache_dtype, k_scale, v_scale):
+    """The same full-size launch over a one-byte cache (e4m3 with one scale,
+    INT8 with one scale per KV head): the widening warpgroup's path at the
+    size the bench times; sampled rows against the oracle on the
+    dequantised cache."""
+    w = W.make_workload("qwen3-prefix", W.config_seed("qwen3-prefix"), device=G.DEV,
+                        overrides=dict(cache_dtype=cache_dtype, k_scale=k_scale, v_scale=v_scale))
+    q_lens = [int(L) - 1024 for L in w.seq_lens]
+    gen = torch.Generator(device=G.DEV).manual_seed(37)
+    q = torch.randn((sum(q_lens), w.Hq, w.d), generator=gen, device=G.DEV).to(w.q.dtype)
+    out, run = _run(w, q, q_lens)
+    assert int(run.err.item()) == 0
+    got = out.float().cpu().numpy()
+    qv = G.bits_to_f64(G.bits(q), w.q_dtype)
+    rng = np.random.default_rng(5)
+    starts = np.concatenate([[0], np.cumsum(q_lens)])
+    tol = G.tolerance(w)
+    worst = 0.0
+    for _ in range(24):
+        s = int(rng.integers(w.S))
+        j = int(rng.integers(q_lens[s]))
+        hq = int(rng.integers(w.Hq))
+        p = int(w.seq_lens[s]) - q_lens[s] + j
+        K, V = G.logical_kv(w, s, hq // w.G)
+        ref = A.attend(qv[starts[s] + j, hq], K[:p + 1], V[:p + 1], w.scale)[0]
+        e = np.abs(got[starts[s] + j, hq] - ref)
+        worst = max(worst, float(e.max()))
+        assert not (e > np.maximum(tol, G.ulp(ref, w.q_dtype))).any(), (s, j, hq, float(e.max()))
+    print(f"{cache_dtype}: sampled rows, max |err| {worst:.2e}")
+
+
 def test_bad_lengths_and_blocks_are_reported():
     lens = [40, 50]
     w = W.random_case(3, 2, 2, 2, 64, 16, "f16", "f16", lens, device=G.DEV)
