@@ -275,6 +275,9 @@ __global__ void __launch_bounds__(pf_threads(is_byte(KVT)), 1) prefill_kernel(co
   const int pos0 = L - n;                               // position of new token 0
   const int kv_end = pos0 + min(n, (cta + 1) * QC);     // keys 0..kv_end-1 are needed
   const int n_stages = (kv_end + kPfKeys - 1) / kPfKeys;
+  // stages a tile needs: tile 0's rows end QT tokens before tile 1's, so its
+  // products stop a stage earlier unless tile 1 is empty
+  auto tile_stages = [&](int t) { return (pos0 + min(n, cta * QC + (t + 1) * QT) + kPfKeys - 1) / kPfKeys; };
   uint8_t *qs = smem + Lay::Q_OFF;
   uint8_t *stages = smem + Lay::STAGE_OFF;
   uint8_t *codes = smem + Lay::CODE_OFF;
@@ -441,7 +444,8 @@ __global__ void __launch_bounds__(pf_threads(is_byte(KVT)), 1) prefill_kernel(co
         if (r == 0) mbar_arrive(&hdr.q_ready[t]);
         c /= f;
       }
-      for (int i = 0; i < n_stages && ok; ++i) {
+      const int nst = tile_stages(t);
+      for (int i = 0; i < nst && ok; ++i) {
         if (!__all_sync(0xffffffffu, mbar_wait(&hdr.s_full[t][i & 1], (i >> 1) & 1, abort))) {
           ok = false;
           break;
@@ -657,9 +661,10 @@ __global__ void __launch_bounds__(pf_threads(is_byte(KVT)), 1) prefill_kernel(co
           tc_commit(&hdr.s_full[t][i & 1]);
           return true;
         };
+        const int nst = tile_stages(t);
         if (ok) ok = issue_qk(0);
-        for (int i = 0; i < n_stages && ok; ++i) {
-          if (i + 1 < n_stages && !issue_qk(i + 1)) {
+        for (int i = 0; i < nst && ok; ++i) {
+          if (i + 1 < nst && !issue_qk(i + 1)) {
             ok = false;
             break;
           }
@@ -675,7 +680,16 @@ __global__ void __launch_bounds__(pf_threads(is_byte(KVT)), 1) prefill_kernel(co
             tc_mma_f16_ta(tt + 2 * kPfKeys, tt + (i & 1) * kPfKeys + kk * 8, b0 + kk * (2 * NH * kPfAtom >> 4), IDESC_PV,
                           (i > 0 || kk > 0) ? 1u : 0u);
           tc_commit(&hdr.pv_done[t]);
-          if (i + 1 == n_stages) tc_commit(&hdr.o_ready[t]);
+          if (i + 1 == nst) tc_commit(&hdr.o_ready[t]);
+          tc_commit(&hdr.kv_empty[i % NS]);
+        }
+        // stages wholly after this tile's rows: each is released once it has
+        // been filled, so that its slot's phase still needs the other tile
+        for (int i = nst; i < n_stages && ok; ++i) {
+          if (!mbar_wait(&hdr.kv_full[i % NS], (i / NS) & 1, abort)) {
+            ok = false;
+            break;
+          }
           tc_commit(&hdr.kv_empty[i % NS]);
         }
         if (!ok) {
