@@ -22,10 +22,15 @@
 //         rescaling: P entries stay below 256).  P has a buffer per stage
 //         parity, so the next stage's softmax does not wait for this P V.
 //   8     TMA: Q once (one 4-D box per tile and 128-byte half of a row),
-//         then K and V in stages of 64 keys, one box per (block, half), all
-//         with the 128-byte swizzle.  Lane j fetches block-table entry j one
-//         stage ahead and issues block j's boxes, so a stage's copies go out
-//         from several threads at once.
+//         then K and V in stages of 64 keys, one tensor copy per (block,
+//         head) tile that lands it as 8-row x 128-byte swizzled atoms (the
+//         stage layout is described at kv_row_off).  Lane j issues block j's
+//         copies, so a stage's copies go out from several threads at once;
+//         the block-table entries come from two 32-entry windows held one
+//         entry per lane, the next fetched while the current one is in use.
+//         This warp initialises the
+//         barriers and issues Q and the first stage before the set-up
+//         barrier.
 //   9,10  MMA, one warp per tile (one thread of each issues): the tile's S of
 //         the next stage is issued before waiting for this stage's P, so the
 //         tensor cores work on it while the softmax warps work on P (S is
@@ -34,7 +39,12 @@
 //         one tile's P V behind the other tile's S; with one per tile, each
 //         answers its own tile's P at once.  tcgen05.commit signals
 //         completions on mbarriers; a K/V stage is free once both tiles'
-//         P V have completed.
+//         P V have completed.  Tile 0's rows end 64 tokens before tile 1's,
+//         so it runs only the stages its rows reach and releases the others
+//         once they are filled.
+// Epilogue: each softmax thread scales its O row by 1 / l, and the tile's
+// rows go through its q buffer (free once the tile's products are done) so
+// that they leave as whole rows, two rows per warp store.
 // TMEM: all 512 columns (per tile S / P: 2 x 64, O: head_dim); one CTA per
 // SM, five K/V stages in flight.
 //
