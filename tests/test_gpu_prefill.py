@@ -68,6 +68,44 @@ def test_prefill_matches_oracle(dtype, d, bs, group):
     _check(w, out, ref)
 
 
+@pytest.mark.parametrize("bs", [8, 16, 32])
+def test_prefill_long_block_tables(bs):
+    """The producer reads block-table entries from 32-entry windows, the next
+    fetched while the current one is in use: tables of up to 263 entries
+    (several window moves at every block size), ranges that start deep in
+    the table, and one-token and whole-tile ranges."""
+    Hkv, group, d = 2, 2, 128
+    lens, q_lens = [2100, 700, 1025, 64], [70, 3, 130, 64]
+    w = W.random_case(_seed("long", bs), len(lens), Hkv * group, Hkv, d, bs, "bf16", "bf16", lens,
+                      device=G.DEV)
+    gen = torch.Generator(device=G.DEV).manual_seed(_seed("qlong", bs))
+    q = torch.randn((sum(q_lens), Hkv * group, d), generator=gen, device=G.DEV).bfloat16()
+    out, run = _run(w, q, q_lens)
+    assert int(run.err.item()) == 0
+    c = G.oracle_cache(w)
+    ref = A.paged_prefill(G.bits_to_f64(G.bits(q), "bf16"), q_lens, c.k, c.v, "bf16",
+                          w.block_tables, w.seq_lens, w.scale)
+    _check(w, out, ref)
+
+
+@pytest.mark.parametrize("lens,q_lens", [([512, 300], [100, 5]), ([1024, 20], [129, 20])])
+def test_prefill_tables_exactly_one_or_two_windows_wide(lens, q_lens):
+    """Block tables 32 and 64 entries wide (block size 16): the windows' last
+    entries are the table's last, and the fetch of the window after them is
+    skipped."""
+    Hkv, group, d = 2, 4, 128
+    w = W.random_case(_seed("win", lens), len(lens), Hkv * group, Hkv, d, 16, "f16", "f16", lens, device=G.DEV)
+    assert w.block_tables.shape[1] == max(lens) // 16
+    gen = torch.Generator(device=G.DEV).manual_seed(_seed("qwin", lens))
+    q = torch.randn((sum(q_lens), Hkv * group, d), generator=gen, device=G.DEV).half()
+    out, run = _run(w, q, q_lens)
+    assert int(run.err.item()) == 0
+    c = G.oracle_cache(w)
+    ref = A.paged_prefill(G.bits_to_f64(G.bits(q), "f16"), q_lens, c.k, c.v, "f16",
+                          w.block_tables, w.seq_lens, w.scale)
+    _check(w, out, ref)
+
+
 BYTE_CASES = [("e4m3", "bf16"), ("e5m2", "f16"), ("int8", "bf16"), ("int8", "f16"), ("e4m3", "f16")]
 
 
