@@ -28,3 +28,19 @@ def test_reference_arm_prints_one_contract_line():
     import workloads as W
     w = W.make_workload(bench.DEFAULT_CONFIG, W.config_seed(bench.DEFAULT_CONFIG), values=False)
     assert d["config"] == bench.decode_config(w, bench.DEFAULT_CONFIG, W.config_seed(bench.DEFAULT_CONFIG), 1)
+
+
+def test_recorded_traffic_applies_only_to_the_captured_source(tmp_path):
+    """roofline.traffic comes from a committed ncu summary only while the
+    kernel's sources hash to the one it records; otherwise it is null."""
+    import bench
+    src = tmp_path / "kernel.cuh"
+    src.write_text("// kernel v1\n")
+    rec = tmp_path / "traffic.txt"
+    rec.write_text(f"# note\nsource_sha: {bench.source_hash([str(src)])}\nbytes_per_launch[wl]: 12345\n")
+    assert bench.recorded_traffic("wl", str(rec), [str(src)]) == 12345.0
+    assert bench.recorded_traffic("other", str(rec), [str(src)]) is None
+    src.write_text("// kernel v2\n")
+    assert bench.recorded_traffic("wl", str(rec), [str(src)]) is None
+    assert bench.recorded_traffic("wl", str(tmp_path / "missing.txt"), [str(src)]) is None
+
