@@ -2,15 +2,19 @@
 
 A step is one pass of the whole hot path over one batch: the copy-on-write
 block copies (when the workload has any), the cache write of the new tokens,
-and paged decode attention.  The default workload is the Llama-2-7B-shaped
-decode (64 sequences of 512..4096 tokens, 32/32 heads, head_dim 128, fp16,
-block size 16); ``--config`` selects another named workload for profiling.
+and paged decode attention.  The default workload is the largest one that
+fits one GPU: the OPT-13B-shaped long-context beam decode (32 prompts of
+2048..8192 tokens forked into 4 beams = 128 decode rows, 40/40 heads,
+head_dim 128, fp16, block size 32, copy-on-write of each shared partial last
+block); ``--config`` selects another named workload.
 
 Metric: KV bytes read per step (every K and V element of every sequence's
-tokens, counted once per distinct slot) / step time, in GB/s; also
-sequence·layer/s.  Inputs are resident in HBM before timing starts; the KV
-working set (2.4 GB for the default workload) is far larger than L2, so no
-flush is needed between steps.
+tokens, counted once per distinct slot: the unique bytes HBM must supply) /
+step time, in GB/s; also sequence·layer/s and, for the workloads that share
+blocks, the logical bytes the definition reads (``kv_logical_gbs``).  Inputs
+are resident in HBM before timing starts; the KV working set (3.8 GB unique
+for the default workload) is far larger than L2, so no flush is needed
+between steps.
 
 ``--impl reference`` times the CPU oracle (float64 NumPy) on a bounded
 sample of the same workload on the host cores instead.
@@ -35,13 +39,14 @@ sys.path.insert(0, ROOT)
 import workloads as W  # noqa: E402
 
 METRIC = "paged decode attention: KV-read HBM GB/s vs GB300 peak; seq·layer/s"
-DEFAULT_CONFIG = "llama2-7b"
+DEFAULT_CONFIG = "opt13b-beam"
 SMI_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "decode_traffic.txt")
 DECODE_SOURCES = [os.path.join(ROOT, "paged_kv_cache_54_gb300", "csrc", f)
-                  for f in ("pa_decode.cuh", "pa_decode_params.h", "pa_common.cuh")]
+                  for f in ("pa_decode.cuh", "pa_decode_params.h", "pa_common.cuh",
+                            "pa_decode_api.cu", "pa_host.cu")]
 PREFILL_TRAFFIC_FILE = os.path.join(ROOT, "profiles", "prefill_traffic.txt")
 PREFILL_SOURCES = [os.path.join(ROOT, "paged_kv_cache_54_gb300", "csrc", f)
                    for f in ("pa_prefill.cuh", "pa_prefill.cu", "pa_common.cuh")]
@@ -331,6 +336,7 @@ def run_ours(args, rank, world, local):
         "data": "synthetic (seeded N(0,1) K/V/q, seeded lengths and shuffled block pool)",
         "config": decode_config(w, args.config, seed, world),
         "seq_layer_per_s": round(world * w.S / step_t, 1),
+        "kv_logical_gbs": round(job_rate(w.kv_logical_bytes(), world, step_t) / 1e9, 2),
         "gpu_launches": launches_per_step * K,
         "device_error": derr,
         "roofline": {

@@ -223,12 +223,14 @@ PA_API pa_status pa_decode(void *out, const void *q, int32_t q_dtype,
  *   out, q         device [num_q_tokens, num_q_heads, head_dim] of q_dtype:
  *                  the cache dtype for 16-bit caches, PA_F16 or PA_BF16 for
  *                  one-byte ones; num_q_tokens = cu_q_lens[num_seqs].
- *   cu_q_lens      device int32 [num_seqs + 1], non-decreasing, from 0.
+ *   cu_q_lens      device int32 [num_seqs + 1], non-decreasing, from 0;
+ *                  every sequence's rows must lie in [0, num_q_tokens).
  *   max_q_len      host upper bound of n_s, used to size the grid.
  *   block_tables, max_blocks_per_seq, seq_lens  as in pa_decode; each
  *                  n_s <= L_s <= max_blocks_per_seq * block_size.
- * Device checks: a length that breaks these bounds (or n_s > max_q_len)
- * skips the sequence and reports error 3; a block id out of range reads
+ * Device checks: a length that breaks these bounds, n_s > max_q_len, or
+ * rows of a sequence outside [0, num_q_tokens) skip that sequence (nothing
+ * of its output is written) and report error 3; a block id out of range reads
  * block 0 instead and reports error 1; a stalled pipeline reports error 4.
  * Supported set: num_q_heads / kv_heads in {1, 2, 4, 8}; block_size and
  * head_dim as in pa_cache_desc; num_seqs and kv_heads <= 65535.  Needs no

@@ -96,6 +96,8 @@ extern "C" pa_status pa_prefill(void *out, const void *q, int32_t q_dtype, int32
   p.num_blocks = cache->num_blocks;
   p.block_size = cache->block_size;
   p.max_blocks = max_blocks_per_seq;
+  p.num_q_tokens = num_q_tokens;
+  p.max_q_len = max_q_len;
   const bool per_head = byte_codes && cache->k_head_scales != nullptr;
   p.qk_scale_log2 = scale * (byte_codes && !per_head ? cache->k_scale : 1.0f) * 1.4426950408889634f;
   p.v_scale = byte_codes && !per_head ? cache->v_scale : 1.0f;

@@ -78,6 +78,8 @@ struct PrefillParams {
   const int32_t *block_tables;
   const int32_t *seq_lens;
   int num_q_heads, num_kv_heads, num_blocks, block_size, max_blocks;
+  int num_q_tokens;     // rows of q and out: every sequence's rows must lie inside
+  int max_q_len;        // the caller's bound on any sequence's new tokens
   float qk_scale_log2;  // softmax scale * log2(e) (* the per-tensor K scale of a one-byte cache)
   float v_scale;        // per-tensor V scale of a one-byte cache, else 1
   const float *k_head_scale;  // one-byte caches: [num_kv_heads] scales, or null
@@ -272,7 +274,10 @@ __global__ void __launch_bounds__(pf_threads(is_byte(KVT)), 1) prefill_kernel(co
   const int q0 = __ldg(p.cu_q + s);
   const int n = __ldg(p.cu_q + s + 1) - q0;
   const int L = __ldg(p.seq_lens + s);
-  if (n < 0 || L < n || L > p.max_blocks * p.block_size || n > static_cast<int>(gridDim.x) * QC) {
+  // the rows [q0, q0 + n) of q and out must exist: out is written with plain
+  // stores, so a bad cu_q_lens entry skips the sequence instead
+  if (n < 0 || q0 < 0 || n > p.num_q_tokens - q0 || n > p.max_q_len || L < n ||
+      L > p.max_blocks * p.block_size) {
     if (threadIdx.x == 0 && blockIdx.x == 0) record_error(p.err, kErrSeqLen);
     return;
   }

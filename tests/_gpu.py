@@ -165,3 +165,97 @@ def ulp(x, dtype):
 
 def tolerance(w):
     return FP8_TOL if w.cache_dtype in W.BYTE_DTYPES else TOL[w.q_dtype]
+
+
+def _head_values(raw_h, w, scale):
+    """float64 values of one KV head's source rows [L, d] (16-bit patterns) as
+    the cache holds them: encoded with the head's scale and decoded for
+    one-byte caches."""
+    if w.cache_dtype not in W.BYTE_DTYPES:
+        return bits_to_f64(raw_h, w.src_dtype)
+    if w.cache_dtype == "int8":
+        return I8.decode(I8.quantize_bits16(raw_h, w.src_dtype, scale)) * scale
+    return F.decode(F.quantize_bits16(raw_h, w.src_dtype, scale, w.cache_dtype), w.cache_dtype) * scale
+
+
+def _logical_raw(w, s):
+    """16-bit patterns [Hkv, L, d] of sequence s's K and V input rows in
+    position order."""
+    rows = w.token_rows(s)
+    ctx_idx = [i for k, i in rows if k == "ctx"]
+    new_idx = [i for k, i in rows if k == "new"]
+    out = []
+    for src_ctx, src_new in ((w.ctx_k, w.new_k), (w.ctx_v, w.new_v)):
+        parts = []
+        if ctx_idx:
+            parts.append(src_ctx[torch.tensor(ctx_idx, device=src_ctx.device)])
+        if new_idx:
+            parts.append(src_new[torch.tensor(new_idx, device=src_new.device)])
+        if parts:
+            out.append(bits(torch.cat(parts).transpose(0, 1)))
+        else:
+            out.append(np.zeros((w.Hkv, 0, w.d), np.uint16))
+    return out
+
+
+def oracle_all_rows(w, threads=None):
+    """Oracle output for every (s, hq), float64 [S, Hq, d], from each
+    sequence's logical tokens (its input rows in position order: independent
+    of the block tables and of the device caches).  Sequences run on a thread
+    pool; each one is the plain ``attend`` of its query group over its
+    tokens."""
+    import os
+    from concurrent.futures import ThreadPoolExecutor
+    q = q_values(w)
+    res = np.empty((w.S, w.Hq, w.d), dtype=np.float64)
+
+    def one(s):
+        rk, rv = _logical_raw(w, s)
+        for h in range(w.Hkv):
+            K = _head_values(rk[h], w, head_scale(w.k_scale, h))
+            V = _head_values(rv[h], w, head_scale(w.v_scale, h))
+            hs = slice(h * w.G, (h + 1) * w.G)
+            res[s, hs] = A.attend(q[s, hs], K, V, w.scale)
+
+    n = threads or min(16, len(os.sched_getaffinity(0)))
+    with ThreadPoolExecutor(n) as ex:
+        list(ex.map(one, range(w.S)))
+    return res
+
+
+def check_written_slots(w, kc, vc, chunk=8192):
+    """Every slot the set-up and the step wrote holds the oracle's code of its
+    source row, bit for bit (rows taken in chunks to bound host memory).
+    Returns the number of slots checked."""
+    new_set = set(int(x) for x in w.new_slots)
+    checked = 0
+    for src_k, src_v, slots, skip in ((w.ctx_k, w.ctx_v, w.ctx_slots, new_set),
+                                      (w.new_k, w.new_v, w.new_slots, set())):
+        for a in range(0, len(slots), chunk):
+            sl = np.asarray(slots[a:a + chunk], dtype=np.int64)
+            keep = np.array([x >= 0 and int(x) not in skip for x in sl], dtype=bool)
+            if not keep.any():
+                continue
+            idx = torch.from_numpy(np.arange(a, a + len(sl))[keep]).to(src_k.device)
+            blk = torch.from_numpy(sl[keep] // w.bs).to(kc.device)
+            off = torch.from_numpy(sl[keep] % w.bs).to(kc.device)
+            for src, cache, which in ((src_k, kc, "k"), (src_v, vc, "v")):
+                want = encode_rows(w, bits(src[idx]), which)
+                got = bits(cache[blk, :, off, :])
+                np.testing.assert_array_equal(got, want)
+            checked += int(keep.sum())
+    return checked
+
+
+def permuted_caches(kc, vc, block_tables, seed):
+    """The same cache contents under a seeded permutation pi of the physical
+    blocks: block b moves to pi[b] and every table entry follows it."""
+    nb = kc.shape[0]
+    pi = np.random.default_rng(seed).permutation(nb)
+    pi_t = torch.from_numpy(pi).to(kc.device)
+    kc2, vc2 = torch.empty_like(kc), torch.empty_like(vc)
+    kc2[pi_t] = kc
+    vc2[pi_t] = vc
+    bt = np.asarray(block_tables)
+    bt2 = np.where((bt >= 0) & (bt < nb), pi[np.clip(bt, 0, nb - 1)], bt).astype(np.int32)
+    return kc2, vc2, bt2

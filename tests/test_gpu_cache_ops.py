@@ -4,6 +4,7 @@ import pytest
 import torch
 
 import workloads as W
+from oracle.cache import PagedKVCache
 from tests import _gpu as G
 
 pytestmark = pytest.mark.gpu
@@ -107,14 +108,13 @@ def test_copy_blocks_bit_exact(cache_dtype, bs):
     rng = np.random.default_rng(bs)
     perm = rng.permutation(nb)
     pairs = np.stack([perm[:12], perm[12:24]], axis=1)      # dst never a src
-    ref_k, ref_v = G.bits(kc).copy(), G.bits(vc).copy()
-    for s, t in pairs:
-        ref_k[t] = ref_k[s]
-        ref_v[t] = ref_v[s]
+    ref = PagedKVCache(nb, H, bs, d, cache_dtype, fill_nan=False)   # the oracle's copy
+    ref.k[:], ref.v[:] = G.bits(kc), G.bits(vc)
+    ref.copy_blocks(pairs)
     pa.pa_copy_blocks(kc, vc, torch.from_numpy(pairs).to(G.DEV), cache_dtype=cache_dtype)
     torch.cuda.synchronize()
-    np.testing.assert_array_equal(G.bits(kc), ref_k)
-    np.testing.assert_array_equal(G.bits(vc), ref_v)
+    np.testing.assert_array_equal(G.bits(kc), ref.k)
+    np.testing.assert_array_equal(G.bits(vc), ref.v)
 
 
 def test_out_of_range_slot_and_pair_are_reported():

@@ -309,6 +309,45 @@ def test_bad_lengths_and_blocks_are_reported():
     assert int(err.item()) == 1
 
 
+def test_rows_outside_q_are_refused_and_out_is_not_overrun():
+    """cu_q_lens entries that name rows outside q/out, or a sequence with more
+    new tokens than max_q_len, skip that sequence with error 3; nothing past
+    ``out`` is written (a guard region follows it in the same buffer)."""
+    lens = [40, 50]
+    w = W.random_case(4, 2, 2, 2, 64, 16, "f16", "f16", lens, device=G.DEV)
+    run = G.GpuRun(w).setup()
+    run.step()
+    q = torch.randn((60, 2, 64), device=G.DEV).half()
+    buf = torch.full((60 + 300, 2, 64), 7.0, dtype=torch.float16, device=G.DEV)
+    out = buf[:60]
+    out.zero_()
+    sl = torch.tensor([40, 50], dtype=torch.int32, device=G.DEV)
+
+    def call(cu, max_q_len):
+        err = torch.zeros(1, dtype=torch.int32, device=G.DEV)
+        pa.pa_prefill(out, q, torch.tensor(cu, dtype=torch.int32, device=G.DEV), run.kc, run.vc,
+                      run.bt, sl, max_q_len, w.scale, device_error=err)
+        torch.cuda.synchronize()
+        return int(err.item())
+
+    # the second sequence's rows 10..309 run 250 rows past the end of q and out
+    assert call([0, 10, 310], 300) == 3
+    assert torch.isfinite(out[:10].float()).all() and torch.all(out[10:] == 0)
+    assert torch.all(buf[60:] == 7.0)
+    # a negative start
+    out.zero_()
+    assert call([-20, 10, 60], 50) == 3
+    assert torch.all(out[:10] == 0) and torch.isfinite(out[10:].float()).all()
+    assert torch.all(buf[60:] == 7.0)
+    # 50 new tokens against a declared max_q_len of 20 (the grid still covers
+    # them: its CTAs take 256 / G tokens each)
+    out.zero_()
+    assert call([0, 10, 60], 20) == 3
+    assert torch.isfinite(out[:10].float()).all() and torch.all(out[10:] == 0)
+    # and the same call within bounds reports nothing
+    assert call([0, 10, 60], 50) == 0
+
+
 def test_unsupported_inputs_are_refused_on_the_host():
     import ctypes
     kc = torch.zeros((4, 2, 16, 64), dtype=torch.float16, device=G.DEV)
