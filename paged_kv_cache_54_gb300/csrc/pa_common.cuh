@@ -217,21 +217,55 @@ __device__ __forceinline__ void bulk_g2s(void *smem_dst, const void *gmem_src, u
 // Tiled TMA load of one tile of a 2-D ([rows, 128 B]) or 3-D ([rows, 2, 128 B])
 // tensor view, rows [row0, row0 + box rows), completing on the mbarrier's
 // transaction count.  The tensor map lives in the kernel's parameter space.
+// L2 eviction priorities.  The decode streams each K/V tile through L2 once
+// (evict first), so the split-K partials it writes stay in L2 until the
+// merge reads them (evict last).
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
+// One (block, head) tile of a cache by tiled TMA: rows [row0, row0 + box)
+// of the [rows, 128 B] (2-D) or [rows, 2, 128 B] (3-D) view, with an L2
+// cache policy.
 template <bool kThreeD>
-__device__ __forceinline__ void tma_load_tile(void *smem_dst, const CUtensorMap *map, int row0, uint64_t *bar) {
+__device__ __forceinline__ void tma_load_tile(void *smem_dst, const CUtensorMap *map, int row0, uint64_t *bar,
+                                              uint64_t policy) {
   if constexpr (kThreeD) {
     asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_addr(smem_dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(0), "r"(row0), "r"(smem_addr(bar))
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_addr(smem_dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(0), "r"(row0), "r"(smem_addr(bar)), "l"(policy)
         : "memory");
   } else {
     asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_addr(smem_dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(row0), "r"(smem_addr(bar))
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_addr(smem_dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(row0), "r"(smem_addr(bar)), "l"(policy)
         : "memory");
   }
+}
+
+// bulk_g2s with an L2 cache policy
+__device__ __forceinline__ void bulk_g2s_hint(void *smem_dst, const void *gmem_src, uint32_t bytes, uint64_t *bar,
+                                              uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+          smem_addr(smem_dst)),
+      "l"(gmem_src), "r"(bytes), "r"(smem_addr(bar)), "l"(policy)
+      : "memory");
+}
+
+// two floats to global memory with an L2 cache policy (8-byte aligned)
+__device__ __forceinline__ void st_global_f2_hint(float *addr, float a, float b, uint64_t policy) {
+  asm volatile("st.global.L2::cache_hint.v2.f32 [%0], {%1, %2}, %3;" ::"l"(addr), "f"(a), "f"(b), "l"(policy)
+               : "memory");
 }
 
 // Tiled TMA load of the 2-D box at (x, y) (x in elements, a multiple of 16

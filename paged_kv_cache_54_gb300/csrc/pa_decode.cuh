@@ -137,53 +137,24 @@ __device__ __forceinline__ int block_exclusive_scan(int x, int *warp_tot, int *t
   return ex;
 }
 
-// Rows s and s-1 of the block table agree over partition q (bpp entries).
-// 16-byte loads when both row segments are aligned, else eight scalar loads
-// at a time; either way a mismatch usually costs one round trip.
-__device__ __forceinline__ bool same_blocks(const DecodeParams &p, int s, int q, int bpp) {
-  const int32_t *a = p.block_tables + static_cast<size_t>(s) * p.max_blocks + static_cast<size_t>(q) * bpp;
-  const int32_t *b = a - p.max_blocks;
-  if ((bpp & 3) == 0 && ((reinterpret_cast<uintptr_t>(a) | reinterpret_cast<uintptr_t>(b)) & 15) == 0) {
-    for (int j0 = 0; j0 < bpp; j0 += 32) {
-      int4 x[8], y[8];
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const bool in = j0 + 4 * u < bpp;
-        x[u] = in ? __ldg(reinterpret_cast<const int4 *>(a + j0) + u) : make_int4(0, 0, 0, 0);
-        y[u] = in ? __ldg(reinterpret_cast<const int4 *>(b + j0) + u) : make_int4(0, 0, 0, 0);
-      }
-      bool eq = true;
-#pragma unroll
-      for (int u = 0; u < 8; ++u)
-        eq = eq && x[u].x == y[u].x && x[u].y == y[u].y && x[u].z == y[u].z && x[u].w == y[u].w;
-      if (!eq) return false;
-    }
-    return true;
-  }
-  for (int j0 = 0; j0 < bpp; j0 += 8) {
-    int x[8], y[8];
-#pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const bool in = j0 + u < bpp;
-      x[u] = in ? __ldg(a + j0 + u) : 0;
-      y[u] = in ? __ldg(b + j0 + u) : 0;
-    }
-    bool eq = true;
-#pragma unroll
-    for (int u = 0; u < 8; ++u) eq = eq && (x[u] == y[u]);
-    if (!eq) return false;
-  }
-  return true;
-}
-
 // Plan tables live in shared memory when they fit, else in the workspace.
 constexpr int kPlanSmemSeqs = 4096;
 constexpr int kPlanSmemPairs = 12288;
 
+// Last index i in [0, n) with a[i] <= x (a non-decreasing, a[0] <= x).
+__device__ __forceinline__ int upper_index(const int *a, int n, int x) {
+  int lo = 0, hi = n - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (a[mid] <= x) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
 __global__ void __launch_bounds__(1024) plan_kernel(const __grid_constant__ DecodeParams p) {
   __shared__ int warp_tot[32];
   __shared__ int base;
-  __shared__ int s_len[kPlanSmemSeqs];
+  __shared__ int s_len[kPlanSmemSeqs + 1];
   __shared__ int s_off[kPlanSmemSeqs + 1];
   __shared__ uint8_t s_join[kPlanSmemPairs];
   const int tid = threadIdx.x;
@@ -198,14 +169,12 @@ __global__ void __launch_bounds__(1024) plan_kernel(const __grid_constant__ Deco
   // in shared memory, else read from the pair list in the workspace
   auto pair_at = [&](int k) -> int2 {
     if (!in_smem) return p.plan_pairs[k];
-    int lo = 0, hi = S - 1;  // the last s with off[s] <= k
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (off[mid] <= k) lo = mid; else hi = mid - 1;
-    }
-    return make_int2(lo, k - off[lo]);
+    const int s = upper_index(off, S, k);
+    return make_int2(s, k - off[s]);
   };
-  // A) lengths, partition counts, and the (s, q) pair list in sequence order
+  // A) lengths, partition counts, and the (s, q) pair list in sequence order.
+  //    Without batching (kmax == 1) every pair is an item of its own and is
+  //    written here.
   if (tid == 0) base = 0;
   __syncthreads();
   for (int b0 = 0; b0 < S; b0 += 1024) {
@@ -222,8 +191,11 @@ __global__ void __launch_bounds__(1024) plan_kernel(const __grid_constant__ Deco
     if (s < S) {
       const int o = b + ex;
       off[s] = o;
-      if (!in_smem)
+      if (p.kmax == 1) {
+        for (int q = 0; q < nP; ++q) p.items[o + q] = make_int4(s, q, 1, 0);
+      } else if (!in_smem) {
         for (int q = 0; q < nP; ++q) p.plan_pairs[o + q] = make_int2(s, q);
+      }
     }
     __syncthreads();     // ... before thread 0 advances it
     if (tid == 0) base = b + tot;
@@ -231,21 +203,102 @@ __global__ void __launch_bounds__(1024) plan_kernel(const __grid_constant__ Deco
   }
   const int npairs = base;
   if (tid == 0) off[S] = npairs;
+  if (p.kmax == 1) {
+    if (tid == 0) {
+      p.work[1] = npairs;
+      p.work[0] = 0;
+    }
+    return;
+  }
   uint8_t *join = npairs <= kPlanSmemPairs ? s_join : p.plan_join;
   __syncthreads();
-  // B) does pair (s, q) join the item of (s-1, q)?  One thread per pair.
-  if (p.kmax > 1) {
-    for (int k = tid; k < npairs; k += 1024) {
-      const int2 sq = pair_at(k);
-      bool jn = false;
-      if (sq.x % p.kmax != 0) {
-        const int need = (sq.y + 1) * P;
-        if (len[sq.x] >= need && len[sq.x - 1] >= need) jn = same_blocks(p, sq.x, sq.y, bpp);
-      }
-      join[k] = jn ? 1 : 0;
+  // B) does pair (s, q) join the item of (s-1, q)?  It may when s is not at
+  //    a multiple of kmax and partition q is full in both sequences; it does
+  //    when their block-table rows agree over the partition.
+  //  B1: the candidates, one thread per pair
+  for (int k = tid; k < npairs; k += 1024) {
+    const int2 sq = pair_at(k);
+    const int need = (sq.y + 1) * P;
+    join[k] = (sq.x % p.kmax != 0 && len[sq.x] >= need && len[sq.x - 1] >= need) ? 1 : 0;
+  }
+  //  B2: the rows compared in chunks of up to 4 entries (a chunk never
+  //      straddles two partitions), consecutive threads on consecutive
+  //      chunks of one row pair (coalesced); a mismatch clears the candidate
+  //      of its partition.  Sequence s has nfull(s) * cpp chunks, nfull(s)
+  //      being the partitions full in s and in s-1.  The chunk offsets
+  //      replace the lengths, which are no longer needed.
+  const int cpp = (bpp + 3) >> 2;  // chunks per partition
+  int my_ch = 0;
+  if (tid < S && tid > 0 && tid % p.kmax != 0) my_ch = (min(len[tid], len[tid - 1]) / P) * cpp;
+  __syncthreads();  // the first 1024 lengths read before the offsets overwrite them
+  int *choff = len;
+  if (tid == 0) base = 0;
+  __syncthreads();
+  for (int b0 = 0; b0 < S; b0 += 1024) {
+    const int s = b0 + tid;
+    int c = 0;
+    if (b0 == 0) {
+      c = my_ch;
+    } else if (s < S && s % p.kmax != 0) {
+      // sequences past the first 1024 read their lengths again
+      const int L = clamp_len(__ldg(p.seq_lens + s), p.len_cap, nullptr);
+      const int Lp = clamp_len(__ldg(p.seq_lens + s - 1), p.len_cap, nullptr);
+      c = (min(L, Lp) / P) * cpp;
     }
+    int tot;
+    const int ex = block_exclusive_scan(c, warp_tot, &tot);
+    const int b = base;
+    if (s < S) choff[s] = b + ex;
+    __syncthreads();
+    if (tid == 0) base = b + tot;
     __syncthreads();
   }
+  const int nch = base;
+  // 16-byte loads when every chunk is four aligned entries
+  const bool vec = (bpp & 3) == 0 && (p.max_blocks & 3) == 0 &&
+                   (reinterpret_cast<uintptr_t>(p.block_tables) & 15) == 0;
+  // Each thread takes chunks tid, tid + 1024, ... four at a time with all
+  // their loads in flight.
+  for (int u0 = 0; u0 < nch; u0 += 4 * 1024) {
+    int4 x[4], y[4];
+    int js[4], jq[4], jn[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int u = u0 + i * 1024 + tid;
+      js[i] = -1;
+      jq[i] = jn[i] = 0;
+      x[i] = y[i] = make_int4(0, 0, 0, 0);
+      if (u < nch) {
+        const int sq = upper_index(choff, S, u);
+        const int c = u - choff[sq];
+        const int q = c / cpp;
+        const int e0 = q * bpp + (c - q * cpp) * 4;  // first entry of the chunk
+        const int nv = min(4, (q + 1) * bpp - e0);   // entries of the chunk (1..4)
+        js[i] = sq;
+        jq[i] = q;
+        jn[i] = nv;
+        const int32_t *ra = p.block_tables + static_cast<size_t>(sq) * p.max_blocks + e0;
+        const int32_t *rb = ra - p.max_blocks;
+        if (vec) {
+          x[i] = __ldg(reinterpret_cast<const int4 *>(ra));
+          y[i] = __ldg(reinterpret_cast<const int4 *>(rb));
+        } else {
+          x[i] = make_int4(__ldg(ra), nv > 1 ? __ldg(ra + 1) : 0, nv > 2 ? __ldg(ra + 2) : 0,
+                           nv > 3 ? __ldg(ra + 3) : 0);
+          y[i] = make_int4(__ldg(rb), nv > 1 ? __ldg(rb + 1) : 0, nv > 2 ? __ldg(rb + 2) : 0,
+                           nv > 3 ? __ldg(rb + 3) : 0);
+        }
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      if (js[i] < 0) continue;
+      const bool differ = (x[i].x != y[i].x) || (jn[i] > 1 && x[i].y != y[i].y) ||
+                          (jn[i] > 2 && x[i].z != y[i].z) || (jn[i] > 3 && x[i].w != y[i].w);
+      if (differ) join[off[js[i]] + jq[i]] = 0;  // several threads may clear one flag
+    }
+  }
+  __syncthreads();
   // C) every pair that does not join leads an item of itself and the pairs
   //    (s+1, q), (s+2, q), ... that join it; items keep sequence order
   if (tid == 0) base = 0;
@@ -256,8 +309,8 @@ __global__ void __launch_bounds__(1024) plan_kernel(const __grid_constant__ Deco
     int2 sq = make_int2(0, 0);
     if (k < npairs) {
       sq = pair_at(k);
-      lead = (p.kmax > 1) ? (join[k] == 0) : 1;
-      if (lead && p.kmax > 1) {
+      lead = join[k] == 0;
+      if (lead) {
         for (int j = 1; j < p.kmax && sq.x + j < S; ++j) {
           const int idx = off[sq.x + j] + sq.y;
           if (idx >= off[sq.x + j + 1] || join[idx] == 0) break;
@@ -282,8 +335,17 @@ __global__ void __launch_bounds__(1024) plan_kernel(const __grid_constant__ Deco
 // ----------------------------------------------------------------------------
 // merge: combine the partials of sequences split into several partitions
 // ----------------------------------------------------------------------------
+// One warp per (sequence, query head), eight to a CTA:
+//   out = sum_q w_q o_q / sum_q w_q,  w_q = exp2(m_q - M) l_q,  M = max_q m_q
+// (the flash-decoding reduction; o_q is normalised by its own l_q).  Lane j
+// holds the weights of partitions j and j + 32 (longer sequences take
+// windows of 64), then reads its D / 32 columns of 16 partial rows at a
+// time, all in flight.
+constexpr int kMergeThreads = 256;
+
 template <int QT, int D>
-__global__ void __launch_bounds__(256) merge_kernel(const __grid_constant__ DecodeParams p) {
+__global__ void __launch_bounds__(kMergeThreads) merge_kernel(const __grid_constant__ DecodeParams p) {
+  constexpr int E = D / 32;  // columns per lane
   const int lane = threadIdx.x & 31;
   const long long gw = (blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x) >> 5;
   if (gw >= static_cast<long long>(p.num_seqs) * p.num_q_heads) return;
@@ -293,62 +355,72 @@ __global__ void __launch_bounds__(256) merge_kernel(const __grid_constant__ Deco
   // before waiting for the decode grid, whose partials come after
   const int L = min(max(__ldg(p.seq_lens + s), 0), p.len_cap);
   const int nP = max(1, (L + p.partition_size - 1) / p.partition_size);
-  if (nP <= 1) return;
-  grid_dependency_wait();  // partials of the decode grid
-  const size_t base = static_cast<size_t>(s) * p.max_parts * p.num_q_heads + hq;
-  // pass 1: the largest partition maximum (lane q reads partition q, q + 32, ...)
+  if (nP <= 1) return;  // the decode wrote this sequence's output itself
+  grid_dependency_wait();
+  const size_t qstride = static_cast<size_t>(p.num_q_heads);
+  const size_t base = static_cast<size_t>(s) * p.max_parts * qstride + hq;
+  const float2 *ml = p.part_ml + base;  // partition q at ml[q * num_q_heads]
   float M = -INFINITY;
-  for (int q = lane; q < nP; q += 32) M = fmaxf(M, p.part_ml[base + static_cast<size_t>(q) * p.num_q_heads].x);
+  float2 a0 = make_float2(-INFINITY, 0.f), a1 = make_float2(-INFINITY, 0.f);
+  if (nP <= 64) {
+    if (lane < nP) a0 = ml[lane * qstride];
+    if (lane + 32 < nP) a1 = ml[(lane + 32) * qstride];
+    M = fmaxf(a0.x, a1.x);
+  } else {
+    for (int q = lane; q < nP; q += 32) M = fmaxf(M, ml[q * qstride].x);
+  }
 #pragma unroll
   for (int o = 16; o; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-  // pass 2: weights w_q = exp2(m_q - M) * l_q, 32 partitions per round;
-  // every lane then accumulates its head_dim columns of each partition
-  constexpr int E = D / 32;
   float acc[E];
 #pragma unroll
   for (int e = 0; e < E; ++e) acc[e] = 0.f;
   float den = 0.f;
-  for (int q0 = 0; q0 < nP; q0 += 32) {
-    const int q = q0 + lane;
-    float w = 0.f;
-    if (q < nP) {
-      const float2 ml = p.part_ml[base + static_cast<size_t>(q) * p.num_q_heads];
-      w = (ml.y > 0.f) ? exp2f(ml.x - M) * ml.y : 0.f;
+  for (int w0 = 0; w0 < nP; w0 += 64) {
+    if (w0 > 0) {
+      a0 = w0 + lane < nP ? ml[(w0 + lane) * qstride] : make_float2(-INFINITY, 0.f);
+      a1 = w0 + lane + 32 < nP ? ml[(w0 + lane + 32) * qstride] : make_float2(-INFINITY, 0.f);
     }
-    float ws = w;
+    const float wt0 = a0.y > 0.f ? exp2f(a0.x - M) * a0.y : 0.f;
+    const float wt1 = a1.y > 0.f ? exp2f(a1.x - M) * a1.y : 0.f;
+    float ws = wt0 + wt1;
 #pragma unroll
     for (int o = 16; o; o >>= 1) ws += __shfl_xor_sync(0xffffffffu, ws, o);
     den += ws;
-    const int cnt = min(32, nP - q0);
-    // eight partitions per batch: their loads are all in flight before the FMAs
-    for (int k0 = 0; k0 < cnt; k0 += 8) {
-      float v[8][E];
+    const int cnt = min(64, nP - w0);
+    for (int k0 = 0; k0 < cnt; k0 += 16) {
+      float v[16][E];
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        if (k0 + u < cnt) {
-          const float *po = p.part_o + (base + static_cast<size_t>(q0 + k0 + u) * p.num_q_heads) * D + lane * E;
-#pragma unroll
-          for (int e = 0; e < E; e += 2) {
-            const float2 t = *reinterpret_cast<const float2 *>(po + e);
-            v[u][e] = t.x;
-            v[u][e + 1] = t.y;
+      for (int j = 0; j < 16; ++j) {
+        if (k0 + j < cnt) {
+          const float *po = p.part_o + (base + static_cast<size_t>(w0 + k0 + j) * qstride) * D + lane * E;
+          if constexpr (E == 4) {
+            const float4 t = *reinterpret_cast<const float4 *>(po);
+            v[j][0] = t.x; v[j][1] = t.y; v[j][2] = t.z; v[j][3] = t.w;
+          } else {
+            const float2 t = *reinterpret_cast<const float2 *>(po);
+            v[j][0] = t.x; v[j][1] = t.y;
           }
         }
       }
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const float wk = __shfl_sync(0xffffffffu, w, (k0 + u) & 31);
-        if (k0 + u < cnt) {
+      for (int j = 0; j < 16; ++j) {
+        const int k = k0 + j;  // warp-uniform
+        if (k < cnt) {
+          const float wk = __shfl_sync(0xffffffffu, k < 32 ? wt0 : wt1, k & 31);
 #pragma unroll
-          for (int e = 0; e < E; ++e) acc[e] = fmaf(wk, v[u][e], acc[e]);
+          for (int e = 0; e < E; ++e) acc[e] = fmaf(wk, v[j][e], acc[e]);
         }
       }
     }
   }
   const float inv = den > 0.f ? 1.f / den : 0.f;
   uint16_t *out = static_cast<uint16_t *>(p.out) + (static_cast<size_t>(s) * p.num_q_heads + hq) * D + lane * E;
-#pragma unroll
-  for (int e = 0; e < E; ++e) out[e] = float_to_storage16<QT>(acc[e] * inv);
+  if constexpr (E == 4) {
+    *reinterpret_cast<uint2 *>(out) = make_uint2(pack2_rn<QT>(acc[0] * inv, acc[1] * inv),
+                                                 pack2_rn<QT>(acc[2] * inv, acc[3] * inv));
+  } else {
+    *reinterpret_cast<uint32_t *>(out) = pack2_rn<QT>(acc[0] * inv, acc[1] * inv);
+  }
 }
 
 // ----------------------------------------------------------------------------
@@ -370,6 +442,7 @@ __device__ __forceinline__ void producer_warp(const DecodeParams &p, uint8_t *sm
   const int n_items = p.work[1];
   const int total = n_items * p.num_kv_heads;
   constexpr uint32_t qbytes = G * D * 2;  // query rows of one sequence's group
+  const uint64_t pol_kv = l2_policy_evict_first();  // each tile passes through L2 once
 
   auto load_table = [&](int w, int4 pr, int L, int (&ph)[4]) {
     const int nblk = (w < total) ? (min(max(L, 0), p.len_cap) + bs - 1) / bs : 0;
@@ -466,12 +539,14 @@ __device__ __forceinline__ void producer_warp(const DecodeParams &p, uint8_t *sm
         if (tiled) {
           // tile rows [row0, row0 + bs) of the [num_blocks * kv_heads * bs, d] view
           const int row0 = (b * p.num_kv_heads + h) * bs;
-          tma_load_tile<(D * elt_bytes(KV) > 128)>(sb + p.k_off + lane * tile, &p.tmap_k, row0, &hdr.full[stage]);
-          tma_load_tile<(D * elt_bytes(KV) > 128)>(sb + p.v_off + lane * tile, &p.tmap_v, row0, &hdr.full[stage]);
+          tma_load_tile<(D * elt_bytes(KV) > 128)>(sb + p.k_off + lane * tile, &p.tmap_k, row0, &hdr.full[stage],
+                                                   pol_kv);
+          tma_load_tile<(D * elt_bytes(KV) > 128)>(sb + p.v_off + lane * tile, &p.tmap_v, row0, &hdr.full[stage],
+                                                   pol_kv);
         } else {
           const size_t off = (static_cast<size_t>(b) * p.num_kv_heads + h) * tile;
-          bulk_g2s(sb + p.k_off + lane * tile, p.k_cache + off, tile, &hdr.full[stage]);
-          bulk_g2s(sb + p.v_off + lane * tile, p.v_cache + off, tile, &hdr.full[stage]);
+          bulk_g2s_hint(sb + p.k_off + lane * tile, p.k_cache + off, tile, &hdr.full[stage], pol_kv);
+          bulk_g2s_hint(sb + p.v_off + lane * tile, p.v_cache + off, tile, &hdr.full[stage], pol_kv);
         }
       }
       if (st == 0 && lane >= 24 && lane - 24 < kseq) {  // one q copy per sequence of the item
@@ -506,6 +581,7 @@ __device__ __forceinline__ void producer_warp(const DecodeParams &p, uint8_t *sm
       ok = false;
     }
   }
+
   if (!ok) {
     if (lane == 0) {
       record_error(p.err, kErrTimeout);
@@ -1050,7 +1126,7 @@ __device__ __forceinline__ void combine_item(const DecodeParams &p, const StageI
     const int Lj = min(max(__ldg(p.seq_lens + sj), 0), p.len_cap);
     if ((Lj + P - 1) / P > 1) {
       const size_t idx = (static_cast<size_t>(sj) * p.max_parts + inf.p) * p.num_q_heads + inf.h * G + j % G;
-      p.part_ml[idx] = make_float2(M, wsum);
+      st_global_f2_hint(reinterpret_cast<float *>(p.part_ml + idx), M, wsum, l2_policy_evict_last());
     }
   }
   mbar_arrive(bar);
@@ -1078,7 +1154,7 @@ __device__ __forceinline__ void combine_item(const DecodeParams &p, const StageI
       *out = pack2_rn<QT>(a0, a1);
     } else {
       const size_t idx = (static_cast<size_t>(sj) * p.max_parts + inf.p) * p.num_q_heads + hq;
-      *reinterpret_cast<float2 *>(p.part_o + idx * D + dd) = make_float2(a0, a1);
+      st_global_f2_hint(p.part_o + idx * D + dd, a0, a1, l2_policy_evict_last());  // kept for the merge
     }
   }
 }
@@ -1326,8 +1402,8 @@ pa_status launch_decode(DecodeParams p, const DeviceInfo &dev, cudaStream_t stre
   if (e != cudaSuccess) return cuda_fail(e);
   if (p.max_parts > 1) {
     const long long warps = static_cast<long long>(p.num_seqs) * p.num_q_heads;
-    cfg.gridDim = dim3(static_cast<unsigned>((warps * 32 + 255) / 256));
-    cfg.blockDim = dim3(256);
+    cfg.gridDim = dim3(static_cast<unsigned>((warps * 32 + kMergeThreads - 1) / kMergeThreads));
+    cfg.blockDim = dim3(kMergeThreads);
     cfg.dynamicSmemBytes = 0;
     e = cudaLaunchKernelEx(&cfg, merge_kernel<QT, D>, p);
     if (e != cudaSuccess) return cuda_fail(e);
