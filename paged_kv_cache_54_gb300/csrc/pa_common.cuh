@@ -262,6 +262,13 @@ __device__ __forceinline__ void bulk_g2s_hint(void *smem_dst, const void *gmem_s
       : "memory");
 }
 
+// four floats to global memory with an L2 cache policy (16-byte aligned)
+__device__ __forceinline__ void st_global_f4_hint(float *addr, float4 v, uint64_t policy) {
+  asm volatile("st.global.L2::cache_hint.v4.f32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(addr), "f"(v.x), "f"(v.y),
+               "f"(v.z), "f"(v.w), "l"(policy)
+               : "memory");
+}
+
 // two floats to global memory with an L2 cache policy (8-byte aligned)
 __device__ __forceinline__ void st_global_f2_hint(float *addr, float a, float b, uint64_t policy) {
   asm volatile("st.global.L2::cache_hint.v2.f32 [%0], {%1, %2}, %3;" ::"l"(addr), "f"(a), "f"(b), "l"(policy)

@@ -77,6 +77,22 @@ __device__ __forceinline__ int scr(int row, int d) {
   return row * D + ((((d >> 2) ^ (row >> 1)) & 3) | ((d >> 2) & ~3)) * 4 + (d & 3);
 }
 
+// The combine scratch of consumer warp c is the part of the item's last
+// stage that only warp c read: its 16 K rows, then its 16 V rows (each run
+// contiguous in the linear and in the swizzled layout).  It holds QM rows of
+// D floats, laid out by scr<D>.
+template <int KV, int D>
+struct WarpScratch {
+  static constexpr int REG = 16 * D * elt_bytes(KV);  // bytes of a warp's 16 rows
+  uint8_t *k, *v;
+  __device__ __forceinline__ WarpScratch(uint8_t *stage, const DecodeParams &p, int c)
+      : k(stage + p.k_off + c * REG), v(stage + p.v_off + c * REG) {}
+  __device__ __forceinline__ float *at(int row, int d) const {
+    const int off = scr<D>(row, d) * 4;
+    return reinterpret_cast<float *>(off < REG ? k + off : v + (off - REG));
+  }
+};
+
 __device__ __forceinline__ uint32_t w32(const uint4 &v, int i) {
   return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
 }
@@ -746,7 +762,7 @@ struct SimtState {
     }
   }
 
-  __device__ __forceinline__ void to_scratch(float *so, float *sm, float *sl, int cw, float /*v_scale*/,
+  __device__ __forceinline__ void to_scratch(const WarpScratch<KV, D> &so, float *sm, float *sl, float /*v_scale*/,
                                              int /*ncols*/) {
     const int lane = threadIdx.x & 31;
 #pragma unroll
@@ -754,16 +770,15 @@ struct SimtState {
       float ls = l[g];
 #pragma unroll
       for (int o2 = 1; o2 < 32; o2 <<= 1) ls += __shfl_xor_sync(0xffffffffu, ls, o2);
-      const int row = cw * QS + g;
       if constexpr (EPL == 4) {
-        *reinterpret_cast<float4 *>(so + scr<D>(row, lane * 4)) = make_float4(o[g][0], o[g][1], o[g][2], o[g][3]);
+        *reinterpret_cast<float4 *>(so.at(g, lane * 4)) = make_float4(o[g][0], o[g][1], o[g][2], o[g][3]);
       } else {
 #pragma unroll
-        for (int e = 0; e < EPL; ++e) so[scr<D>(row, lane * EPL + e)] = o[g][e];
+        for (int e = 0; e < EPL; ++e) *so.at(g, lane * EPL + e) = o[g][e];
       }
       if (lane == 0) {
-        sm[cw * QS + g] = m[g];
-        sl[cw * QS + g] = ls;
+        sm[g] = m[g];
+        sl[g] = ls;
       }
     }
   }
@@ -1054,7 +1069,7 @@ struct MmaState {
     (void)v_scale;
   }
 
-  __device__ __forceinline__ void to_scratch(float *so, float *sm, float *sl, int cw, float v_scale,
+  __device__ __forceinline__ void to_scratch(const WarpScratch<KV, D> &so, float *sm, float *sl, float v_scale,
                                              int ncols) {
     const int lane = threadIdx.x & 31;
     const int gq = lane >> 2, tq = lane & 3;
@@ -1077,19 +1092,17 @@ struct MmaState {
         vb[u] = (c < MTILES ? oacc[c % MTILES][1] : oacc[c % MTILES][3]) * v_scale;
       }
       const int d = vcol(gq, c0);
-      if (qa < ncols)
-        *reinterpret_cast<float4 *>(so + scr<D>(cw * QS + qa, d)) = make_float4(va[0], va[1], va[2], va[3]);
-      if (qb2 < ncols)
-        *reinterpret_cast<float4 *>(so + scr<D>(cw * QS + qb2, d)) = make_float4(vb[0], vb[1], vb[2], vb[3]);
+      if (qa < ncols) *reinterpret_cast<float4 *>(so.at(qa, d)) = make_float4(va[0], va[1], va[2], va[3]);
+      if (qb2 < ncols) *reinterpret_cast<float4 *>(so.at(qb2, d)) = make_float4(vb[0], vb[1], vb[2], vb[3]);
     }
     if (gq == 0) {
       if (qa < ncols) {
-        sm[cw * QS + qa] = m2[0];
-        sl[cw * QS + qa] = ls0;
+        sm[qa] = m2[0];
+        sl[qa] = ls0;
       }
       if (qb2 < ncols) {
-        sm[cw * QS + qb2] = m2[1];
-        sl[cw * QS + qb2] = ls1;
+        sm[qb2] = m2[1];
+        sl[qb2] = ls1;
       }
     }
   }
@@ -1099,62 +1112,68 @@ struct MmaState {
 // combine the four consumer warps' states and write the item's result
 // ----------------------------------------------------------------------------
 // Query column j of an item is head h*G + j%G of sequence s + j/G.
-template <int QT, int D, int G, int QM>
-__device__ __forceinline__ void combine_item(const DecodeParams &p, const StageInfo &inf, int ncols,
-                                             const float *so, float *sm, const float *sl, uint64_t *bar,
-                                             uint32_t parity, const volatile int *abort, bool &ok) {
-  const int ct = threadIdx.x - 32;
+// Consumer warp c takes the columns c, c + 4, ...; lanes 0..3 weigh the
+// four warps' states, w_c = exp2(m_c - M) / sum_c exp2(m_c - M) l_c, and
+// every lane then sums its D / 32 columns of the four states.
+template <int KV, int QT, int D, int G, int QM>
+__device__ __forceinline__ void combine_item(const DecodeParams &p, const StageInfo &inf, int ncols, uint8_t *last,
+                                             const float (*sm)[8], const float (*sl)[8]) {
+  constexpr int E = D / 32;  // columns per lane
+  const int cw = (threadIdx.x >> 5) - 1, lane = threadIdx.x & 31;
   const int P = p.partition_size;
-  // 1) per column j: weights w_c = exp2(m_c - M) / sum_c exp2(m_c - M) l_c,
-  //    written over the maxima in place
-  if (ct < ncols) {
-    const int j = ct;
+  for (int j = cw; j < ncols; j += kConsumerWarps) {
     float M = -INFINITY;
 #pragma unroll
-    for (int c = 0; c < kConsumerWarps; ++c) M = fmaxf(M, sm[c * QM + j]);
-    float w[kConsumerWarps], wsum = 0.f;
-#pragma unroll
-    for (int c = 0; c < kConsumerWarps; ++c) {
-      const float mc = sm[c * QM + j];
-      w[c] = (mc == -INFINITY) ? 0.f : exp2f(mc - M);
-      wsum = fmaf(w[c], sl[c * QM + j], wsum);
+    for (int c = 0; c < kConsumerWarps; ++c) M = fmaxf(M, sm[c][j]);
+    float w = 0.f, wl = 0.f;
+    if (lane < kConsumerWarps) {
+      const float mc = sm[lane][j];
+      w = (mc == -INFINITY) ? 0.f : exp2f(mc - M);
+      wl = w * sl[lane][j];
     }
+    wl += __shfl_xor_sync(0xffffffffu, wl, 1);
+    wl += __shfl_xor_sync(0xffffffffu, wl, 2);
+    const float wsum = __shfl_sync(0xffffffffu, wl, 0);
     const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+    float acc[E];
 #pragma unroll
-    for (int c = 0; c < kConsumerWarps; ++c) sm[c * QM + j] = w[c] * inv;
-    const int sj = inf.s + j / G;
-    const int Lj = min(max(__ldg(p.seq_lens + sj), 0), p.len_cap);
-    if ((Lj + P - 1) / P > 1) {
-      const size_t idx = (static_cast<size_t>(sj) * p.max_parts + inf.p) * p.num_q_heads + inf.h * G + j % G;
-      st_global_f2_hint(reinterpret_cast<float *>(p.part_ml + idx), M, wsum, l2_policy_evict_last());
-    }
-  }
-  mbar_arrive(bar);
-  if (!mbar_wait(bar, parity, abort)) {
-    ok = false;
-    return;
-  }
-  // 2) out[j, d] = sum_c w_c * o_c[j, d], two adjacent columns per thread
-  for (int e = 2 * ct; e < ncols * D; e += 2 * kConsumerThreads) {
-    const int j = e / D, dd = e % D;
-    float a0 = 0.f, a1 = 0.f;
+    for (int e = 0; e < E; ++e) acc[e] = 0.f;
 #pragma unroll
     for (int c = 0; c < kConsumerWarps; ++c) {
-      const float wc = sm[c * QM + j];
-      const float2 oc = *reinterpret_cast<const float2 *>(so + scr<D>(c * QM + j, dd));
-      a0 = fmaf(wc, oc.x, a0);
-      a1 = fmaf(wc, oc.y, a1);
+      const float wc = __shfl_sync(0xffffffffu, w, c) * inv;
+      const float *src = WarpScratch<KV, D>(last, p, c).at(j, lane * E);
+      if constexpr (E == 4) {
+        const float4 v = *reinterpret_cast<const float4 *>(src);
+        acc[0] = fmaf(wc, v.x, acc[0]);
+        acc[1] = fmaf(wc, v.y, acc[1]);
+        acc[2] = fmaf(wc, v.z, acc[2]);
+        acc[3] = fmaf(wc, v.w, acc[3]);
+      } else {
+        const float2 v = *reinterpret_cast<const float2 *>(src);
+        acc[0] = fmaf(wc, v.x, acc[0]);
+        acc[1] = fmaf(wc, v.y, acc[1]);
+      }
     }
     const int sj = inf.s + j / G;
     const int hq = inf.h * G + j % G;
     const int Lj = (G == 1 && inf.k == 1) ? inf.L : min(max(__ldg(p.seq_lens + sj), 0), p.len_cap);
     if ((Lj + P - 1) / P <= 1) {
-      uint32_t *out = reinterpret_cast<uint32_t *>(static_cast<uint16_t *>(p.out) +
-                                                   (static_cast<size_t>(sj) * p.num_q_heads + hq) * D + dd);
-      *out = pack2_rn<QT>(a0, a1);
+      uint16_t *out = static_cast<uint16_t *>(p.out) + (static_cast<size_t>(sj) * p.num_q_heads + hq) * D + lane * E;
+      if constexpr (E == 4) {
+        *reinterpret_cast<uint2 *>(out) = make_uint2(pack2_rn<QT>(acc[0], acc[1]), pack2_rn<QT>(acc[2], acc[3]));
+      } else {
+        *reinterpret_cast<uint32_t *>(out) = pack2_rn<QT>(acc[0], acc[1]);
+      }
     } else {
       const size_t idx = (static_cast<size_t>(sj) * p.max_parts + inf.p) * p.num_q_heads + hq;
-      st_global_f2_hint(p.part_o + idx * D + dd, a0, a1, l2_policy_evict_last());  // kept for the merge
+      const uint64_t keep = l2_policy_evict_last();  // the merge reads the partials next
+      float *po = p.part_o + idx * D + lane * E;
+      if constexpr (E == 4) {
+        st_global_f4_hint(po, make_float4(acc[0], acc[1], acc[2], acc[3]), keep);
+      } else {
+        st_global_f2_hint(po, acc[0], acc[1], keep);
+      }
+      if (lane == 0) st_global_f2_hint(reinterpret_cast<float *>(p.part_ml + idx), M, wsum, keep);
     }
   }
 }
@@ -1164,7 +1183,8 @@ __device__ __forceinline__ void combine_item(const DecodeParams &p, const StageI
 // ----------------------------------------------------------------------------
 template <int KV, int QT, int D, int G, int QM, class State>
 __device__ __forceinline__ bool run_item(const DecodeParams &p, SmemHeader &hdr, uint8_t *stages, int cw,
-                                         int &stage, uint32_t &phase, StageInfo inf, const volatile int *abort) {
+                                         int &stage, uint32_t &phase, uint32_t &cpar, StageInfo inf,
+                                         const volatile int *abort) {
   const int lane = threadIdx.x & 31;
   const int ncols = inf.k * G;
   // scales of the item's KV head: per tensor (folded in by the host) or per head
@@ -1193,24 +1213,17 @@ __device__ __forceinline__ bool run_item(const DecodeParams &p, SmemHeader &hdr,
     inf.ntok = nxt.ntok;
     inf.flags = nxt.flags;
   }
-  // The four warps' states meet in the item's last stage buffer, once all
-  // of them are done reading it.  Four consumer-wide barriers an item (so
-  // the combine barrier's phase parity is the barrier's index mod 2): the
-  // stage read, the states written, the weights computed, the scratch read;
-  // then the stage goes back to the producer.
-  float *so = reinterpret_cast<float *>(stages + static_cast<size_t>(stage) * p.stage_bytes);
-  float *sm = so + kConsumerWarps * QM * D;
-  float *sl = sm + kConsumerWarps * QM;
+  // The four warps' states meet in the item's last stage: each warp writes
+  // its state over the rows only it read (no wait for the others), and
+  // (m, l) into the header's buffer of this item's parity.  One
+  // consumer-wide barrier (its phase parity alternates with the items), then
+  // every warp reads all four states and hands the stage back by itself.
+  uint8_t *last = stages + static_cast<size_t>(stage) * p.stage_bytes;
+  st.to_scratch(WarpScratch<KV, D>(last, p, cw), hdr.comb_m[cpar][cw], hdr.comb_l[cpar][cw], v_scale, ncols);
   mbar_arrive(&hdr.combine);
-  if (!mbar_wait(&hdr.combine, 0, abort)) return false;
-  st.to_scratch(so, sm, sl, cw, v_scale, ncols);
-  mbar_arrive(&hdr.combine);
-  if (!mbar_wait(&hdr.combine, 1, abort)) return false;
-  bool ok = true;
-  combine_item<QT, D, G, QM>(p, inf, ncols, so, sm, sl, &hdr.combine, 0, abort, ok);
-  if (!ok) return false;
-  mbar_arrive(&hdr.combine);
-  if (!mbar_wait(&hdr.combine, 1, abort)) return false;
+  if (!mbar_wait(&hdr.combine, cpar, abort)) return false;
+  combine_item<KV, QT, D, G, QM>(p, inf, ncols, last, hdr.comb_m[cpar], hdr.comb_l[cpar]);
+  cpar ^= 1u;
   __syncwarp();
   if (lane == 0) mbar_arrive(&hdr.empty[stage]);
   if (++stage == p.num_stages) {
@@ -1228,8 +1241,8 @@ __device__ __forceinline__ bool run_item(const DecodeParams &p, SmemHeader &hdr,
 template <int KV, int QT, int D, int G, bool MMA>
 __device__ __forceinline__ void decode_body(const DecodeParams &p) {
   constexpr int QM = query_capacity(G);
-  static_assert(kConsumerWarps * (QM * D + 2 * QM) * 4 <= 2 * kStageTok * D * elt_bytes(KV) + QM * D * 2,
-                "the combine scratch must fit in one pipeline stage");
+  static_assert(QM * D * 4 <= 2 * WarpScratch<KV, D>::REG && QM <= 8,
+                "a warp's combine state must fit in the stage rows it read");
   extern __shared__ __align__(128) uint8_t smem[];
   SmemHeader &hdr = *reinterpret_cast<SmemHeader *>(smem);
   const int warp = threadIdx.x >> 5;
@@ -1260,7 +1273,7 @@ __device__ __forceinline__ void decode_body(const DecodeParams &p) {
   uint8_t *stages = smem + p.stages_off;
   using Mma = MmaState<KV, QT, D, G, QM>;
   int stage = 0;
-  uint32_t phase = 0;
+  uint32_t phase = 0, cpar = 0;
   bool failed = false;
   while (true) {
     if (!mbar_wait(&hdr.full[stage], phase, abort)) {
@@ -1271,13 +1284,13 @@ __device__ __forceinline__ void decode_body(const DecodeParams &p) {
     if (inf.flags & kEnd) break;
     bool ok;
     if constexpr (MMA) {
-      ok = run_item<KV, QT, D, G, QM, Mma>(p, hdr, stages, cw, stage, phase, inf, abort);
+      ok = run_item<KV, QT, D, G, QM, Mma>(p, hdr, stages, cw, stage, phase, cpar, inf, abort);
     } else {
       using Simt = SimtState<KV, QT, D, G, QM>;
       if (QM > G && inf.k > 1)
-        ok = run_item<KV, QT, D, G, QM, Mma>(p, hdr, stages, cw, stage, phase, inf, abort);
+        ok = run_item<KV, QT, D, G, QM, Mma>(p, hdr, stages, cw, stage, phase, cpar, inf, abort);
       else
-        ok = run_item<KV, QT, D, G, QM, Simt>(p, hdr, stages, cw, stage, phase, inf, abort);
+        ok = run_item<KV, QT, D, G, QM, Simt>(p, hdr, stages, cw, stage, phase, cpar, inf, abort);
     }
     if (!ok) {
       failed = true;

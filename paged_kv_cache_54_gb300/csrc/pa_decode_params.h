@@ -54,6 +54,11 @@ struct SmemHeader {
   uint64_t empty[kMaxStages];
   uint64_t combine;
   StageInfo info[kMaxStages];
+  // (m, l) of each consumer warp's query columns at an item's end, one
+  // buffer per item parity (a warp may reach the next item's end while
+  // another still reads this one's)
+  float comb_m[2][kConsumerWarps][8];
+  float comb_l[2][kConsumerWarps][8];
   int abort;
 };
 
