@@ -6,10 +6,12 @@
 // sequences' block tables name the same physical blocks over the whole
 // partition (a shared prefix, the beams of one prompt: blocks shared through
 // reference counts and copy-on-write), so each shared tile is read once for
-// all k * G queries.  A plan kernel lists the items; a persistent kernel
-// (several CTAs per SM) claims them from an atomic counter in the order
-// (h, s, p), so CTAs running at the same time read the same KV head of
-// neighbouring sequences.  Sequences with more than one partition leave
+// all k * G queries.  A plan kernel lists the items in sequence order; a
+// persistent kernel (several CTAs per SM) claims them from an atomic counter.
+// With 16 or more KV heads the claims go item by item, every KV head of an
+// item in turn, so CTAs running at the same time read the (block, head) tiles
+// of one block, which lie next to each other in the cache; with fewer, head
+// by head (each head's items in sequence order).  Sequences with more than one partition leave
 // (m, l, o) partials that a merge kernel combines exactly (the
 // flash-decoding reduction).
 //
@@ -154,7 +156,7 @@ __device__ __forceinline__ int block_exclusive_scan(int x, int *warp_tot, int *t
 }
 
 // Plan tables live in shared memory when they fit, else in the workspace.
-constexpr int kPlanSmemSeqs = 4096;
+constexpr int kPlanSmemSeqs = 2048;
 constexpr int kPlanSmemPairs = 12288;
 
 // Last index i in [0, n) with a[i] <= x (a non-decreasing, a[0] <= x).
@@ -170,8 +172,9 @@ __device__ __forceinline__ int upper_index(const int *a, int n, int x) {
 __global__ void __launch_bounds__(1024) plan_kernel(const __grid_constant__ DecodeParams p) {
   __shared__ int warp_tot[32];
   __shared__ int base;
-  __shared__ int s_len[kPlanSmemSeqs + 1];
+  __shared__ int s_len[kPlanSmemSeqs];
   __shared__ int s_off[kPlanSmemSeqs + 1];
+  __shared__ int s_choff[kPlanSmemSeqs];
   __shared__ uint8_t s_join[kPlanSmemPairs];
   const int tid = threadIdx.x;
   const int P = p.partition_size;
@@ -188,9 +191,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(const __grid_constant__ Deco
     const int s = upper_index(off, S, k);
     return make_int2(s, k - off[s]);
   };
-  // A) lengths, partition counts, and the (s, q) pair list in sequence order.
-  //    Without batching (kmax == 1) every pair is an item of its own and is
-  //    written here.
+  // A) lengths, partition counts, and the (s, q) pair list in sequence order
   if (tid == 0) base = 0;
   __syncthreads();
   for (int b0 = 0; b0 < S; b0 += 1024) {
@@ -207,11 +208,8 @@ __global__ void __launch_bounds__(1024) plan_kernel(const __grid_constant__ Deco
     if (s < S) {
       const int o = b + ex;
       off[s] = o;
-      if (p.kmax == 1) {
-        for (int q = 0; q < nP; ++q) p.items[o + q] = make_int4(s, q, 1, 0);
-      } else if (!in_smem) {
+      if (!in_smem)
         for (int q = 0; q < nP; ++q) p.plan_pairs[o + q] = make_int2(s, q);
-      }
     }
     __syncthreads();     // ... before thread 0 advances it
     if (tid == 0) base = b + tot;
@@ -219,102 +217,85 @@ __global__ void __launch_bounds__(1024) plan_kernel(const __grid_constant__ Deco
   }
   const int npairs = base;
   if (tid == 0) off[S] = npairs;
-  if (p.kmax == 1) {
-    if (tid == 0) {
-      p.work[1] = npairs;
-      p.work[0] = 0;
-    }
-    return;
-  }
   uint8_t *join = npairs <= kPlanSmemPairs ? s_join : p.plan_join;
   __syncthreads();
-  // B) does pair (s, q) join the item of (s-1, q)?  It may when s is not at
-  //    a multiple of kmax and partition q is full in both sequences; it does
-  //    when their block-table rows agree over the partition.
-  //  B1: the candidates, one thread per pair
-  for (int k = tid; k < npairs; k += 1024) {
-    const int2 sq = pair_at(k);
-    const int need = (sq.y + 1) * P;
-    join[k] = (sq.x % p.kmax != 0 && len[sq.x] >= need && len[sq.x - 1] >= need) ? 1 : 0;
-  }
-  //  B2: the rows compared in chunks of up to 4 entries (a chunk never
-  //      straddles two partitions), consecutive threads on consecutive
-  //      chunks of one row pair (coalesced); a mismatch clears the candidate
-  //      of its partition.  Sequence s has nfull(s) * cpp chunks, nfull(s)
-  //      being the partitions full in s and in s-1.  The chunk offsets
-  //      replace the lengths, which are no longer needed.
-  const int cpp = (bpp + 3) >> 2;  // chunks per partition
-  int my_ch = 0;
-  if (tid < S && tid > 0 && tid % p.kmax != 0) my_ch = (min(len[tid], len[tid - 1]) / P) * cpp;
-  __syncthreads();  // the first 1024 lengths read before the offsets overwrite them
-  int *choff = len;
-  if (tid == 0) base = 0;
-  __syncthreads();
-  for (int b0 = 0; b0 < S; b0 += 1024) {
-    const int s = b0 + tid;
-    int c = 0;
-    if (b0 == 0) {
-      c = my_ch;
-    } else if (s < S && s % p.kmax != 0) {
-      // sequences past the first 1024 read their lengths again
-      const int L = clamp_len(__ldg(p.seq_lens + s), p.len_cap, nullptr);
-      const int Lp = clamp_len(__ldg(p.seq_lens + s - 1), p.len_cap, nullptr);
-      c = (min(L, Lp) / P) * cpp;
+  if (p.kmax > 1) {  // (without batching every pair is an item of its own)
+    // B) does pair (s, q) join the item of (s-1, q)?  It may when s is not at
+    //    a multiple of kmax and partition q is full in both sequences; it does
+    //    when their block-table rows agree over the partition.
+    //  B1: the candidates, one thread per pair
+    for (int k = tid; k < npairs; k += 1024) {
+      const int2 sq = pair_at(k);
+      const int need = (sq.y + 1) * P;
+      join[k] = (sq.x % p.kmax != 0 && len[sq.x] >= need && len[sq.x - 1] >= need) ? 1 : 0;
     }
-    int tot;
-    const int ex = block_exclusive_scan(c, warp_tot, &tot);
-    const int b = base;
-    if (s < S) choff[s] = b + ex;
+    //  B2: the rows compared in chunks of up to 4 entries (a chunk never
+    //      straddles two partitions), consecutive threads on consecutive
+    //      chunks of one row pair (coalesced); a mismatch clears the candidate
+    //      of its partition.  Sequence s has nfull(s) * cpp chunks, nfull(s)
+    //      being the partitions full in s and in s-1.
+    const int cpp = (bpp + 3) >> 2;  // chunks per partition
+    int *choff = in_smem ? s_choff : p.plan_choff;
+    if (tid == 0) base = 0;
     __syncthreads();
-    if (tid == 0) base = b + tot;
-    __syncthreads();
-  }
-  const int nch = base;
-  // 16-byte loads when every chunk is four aligned entries
-  const bool vec = (bpp & 3) == 0 && (p.max_blocks & 3) == 0 &&
-                   (reinterpret_cast<uintptr_t>(p.block_tables) & 15) == 0;
-  // Each thread takes chunks tid, tid + 1024, ... four at a time with all
-  // their loads in flight.
-  for (int u0 = 0; u0 < nch; u0 += 4 * 1024) {
-    int4 x[4], y[4];
-    int js[4], jq[4], jn[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int u = u0 + i * 1024 + tid;
-      js[i] = -1;
-      jq[i] = jn[i] = 0;
-      x[i] = y[i] = make_int4(0, 0, 0, 0);
-      if (u < nch) {
-        const int sq = upper_index(choff, S, u);
-        const int c = u - choff[sq];
-        const int q = c / cpp;
-        const int e0 = q * bpp + (c - q * cpp) * 4;  // first entry of the chunk
-        const int nv = min(4, (q + 1) * bpp - e0);   // entries of the chunk (1..4)
-        js[i] = sq;
-        jq[i] = q;
-        jn[i] = nv;
-        const int32_t *ra = p.block_tables + static_cast<size_t>(sq) * p.max_blocks + e0;
-        const int32_t *rb = ra - p.max_blocks;
-        if (vec) {
-          x[i] = __ldg(reinterpret_cast<const int4 *>(ra));
-          y[i] = __ldg(reinterpret_cast<const int4 *>(rb));
-        } else {
-          x[i] = make_int4(__ldg(ra), nv > 1 ? __ldg(ra + 1) : 0, nv > 2 ? __ldg(ra + 2) : 0,
-                           nv > 3 ? __ldg(ra + 3) : 0);
-          y[i] = make_int4(__ldg(rb), nv > 1 ? __ldg(rb + 1) : 0, nv > 2 ? __ldg(rb + 2) : 0,
-                           nv > 3 ? __ldg(rb + 3) : 0);
+    for (int b0 = 0; b0 < S; b0 += 1024) {
+      const int s = b0 + tid;
+      const int c = (s < S && s % p.kmax != 0) ? (min(len[s], len[s - 1]) / P) * cpp : 0;
+      int tot;
+      const int ex = block_exclusive_scan(c, warp_tot, &tot);
+      const int b = base;
+      if (s < S) choff[s] = b + ex;
+      __syncthreads();
+      if (tid == 0) base = b + tot;
+      __syncthreads();
+    }
+    const int nch = base;
+    // 16-byte loads when every chunk is four aligned entries
+    const bool vec = (bpp & 3) == 0 && (p.max_blocks & 3) == 0 &&
+                     (reinterpret_cast<uintptr_t>(p.block_tables) & 15) == 0;
+    // Each thread takes chunks tid, tid + 1024, ... four at a time with all
+    // their loads in flight.
+    for (int u0 = 0; u0 < nch; u0 += 4 * 1024) {
+      int4 x[4], y[4];
+      int js[4], jq[4], jn[4];
+  #pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int u = u0 + i * 1024 + tid;
+        js[i] = -1;
+        jq[i] = jn[i] = 0;
+        x[i] = y[i] = make_int4(0, 0, 0, 0);
+        if (u < nch) {
+          const int sq = upper_index(choff, S, u);
+          const int c = u - choff[sq];
+          const int q = c / cpp;
+          const int e0 = q * bpp + (c - q * cpp) * 4;  // first entry of the chunk
+          const int nv = min(4, (q + 1) * bpp - e0);   // entries of the chunk (1..4)
+          js[i] = sq;
+          jq[i] = q;
+          jn[i] = nv;
+          const int32_t *ra = p.block_tables + static_cast<size_t>(sq) * p.max_blocks + e0;
+          const int32_t *rb = ra - p.max_blocks;
+          if (vec) {
+            x[i] = __ldg(reinterpret_cast<const int4 *>(ra));
+            y[i] = __ldg(reinterpret_cast<const int4 *>(rb));
+          } else {
+            x[i] = make_int4(__ldg(ra), nv > 1 ? __ldg(ra + 1) : 0, nv > 2 ? __ldg(ra + 2) : 0,
+                             nv > 3 ? __ldg(ra + 3) : 0);
+            y[i] = make_int4(__ldg(rb), nv > 1 ? __ldg(rb + 1) : 0, nv > 2 ? __ldg(rb + 2) : 0,
+                             nv > 3 ? __ldg(rb + 3) : 0);
+          }
         }
       }
+  #pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        if (js[i] < 0) continue;
+        const bool differ = (x[i].x != y[i].x) || (jn[i] > 1 && x[i].y != y[i].y) ||
+                            (jn[i] > 2 && x[i].z != y[i].z) || (jn[i] > 3 && x[i].w != y[i].w);
+        if (differ) join[off[js[i]] + jq[i]] = 0;  // several threads may clear one flag
+      }
     }
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      if (js[i] < 0) continue;
-      const bool differ = (x[i].x != y[i].x) || (jn[i] > 1 && x[i].y != y[i].y) ||
-                          (jn[i] > 2 && x[i].z != y[i].z) || (jn[i] > 3 && x[i].w != y[i].w);
-      if (differ) join[off[js[i]] + jq[i]] = 0;  // several threads may clear one flag
-    }
-  }
-  __syncthreads();
+    __syncthreads();
+  }  // B
   // C) every pair that does not join leads an item of itself and the pairs
   //    (s+1, q), (s+2, q), ... that join it; items keep sequence order
   if (tid == 0) base = 0;
@@ -325,7 +306,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(const __grid_constant__ Deco
     int2 sq = make_int2(0, 0);
     if (k < npairs) {
       sq = pair_at(k);
-      lead = join[k] == 0;
+      lead = p.kmax == 1 || join[k] == 0;
       if (lead) {
         for (int j = 1; j < p.kmax && sq.x + j < S; ++j) {
           const int idx = off[sq.x + j] + sq.y;
@@ -475,7 +456,10 @@ __device__ __forceinline__ void producer_warp(const DecodeParams &p, uint8_t *sm
   int w_c = 0;
   if (lane == 0) w_c = atomicAdd(p.work, 1);
   w_c = __shfl_sync(0xffffffffu, w_c, 0);
-  int4 pr_c = (w_c < total) ? p.items[w_c % n_items] : make_int4(0, 0, 1, 0);
+  // claim w -> (item, head): every head of an item in turn with many KV
+  // heads (a block's tiles of all heads lie together), else head by head
+  auto item_of = [&](int w) { return p.item_major ? w / p.num_kv_heads : w % n_items; };
+  int4 pr_c = (w_c < total) ? p.items[item_of(w_c)] : make_int4(0, 0, 1, 0);
   int L_c = (w_c < total) ? __ldg(p.seq_lens + pr_c.x) : 0;
   int ph_c[4];
   load_table(w_c, pr_c, L_c, ph_c);
@@ -492,7 +476,7 @@ __device__ __forceinline__ void producer_warp(const DecodeParams &p, uint8_t *sm
         break;
       case 1:
         w_n = __shfl_sync(0xffffffffu, w_raw, 0);
-        pr_n = (w_n < total) ? p.items[w_n % n_items] : make_int4(0, 0, 1, 0);
+        pr_n = (w_n < total) ? p.items[item_of(w_n)] : make_int4(0, 0, 1, 0);
         break;
       case 2:
         L_n = (w_n < total) ? __ldg(p.seq_lens + pr_n.x) : 0;
@@ -509,7 +493,7 @@ __device__ __forceinline__ void producer_warp(const DecodeParams &p, uint8_t *sm
   uint32_t phase = 0;    // (it / NS) & 1
   bool ok = true;
   while (w_c < total) {
-    const int h = w_c / n_items;
+    const int h = p.item_major ? w_c % p.num_kv_heads : w_c / n_items;
     const int s = pr_c.x, pi = pr_c.y, kseq = pr_c.z;
     const int L = clamp_len(L_c, p.len_cap, lane == 0 ? p.err : nullptr);
     const int t_begin = pi * P;
@@ -1380,6 +1364,7 @@ pa_status launch_decode(DecodeParams p, const DeviceInfo &dev, cudaStream_t stre
   p.q_off = sp.q_off;
   p.stages_off = sp.stages_off;
   p.kmax = query_capacity(G) / G;
+  p.item_major = p.num_kv_heads >= 16;
   void (*kern)(DecodeParams);
   if constexpr (tiled_rows<KV, D>()) {
     kern = decode_kernel_tma<KV, QT, D, G, MMA>;

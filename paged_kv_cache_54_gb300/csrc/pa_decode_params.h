@@ -80,12 +80,14 @@ struct DecodeParams {
   const float *v_head_scale;
   int num_stages, stage_bytes, k_off, v_off, q_off, stages_off;
   int kmax;   // most sequences one item may batch
+  int item_major;  // claims take every KV head of an item in turn (else head by head)
   int *work;  // [0] claim counter, [1] number of items
   int4 *items;  // (first sequence, partition, sequences, 0)
   int *plan_len;       // [S] clamped lengths
   int *plan_off;       // [S + 1] first (s, q) pair of each sequence
   int2 *plan_pairs;    // [S * max_parts] (s, q) pairs in sequence order
   uint8_t *plan_join;  // [S * max_parts] pair joins the previous sequence's item
+  int *plan_choff;     // [S] first table-compare chunk of each sequence
   float2 *part_ml;  // [S * max_parts * Hq] (max in log2 units, sum)
   float *part_o;    // [S * max_parts * Hq * D], normalised by its own sum
   int *err;
