@@ -441,7 +441,8 @@ def _oracle_sample(config: str, seed: int, n_seqs: int):
     return w, c, w.block_tables, w.seq_lens, qv, kv
 
 
-def cpu_baseline(config: str, seed: int, budget_s: float = 12.0, n_seqs: int = 4):
+def _oracle_rate(config: str, seed: int, budget_s: float, n_seqs: int = 4) -> dict:
+    """The oracle's decode of a bounded sample, repeated for about budget_s."""
     from oracle import attention as A
     w, c, tables, lens, qv, kv = _oracle_sample(config, seed, n_seqs)
     t0 = time.perf_counter()
@@ -452,11 +453,40 @@ def cpu_baseline(config: str, seed: int, budget_s: float = 12.0, n_seqs: int = 4
         if time.perf_counter() - t0 >= budget_s:
             break
     dt = (time.perf_counter() - t0) / reps
-    return {"value": round(kv / dt / 1e9, 4), "unit": "GB/s", "cores": _cores(),
-            "kind": "oracle",
-            "sample": f"first {len(lens)} sequences of {config} (all {w.Hq} query heads, "
-                      f"{int(lens.sum())} tokens), float64 NumPy oracle, {reps} passes in {budget_s:.0f} s",
-            "seq_layer_per_s": round(len(lens) / dt, 3)}
+    return {"gbs": kv / dt / 1e9, "seq_per_s": len(lens) / dt, "reps": reps, "tokens": int(lens.sum()),
+            "seqs": len(lens), "q_heads": w.Hq}
+
+
+def _single_core_rate(config: str, seed: int, budget_s: float) -> dict | None:
+    """_oracle_rate in a child process pinned to one core, with one BLAS
+    thread; None if the child fails."""
+    cpu = min(os.sched_getaffinity(0))
+    code = ("import json, os, sys; os.sched_setaffinity(0, {%d}); sys.path.insert(0, %r); import bench; "
+            "print(json.dumps(bench._oracle_rate(%r, %d, %r)))" % (cpu, ROOT, config, seed, budget_s))
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    env.pop("CUDA_VISIBLE_DEVICES", None)
+    try:
+        r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env,
+                           timeout=budget_s + 240)
+        return json.loads(r.stdout.strip().splitlines()[-1]) if r.returncode == 0 else None
+    except (subprocess.TimeoutExpired, ValueError, IndexError):
+        return None
+
+
+def cpu_baseline(config: str, seed: int, budget_s: float = 12.0, n_seqs: int = 4,
+                 single_budget_s: float = 8.0):
+    r = _oracle_rate(config, seed, budget_s, n_seqs)
+    out = {"value": round(r["gbs"], 4), "unit": "GB/s", "cores": _cores(), "kind": "oracle",
+           "sample": f"first {r['seqs']} sequences of {config} (all {r['q_heads']} query heads, "
+                     f"{r['tokens']} tokens), float64 NumPy oracle, {r['reps']} passes in {budget_s:.0f} s",
+           "seq_layer_per_s": round(r["seq_per_s"], 3)}
+    one = _single_core_rate(config, seed, single_budget_s) if single_budget_s > 0 else None
+    if one is not None:
+        out["single_core"] = {"value": round(one["gbs"], 4), "unit": "GB/s", "cores": 1,
+                              "seq_layer_per_s": round(one["seq_per_s"], 3),
+                              "sample": f"the same sample in a process pinned to one core with one BLAS "
+                                        f"thread, {one['reps']} passes in {single_budget_s:.0f} s"}
+    return out
 
 
 def _cores() -> int:
