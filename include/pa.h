@@ -194,6 +194,14 @@ PA_API size_t pa_decode_workspace_size(int32_t num_seqs, int32_t num_q_heads,
  *                  Calls sharing one workspace must be stream-ordered.
  * Supported set: num_q_heads / kv_heads in {1, 2, 4, 8}; cache dtypes of
  * pa_cache_desc; one-byte caches accept q in PA_F16 or PA_BF16.
+ * Stream order: the call's first kernel may begin reading block_tables and
+ * seq_lens while the kernel before it on the stream is still running, if
+ * that kernel has signalled programmatic completion early
+ * (griddepcontrol.launch_dependents).  pa_reshape_and_cache and
+ * pa_copy_blocks do so; they never write those arrays.  A caller's kernel
+ * that writes block_tables or seq_lens must not signal before its writes.
+ * Everything else the call reads (q, the caches) is read only after all
+ * earlier work on the stream has completed.
  */
 PA_API pa_status pa_decode(void *out, const void *q, int32_t q_dtype,
                     int32_t num_seqs, int32_t num_q_heads,

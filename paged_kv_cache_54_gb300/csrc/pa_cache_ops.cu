@@ -24,6 +24,10 @@ __global__ void __launch_bounds__(256) reshape_and_cache_kernel(
     int block_size, long long num_slots, uint8_t *__restrict__ k_cache,
     uint8_t *__restrict__ v_cache, float k_scale, float v_scale,
     const float *__restrict__ k_head_scales, const float *__restrict__ v_head_scales, int *err) {
+  // A pa_decode enqueued next may start its plan now: the plan reads only the
+  // block tables and lengths, which this kernel never writes, and the decode
+  // itself runs after this grid has completed.
+  launch_dependents();
   constexpr int DE = elt_bytes(DST);
   constexpr int CE = 16 / DE;  // elements per destination chunk
   const int cpr = head_dim / CE;
@@ -90,6 +94,7 @@ __global__ void __launch_bounds__(256) copy_blocks_kernel(uint8_t *__restrict__ 
                                                           const int64_t *__restrict__ mapping,
                                                           int num_pairs, long long block_bytes,
                                                           long long num_blocks, int *err) {
+  launch_dependents();  // as in reshape_and_cache_kernel: no block table or length is written here
   const long long vecs = block_bytes / 16;
   const long long total = static_cast<long long>(num_pairs) * 2 * vecs;
   for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < total;

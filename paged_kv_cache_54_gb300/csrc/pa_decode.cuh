@@ -181,6 +181,11 @@ __global__ void __launch_bounds__(1024) plan_kernel(const __grid_constant__ Deco
   const int bpp = P / p.block_size;
   const int S = p.num_seqs;
   launch_dependents();  // the decode grid may become resident; it waits for us
+  // This kernel is a programmatic dependent of whatever precedes it on the
+  // stream: it reads only the block tables and lengths (which the cache
+  // writes before it never touch) and writes only this call's workspace, and
+  // it waits for the preceding kernel before it ends, so the decode that
+  // waits for it also follows every kernel before the call.
   const bool in_smem = S <= kPlanSmemSeqs;
   int *len = in_smem ? s_len : p.plan_len;
   int *off = in_smem ? s_off : p.plan_off;
@@ -327,6 +332,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(const __grid_constant__ Deco
     p.work[1] = base;
     p.work[0] = 0;
   }
+  grid_dependency_wait();
 }
 
 // ----------------------------------------------------------------------------
@@ -1246,7 +1252,10 @@ __device__ __forceinline__ void decode_body(const DecodeParams &p) {
   }
   // the plan (and every kernel before it: the cache writes) must be complete
   grid_dependency_wait();
-  launch_dependents();
+  // Only the merge of this call may start early.  Without one the next
+  // kernel on the stream waits for this grid to end: a later call's plan
+  // rewrites the workspace this grid reads.
+  if (p.max_parts > 1) launch_dependents();
   if (warp == 0) {
     producer_warp<KV, D, G>(p, smem);
     return;
@@ -1380,22 +1389,27 @@ pa_status launch_decode(DecodeParams p, const DeviceInfo &dev, cudaStream_t stre
     if (e != cudaSuccess) return cuda_fail(e);
     if (dev_id >= 0 && dev_id < 64) configured_bytes[dev_id] = sp.total;
   }
-  plan_kernel<<<1, 1024, 0, stream>>>(p);
-  const long long items = static_cast<long long>(p.num_seqs) * p.max_parts * p.num_kv_heads;
-  const long long slots = static_cast<long long>(dev.sm_count) * ctas;
-  const int grid = static_cast<int>(items < slots ? items : slots);
-  // decode and merge are launched as programmatic dependents of the kernel
-  // before them, so their launch overlaps its tail (each waits on the device)
+  // the plan, the decode and the merge are launched as programmatic
+  // dependents: each may start before the kernel ahead of it ends (each
+  // waits on the device for what it needs)
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = sp.total;
+  cfg.gridDim = dim3(1);
+  cfg.blockDim = dim3(1024);
+  cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, plan_kernel, p);
+  if (e != cudaSuccess) return cuda_fail(e);
+  const long long items = static_cast<long long>(p.num_seqs) * p.max_parts * p.num_kv_heads;
+  const long long slots = static_cast<long long>(dev.sm_count) * ctas;
+  const int grid = static_cast<int>(items < slots ? items : slots);
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = sp.total;
   e = cudaLaunchKernelEx(&cfg, kern, p);
   if (e != cudaSuccess) return cuda_fail(e);
   if (p.max_parts > 1) {
