@@ -16,6 +16,12 @@ are resident in HBM before timing starts; the KV working set (3.8 GB unique
 for the default workload) is far larger than L2, so no flush is needed
 between steps.
 
+Timing: K steps back to back between two CUDA events give ``value`` (the
+calls' kernels overlap as they do in use: the decode's plan may start while
+the cache write is still running); K more steps with an event pair around
+each ``pa_decode`` call give the decode launch group's duration for
+``roofline``.
+
 ``--impl reference`` times the CPU oracle (float64 NumPy) on a bounded
 sample of the same workload on the host cores instead.
 """
@@ -346,7 +352,7 @@ def run_ours(args, rank, world, local):
         "config": decode_config(w, args.config, seed, world),
         "seq_layer_per_s": round(world * w.S / step_t, 1),
         "kv_logical_gbs": round(job_rate(w.kv_logical_bytes(), world, step_t) / 1e9, 2),
-        "gpu_launches": launches_per_step * K,
+        "gpu_launches": launches_per_step * 2 * K,  # both timed loops
         "device_error": derr,
         "roofline": {
             "kernel": "pa_decode (plan + persistent decode + merge, CUDA events)",
