@@ -67,6 +67,10 @@ def parse():
     ap.add_argument("--config", default=DEFAULT_CONFIG, choices=W.ALL_CONFIGS)
     ap.add_argument("--seed", type=int, default=None)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--seqs", type=int, default=None,
+                    help="a smaller copy of the workload for profiling captures: this many "
+                         "sequences (beam workloads: this many prompts); the line then names "
+                         "the reduced workload and is not a bench result")
     ap.add_argument("--op", default="step", choices=["step", "swap", "prefix-cache", "prefill"],
                     help="step: the decode step (default); swap: pa_swap_blocks of "
                          "preempted sequences' blocks out to pinned host memory and back; "
@@ -78,6 +82,14 @@ def parse():
                     help="cache type of the prefill bench (one-byte caches: codes of N(0,1) K/V "
                          "with scale 1, or 1/32 for int8)")
     return ap.parse_args()
+
+
+def seqs_override(args):
+    """Workload override for --seqs (None: the named workload as it is)."""
+    if args.seqs is None:
+        return None
+    key = "prompts" if W.CONFIGS[args.config]["kind"] == "beam" else "S"
+    return {key: int(args.seqs)}
 
 
 def dist_env():
@@ -202,7 +214,7 @@ def run_ours(args, rank, world, local):
     torch.cuda.set_device(local)
     dev = f"cuda:{local}"
     seed = args.seed if args.seed is not None else W.config_seed(args.config)
-    w = W.make_workload(args.config, seed, device=dev)
+    w = W.make_workload(args.config, seed, device=dev, overrides=seqs_override(args))
     shape = (w.num_blocks, w.Hkv, w.bs, w.d)
     if w.cache_dtype in W.BYTE_DTYPES:
         kc = torch.zeros(shape, dtype=torch.uint8, device=dev)
@@ -377,11 +389,16 @@ def run_ours(args, rank, world, local):
     print(json.dumps(line), flush=True)
 
 
+def _named_seqs(config: str) -> int:
+    cfg = W.CONFIGS[config]
+    return cfg["prompts"] * cfg["beams"] if cfg["kind"] == "beam" else cfg["S"]
+
+
 def decode_config(w, config: str, seed: int, world: int) -> dict:
     """The workload description of a decode bench line (both arms)."""
     kv_bytes, _ = workload_bytes(w)
     return {
-        "workload": f"{config}: {_describe(w)}",
+        "workload": f"{config}{'' if w.S == _named_seqs(config) else ' (reduced)'}: {_describe(w)}",
         "num_seqs": w.S, "q_heads": w.Hq, "kv_heads": w.Hkv, "head_dim": w.d,
         "block_size": w.bs, "cache_dtype": w.cache_dtype, "q_dtype": w.q_dtype,
         "partition_size": w.partition_size or _auto_partition(w),
