@@ -157,6 +157,7 @@ __device__ __forceinline__ int block_exclusive_scan(int x, int *warp_tot, int *t
 
 // Plan tables live in shared memory when they fit, else in the workspace.
 constexpr int kPlanSmemSeqs = 2048;
+constexpr int kPlanWideFlags = 4096;  // (wide chunk, partition) flags in shared memory
 constexpr int kPlanSmemPairs = 12288;
 
 // Last index i in [0, n) with a[i] <= x (a non-decreasing, a[0] <= x).
@@ -176,6 +177,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(const __grid_constant__ Deco
   __shared__ int s_off[kPlanSmemSeqs + 1];
   __shared__ int s_choff[kPlanSmemSeqs];
   __shared__ uint8_t s_join[kPlanSmemPairs];
+  __shared__ uint8_t s_wide[kPlanWideFlags];
   const int tid = threadIdx.x;
   const int P = p.partition_size;
   const int bpp = P / p.block_size;
@@ -223,16 +225,26 @@ __global__ void __launch_bounds__(1024) plan_kernel(const __grid_constant__ Deco
   const int npairs = base;
   if (tid == 0) off[S] = npairs;
   uint8_t *join = npairs <= kPlanSmemPairs ? s_join : p.plan_join;
+  // Wide chunks: W = p.wide_seqs sequences from a multiple of W whose rows
+  // all agree over a full partition become one wide item (decoded on the
+  // tensor cores by the wide kernel) when there are at least p.wide_min of
+  // them and each has more than one partition.
+  const int W = p.wide_seqs;
+  const int nchunks = W > 0 ? (S + W - 1) / W : 0;
+  const bool use_wide = W > 0 && nchunks * p.max_parts <= kPlanWideFlags;
+  // a sequence may join its predecessor: within a group of kmax (batched
+  // items), or anywhere when wide chunks are looked for
+  auto may_join = [&](int s) { return s > 0 && (use_wide || s % p.kmax != 0); };
   __syncthreads();
-  if (p.kmax > 1) {  // (without batching every pair is an item of its own)
-    // B) does pair (s, q) join the item of (s-1, q)?  It may when s is not at
-    //    a multiple of kmax and partition q is full in both sequences; it does
-    //    when their block-table rows agree over the partition.
+  if (p.kmax > 1 || use_wide) {  // (without batching every pair is an item of its own)
+    // B) does pair (s, q) join the item of (s-1, q)?  It may when may_join(s)
+    //    and partition q is full in both sequences; it does when their
+    //    block-table rows agree over the partition.
     //  B1: the candidates, one thread per pair
     for (int k = tid; k < npairs; k += 1024) {
       const int2 sq = pair_at(k);
       const int need = (sq.y + 1) * P;
-      join[k] = (sq.x % p.kmax != 0 && len[sq.x] >= need && len[sq.x - 1] >= need) ? 1 : 0;
+      join[k] = (may_join(sq.x) && len[sq.x] >= need && len[sq.x - 1] >= need) ? 1 : 0;
     }
     //  B2: the rows compared in chunks of up to 4 entries (a chunk never
     //      straddles two partitions), consecutive threads on consecutive
@@ -245,7 +257,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(const __grid_constant__ Deco
     __syncthreads();
     for (int b0 = 0; b0 < S; b0 += 1024) {
       const int s = b0 + tid;
-      const int c = (s < S && s % p.kmax != 0) ? (min(len[s], len[s - 1]) / P) * cpp : 0;
+      const int c = (s < S && may_join(s)) ? (min(len[s], len[s - 1]) / P) * cpp : 0;
       int tot;
       const int ex = block_exclusive_scan(c, warp_tot, &tot);
       const int b = base;
@@ -301,35 +313,69 @@ __global__ void __launch_bounds__(1024) plan_kernel(const __grid_constant__ Deco
     }
     __syncthreads();
   }  // B
+  // C0) the wide (chunk, partition) flags: set for chunks of enough
+  //     sequences, then cleared by every (sequence, partition) of the chunk
+  //     that does not qualify (one thread each)
+  if (use_wide) {
+    for (int i = tid; i < nchunks * p.max_parts; i += 1024) {
+      const int n = min(W, S - (i / p.max_parts) * W);
+      s_wide[i] = (n >= p.wide_min && n >= 2) ? 1 : 0;
+    }
+    __syncthreads();
+    for (int i = tid; i < S * p.max_parts; i += 1024) {
+      const int s = i / p.max_parts, q = i % p.max_parts;
+      const int fi = (s / W) * p.max_parts + q;
+      if (s_wide[fi] == 0) continue;
+      const int idx = off[s] + q;
+      // the partition must exist and be full in s, shared with s - 1 inside
+      // the chunk, and s must have more than one partition
+      const bool ok = idx < off[s + 1] && len[s] > P && len[s] >= (q + 1) * P && (s % W == 0 || join[idx] != 0);
+      if (!ok) s_wide[fi] = 0;  // several threads may clear one flag
+    }
+    __syncthreads();
+  }
   // C) every pair that does not join leads an item of itself and the pairs
-  //    (s+1, q), (s+2, q), ... that join it; items keep sequence order
+  //    (s+1, q), (s+2, q), ... of its kmax group that join it; items keep
+  //    sequence order.  Pairs of a wide chunk are left to the wide item its
+  //    first sequence leads.
+  int wtotal = 0;
   if (tid == 0) base = 0;
   __syncthreads();
   for (int k0 = 0; k0 < npairs; k0 += 1024) {
     const int k = k0 + tid;
-    int lead = 0, ksz = 1;
+    int lead = 0, ksz = 1, wlead = 0;
     int2 sq = make_int2(0, 0);
     if (k < npairs) {
       sq = pair_at(k);
-      lead = p.kmax == 1 || join[k] == 0;
-      if (lead) {
-        for (int j = 1; j < p.kmax && sq.x + j < S; ++j) {
-          const int idx = off[sq.x + j] + sq.y;
-          if (idx >= off[sq.x + j + 1] || join[idx] == 0) break;
-          ++ksz;
+      const bool in_wide = use_wide && s_wide[(sq.x / W) * p.max_parts + sq.y] != 0;
+      if (in_wide) {
+        wlead = sq.x % W == 0;
+        if (wlead) ksz = min(W, S - sq.x);
+      } else {
+        lead = p.kmax == 1 || sq.x % p.kmax == 0 || join[k] == 0;
+        if (lead) {
+          for (int j = 1; j < p.kmax && sq.x + j < S && (sq.x + j) % p.kmax != 0; ++j) {
+            const int idx = off[sq.x + j] + sq.y;
+            if (idx >= off[sq.x + j + 1] || join[idx] == 0) break;
+            ++ksz;
+          }
         }
       }
     }
-    int tot;
+    int tot, wtot;
     const int ex = block_exclusive_scan(lead, warp_tot, &tot);
+    const int wex = block_exclusive_scan(wlead, warp_tot, &wtot);
     const int b = base;
     if (lead) p.items[b + ex] = make_int4(sq.x, sq.y, ksz, 0);
+    if (wlead) p.wide_items[wtotal + wex] = make_int4(sq.x, sq.y, ksz, 0);
+    wtotal += wtot;
     __syncthreads();
     if (tid == 0) base = b + tot;
     __syncthreads();
   }
   if (tid == 0) {
     p.work[1] = base;
+    p.work[2] = wtotal;
     p.work[0] = 0;
   }
   grid_dependency_wait();
@@ -442,7 +488,7 @@ __device__ __forceinline__ void producer_warp(const DecodeParams &p, uint8_t *sm
   const int P = p.partition_size;
   const int bpp = P / bs;  // <= 128
   const int NS = p.num_stages;
-  const int n_items = p.work[1];
+  const int n_items = __ldcg(p.work + 1);  // the plan's outputs are read from L2
   const int total = n_items * p.num_kv_heads;
   constexpr uint32_t qbytes = G * D * 2;  // query rows of one sequence's group
   const uint64_t pol_kv = l2_policy_evict_first();  // each tile passes through L2 once
@@ -465,7 +511,7 @@ __device__ __forceinline__ void producer_warp(const DecodeParams &p, uint8_t *sm
   // claim w -> (item, head): every head of an item in turn with many KV
   // heads (a block's tiles of all heads lie together), else head by head
   auto item_of = [&](int w) { return p.item_major ? w / p.num_kv_heads : w % n_items; };
-  int4 pr_c = (w_c < total) ? p.items[item_of(w_c)] : make_int4(0, 0, 1, 0);
+  int4 pr_c = (w_c < total) ? __ldcg(p.items + item_of(w_c)) : make_int4(0, 0, 1, 0);
   int L_c = (w_c < total) ? __ldg(p.seq_lens + pr_c.x) : 0;
   int ph_c[4];
   load_table(w_c, pr_c, L_c, ph_c);
@@ -482,7 +528,7 @@ __device__ __forceinline__ void producer_warp(const DecodeParams &p, uint8_t *sm
         break;
       case 1:
         w_n = __shfl_sync(0xffffffffu, w_raw, 0);
-        pr_n = (w_n < total) ? p.items[item_of(w_n)] : make_int4(0, 0, 1, 0);
+        pr_n = (w_n < total) ? __ldcg(p.items + item_of(w_n)) : make_int4(0, 0, 1, 0);
         break;
       case 2:
         L_n = (w_n < total) ? __ldg(p.seq_lens + pr_n.x) : 0;
@@ -1250,14 +1296,19 @@ __device__ __forceinline__ void decode_body(const DecodeParams &p) {
     if (threadIdx.x == 0) record_error(p.err, kErrSmemAlign);
     return;
   }
-  // the plan (and every kernel before it: the cache writes) must be complete
-  grid_dependency_wait();
+  // The plan (and every kernel before it: the cache writes) must be
+  // complete.  After the wide kernel, this grid starts only once every wide
+  // CTA has seen the plan end, so it does not wait here: it waits for the
+  // wide grid before it ends (its first CTA, below), so that the merge,
+  // which waits for this grid, follows both.
+  if (!p.after_wide) grid_dependency_wait();
   // Only the merge of this call may start early.  Without one the next
   // kernel on the stream waits for this grid to end: a later call's plan
   // rewrites the workspace this grid reads.
   if (p.max_parts > 1) launch_dependents();
   if (warp == 0) {
     producer_warp<KV, D, G>(p, smem);
+    if (p.after_wide && blockIdx.x == 0 && threadIdx.x == 0) grid_dependency_wait();
     return;
   }
   const int cw = warp - 1;
@@ -1374,6 +1425,11 @@ pa_status launch_decode(DecodeParams p, const DeviceInfo &dev, cudaStream_t stre
   p.stages_off = sp.stages_off;
   p.kmax = query_capacity(G) / G;
   p.item_major = p.num_kv_heads >= 16;
+  // runs of sequences sharing a whole partition's blocks go to the tensor
+  // cores (16-bit caches, query groups of 2 or more, split sequences)
+  const bool wide = !is_byte(KV) && G >= 2 && p.max_parts > 1;
+  p.wide_seqs = wide ? kWideRows / G : 0;
+  p.wide_min = kWideMinRows / G;
   void (*kern)(DecodeParams);
   if constexpr (tiled_rows<KV, D>()) {
     kern = decode_kernel_tma<KV, QT, D, G, MMA>;
@@ -1404,6 +1460,12 @@ pa_status launch_decode(DecodeParams p, const DeviceInfo &dev, cudaStream_t stre
   cfg.numAttrs = 1;
   e = cudaLaunchKernelEx(&cfg, plan_kernel, p);
   if (e != cudaSuccess) return cuda_fail(e);
+  // the wide items first, on their own SMs; the decode kernel fills the rest
+  p.after_wide = wide ? 1 : 0;
+  if (wide) {
+    const pa_status st = launch_wide_items(p, KV, D, stream);
+    if (st != PA_OK) return st;
+  }
   const long long items = static_cast<long long>(p.num_seqs) * p.max_parts * p.num_kv_heads;
   const long long slots = static_cast<long long>(dev.sm_count) * ctas;
   const int grid = static_cast<int>(items < slots ? items : slots);

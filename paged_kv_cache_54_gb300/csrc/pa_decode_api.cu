@@ -22,7 +22,7 @@ int choose_partition(int num_seqs, int kv_heads, int max_seq_len, int requested)
 }
 
 struct WorkspaceLayout {
-  size_t pairs_off, len_off, seqoff_off, choff_off, plist_off, join_off, ml_off, o_off, total;
+  size_t pairs_off, wide_off, len_off, seqoff_off, choff_off, plist_off, join_off, ml_off, o_off, total;
   int partition, max_parts;
 };
 
@@ -38,7 +38,10 @@ bool layout_for(int num_seqs, int num_q_heads, int kv_heads, int head_dim, int m
   w.max_parts = max_seq_len > 0 ? (max_seq_len + w.partition - 1) / w.partition : 1;
   const size_t units = static_cast<size_t>(num_seqs) * w.max_parts;
   w.pairs_off = 256;                                            // items (int4)
-  w.len_off = align256(w.pairs_off + units * sizeof(int4));      // lengths
+  // wide items: a chunk holds at least kWideRows / 8 sequences
+  const size_t wide_units = static_cast<size_t>((num_seqs + kWideRows / 8 - 1) / (kWideRows / 8)) * w.max_parts;
+  w.wide_off = align256(w.pairs_off + units * sizeof(int4));
+  w.len_off = align256(w.wide_off + wide_units * sizeof(int4));  // lengths
   w.seqoff_off = align256(w.len_off + num_seqs * sizeof(int));   // pair offsets
   w.choff_off = align256(w.seqoff_off + (num_seqs + 1) * sizeof(int));
   w.plist_off = align256(w.choff_off + num_seqs * sizeof(int));
@@ -159,6 +162,7 @@ extern "C" pa_status pa_decode(void *out, const void *q, int32_t q_dtype, int32_
   p.v_head_scale = per_head ? cache->v_head_scales : nullptr;
   p.work = reinterpret_cast<int *>(ws);
   p.items = reinterpret_cast<int4 *>(ws + w.pairs_off);
+  p.wide_items = reinterpret_cast<int4 *>(ws + w.wide_off);
   p.plan_len = reinterpret_cast<int *>(ws + w.len_off);
   p.plan_off = reinterpret_cast<int *>(ws + w.seqoff_off);
   p.plan_pairs = reinterpret_cast<int2 *>(ws + w.plist_off);

@@ -16,6 +16,10 @@ constexpr int kThreads = 32 * (1 + kConsumerWarps);
 constexpr int kConsumerThreads = 32 * kConsumerWarps;
 constexpr int kMaxStages = 12;
 constexpr int kMaxPartition = 1024;
+// Wide items (runs of sequences that share a partition's blocks, decoded on
+// the tensor cores): the query rows of one, and the fewest worth taking.
+constexpr int kWideRows = 256;
+constexpr int kWideMinRows = 64;
 #ifndef PA_DECODE_CTAS_PER_SM
 #define PA_DECODE_CTAS_PER_SM 3
 #endif
@@ -81,8 +85,12 @@ struct DecodeParams {
   int num_stages, stage_bytes, k_off, v_off, q_off, stages_off;
   int kmax;   // most sequences one item may batch
   int item_major;  // claims take every KV head of an item in turn (else head by head)
-  int *work;  // [0] claim counter, [1] number of items
+  int *work;  // [0] claim counter, [1] number of items, [2] number of wide items
   int4 *items;  // (first sequence, partition, sequences, 0)
+  int4 *wide_items;  // the same, for the wide kernel
+  int wide_seqs;     // sequences of a wide chunk (0: no wide items)
+  int wide_min;      // fewest sequences that make a wide item
+  int after_wide;    // the decode kernel follows the wide kernel (see decode_body)
   int *plan_len;       // [S] clamped lengths
   int *plan_off;       // [S + 1] first (s, q) pair of each sequence
   int2 *plan_pairs;    // [S * max_parts] (s, q) pairs in sequence order
@@ -93,6 +101,10 @@ struct DecodeParams {
   int *err;
 };
 
+
+// The wide items (runs of sequences sharing a partition's blocks) on the
+// tensor cores, after the decode kernel (pa_prefill.cu).
+pa_status launch_wide_items(const DecodeParams &d, int cache_dtype, int head_dim, cudaStream_t stream);
 
 // One instantiation family per cache dtype (separate translation units).
 pa_status dispatch_decode_f16(int q_dtype, int head_dim, int group, DecodeParams p,

@@ -4,6 +4,7 @@
 #include <limits.h>
 #include <math.h>
 
+#include "pa_decode_params.h"
 #include "pa_prefill.cuh"
 
 namespace pa {
@@ -50,6 +51,51 @@ bool encode_q_view(CUtensorMap *map, const void *q, int num_tokens, int kv_heads
 }
 
 }  // namespace
+
+// The decode's wide items on the tensor cores (16-bit caches, G = 2, 4, 8):
+// the tile views of q and the caches, then the wide kernel over the wide
+// item slots (those past the plan's count return at once).
+pa_status launch_wide_items(const DecodeParams &d, int cache_dtype, int head_dim, cudaStream_t stream) {
+  if ((cache_dtype != PA_F16 && cache_dtype != PA_BF16) || d.wide_seqs <= 0) return PA_ERR_UNSUPPORTED;
+  const int G = d.num_q_heads / d.num_kv_heads;
+  pa_cache_desc c{};
+  c.num_blocks = d.num_blocks;
+  c.kv_heads = d.num_kv_heads;
+  c.block_size = d.block_size;
+  c.head_dim = head_dim;
+  c.dtype = cache_dtype;
+  c.k_scale = c.v_scale = 1.f;
+  PrefillParams p{};
+  if (!encode_q_view(&p.tmap_q, d.q, d.num_seqs, d.num_kv_heads, G, head_dim) ||
+      !encode_cache_view(&p.tmap_k, d.k_cache, &c) || !encode_cache_view(&p.tmap_v, d.v_cache, &c))
+    return cuda_fail(cudaErrorInvalidValue);
+  p.k_cache = d.k_cache;
+  p.v_cache = d.v_cache;
+  p.block_tables = d.block_tables;
+  p.seq_lens = d.seq_lens;
+  p.num_q_heads = d.num_q_heads;
+  p.num_kv_heads = d.num_kv_heads;
+  p.num_blocks = d.num_blocks;
+  p.block_size = d.block_size;
+  p.max_blocks = d.max_blocks;
+  p.num_q_tokens = d.num_seqs;
+  p.qk_scale_log2 = d.qk_scale_log2;
+  p.v_scale = 1.f;
+  p.err = d.err;
+  p.wide_items = d.wide_items;
+  p.wide_count = d.work + 2;
+  p.part_ml = d.part_ml;
+  p.part_o = d.part_o;
+  p.max_parts = d.max_parts;
+  p.partition_size = d.partition_size;
+  const long long slots = static_cast<long long>((d.num_seqs + d.wide_seqs - 1) / d.wide_seqs) * d.max_parts;
+  if (slots > 0x7fffffff) return PA_ERR_UNSUPPORTED;
+  const int gx = static_cast<int>(slots);
+  if (cache_dtype == PA_F16)
+    return head_dim == 64 ? wide_by_group<kF16, 64>(G, p, gx, stream) : wide_by_group<kF16, 128>(G, p, gx, stream);
+  return head_dim == 64 ? wide_by_group<kBF16, 64>(G, p, gx, stream) : wide_by_group<kBF16, 128>(G, p, gx, stream);
+}
+
 }  // namespace pa
 
 using namespace pa;

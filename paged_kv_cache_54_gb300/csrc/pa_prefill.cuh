@@ -85,6 +85,13 @@ struct PrefillParams {
   const float *k_head_scale;  // one-byte caches: [num_kv_heads] scales, or null
   const float *v_head_scale;
   int *err;
+  // the decode's wide items (shared-prefix chunks), for wide_decode_kernel:
+  // (first sequence, partition, sequences) each; their count on the device
+  const int4 *wide_items;
+  const int *wide_count;
+  float2 *part_ml;  // the decode's split-K partials, [S * max_parts * Hq] (m, l)
+  float *part_o;    // and [S * max_parts * Hq * D], normalised by l
+  int max_parts, partition_size;
 };
 
 namespace {
@@ -233,9 +240,18 @@ __device__ __forceinline__ uint64_t fadd2(uint64_t a, uint64_t b) {
   return d;
 }
 
-// DT: the type of q and out; KVT: the cache's (DT itself for 16-bit caches)
-template <int DT, int KVT, int D, int G>
-__global__ void __launch_bounds__(pf_threads(is_byte(KVT)), 1) prefill_kernel(const __grid_constant__ PrefillParams p) {
+// DT: the type of q and out; KVT: the cache's (DT itself for 16-bit caches).
+// SD (shared decode): the CTA decodes one wide item of the paged decode
+// instead of prefilling new tokens.  A wide item is a run of k sequences
+// whose block tables agree over partition q (a shared prefix): their decode
+// queries are the rows of the tiles (row r: sequence s0 + r / G, query head
+// h * G + r % G, read from q [S, Hq, D] exactly as new tokens are read from
+// a prefill's q), the keys are the partition's P tokens of the shared blocks
+// (no mask: every row follows them all), and each row's (m, l) and O / l go
+// to the decode's split-K partials of (sequence, partition q), which the
+// decode's merge combines with the other partitions.
+template <int DT, int KVT, int D, int G, bool SD>
+__device__ __forceinline__ void prefill_body(const PrefillParams &p) {
   constexpr bool KV8 = is_byte(KVT);
   constexpr int MT = KV8 ? kF16 : DT;          // the products' operand type
   constexpr bool QCONV = KV8 && DT == kBF16;   // q is rewritten as fp16 first
@@ -251,8 +267,16 @@ __global__ void __launch_bounds__(pf_threads(is_byte(KVT)), 1) prefill_kernel(co
   constexpr uint32_t IDESC_PV = umma_idesc_f16(AB, kPfTileRows, D, true);
   extern __shared__ __align__(1024) uint8_t smem[];
   PfHeader &hdr = *reinterpret_cast<PfHeader *>(smem);
-  const int cta = gridDim.x - 1 - blockIdx.x;  // the longest (last) token ranges start first
-  const int s = blockIdx.y, h = blockIdx.z;
+  const int cta = SD ? 0 : gridDim.x - 1 - blockIdx.x;  // the longest (last) token ranges start first
+  const int h = blockIdx.z;
+  int s = blockIdx.y, qpart = 0, nseq = 0;
+  if constexpr (SD) {  // the wide item: read from L2 (the plan wrote it in an earlier grid)
+    if (static_cast<int>(blockIdx.x) >= __ldcg(p.wide_count)) return;
+    const int4 it = __ldcg(p.wide_items + blockIdx.x);
+    s = it.x;
+    qpart = it.y;
+    nseq = it.z;
+  }
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // the tensor-map descriptors are fetched while the lengths are read
   if (warp == kPfTmaWarp && lane == 0) {
@@ -264,35 +288,53 @@ __global__ void __launch_bounds__(pf_threads(is_byte(KVT)), 1) prefill_kernel(co
   }
   // and the TMA warp reads the sequence's first 64 block-table entries: a
   // window of 32 (lane j: entry 32 w + j) in use and the next one
-  const int32_t *table = p.block_tables + static_cast<size_t>(s) * p.max_blocks;
+  // (SD: the partition's entries, from its first)
+  const int kofs = SD ? qpart * (p.partition_size / p.block_size) : 0;
+  const int tbl_len = p.max_blocks - kofs;
+  const int32_t *table = p.block_tables + static_cast<size_t>(s) * p.max_blocks + kofs;
   int win = 0, win_next = 0;
   if (warp == kPfTmaWarp) {
-    if (lane < p.max_blocks) win = __ldg(table + lane);
-    if (32 + lane < p.max_blocks) win_next = __ldg(table + 32 + lane);
+    if (lane < tbl_len) win = __ldg(table + lane);
+    if (32 + lane < tbl_len) win_next = __ldg(table + 32 + lane);
   }
 
-  const int q0 = __ldg(p.cu_q + s);
-  const int n = __ldg(p.cu_q + s + 1) - q0;
-  const int L = __ldg(p.seq_lens + s);
-  // the rows [q0, q0 + n) of q and out must exist: out is written with plain
-  // stores, so a bad cu_q_lens entry skips the sequence instead
-  if (n < 0 || q0 < 0 || n > p.num_q_tokens - q0 || n > p.max_q_len || L < n ||
-      L > p.max_blocks * p.block_size) {
-    if (threadIdx.x == 0 && blockIdx.x == 0) record_error(p.err, kErrSeqLen);
-    return;
+  int q0, n, L;
+  if constexpr (SD) {
+    q0 = s;                  // the sequences' query rows
+    n = nseq;
+    L = p.partition_size;    // the keys of the partition
+    if (n < 1 || n > QC || s < 0 || n > p.num_q_tokens - s || qpart < 0 || qpart >= p.max_parts ||
+        tbl_len < L / p.block_size) {
+      if (threadIdx.x == 0) record_error(p.err, kErrSeqLen);
+      return;
+    }
+  } else {
+    q0 = __ldg(p.cu_q + s);
+    n = __ldg(p.cu_q + s + 1) - q0;
+    L = __ldg(p.seq_lens + s);
+    // the rows [q0, q0 + n) of q and out must exist: out is written with plain
+    // stores, so a bad cu_q_lens entry skips the sequence instead
+    if (n < 0 || q0 < 0 || n > p.num_q_tokens - q0 || n > p.max_q_len || L < n ||
+        L > p.max_blocks * p.block_size) {
+      if (threadIdx.x == 0 && blockIdx.x == 0) record_error(p.err, kErrSeqLen);
+      return;
+    }
+    if (cta * QC >= n) return;
   }
-  if (cta * QC >= n) return;
   if ((smem_addr(smem) & 1023u) != 0) {  // the swizzle needs 1024-byte atoms
     if (threadIdx.x == 0) record_error(p.err, kErrSmemAlign);
     return;
   }
   const int tiles = cta * QC + QT < n ? 2 : 1;          // the second tile may hold no new token
-  const int pos0 = L - n;                               // position of new token 0
-  const int kv_end = pos0 + min(n, (cta + 1) * QC);     // keys 0..kv_end-1 are needed
+  // position of new token 0 (SD: past every key, so nothing is masked)
+  const int pos0 = SD ? (1 << 29) : L - n;
+  const int kv_end = SD ? L : pos0 + min(n, (cta + 1) * QC);  // keys 0..kv_end-1 are needed
   const int n_stages = (kv_end + kPfKeys - 1) / kPfKeys;
   // stages a tile needs: tile 0's rows end QT tokens before tile 1's, so its
-  // products stop a stage earlier unless tile 1 is empty
-  auto tile_stages = [&](int t) { return (pos0 + min(n, cta * QC + (t + 1) * QT) + kPfKeys - 1) / kPfKeys; };
+  // products stop a stage earlier unless tile 1 is empty (SD: all of them)
+  auto tile_stages = [&](int t) {
+    return SD ? n_stages : (pos0 + min(n, cta * QC + (t + 1) * QT) + kPfKeys - 1) / kPfKeys;
+  };
   uint8_t *qs = smem + Lay::Q_OFF;
   uint8_t *stages = smem + Lay::STAGE_OFF;
   uint8_t *codes = smem + Lay::CODE_OFF;
@@ -313,7 +355,7 @@ __global__ void __launch_bounds__(pf_threads(is_byte(KVT)), 1) prefill_kernel(co
     int phys = __shfl_sync(0xffffffffu, win, (e0 & 31) + (lane & (bpt - 1)));
     if (((e0 + bpt) & 31) == 0) {
       win = win_next;
-      win_next = e0 + bpt + 32 + lane < p.max_blocks ? __ldg(table + e0 + bpt + 32 + lane) : 0;
+      win_next = e0 + bpt + 32 + lane < tbl_len ? __ldg(table + e0 + bpt + 32 + lane) : 0;
     }
     if (lane < nblk && (phys < 0 || phys >= p.num_blocks)) {
       record_error(p.err, kErrBlockIndex);
@@ -580,12 +622,36 @@ __global__ void __launch_bounds__(pf_threads(is_byte(KVT)), 1) prefill_kernel(co
         // so the last two may both be pending and a parity wait would take the
         // older phase for the newer)
         tc_fence_after_sync();
+        const float inv = vsc / l;
+        if constexpr (SD) {
+          // the row's split-K partial of partition qpart: O / l and (m, l),
+          // kept in L2 for the merge (rows past the item's sequences skipped)
+          const int rows = min(kPfTileRows, (n - t * QT) * G);
+          const bool mine = r < rows;
+          const int sr = q0 + t * QT + r / G;
+          const size_t idx = (static_cast<size_t>(sr) * p.max_parts + qpart) * p.num_q_heads + h * G + r % G;
+          float *po = p.part_o + idx * D;
+          const uint64_t keep = l2_policy_evict_last();
+  #pragma unroll
+          for (int c = 0; c < D; c += 32) {
+            uint32_t ov[32];
+            tc_ld32(trow + 2 * kPfKeys + c, ov);
+            if (mine) {
+  #pragma unroll
+              for (int j = 0; j < 32; j += 4)
+                st_global_f4_hint(po + c + j,
+                                  make_float4(__uint_as_float(ov[j]) * inv, __uint_as_float(ov[j + 1]) * inv,
+                                              __uint_as_float(ov[j + 2]) * inv, __uint_as_float(ov[j + 3]) * inv),
+                                  keep);
+            }
+          }
+          if (mine) st_global_f2_hint(reinterpret_cast<float *>(p.part_ml + idx), m, l, keep);
+        } else {
         // O / l goes through this tile's q buffer (its products have all
         // completed, so no product reads it any more): each thread writes
         // its row, 16-byte chunk ch at ch ^ (row mod 8), then the tile's
         // threads copy whole rows out, each warp instruction two rows of
         // 16-bit outputs (rows past the sequence's new tokens are skipped).
-        const float inv = vsc / l;
         constexpr int RB = D * 2;      // bytes of an output row
         constexpr int CPR = RB / 16;   // 16-byte chunks of a row
         uint8_t *stg = qs + t * Lay::Q_TILE;
@@ -614,6 +680,7 @@ __global__ void __launch_bounds__(pf_threads(is_byte(KVT)), 1) prefill_kernel(co
           const uint4 v = *reinterpret_cast<const uint4 *>(stg + rr * RB + ((ch ^ (rr & 7)) << 4));
           *reinterpret_cast<uint4 *>(obase + (rr / G) * tok_stride + (rr % G) * RB + ch * 16) = v;
         }
+        }  // SD
       } else {
         record_error(p.err, kErrTimeout);
         *abort = 1;
@@ -763,6 +830,22 @@ __global__ void __launch_bounds__(pf_threads(is_byte(KVT)), 1) prefill_kernel(co
 }
 
 template <int DT, int KVT, int D, int G>
+__global__ void __launch_bounds__(pf_threads(is_byte(KVT)), 1) prefill_kernel(const __grid_constant__ PrefillParams p) {
+  prefill_body<DT, KVT, D, G, false>(p);
+}
+
+// The decode's wide items (16-bit caches).  Launched as a programmatic
+// dependent of the decode's plan; once the plan has ended, it lets the decode
+// kernel start beside it (their items are disjoint), and that kernel waits
+// for this grid only before it ends.
+template <int DT, int D, int G>
+__global__ void __launch_bounds__(pf_threads(false), 1) wide_decode_kernel(const __grid_constant__ PrefillParams p) {
+  grid_dependency_wait();  // the plan, and everything before it
+  launch_dependents();
+  prefill_body<DT, DT, D, G, true>(p);
+}
+
+template <int DT, int KVT, int D, int G>
 pa_status launch_prefill(const PrefillParams &p, int num_seqs, int max_q_len, cudaStream_t stream) {
   using Lay = PfLayout<D, is_byte(KVT)>;
   constexpr int QC = kPfRows / G;
@@ -780,6 +863,44 @@ pa_status launch_prefill(const PrefillParams &p, int num_seqs, int max_q_len, cu
   prefill_kernel<DT, KVT, D, G><<<grid, pf_threads(is_byte(KVT)), Lay::SMEM, stream>>>(p);
   e = cudaGetLastError();
   return e == cudaSuccess ? PA_OK : cuda_fail(e);
+}
+
+// The wide kernel of one instantiation, as a programmatic dependent of the
+// kernel before it (the plan).
+template <int DT, int D, int G>
+pa_status launch_wide(const PrefillParams &p, int grid_x, cudaStream_t stream) {
+  using Lay = PfLayout<D, false>;
+  static bool configured[64];  // per device: dynamic shared memory already allowed
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (dev < 0 || dev >= 64 || !configured[dev]) {
+    e = cudaFuncSetAttribute(wide_decode_kernel<DT, D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::SMEM);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (dev >= 0 && dev < 64) configured[dev] = true;
+  }
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid_x, 1, p.num_kv_heads);
+  cfg.blockDim = dim3(pf_threads(false));
+  cfg.dynamicSmemBytes = Lay::SMEM;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, wide_decode_kernel<DT, D, G>, p);
+  return e == cudaSuccess ? PA_OK : cuda_fail(e);
+}
+
+template <int DT, int D>
+pa_status wide_by_group(int G, const PrefillParams &p, int grid_x, cudaStream_t stream) {
+  switch (G) {
+    case 2: return launch_wide<DT, D, 2>(p, grid_x, stream);
+    case 4: return launch_wide<DT, D, 4>(p, grid_x, stream);
+    case 8: return launch_wide<DT, D, 8>(p, grid_x, stream);
+  }
+  return PA_ERR_UNSUPPORTED;
 }
 
 template <int DT, int KVT, int D>

@@ -185,6 +185,31 @@ def test_shared_prefix_matches_oracle(cache_dtype, q_dtype, group, bs):
         _check(w, run.out, ref)
 
 
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("group", [2, 4, 8])
+@pytest.mark.parametrize("bs,d", [(8, 128), (16, 128), (32, 128), (16, 64)])
+def test_wide_shared_prefix_matches_oracle(dtype, group, bs, d):
+    """Many sequences sharing a prefix: runs of 256 / G sequences (from a
+    multiple of that count) whose tables agree over a whole partition are
+    decoded on the tensor cores as wide items, the rest as usual.  Two full
+    runs and a short third one; the prefix (300 tokens) ends inside a
+    partition, so its last partition is only partly shared; partitions of
+    64 tokens and the automatic size."""
+    Hkv = 2
+    W_seqs = 256 // group
+    S = 2 * W_seqs + 7
+    w = W.make_workload("qwen3-prefix", 101 + group + bs + d, device=G.DEV, overrides=dict(
+        S=S, prefix=304 if bs == 16 else 320, suffix_lo=1, suffix_hi=200, Hq=Hkv * group, Hkv=Hkv, d=d,
+        bs=bs, cache_dtype=dtype, q_dtype=dtype, src_dtype=dtype))
+    ref = G.oracle_decode(w, G.oracle_cache(w))
+    for P in (64, 0):
+        run = G.GpuRun(w, partition_size=P).setup()
+        run.step()
+        torch.cuda.synchronize()
+        assert int(run.err.item()) == 0
+        _check(w, run.out, ref)
+
+
 @pytest.mark.parametrize("cache_dtype,q_dtype", SHARED_DTYPES)
 @pytest.mark.parametrize("bs", [16, 32])
 @pytest.mark.parametrize("heads", [(2, 2), (4, 2), (8, 1)])
