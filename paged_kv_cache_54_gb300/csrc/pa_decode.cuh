@@ -388,12 +388,13 @@ __global__ void __launch_bounds__(1024) plan_kernel(const __grid_constant__ Deco
 //   out = sum_q w_q o_q / sum_q w_q,  w_q = exp2(m_q - M) l_q,  M = max_q m_q
 // (the flash-decoding reduction; o_q is normalised by its own l_q).  Lane j
 // holds the weights of partitions j and j + 32 (longer sequences take
-// windows of 64), then reads its D / 32 columns of B partial rows at a
-// time, all in flight (B = 8 when no sequence has more than 8 partitions:
-// fewer registers, more warps resident).
+// windows of 64), then reads its D / 32 columns of 8 partial rows at a
+// time, all in flight (75 registers a thread; 16 rows in flight took 119
+// and fewer warps were resident).
 constexpr int kMergeThreads = 256;
+constexpr int kMergeRows = 8;
 
-template <int QT, int D, int B>
+template <int QT, int D>
 __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const __grid_constant__ DecodeParams p) {
   constexpr int E = D / 32;  // columns per lane
   const int lane = threadIdx.x & 31;
@@ -437,10 +438,10 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const __grid_const
     for (int o = 16; o; o >>= 1) ws += __shfl_xor_sync(0xffffffffu, ws, o);
     den += ws;
     const int cnt = min(64, nP - w0);
-    for (int k0 = 0; k0 < cnt; k0 += B) {
-      float v[B][E];
+    for (int k0 = 0; k0 < cnt; k0 += kMergeRows) {
+      float v[kMergeRows][E];
 #pragma unroll
-      for (int j = 0; j < B; ++j) {
+      for (int j = 0; j < kMergeRows; ++j) {
         if (k0 + j < cnt) {
           const float *po = p.part_o + (base + static_cast<size_t>(w0 + k0 + j) * qstride) * D + lane * E;
           if constexpr (E == 4) {
@@ -453,7 +454,7 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const __grid_const
         }
       }
 #pragma unroll
-      for (int j = 0; j < B; ++j) {
+      for (int j = 0; j < kMergeRows; ++j) {
         const int k = k0 + j;  // warp-uniform
         if (k < cnt) {
           const float wk = __shfl_sync(0xffffffffu, k < 32 ? wt0 : wt1, k & 31);
@@ -1480,8 +1481,7 @@ pa_status launch_decode(DecodeParams p, const DeviceInfo &dev, cudaStream_t stre
     cfg.gridDim = dim3(static_cast<unsigned>((warps * 32 + kMergeThreads - 1) / kMergeThreads));
     cfg.blockDim = dim3(kMergeThreads);
     cfg.dynamicSmemBytes = 0;
-    e = p.max_parts <= 8 ? cudaLaunchKernelEx(&cfg, merge_kernel<QT, D, 8>, p)
-                         : cudaLaunchKernelEx(&cfg, merge_kernel<QT, D, 16>, p);
+    e = cudaLaunchKernelEx(&cfg, merge_kernel<QT, D>, p);
     if (e != cudaSuccess) return cuda_fail(e);
   }
   e = cudaGetLastError();
