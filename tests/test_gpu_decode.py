@@ -210,6 +210,42 @@ def test_wide_shared_prefix_matches_oracle(dtype, group, bs, d):
         _check(w, run.out, ref)
 
 
+@pytest.mark.parametrize("group", [2, 8])
+def test_wide_chunk_broken_by_a_copied_block(group):
+    """One sequence in the middle of a would-be wide chunk reads one shared
+    block through a copy (same contents, another physical block): the plan
+    must find the rows differ, so that partition of the chunk is decoded as
+    ordinary items, and every output still equals the oracle's."""
+    import paged_kv_cache_54_gb300 as pa
+    from oracle.cache import PagedKVCache
+    Hkv, bs, d = 2, 16, 128
+    W_seqs = 256 // group
+    S = 2 * W_seqs
+    w = W.make_workload("qwen3-prefix", 211 + group, device=G.DEV, overrides=dict(
+        S=S, prefix=256, suffix_lo=1, suffix_hi=100, Hq=Hkv * group, Hkv=Hkv, d=d, bs=bs,
+        cache_dtype="bf16", q_dtype="bf16", src_dtype="bf16"))
+    run = G.GpuRun(w, partition_size=64).setup()
+    run.step()
+    torch.cuda.synchronize()
+    # a free physical block, and the sequence and entry that will use it
+    used = {int(b) for srow, L in zip(w.block_tables, w.seq_lens) for b in srow[:-(-int(L) // bs)]}
+    free = next(b for b in range(w.num_blocks) if b not in used)
+    s_star, entry = W_seqs // 2 + 1, 5          # partition 1 (entries 4..7) of chunk 0
+    old = int(w.block_tables[s_star, entry])
+    pa.pa_copy_blocks(run.kc, run.vc, torch.tensor([[old, free]], dtype=torch.int64, device=G.DEV),
+                      cache_dtype="bf16", device_error=run.err)
+    w.block_tables = w.block_tables.copy()
+    w.block_tables[s_star, entry] = free
+    run.bt = torch.from_numpy(w.block_tables).to(G.DEV)
+    run.decode()
+    torch.cuda.synchronize()
+    assert int(run.err.item()) == 0
+    c = G.oracle_cache(w)
+    c.copy_blocks([(old, free)])
+    ref = G.oracle_decode(w, c)
+    _check(w, run.out, ref)
+
+
 @pytest.mark.parametrize("cache_dtype,q_dtype", SHARED_DTYPES)
 @pytest.mark.parametrize("bs", [16, 32])
 @pytest.mark.parametrize("heads", [(2, 2), (4, 2), (8, 1)])
