@@ -65,6 +65,17 @@ __device__ __forceinline__ void i8x4_to_half2x2(uint32_t w, uint32_t &lo, uint32
   hi = *reinterpret_cast<const uint32_t *>(&y);
 }
 
+// Four INT8 codes -> two __half2 of 1152 + c (exact integers in
+// [1024, 1279]): the widening above without its subtraction.  For a sum
+// over codes, sum_i (1152 + c_i) x_i = sum_i c_i x_i + 1152 sum_i x_i, so a
+// caller that removes 1152 sum_i x_i once saves the subtraction per pair.
+__device__ __forceinline__ void i8x4_to_half2x2_offset(uint32_t w, uint32_t &lo, uint32_t &hi) {
+  const uint32_t u = w ^ 0x80808080u;
+  asm("prmt.b32 %0, %1, %2, 0x4140;" : "=r"(lo) : "r"(u), "r"(0x64646464u));
+  asm("prmt.b32 %0, %1, %2, 0x4342;" : "=r"(hi) : "r"(u), "r"(0x64646464u));
+}
+constexpr float kI8Offset = 1152.f;
+
 // two one-byte codes (low byte = first element) -> __half2 bits (exact:
 // every e4m3 / e5m2 value and every int8 is an fp16 value)
 template <int DT>
@@ -425,5 +436,21 @@ __device__ __forceinline__ void launch_dependents() { asm volatile("griddepcontr
 __device__ __forceinline__ uint4 lds128(const void *p) {
   return *reinterpret_cast<const uint4 *>(p);
 }
+
+// Per-thread asynchronous copy of BYTES (8 or 16, both addresses aligned to
+// it) from global to shared memory, bypassing L1 for 16.  Copies are grouped
+// by commit; cp_async_wait<N>() returns once at most N of the thread's most
+// recent groups are still in flight.
+template <int BYTES>
+__device__ __forceinline__ void cp_async(void *smem_dst, const void *gmem_src) {
+  static_assert(BYTES == 8 || BYTES == 16, "cp.async of 8 or 16 bytes");
+  if constexpr (BYTES == 16)
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(smem_dst)), "l"(gmem_src) : "memory");
+  else
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(smem_addr(smem_dst)), "l"(gmem_src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
 }  // namespace pa

@@ -384,21 +384,31 @@ __global__ void __launch_bounds__(1024) plan_kernel(const __grid_constant__ Deco
 // ----------------------------------------------------------------------------
 // merge: combine the partials of sequences split into several partitions
 // ----------------------------------------------------------------------------
-// One warp per (sequence, query head), eight to a CTA:
+// One warp per (sequence, query head), kMergeWarps to a CTA:
 //   out = sum_q w_q o_q / sum_q w_q,  w_q = exp2(m_q - M) l_q,  M = max_q m_q
 // (the flash-decoding reduction; o_q is normalised by its own l_q).  Lane j
 // holds the weights of partitions j and j + 32 (longer sequences take
-// windows of 64), then reads its D / 32 columns of 8 partial rows at a
-// time, all in flight (75 registers a thread; 16 rows in flight took 119
-// and fewer warps were resident).
-constexpr int kMergeThreads = 256;
-constexpr int kMergeRows = 8;
+// windows of 64) and owns D / 32 columns of every partial row.  The rows
+// stream through a ring of kMergeRing rows of shared memory per warp: each
+// lane copies its own columns with cp.async, so kMergeRing rows stay in
+// flight with few registers live (16 rows a warp at 24 warps an SM; held in
+// registers, 8 rows took 75 registers for the same residency), and the
+// first copies leave before the weights are read.  A lane reads back only
+// what it copied itself.
+#ifndef PA_MERGE_RING
+#define PA_MERGE_RING 16
+#endif
+constexpr int kMergeWarps = 4;
+constexpr int kMergeThreads = 32 * kMergeWarps;
+constexpr int kMergeRing = PA_MERGE_RING;
 
 template <int QT, int D>
 __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const __grid_constant__ DecodeParams p) {
   constexpr int E = D / 32;  // columns per lane
-  const int lane = threadIdx.x & 31;
-  const long long gw = (blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x) >> 5;
+  constexpr int CB = E * 4;  // bytes a lane copies from a row
+  __shared__ __align__(16) float ring[kMergeWarps][kMergeRing][D];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const long long gw = blockIdx.x * static_cast<long long>(kMergeWarps) + warp;
   if (gw >= static_cast<long long>(p.num_seqs) * p.num_q_heads) return;
   const int s = static_cast<int>(gw / p.num_q_heads);
   const int hq = static_cast<int>(gw % p.num_q_heads);
@@ -410,7 +420,16 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const __grid_const
   grid_dependency_wait();
   const size_t qstride = static_cast<size_t>(p.num_q_heads);
   const size_t base = static_cast<size_t>(s) * p.max_parts * qstride + hq;
-  const float2 *ml = p.part_ml + base;  // partition q at ml[q * num_q_heads]
+  const float2 *ml = p.part_ml + base;                  // partition q at ml[q * qstride]
+  const float *po = p.part_o + base * D + lane * E;     // partition q at po + q * qstride * D
+  float *slot = &ring[warp][0][lane * E];               // ring row r at slot + r * D
+  // one commit group per row, empty past the last partition, so that the
+  // group of row q is always the q-th committed
+#pragma unroll
+  for (int j = 0; j < kMergeRing; ++j) {
+    if (j < nP) cp_async<CB>(slot + j * D, po + j * qstride * D);
+    cp_async_commit();
+  }
   float M = -INFINITY;
   float2 a0 = make_float2(-INFINITY, 0.f), a1 = make_float2(-INFINITY, 0.f);
   if (nP <= 64) {
@@ -438,32 +457,27 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const __grid_const
     for (int o = 16; o; o >>= 1) ws += __shfl_xor_sync(0xffffffffu, ws, o);
     den += ws;
     const int cnt = min(64, nP - w0);
-    for (int k0 = 0; k0 < cnt; k0 += kMergeRows) {
-      float v[kMergeRows][E];
-#pragma unroll
-      for (int j = 0; j < kMergeRows; ++j) {
-        if (k0 + j < cnt) {
-          const float *po = p.part_o + (base + static_cast<size_t>(w0 + k0 + j) * qstride) * D + lane * E;
-          if constexpr (E == 4) {
-            const float4 t = *reinterpret_cast<const float4 *>(po);
-            v[j][0] = t.x; v[j][1] = t.y; v[j][2] = t.z; v[j][3] = t.w;
-          } else {
-            const float2 t = *reinterpret_cast<const float2 *>(po);
-            v[j][0] = t.x; v[j][1] = t.y;
-          }
-        }
+    for (int k = 0; k < cnt; ++k) {  // warp-uniform
+      const int q = w0 + k;
+      cp_async_wait<kMergeRing - 1>();  // row q has landed
+      const float *src = slot + (q % kMergeRing) * D;
+      float v[E];
+      if constexpr (E == 4) {
+        const float4 t = *reinterpret_cast<const float4 *>(src);
+        v[0] = t.x; v[1] = t.y; v[2] = t.z; v[3] = t.w;
+      } else {
+        const float2 t = *reinterpret_cast<const float2 *>(src);
+        v[0] = t.x; v[1] = t.y;
       }
+      // the slot, read, takes row q + kMergeRing
+      if (q + kMergeRing < nP) cp_async<CB>(slot + (q % kMergeRing) * D, po + (q + kMergeRing) * qstride * D);
+      cp_async_commit();
+      const float wk = __shfl_sync(0xffffffffu, k < 32 ? wt0 : wt1, k & 31);
 #pragma unroll
-      for (int j = 0; j < kMergeRows; ++j) {
-        const int k = k0 + j;  // warp-uniform
-        if (k < cnt) {
-          const float wk = __shfl_sync(0xffffffffu, k < 32 ? wt0 : wt1, k & 31);
-#pragma unroll
-          for (int e = 0; e < E; ++e) acc[e] = fmaf(wk, v[j][e], acc[e]);
-        }
-      }
+      for (int e = 0; e < E; ++e) acc[e] = fmaf(wk, v[e], acc[e]);
     }
   }
+  cp_async_wait<0>();
   const float inv = den > 0.f ? 1.f / den : 0.f;
   uint16_t *out = static_cast<uint16_t *>(p.out) + (static_cast<size_t>(s) * p.num_q_heads + hq) * D + lane * E;
   if constexpr (E == 4) {
@@ -856,11 +870,25 @@ struct MmaState {
   static constexpr int LCH = (D / 4) / CE;  // chunks of a K row per lane
   static constexpr int DPL = D / 8;         // output columns per lane group
   static constexpr int QS = QM;  // query rows per warp in the combine scratch
+  // INT8 codes enter the products as 1152 + c (two instructions fewer per
+  // four codes); the offset comes off the scores as 1152 * sum(q) and off
+  // the output as 1152 * l, with l summed from the rounded weights the
+  // products used
+  static constexpr bool I8OFF = KV == kI8;
 
   uint32_t qb[KSTEPS][2];
   float oacc[MTILES][4];
   float m2[2], l2[2];
   float qk_mult;
+  float kcorr[2];  // (INT8) -1152 * sum(q) * qk_mult of query columns 2tq, 2tq+1
+
+  __device__ __forceinline__ static void widen4(uint32_t w, uint32_t &lo, uint32_t &hi) {
+    if constexpr (I8OFF) {
+      i8x4_to_half2x2_offset(w, lo, hi);
+    } else {
+      byte4_to_half2x2<KV>(w, lo, hi);
+    }
+  }
 
   // 16-byte chunk j of a K row read by lane tq: contiguous chunks on the
   // swizzled layout, chunks tq, tq+4, ... on the linear one (fewest bank
@@ -930,6 +958,21 @@ struct MmaState {
       qb[kk][1] = qw[2 * kk + 1];
     }
     qk_mult = qk_scale / f;
+    if constexpr (I8OFF) {
+      // sum of the fp16 q the products use, row gq, then columns 2tq, 2tq+1
+      float qs = 0.f;
+#pragma unroll
+      for (int w = 0; w < QW; ++w) {
+        const float2 x = half2_bits_to_float2<kF16>(qw[w]);
+        qs += x.x + x.y;
+      }
+      qs += __shfl_xor_sync(0xffffffffu, qs, 1);
+      qs += __shfl_xor_sync(0xffffffffu, qs, 2);
+      const float qs0 = __shfl_sync(0xffffffffu, qs, (2 * tq) * 4);
+      const float qs1 = __shfl_sync(0xffffffffu, qs, (2 * tq + 1) * 4);
+      kcorr[0] = -kI8Offset * qs0 * qk_mult;
+      kcorr[1] = -kI8Offset * qs1 * qk_mult;
+    }
 #pragma unroll
     for (int mi = 0; mi < MTILES; ++mi)
 #pragma unroll
@@ -970,7 +1013,7 @@ struct MmaState {
                                                  uint32_t &lo, uint32_t &hi) {
     const uint32_t b = col & 3;
     const uint32_t two = prmt(ra[col / 4], rb[col / 4], b | ((4 + b) << 4) | ((b + 1) << 8) | ((5 + b) << 12));
-    byte4_to_half2x2<KV>(two, lo, hi);
+    widen4(two, lo, hi);
   }
 
   __device__ __forceinline__ void slice(const uint8_t *Kb, const uint8_t *Vb, int row0, int n, float v_scale) {
@@ -999,15 +1042,21 @@ struct MmaState {
         a3 = k_reg(k1, kk, 1);
       } else {  // local elements 4kk..4kk+3 are one word of the row's chunk
         const int e = 4 * kk;
-        byte4_to_half2x2<KV>(w32(k0[e / CE], (e % CE) / 4), a0, a2);
-        byte4_to_half2x2<KV>(w32(k1[e / CE], (e % CE) / 4), a1, a3);
+        widen4(w32(k0[e / CE], (e % CE) / 4), a0, a2);
+        widen4(w32(k1[e / CE], (e % CE) / 4), a1, a3);
       }
       mma16816<MT>(sacc[kk & 3], a0, a1, a2, a3, qb[kk][0], qb[kk][1]);
     }
     float sc[4];
 #pragma unroll
-    for (int k = 0; k < 4; ++k)
-      sc[k] = ((sacc[0][k] + sacc[1][k]) + (sacc[2][k] + sacc[3][k])) * qk_mult;
+    for (int k = 0; k < 4; ++k) {
+      const float sum = (sacc[0][k] + sacc[1][k]) + (sacc[2][k] + sacc[3][k]);
+      if constexpr (I8OFF) {
+        sc[k] = fmaf(sum, qk_mult, kcorr[k & 1]);
+      } else {
+        sc[k] = sum * qk_mult;
+      }
+    }
     // rows gq (regs 0,1) and gq+8 (regs 2,3); columns 2tq, 2tq+1
     if (gq >= n) sc[0] = sc[1] = -INFINITY;
     if (gq + 8 >= n) sc[2] = sc[3] = -INFINITY;
@@ -1035,11 +1084,17 @@ struct MmaState {
     }
     const float p0 = exp2f(sc[0] - m2[0]), p1 = exp2f(sc[1] - m2[1]);
     const float p2 = exp2f(sc[2] - m2[0]), p3 = exp2f(sc[3] - m2[1]);
-    l2[0] += p0 + p2;
-    l2[1] += p1 + p3;
     // P^T as the B operand: query gq, tokens (2tq, 2tq+8) and (2tq+1, 2tq+9)
     const uint32_t packA = pack2_rn<MT>(p0, p2);  // query 2tq
     const uint32_t packB = pack2_rn<MT>(p1, p3);  // query 2tq+1
+    if constexpr (I8OFF) {  // the weights as rounded for the products
+      const float2 ra = half2_bits_to_float2<kF16>(packA), rb = half2_bits_to_float2<kF16>(packB);
+      l2[0] += ra.x + ra.y;
+      l2[1] += rb.x + rb.y;
+    } else {
+      l2[0] += p0 + p2;
+      l2[1] += p1 + p3;
+    }
     const int src0 = (2 * tq) * 4 + (gq >> 1), src1 = (2 * tq + 1) * 4 + (gq >> 1);
     const uint32_t xA0 = __shfl_sync(0xffffffffu, packA, src0), xB0 = __shfl_sync(0xffffffffu, packB, src0);
     const uint32_t xA1 = __shfl_sync(0xffffffffu, packA, src1), xB1 = __shfl_sync(0xffffffffu, packB, src1);
@@ -1126,8 +1181,14 @@ struct MmaState {
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         const int c = c0 + u;
-        va[u] = (c < MTILES ? oacc[c % MTILES][0] : oacc[c % MTILES][2]) * v_scale;
-        vb[u] = (c < MTILES ? oacc[c % MTILES][1] : oacc[c % MTILES][3]) * v_scale;
+        va[u] = (c < MTILES ? oacc[c % MTILES][0] : oacc[c % MTILES][2]);
+        vb[u] = (c < MTILES ? oacc[c % MTILES][1] : oacc[c % MTILES][3]);
+        if constexpr (I8OFF) {
+          va[u] = fmaf(-kI8Offset, ls0, va[u]);
+          vb[u] = fmaf(-kI8Offset, ls1, vb[u]);
+        }
+        va[u] *= v_scale;
+        vb[u] *= v_scale;
       }
       const int d = vcol(gq, c0);
       if (qa < ncols) *reinterpret_cast<float4 *>(so.at(qa, d)) = make_float4(va[0], va[1], va[2], va[3]);
@@ -1478,7 +1539,7 @@ pa_status launch_decode(DecodeParams p, const DeviceInfo &dev, cudaStream_t stre
   if (e != cudaSuccess) return cuda_fail(e);
   if (p.max_parts > 1) {
     const long long warps = static_cast<long long>(p.num_seqs) * p.num_q_heads;
-    cfg.gridDim = dim3(static_cast<unsigned>((warps * 32 + kMergeThreads - 1) / kMergeThreads));
+    cfg.gridDim = dim3(static_cast<unsigned>((warps + kMergeWarps - 1) / kMergeWarps));
     cfg.blockDim = dim3(kMergeThreads);
     cfg.dynamicSmemBytes = 0;
     e = cudaLaunchKernelEx(&cfg, merge_kernel<QT, D>, p);
