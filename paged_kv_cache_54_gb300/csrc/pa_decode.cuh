@@ -123,150 +123,148 @@ __host__ __device__ constexpr int query_capacity(int G) { return G == 1 ? (PA_SH
 // ----------------------------------------------------------------------------
 // plan: list the work items in sequence order; reset the claim counter
 // ----------------------------------------------------------------------------
-// Partition q of sequence s is "full" when all its P tokens exist.  Sequence
-// s joins the item of s-1 for partition q when both partitions are full, s is
-// not at a multiple of kmax, and their block-table entries over the
-// partition are equal; otherwise it leads an item of its own.
+// Work is indexed by slot (s, q), which exists when q is below the
+// sequence's partition count.  Partition q of sequence s is "full" when all
+// its P tokens exist.  Slot (s, q) joins the item of (s-1, q) when s may join
+// its predecessor, partition q is full in both and their block-table entries
+// over it are equal; otherwise it leads an item of its own and takes the
+// following slots (s+1, q), ... of its kmax group that join.
+//
+// The plan is one cluster of CTAs (its work is a few thousand small steps,
+// and more SMs finish it sooner).  Each CTA owns a run of whole kmax groups
+// (whole wide chunks when they are looked for), so every decision it makes
+// needs only its own sequences' flags:
+//  1) its rows of the block tables start towards shared memory; its lengths;
+//     its flags cleared or set;
+//  2) the rows of s and s-1 (s inside the run, not its first) compared in
+//     chunks of up to 4 entries (a chunk never straddles two partitions),
+//     consecutive threads on consecutive chunks of one row: a mismatch flags
+//     (s, q) and clears the wide flag of its (chunk, partition); so does a
+//     sequence of the chunk whose partition is not full, or that has one
+//     partition only;
+//  3) each thread takes a run of consecutive slots and counts the items they
+//     lead; a block scan places them within the CTA, and the CTAs' totals,
+//     stored into every CTA's shared memory before one cluster barrier,
+//     place the CTA; the items are written in slot order.
 
-// Exclusive prefix sum over the 1024 threads of the block; *total = sum.
-__device__ __forceinline__ int block_exclusive_scan(int x, int *warp_tot, int *total) {
+// Exclusive prefix sums of two counts over the 1024 threads of the block;
+// *total = the block's sums.
+__device__ __forceinline__ int2 block_exclusive_scan2(int x, int y, int2 *warp_tot, int2 *total) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  int v = x;
+  int vx = x, vy = y;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    const int y = __shfl_up_sync(0xffffffffu, v, o);
-    if (lane >= o) v += y;
+    const int ax = __shfl_up_sync(0xffffffffu, vx, o), ay = __shfl_up_sync(0xffffffffu, vy, o);
+    if (lane >= o) {
+      vx += ax;
+      vy += ay;
+    }
   }
-  if (lane == 31) warp_tot[warp] = v;
+  if (lane == 31) warp_tot[warp] = make_int2(vx, vy);
   __syncthreads();
   if (warp == 0) {
-    int t = warp_tot[lane];
+    int2 t = warp_tot[lane];
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, t, o);
-      if (lane >= o) t += y;
+      const int ax = __shfl_up_sync(0xffffffffu, t.x, o), ay = __shfl_up_sync(0xffffffffu, t.y, o);
+      if (lane >= o) {
+        t.x += ax;
+        t.y += ay;
+      }
     }
     warp_tot[lane] = t;  // inclusive over warps
   }
   __syncthreads();
-  const int ex = (warp ? warp_tot[warp - 1] : 0) + v - x;
+  const int2 before = warp ? warp_tot[warp - 1] : make_int2(0, 0);
   *total = warp_tot[31];
-  __syncthreads();
-  return ex;
+  return make_int2(before.x + vx - x, before.y + vy - y);
 }
 
-// Plan tables live in shared memory when they fit, else in the workspace.
-constexpr int kPlanSmemSeqs = 2048;
-constexpr int kPlanWideFlags = 4096;  // (wide chunk, partition) flags in shared memory
-constexpr int kPlanSmemPairs = 12288;
-
-// Last index i in [0, n) with a[i] <= x (a non-decreasing, a[0] <= x).
-__device__ __forceinline__ int upper_index(const int *a, int n, int x) {
-  int lo = 0, hi = n - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (a[mid] <= x) lo = mid; else hi = mid - 1;
-  }
-  return lo;
-}
+constexpr int kPlanCluster = 8;             // CTAs of the plan's cluster (1 if a cluster cannot be had)
+constexpr int kPlanSmemSeqs = 2048;         // a CTA's lengths in shared memory up to this many
+constexpr int kPlanSmemSlots = 16384;       // a CTA's mismatch flags, one byte a slot
+constexpr int kPlanWideFlags = 4096;        // most (wide chunk, partition) flags
+constexpr int kPlanTableBytes = 96 * 1024;  // a CTA's block-table rows in shared memory up to this
 
 __global__ void __launch_bounds__(1024) plan_kernel(const __grid_constant__ DecodeParams p) {
-  __shared__ int warp_tot[32];
-  __shared__ int base;
+  __shared__ int2 warp_tot[32];
+  __shared__ int2 s_tot[kPlanCluster];  // the CTAs' item counts, stored by each CTA
   __shared__ int s_len[kPlanSmemSeqs];
-  __shared__ int s_off[kPlanSmemSeqs + 1];
-  __shared__ int s_choff[kPlanSmemSeqs];
-  __shared__ uint8_t s_join[kPlanSmemPairs];
+  __shared__ __align__(4) uint8_t s_mis[kPlanSmemSlots];
   __shared__ uint8_t s_wide[kPlanWideFlags];
+  extern __shared__ __align__(16) int4 s_tbl[];  // the run's table rows, when staged
   const int tid = threadIdx.x;
+  const int rank = cluster_rank(), nranks = cluster_ctas();
   const int P = p.partition_size;
   const int bpp = P / p.block_size;
   const int S = p.num_seqs;
+  const int MP = p.max_parts;
   launch_dependents();  // the decode grid may become resident; it waits for us
+  // This CTA has started: the others may store into its shared memory once
+  // they have waited on this arrival.
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
   // This kernel is a programmatic dependent of whatever precedes it on the
   // stream: it reads only the block tables and lengths (which the cache
   // writes before it never touch) and writes only this call's workspace, and
   // it waits for the preceding kernel before it ends, so the decode that
   // waits for it also follows every kernel before the call.
-  const bool in_smem = S <= kPlanSmemSeqs;
-  int *len = in_smem ? s_len : p.plan_len;
-  int *off = in_smem ? s_off : p.plan_off;
-  // pair k = (s, q): found by a binary search of the offsets when they are
-  // in shared memory, else read from the pair list in the workspace
-  auto pair_at = [&](int k) -> int2 {
-    if (!in_smem) return p.plan_pairs[k];
-    const int s = upper_index(off, S, k);
-    return make_int2(s, k - off[s]);
-  };
-  // A) lengths, partition counts, and the (s, q) pair list in sequence order
-  if (tid == 0) base = 0;
-  __syncthreads();
-  for (int b0 = 0; b0 < S; b0 += 1024) {
-    const int s = b0 + tid;
-    int nP = 0;
-    if (s < S) {
-      const int L = clamp_len(__ldg(p.seq_lens + s), p.len_cap, p.err);
-      nP = max(1, (L + P - 1) / P);
-      len[s] = L;
-    }
-    int tot;
-    const int ex = block_exclusive_scan(nP, warp_tot, &tot);
-    const int b = base;  // every thread reads the running base ...
-    if (s < S) {
-      const int o = b + ex;
-      off[s] = o;
-      if (!in_smem)
-        for (int q = 0; q < nP; ++q) p.plan_pairs[o + q] = make_int2(s, q);
-    }
-    __syncthreads();     // ... before thread 0 advances it
-    if (tid == 0) base = b + tot;
-    __syncthreads();
-  }
-  const int npairs = base;
-  if (tid == 0) off[S] = npairs;
-  uint8_t *join = npairs <= kPlanSmemPairs ? s_join : p.plan_join;
+  //
   // Wide chunks: W = p.wide_seqs sequences from a multiple of W whose rows
   // all agree over a full partition become one wide item (decoded on the
   // tensor cores by the wide kernel) when there are at least p.wide_min of
   // them and each has more than one partition.
   const int W = p.wide_seqs;
   const int nchunks = W > 0 ? (S + W - 1) / W : 0;
-  const bool use_wide = W > 0 && nchunks * p.max_parts <= kPlanWideFlags;
+  const bool use_wide = W > 0 && nchunks * MP <= kPlanWideFlags;
+  // rows are compared when items batch sequences or wide chunks are looked for
+  const bool compare = p.kmax > 1 || use_wide;
   // a sequence may join its predecessor: within a group of kmax (batched
   // items), or anywhere when wide chunks are looked for
   auto may_join = [&](int s) { return s > 0 && (use_wide || s % p.kmax != 0); };
+  // this CTA's run of sequences [s_lo, s_hi): whole units of U
+  const int U = use_wide ? W : p.kmax;  // (W is a multiple of kmax)
+  const int nu = (S + U - 1) / U;
+  const int s_lo = min(S, static_cast<int>(static_cast<long long>(rank) * nu / nranks) * U);
+  const int s_hi = min(S, static_cast<int>(static_cast<long long>(rank + 1) * nu / nranks) * U);
+  const int ns = s_hi - s_lo;
+  const bool len_smem = ns <= kPlanSmemSeqs;
+  auto length = [&](int s) {
+    return len_smem ? s_len[s - s_lo] : min(max(__ldg(p.seq_lens + s), 0), p.len_cap);
+  };
+  auto full = [&](int s, int q) { return length(s) >= (q + 1) * P; };
+  const int nslots = ns * MP;
+  uint8_t *mis = nslots <= kPlanSmemSlots ? s_mis : p.plan_join + static_cast<size_t>(s_lo) * MP;
+  const int c_lo = use_wide ? s_lo / W : 0;  // this CTA's first wide chunk
+  // 1) the table rows of the run start towards shared memory (they are
+  //    compared once the lengths are known); lengths; flags
+  const long long tbl_words = static_cast<long long>(ns) * p.max_blocks;
+  const bool tbl_smem = compare && p.plan_tbl_bytes > 0 && tbl_words * 4 <= p.plan_tbl_bytes;
+  const int32_t *tbl = p.block_tables + static_cast<size_t>(s_lo) * p.max_blocks;  // row s at (s - s_lo)
+  if (tbl_smem) {
+    const int4 *src = reinterpret_cast<const int4 *>(tbl);
+    for (int i = tid; i < tbl_words / 4; i += 1024) cp_async<16>(s_tbl + i, src + i);
+    cp_async_commit();
+    tbl = reinterpret_cast<const int32_t *>(s_tbl);
+  }
+  for (int s = s_lo + tid; s < s_hi; s += 1024) {
+    const int L = clamp_len(__ldg(p.seq_lens + s), p.len_cap, p.err);
+    if (len_smem) s_len[s - s_lo] = L;
+  }
+  if (compare)  // (the workspace region is 256-byte aligned and padded: whole words)
+    for (int i = tid * 4; i < nslots; i += 4 * 1024) *reinterpret_cast<uint32_t *>(mis + i) = 0u;
+  if (use_wide) {
+    for (int i = tid; i < ((ns + W - 1) / W) * MP; i += 1024) {
+      const int n = min(W, S - (c_lo + i / MP) * W);
+      s_wide[i] = (n >= p.wide_min && n >= 2) ? 1 : 0;
+    }
+  }
+  if (tbl_smem) cp_async_wait<0>();
   __syncthreads();
-  if (p.kmax > 1 || use_wide) {  // (without batching every pair is an item of its own)
-    // B) does pair (s, q) join the item of (s-1, q)?  It may when may_join(s)
-    //    and partition q is full in both sequences; it does when their
-    //    block-table rows agree over the partition.
-    //  B1: the candidates, one thread per pair
-    for (int k = tid; k < npairs; k += 1024) {
-      const int2 sq = pair_at(k);
-      const int need = (sq.y + 1) * P;
-      join[k] = (may_join(sq.x) && len[sq.x] >= need && len[sq.x - 1] >= need) ? 1 : 0;
-    }
-    //  B2: the rows compared in chunks of up to 4 entries (a chunk never
-    //      straddles two partitions), consecutive threads on consecutive
-    //      chunks of one row pair (coalesced); a mismatch clears the candidate
-    //      of its partition.  Sequence s has nfull(s) * cpp chunks, nfull(s)
-    //      being the partitions full in s and in s-1.
+  // 2) the rows compared
+  if (compare) {
     const int cpp = (bpp + 3) >> 2;  // chunks per partition
-    int *choff = in_smem ? s_choff : p.plan_choff;
-    if (tid == 0) base = 0;
-    __syncthreads();
-    for (int b0 = 0; b0 < S; b0 += 1024) {
-      const int s = b0 + tid;
-      const int c = (s < S && may_join(s)) ? (min(len[s], len[s - 1]) / P) * cpp : 0;
-      int tot;
-      const int ex = block_exclusive_scan(c, warp_tot, &tot);
-      const int b = base;
-      if (s < S) choff[s] = b + ex;
-      __syncthreads();
-      if (tid == 0) base = b + tot;
-      __syncthreads();
-    }
-    const int nch = base;
+    const int cpr = MP * cpp;        // chunk slots per sequence
+    const int nch = ns * cpr;
     // 16-byte loads when every chunk is four aligned entries
     const bool vec = (bpp & 3) == 0 && (p.max_blocks & 3) == 0 &&
                      (reinterpret_cast<uintptr_t>(p.block_tables) & 15) == 0;
@@ -275,107 +273,115 @@ __global__ void __launch_bounds__(1024) plan_kernel(const __grid_constant__ Deco
     for (int u0 = 0; u0 < nch; u0 += 4 * 1024) {
       int4 x[4], y[4];
       int js[4], jq[4], jn[4];
-  #pragma unroll
+#pragma unroll
       for (int i = 0; i < 4; ++i) {
         const int u = u0 + i * 1024 + tid;
         js[i] = -1;
         jq[i] = jn[i] = 0;
         x[i] = y[i] = make_int4(0, 0, 0, 0);
         if (u < nch) {
-          const int sq = upper_index(choff, S, u);
-          const int c = u - choff[sq];
+          const int sl = u / cpr;  // sequence s_lo + sl
+          const int c = u - sl * cpr;
           const int q = c / cpp;
-          const int e0 = q * bpp + (c - q * cpp) * 4;  // first entry of the chunk
-          const int nv = min(4, (q + 1) * bpp - e0);   // entries of the chunk (1..4)
-          js[i] = sq;
-          jq[i] = q;
-          jn[i] = nv;
-          const int32_t *ra = p.block_tables + static_cast<size_t>(sq) * p.max_blocks + e0;
-          const int32_t *rb = ra - p.max_blocks;
-          if (vec) {
-            x[i] = __ldg(reinterpret_cast<const int4 *>(ra));
-            y[i] = __ldg(reinterpret_cast<const int4 *>(rb));
-          } else {
-            x[i] = make_int4(__ldg(ra), nv > 1 ? __ldg(ra + 1) : 0, nv > 2 ? __ldg(ra + 2) : 0,
-                             nv > 3 ? __ldg(ra + 3) : 0);
-            y[i] = make_int4(__ldg(rb), nv > 1 ? __ldg(rb + 1) : 0, nv > 2 ? __ldg(rb + 2) : 0,
-                             nv > 3 ? __ldg(rb + 3) : 0);
+          const int sq = s_lo + sl;
+          if (sl > 0 && may_join(sq) && full(sq, q) && full(sq - 1, q)) {
+            const int e0 = q * bpp + (c - q * cpp) * 4;  // first entry of the chunk
+            const int nv = min(4, (q + 1) * bpp - e0);   // entries of the chunk (1..4)
+            js[i] = sl;
+            jq[i] = q;
+            jn[i] = nv;
+            const int32_t *ra = tbl + static_cast<size_t>(sl) * p.max_blocks + e0;
+            const int32_t *rb = ra - p.max_blocks;
+            if (vec) {
+              x[i] = *reinterpret_cast<const int4 *>(ra);
+              y[i] = *reinterpret_cast<const int4 *>(rb);
+            } else {
+              x[i] = make_int4(ra[0], nv > 1 ? ra[1] : 0, nv > 2 ? ra[2] : 0, nv > 3 ? ra[3] : 0);
+              y[i] = make_int4(rb[0], nv > 1 ? rb[1] : 0, nv > 2 ? rb[2] : 0, nv > 3 ? rb[3] : 0);
+            }
           }
         }
       }
-  #pragma unroll
+#pragma unroll
       for (int i = 0; i < 4; ++i) {
         if (js[i] < 0) continue;
         const bool differ = (x[i].x != y[i].x) || (jn[i] > 1 && x[i].y != y[i].y) ||
                             (jn[i] > 2 && x[i].z != y[i].z) || (jn[i] > 3 && x[i].w != y[i].w);
-        if (differ) join[off[js[i]] + jq[i]] = 0;  // several threads may clear one flag
-      }
-    }
-    __syncthreads();
-  }  // B
-  // C0) the wide (chunk, partition) flags: set for chunks of enough
-  //     sequences, then cleared by every (sequence, partition) of the chunk
-  //     that does not qualify (one thread each)
-  if (use_wide) {
-    for (int i = tid; i < nchunks * p.max_parts; i += 1024) {
-      const int n = min(W, S - (i / p.max_parts) * W);
-      s_wide[i] = (n >= p.wide_min && n >= 2) ? 1 : 0;
-    }
-    __syncthreads();
-    for (int i = tid; i < S * p.max_parts; i += 1024) {
-      const int s = i / p.max_parts, q = i % p.max_parts;
-      const int fi = (s / W) * p.max_parts + q;
-      if (s_wide[fi] == 0) continue;
-      const int idx = off[s] + q;
-      // the partition must exist and be full in s, shared with s - 1 inside
-      // the chunk, and s must have more than one partition
-      const bool ok = idx < off[s + 1] && len[s] > P && len[s] >= (q + 1) * P && (s % W == 0 || join[idx] != 0);
-      if (!ok) s_wide[fi] = 0;  // several threads may clear one flag
-    }
-    __syncthreads();
-  }
-  // C) every pair that does not join leads an item of itself and the pairs
-  //    (s+1, q), (s+2, q), ... of its kmax group that join it; items keep
-  //    sequence order.  Pairs of a wide chunk are left to the wide item its
-  //    first sequence leads.
-  int wtotal = 0;
-  if (tid == 0) base = 0;
-  __syncthreads();
-  for (int k0 = 0; k0 < npairs; k0 += 1024) {
-    const int k = k0 + tid;
-    int lead = 0, ksz = 1, wlead = 0;
-    int2 sq = make_int2(0, 0);
-    if (k < npairs) {
-      sq = pair_at(k);
-      const bool in_wide = use_wide && s_wide[(sq.x / W) * p.max_parts + sq.y] != 0;
-      if (in_wide) {
-        wlead = sq.x % W == 0;
-        if (wlead) ksz = min(W, S - sq.x);
-      } else {
-        lead = p.kmax == 1 || sq.x % p.kmax == 0 || join[k] == 0;
-        if (lead) {
-          for (int j = 1; j < p.kmax && sq.x + j < S && (sq.x + j) % p.kmax != 0; ++j) {
-            const int idx = off[sq.x + j] + sq.y;
-            if (idx >= off[sq.x + j + 1] || join[idx] == 0) break;
-            ++ksz;
-          }
+        if (differ) {  // several threads may write one flag, all the same value
+          mis[js[i] * MP + jq[i]] = 1;
+          if (use_wide && (s_lo + js[i]) % W != 0) s_wide[(js[i] / W) * MP + jq[i]] = 0;
         }
       }
     }
-    int tot, wtot;
-    const int ex = block_exclusive_scan(lead, warp_tot, &tot);
-    const int wex = block_exclusive_scan(wlead, warp_tot, &wtot);
-    const int b = base;
-    if (lead) p.items[b + ex] = make_int4(sq.x, sq.y, ksz, 0);
-    if (wlead) p.wide_items[wtotal + wex] = make_int4(sq.x, sq.y, ksz, 0);
-    wtotal += wtot;
-    __syncthreads();
-    if (tid == 0) base = b + tot;
+    if (use_wide) {  // every sequence of a wide chunk: the partition full, more than one
+      for (int i = tid; i < nslots; i += 1024) {
+        const int sl = i / MP, q = i - sl * MP;
+        if (!(length(s_lo + sl) > P && full(s_lo + sl, q))) s_wide[(sl / W) * MP + q] = 0;
+      }
+    }
     __syncthreads();
   }
-  if (tid == 0) {
-    p.work[1] = base;
-    p.work[2] = wtotal;
+  // 3) items.  Slot (s, q) of the run joins (s-1, q):
+  auto joins = [&](int sq, int q) {
+    return compare && may_join(sq) && full(sq, q) && full(sq - 1, q) && mis[(sq - s_lo) * MP + q] == 0;
+  };
+  const int per = (nslots + 1023) / 1024;  // a run of slots per thread
+  const int i0 = min(nslots, tid * per), i1 = min(nslots, i0 + per);
+  // pass 0 counts the items the run leads, pass 1 writes them
+  int nlead = 0, nwide = 0;
+  int2 at = make_int2(0, 0), tot = make_int2(0, 0);
+  for (int pass = 0; pass < 2; ++pass) {
+    if (pass == 1) {
+      int2 cta;
+      at = block_exclusive_scan2(nlead, nwide, warp_tot, &cta);
+      asm volatile("barrier.cluster.wait.aligned;" ::: "memory");  // every CTA has started
+      if (tid < nranks) {  // this CTA's counts into CTA tid's table
+        uint32_t remote;
+        asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_addr(&s_tot[rank])), "r"(tid));
+        asm volatile("st.shared::cluster.v2.s32 [%0], {%1, %2};" ::"r"(remote), "r"(cta.x), "r"(cta.y) : "memory");
+      }
+      cluster_sync();  // every CTA's counts are here; no access to another CTA follows
+      for (int r = 0; r < nranks; ++r) {
+        const int2 t = s_tot[r];
+        if (r < rank) {
+          at.x += t.x;
+          at.y += t.y;
+        }
+        tot.x += t.x;
+        tot.y += t.y;
+      }
+    }
+    int sl = i0 / MP, q = i0 - sl * MP;
+    for (int i = i0; i < i1; ++i) {
+      const int sq = s_lo + sl;
+      if (q * P < max(length(sq), 1)) {  // the slot exists
+        if (use_wide && s_wide[(sl / W) * MP + q] != 0) {
+          if (sq % W == 0) {  // the chunk's first sequence leads its wide item
+            if (pass == 0) ++nwide;
+            else p.wide_items[at.y++] = make_int4(sq, q, min(W, S - sq), 0);
+          }
+        } else if (p.kmax == 1 || sq % p.kmax == 0 || !joins(sq, q)) {
+          if (pass == 0) {
+            ++nlead;
+          } else {
+            int ksz = 1;
+            for (int j = 1; j < p.kmax && sq + j < S && (sq + j) % p.kmax != 0; ++j) {
+              if (!joins(sq + j, q)) break;
+              ++ksz;
+            }
+            p.items[at.x++] = make_int4(sq, q, ksz, 0);
+          }
+        }
+      }
+      if (++q == MP) {
+        q = 0;
+        ++sl;
+      }
+    }
+  }
+  if (rank == 0 && tid == 0) {
+    p.work[1] = tot.x;
+    p.work[2] = tot.y;
     p.work[0] = 0;
   }
   grid_dependency_wait();
@@ -1515,14 +1521,44 @@ pa_status launch_decode(DecodeParams p, const DeviceInfo &dev, cudaStream_t stre
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(1);
   cfg.blockDim = dim3(1024);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;
+  // the plan: one cluster of kPlanCluster CTAs, or one CTA where no cluster
+  // of that size can be placed; each stages its run's block-table rows in
+  // shared memory when they are 16-byte aligned and fit
+  p.plan_tbl_bytes = ((p.kmax > 1 || wide) && (p.max_blocks & 3) == 0 &&
+                      (reinterpret_cast<uintptr_t>(p.block_tables) & 15) == 0)
+                         ? kPlanTableBytes
+                         : 0;
+  static bool plan_configured[64];  // per device: the plan's dynamic shared memory allowed
+  if (dev_id < 0 || dev_id >= 64 || !plan_configured[dev_id]) {
+    e = cudaFuncSetAttribute(plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kPlanTableBytes);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (dev_id >= 0 && dev_id < 64) plan_configured[dev_id] = true;
+  }
+  cfg.dynamicSmemBytes = p.plan_tbl_bytes;
+  {
+    cudaLaunchAttribute pattr[2];
+    pattr[0] = attr[0];
+    pattr[1].id = cudaLaunchAttributeClusterDimension;
+    pattr[1].val.clusterDim.x = kPlanCluster;
+    pattr[1].val.clusterDim.y = 1;
+    pattr[1].val.clusterDim.z = 1;
+    cfg.gridDim = dim3(kPlanCluster);
+    cfg.attrs = pattr;
+    cfg.numAttrs = 2;
+    e = cudaLaunchKernelEx(&cfg, plan_kernel, p);
+    if (e != cudaSuccess) {
+      (void)cudaGetLastError();
+      cfg.gridDim = dim3(1);
+      cfg.numAttrs = 1;
+      e = cudaLaunchKernelEx(&cfg, plan_kernel, p);
+    }
+    if (e != cudaSuccess) return cuda_fail(e);
+  }
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, plan_kernel, p);
-  if (e != cudaSuccess) return cuda_fail(e);
   // the wide items first, on their own SMs; the decode kernel fills the rest
   p.after_wide = wide ? 1 : 0;
   if (wide) {

@@ -22,7 +22,7 @@ int choose_partition(int num_seqs, int kv_heads, int max_seq_len, int requested)
 }
 
 struct WorkspaceLayout {
-  size_t pairs_off, wide_off, len_off, seqoff_off, choff_off, plist_off, join_off, ml_off, o_off, total;
+  size_t pairs_off, wide_off, join_off, ml_off, o_off, total;
   int partition, max_parts;
 };
 
@@ -41,11 +41,7 @@ bool layout_for(int num_seqs, int num_q_heads, int kv_heads, int head_dim, int m
   // wide items: a chunk holds at least kWideRows / 8 sequences
   const size_t wide_units = static_cast<size_t>((num_seqs + kWideRows / 8 - 1) / (kWideRows / 8)) * w.max_parts;
   w.wide_off = align256(w.pairs_off + units * sizeof(int4));
-  w.len_off = align256(w.wide_off + wide_units * sizeof(int4));  // lengths
-  w.seqoff_off = align256(w.len_off + num_seqs * sizeof(int));   // pair offsets
-  w.choff_off = align256(w.seqoff_off + (num_seqs + 1) * sizeof(int));
-  w.plist_off = align256(w.choff_off + num_seqs * sizeof(int));
-  w.join_off = align256(w.plist_off + units * sizeof(int2));
+  w.join_off = align256(w.wide_off + wide_units * sizeof(int4));  // row mismatch flags
   w.ml_off = align256(w.join_off + units);
   w.o_off = align256(w.ml_off + units * num_q_heads * sizeof(float2));
   w.total = align256(w.o_off + units * num_q_heads * head_dim * sizeof(float));
@@ -163,11 +159,7 @@ extern "C" pa_status pa_decode(void *out, const void *q, int32_t q_dtype, int32_
   p.work = reinterpret_cast<int *>(ws);
   p.items = reinterpret_cast<int4 *>(ws + w.pairs_off);
   p.wide_items = reinterpret_cast<int4 *>(ws + w.wide_off);
-  p.plan_len = reinterpret_cast<int *>(ws + w.len_off);
-  p.plan_off = reinterpret_cast<int *>(ws + w.seqoff_off);
-  p.plan_pairs = reinterpret_cast<int2 *>(ws + w.plist_off);
   p.plan_join = ws + w.join_off;
-  p.plan_choff = reinterpret_cast<int *>(ws + w.choff_off);
   p.part_ml = reinterpret_cast<float2 *>(ws + w.ml_off);
   p.part_o = reinterpret_cast<float *>(ws + w.o_off);
   p.err = device_error;

@@ -91,11 +91,9 @@ struct DecodeParams {
   int wide_seqs;     // sequences of a wide chunk (0: no wide items)
   int wide_min;      // fewest sequences that make a wide item
   int after_wide;    // the decode kernel follows the wide kernel (see decode_body)
-  int *plan_len;       // [S] clamped lengths
-  int *plan_off;       // [S + 1] first (s, q) pair of each sequence
-  int2 *plan_pairs;    // [S * max_parts] (s, q) pairs in sequence order
-  uint8_t *plan_join;  // [S * max_parts] pair joins the previous sequence's item
-  int *plan_choff;     // [S] first table-compare chunk of each sequence
+  uint8_t *plan_join;  // [S * max_parts] rows of (s, q) and (s-1, q) differ (a CTA's
+                       // flags, when they do not fit its shared memory)
+  int plan_tbl_bytes;  // shared memory for a plan CTA's block-table rows (0: read in place)
   float2 *part_ml;  // [S * max_parts * Hq] (max in log2 units, sum)
   float *part_o;    // [S * max_parts * Hq * D], normalised by its own sum
   int *err;
