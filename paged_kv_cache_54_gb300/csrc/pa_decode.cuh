@@ -131,17 +131,19 @@ __host__ __device__ constexpr int query_capacity(int G) { return G == 1 ? (PA_SH
 // following slots (s+1, q), ... of its kmax group that join.
 //
 // The plan is one cluster of CTAs (its work is a few thousand small steps,
-// and more SMs finish it sooner).  Each CTA owns a run of whole kmax groups
-// (whole wide chunks when they are looked for), so every decision it makes
-// needs only its own sequences' flags:
+// and more SMs finish it sooner).  Each CTA owns a run of whole kmax groups,
+// so its join decisions need only its own sequences' flags:
 //  1) its rows of the block tables start towards shared memory; its lengths;
-//     its flags cleared or set;
-//  2) the rows of s and s-1 (s inside the run, not its first) compared in
-//     chunks of up to 4 entries (a chunk never straddles two partitions),
-//     consecutive threads on consecutive chunks of one row: a mismatch flags
-//     (s, q) and clears the wide flag of its (chunk, partition); so does a
-//     sequence of the chunk whose partition is not full, or that has one
-//     partition only;
+//     its flags cleared, and every wide flag set for chunks of enough
+//     sequences;
+//  2) the rows of s and s-1 (s inside the run; its first only when wide
+//     chunks are looked for) compared in chunks of up to 4 entries (a chunk
+//     never straddles two partitions), consecutive threads on consecutive
+//     chunks of one row: a mismatch flags (s, q) and clears the wide flag of
+//     its (chunk, partition); so does a sequence of the chunk whose
+//     partition is not full, or that has one partition only.  A wide chunk
+//     may span several runs: each CTA then stores the wide flags it cleared
+//     into every CTA's copy before a cluster barrier;
 //  3) each thread takes a run of consecutive slots and counts the items they
 //     lead; a block scan places them within the CTA, and the CTAs' totals,
 //     stored into every CTA's shared memory before one cluster barrier,
@@ -200,9 +202,6 @@ __global__ void __launch_bounds__(1024) plan_kernel(const __grid_constant__ Deco
   const int S = p.num_seqs;
   const int MP = p.max_parts;
   launch_dependents();  // the decode grid may become resident; it waits for us
-  // This CTA has started: the others may store into its shared memory once
-  // they have waited on this arrival.
-  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
   // This kernel is a programmatic dependent of whatever precedes it on the
   // stream: it reads only the block tables and lengths (which the cache
   // writes before it never touch) and writes only this call's workspace, and
@@ -221,45 +220,51 @@ __global__ void __launch_bounds__(1024) plan_kernel(const __grid_constant__ Deco
   // a sequence may join its predecessor: within a group of kmax (batched
   // items), or anywhere when wide chunks are looked for
   auto may_join = [&](int s) { return s > 0 && (use_wide || s % p.kmax != 0); };
-  // this CTA's run of sequences [s_lo, s_hi): whole units of U
-  const int U = use_wide ? W : p.kmax;  // (W is a multiple of kmax)
+  // this CTA's run of sequences [s_lo, s_hi): whole kmax groups
+  const int U = p.kmax;
   const int nu = (S + U - 1) / U;
   const int s_lo = min(S, static_cast<int>(static_cast<long long>(rank) * nu / nranks) * U);
   const int s_hi = min(S, static_cast<int>(static_cast<long long>(rank + 1) * nu / nranks) * U);
   const int ns = s_hi - s_lo;
-  const bool len_smem = ns <= kPlanSmemSeqs;
+  // rows and lengths from r0: the run, and the sequence before it when its
+  // first sequence is compared (wide chunks)
+  const int r0 = (use_wide && s_lo > 0) ? s_lo - 1 : s_lo;
+  const int nr = s_hi - r0;
+  const bool len_smem = nr <= kPlanSmemSeqs;
   auto length = [&](int s) {
-    return len_smem ? s_len[s - s_lo] : min(max(__ldg(p.seq_lens + s), 0), p.len_cap);
+    return len_smem ? s_len[s - r0] : min(max(__ldg(p.seq_lens + s), 0), p.len_cap);
   };
   auto full = [&](int s, int q) { return length(s) >= (q + 1) * P; };
   const int nslots = ns * MP;
   uint8_t *mis = nslots <= kPlanSmemSlots ? s_mis : p.plan_join + static_cast<size_t>(s_lo) * MP;
-  const int c_lo = use_wide ? s_lo / W : 0;  // this CTA's first wide chunk
-  // 1) the table rows of the run start towards shared memory (they are
-  //    compared once the lengths are known); lengths; flags
-  const long long tbl_words = static_cast<long long>(ns) * p.max_blocks;
+  // 1) the table rows start towards shared memory (they are compared once
+  //    the lengths are known); lengths; flags
+  const long long tbl_words = static_cast<long long>(nr) * p.max_blocks;
   const bool tbl_smem = compare && p.plan_tbl_bytes > 0 && tbl_words * 4 <= p.plan_tbl_bytes;
-  const int32_t *tbl = p.block_tables + static_cast<size_t>(s_lo) * p.max_blocks;  // row s at (s - s_lo)
+  const int32_t *tbl = p.block_tables + static_cast<size_t>(r0) * p.max_blocks;  // row s at (s - r0)
   if (tbl_smem) {
     const int4 *src = reinterpret_cast<const int4 *>(tbl);
     for (int i = tid; i < tbl_words / 4; i += 1024) cp_async<16>(s_tbl + i, src + i);
     cp_async_commit();
     tbl = reinterpret_cast<const int32_t *>(s_tbl);
   }
-  for (int s = s_lo + tid; s < s_hi; s += 1024) {
-    const int L = clamp_len(__ldg(p.seq_lens + s), p.len_cap, p.err);
-    if (len_smem) s_len[s - s_lo] = L;
+  for (int s = r0 + tid; s < s_hi; s += 1024) {
+    const int L = clamp_len(__ldg(p.seq_lens + s), p.len_cap, s >= s_lo ? p.err : nullptr);
+    if (len_smem) s_len[s - r0] = L;
   }
   if (compare)  // (the workspace region is 256-byte aligned and padded: whole words)
     for (int i = tid * 4; i < nslots; i += 4 * 1024) *reinterpret_cast<uint32_t *>(mis + i) = 0u;
-  if (use_wide) {
-    for (int i = tid; i < ((ns + W - 1) / W) * MP; i += 1024) {
-      const int n = min(W, S - (c_lo + i / MP) * W);
+  if (use_wide) {  // every chunk's flags (a CTA's run may reach into a chunk another's starts)
+    for (int i = tid; i < nchunks * MP; i += 1024) {
+      const int n = min(W, S - (i / MP) * W);
       s_wide[i] = (n >= p.wide_min && n >= 2) ? 1 : 0;
     }
   }
   if (tbl_smem) cp_async_wait<0>();
   __syncthreads();
+  // This CTA's flags are set: the others may store into its shared memory
+  // once they have waited on this arrival.
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
   // 2) the rows compared
   if (compare) {
     const int cpp = (bpp + 3) >> 2;  // chunks per partition
@@ -284,13 +289,15 @@ __global__ void __launch_bounds__(1024) plan_kernel(const __grid_constant__ Deco
           const int c = u - sl * cpr;
           const int q = c / cpp;
           const int sq = s_lo + sl;
-          if (sl > 0 && may_join(sq) && full(sq, q) && full(sq - 1, q)) {
+          // (a run's first sequence leads its kmax group: compared only for
+          // the wide chunks)
+          if ((sl > 0 || use_wide) && may_join(sq) && full(sq, q) && full(sq - 1, q)) {
             const int e0 = q * bpp + (c - q * cpp) * 4;  // first entry of the chunk
             const int nv = min(4, (q + 1) * bpp - e0);   // entries of the chunk (1..4)
             js[i] = sl;
             jq[i] = q;
             jn[i] = nv;
-            const int32_t *ra = tbl + static_cast<size_t>(sl) * p.max_blocks + e0;
+            const int32_t *ra = tbl + static_cast<size_t>(sq - r0) * p.max_blocks + e0;
             const int32_t *rb = ra - p.max_blocks;
             if (vec) {
               x[i] = *reinterpret_cast<const int4 *>(ra);
@@ -309,18 +316,34 @@ __global__ void __launch_bounds__(1024) plan_kernel(const __grid_constant__ Deco
                             (jn[i] > 2 && x[i].z != y[i].z) || (jn[i] > 3 && x[i].w != y[i].w);
         if (differ) {  // several threads may write one flag, all the same value
           mis[js[i] * MP + jq[i]] = 1;
-          if (use_wide && (s_lo + js[i]) % W != 0) s_wide[(js[i] / W) * MP + jq[i]] = 0;
+          if (use_wide && (s_lo + js[i]) % W != 0) s_wide[((s_lo + js[i]) / W) * MP + jq[i]] = 0;
         }
       }
     }
     if (use_wide) {  // every sequence of a wide chunk: the partition full, more than one
       for (int i = tid; i < nslots; i += 1024) {
         const int sl = i / MP, q = i - sl * MP;
-        if (!(length(s_lo + sl) > P && full(s_lo + sl, q))) s_wide[(sl / W) * MP + q] = 0;
+        if (!(length(s_lo + sl) > P && full(s_lo + sl, q))) s_wide[((s_lo + sl) / W) * MP + q] = 0;
       }
     }
     __syncthreads();
   }
+  asm volatile("barrier.cluster.wait.aligned;" ::: "memory");  // every CTA's flags are set
+  if (use_wide && ns > 0) {
+    // the wide flags this CTA cleared, for the chunks its run reaches, into
+    // every other CTA's copy (only zeros are stored, so the order of these
+    // stores does not matter)
+    const int c0 = s_lo / W, nc = (s_hi - 1) / W - c0 + 1;
+    for (int t = tid; t < nc * MP * nranks; t += 1024) {
+      const int f = c0 * MP + t / nranks, r = t % nranks;
+      if (r != rank && s_wide[f] == 0) {
+        uint32_t remote;
+        asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_addr(&s_wide[f])), "r"(r));
+        asm volatile("st.shared::cluster.u8 [%0], %1;" ::"r"(remote), "h"(static_cast<unsigned short>(0)) : "memory");
+      }
+    }
+  }
+  if (use_wide) cluster_sync();  // every CTA's wide flags are the cluster's
   // 3) items.  Slot (s, q) of the run joins (s-1, q):
   auto joins = [&](int sq, int q) {
     return compare && may_join(sq) && full(sq, q) && full(sq - 1, q) && mis[(sq - s_lo) * MP + q] == 0;
@@ -334,7 +357,6 @@ __global__ void __launch_bounds__(1024) plan_kernel(const __grid_constant__ Deco
     if (pass == 1) {
       int2 cta;
       at = block_exclusive_scan2(nlead, nwide, warp_tot, &cta);
-      asm volatile("barrier.cluster.wait.aligned;" ::: "memory");  // every CTA has started
       if (tid < nranks) {  // this CTA's counts into CTA tid's table
         uint32_t remote;
         asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_addr(&s_tot[rank])), "r"(tid));
@@ -355,7 +377,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(const __grid_constant__ Deco
     for (int i = i0; i < i1; ++i) {
       const int sq = s_lo + sl;
       if (q * P < max(length(sq), 1)) {  // the slot exists
-        if (use_wide && s_wide[(sl / W) * MP + q] != 0) {
+        if (use_wide && s_wide[(sq / W) * MP + q] != 0) {
           if (sq % W == 0) {  // the chunk's first sequence leads its wide item
             if (pass == 0) ++nwide;
             else p.wide_items[at.y++] = make_int4(sq, q, min(W, S - sq), 0);
