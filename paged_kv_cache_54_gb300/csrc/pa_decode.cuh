@@ -417,20 +417,17 @@ __global__ void __launch_bounds__(1024) plan_kernel(const __grid_constant__ Deco
 // (the flash-decoding reduction; o_q is normalised by its own l_q).  Lane j
 // holds the weights of partitions j and j + 32 (longer sequences take
 // windows of 64) and owns D / 32 columns of every partial row.  The rows
-// stream through a ring of kMergeRing rows of shared memory per warp: each
-// lane copies its own columns with cp.async, so kMergeRing rows stay in
-// flight with few registers live (16 rows a warp at 24 warps an SM; held in
-// registers, 8 rows took 75 registers for the same residency), and the
-// first copies leave before the weights are read.  A lane reads back only
-// what it copied itself.
-#ifndef PA_MERGE_RING
-#define PA_MERGE_RING 16
-#endif
+// stream through a ring of R rows of shared memory per warp: each lane
+// copies its own columns with cp.async, so R rows stay in flight with few
+// registers live (16 rows a warp at 24 warps an SM; held in registers, 8
+// rows took 75 registers for the same residency), and the first copies
+// leave before the weights are read.  A lane reads back only what it copied
+// itself.  R is 4 when no sequence has more than 4 partitions (room for
+// more warps), else 16.
 constexpr int kMergeWarps = 4;
 constexpr int kMergeThreads = 32 * kMergeWarps;
-constexpr int kMergeRing = PA_MERGE_RING;
 
-template <int QT, int D>
+template <int QT, int D, int kMergeRing>
 __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const __grid_constant__ DecodeParams p) {
   constexpr int E = D / 32;  // columns per lane
   constexpr int CB = E * 4;  // bytes a lane copies from a row
@@ -1600,7 +1597,7 @@ pa_status launch_decode(DecodeParams p, const DeviceInfo &dev, cudaStream_t stre
     cfg.gridDim = dim3(static_cast<unsigned>((warps + kMergeWarps - 1) / kMergeWarps));
     cfg.blockDim = dim3(kMergeThreads);
     cfg.dynamicSmemBytes = 0;
-    e = cudaLaunchKernelEx(&cfg, merge_kernel<QT, D>, p);
+    e = cudaLaunchKernelEx(&cfg, p.max_parts <= 4 ? merge_kernel<QT, D, 4> : merge_kernel<QT, D, 16>, p);
     if (e != cudaSuccess) return cuda_fail(e);
   }
   e = cudaGetLastError();
