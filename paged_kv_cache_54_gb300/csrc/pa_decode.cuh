@@ -1543,9 +1543,11 @@ pa_status launch_decode(DecodeParams p, const DeviceInfo &dev, cudaStream_t stre
   cfg.blockDim = dim3(1024);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;
-  // the plan: one cluster of kPlanCluster CTAs, or one CTA where no cluster
-  // of that size can be placed; each stages its run's block-table rows in
-  // shared memory when they are 16-byte aligned and fit
+  // the plan: one cluster of up to kPlanCluster CTAs (no more than there
+  // are kmax groups), or a cluster of one CTA where no such cluster can be
+  // placed; each
+  // stages its run's block-table rows in shared memory when they are
+  // 16-byte aligned and fit
   p.plan_tbl_bytes = ((p.kmax > 1 || wide) && (p.max_blocks & 3) == 0 &&
                       (reinterpret_cast<uintptr_t>(p.block_tables) & 15) == 0)
                          ? kPlanTableBytes
@@ -1558,20 +1560,22 @@ pa_status launch_decode(DecodeParams p, const DeviceInfo &dev, cudaStream_t stre
   }
   cfg.dynamicSmemBytes = p.plan_tbl_bytes;
   {
+    const int groups = (p.num_seqs + p.kmax - 1) / p.kmax;
+    const int nc = groups < kPlanCluster ? groups : kPlanCluster;
     cudaLaunchAttribute pattr[2];
     pattr[0] = attr[0];
     pattr[1].id = cudaLaunchAttributeClusterDimension;
-    pattr[1].val.clusterDim.x = kPlanCluster;
+    pattr[1].val.clusterDim.x = nc;
     pattr[1].val.clusterDim.y = 1;
     pattr[1].val.clusterDim.z = 1;
-    cfg.gridDim = dim3(kPlanCluster);
+    cfg.gridDim = dim3(nc);
     cfg.attrs = pattr;
     cfg.numAttrs = 2;
     e = cudaLaunchKernelEx(&cfg, plan_kernel, p);
-    if (e != cudaSuccess) {
+    if (e != cudaSuccess && nc > 1) {  // a cluster of one CTA
       (void)cudaGetLastError();
+      pattr[1].val.clusterDim.x = 1;
       cfg.gridDim = dim3(1);
-      cfg.numAttrs = 1;
       e = cudaLaunchKernelEx(&cfg, plan_kernel, p);
     }
     if (e != cudaSuccess) return cuda_fail(e);

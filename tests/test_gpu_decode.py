@@ -265,9 +265,9 @@ def test_beam_fork_matches_oracle(cache_dtype, q_dtype, bs, heads):
 
 @pytest.mark.parametrize("cache_dtype,q_dtype,heads", [("f16", "f16", (1, 1)),
                                                        ("bf16", "bf16", (2, 1))])
-def test_many_sequences_exceed_plan_shared_memory(cache_dtype, q_dtype, heads):
-    """5000 sequences and > 12288 (sequence, partition) pairs: the plan's
-    tables spill from shared memory to the workspace."""
+def test_many_sequences(cache_dtype, q_dtype, heads):
+    """5000 sequences of 1..329 tokens in partitions of 64 (a table width that
+    is not a multiple of four entries, so the plan reads the rows in place)."""
     rng = np.random.default_rng(5)
     lens = rng.integers(1, 330, 5000).tolist()
     Hq, Hkv = heads
@@ -278,6 +278,38 @@ def test_many_sequences_exceed_plan_shared_memory(cache_dtype, q_dtype, heads):
     assert int(run.err.item()) == 0
     ref = G.oracle_decode(w, G.oracle_cache(w))
     _check(w, run.out, ref)
+
+
+def test_plan_tables_beyond_shared_memory():
+    """17 000 sequences sharing a 384-token prefix, each with 1..128 tokens of
+    its own, in partitions of 64: each of the plan's eight CTAs owns more
+    than 2048 sequences and 16 384 (sequence, partition) slots, so its
+    lengths and join flags live in the workspace and its block-table rows
+    are read in place; the shared partitions also form wide chunks across
+    the CTAs' runs.  Sampled rows (the sequences around every CTA's first and
+    last, and a spread between) against the oracle."""
+    w = W.make_workload("qwen3-prefix", 91, device=G.DEV, overrides=dict(
+        S=17000, prefix=384, suffix_lo=1, suffix_hi=128, Hq=2, Hkv=1, d=64, bs=16,
+        cache_dtype="bf16", q_dtype="bf16", src_dtype="bf16"))
+    run = G.GpuRun(w, partition_size=64).setup()
+    run.step()
+    torch.cuda.synchronize()
+    assert int(run.err.item()) == 0
+    groups = -(-w.S // 4)                      # kmax = 4 sequences at G = 2
+    edges = {min(w.S, (r * groups // 8) * 4) for r in range(9)}
+    seqs = {x for e in edges for x in range(e - 2, e + 3) if 0 <= x < w.S}
+    seqs |= set(range(0, w.S, 97))
+    rows = [(s, hq) for s in sorted(seqs) for hq in range(w.Hq)]
+    ref = G.oracle_rows(w, rows)
+    got = run.out.float().cpu().numpy().astype(np.float64)
+    tol = G.tolerance(w)
+    worst = 0.0
+    for (s, hq), r in ref.items():
+        err = np.abs(got[s, hq] - r)
+        bound = np.maximum(tol, G.ulp(r, w.q_dtype))
+        assert not (err > bound).any(), (s, hq, float(err.max()))
+        worst = max(worst, float(err.max()))
+    print(f"{len(rows)} sampled rows of {w.S * w.Hq}, max |err| {worst:.2e}")
 
 
 def test_shared_prefix_across_plan_chunks():
