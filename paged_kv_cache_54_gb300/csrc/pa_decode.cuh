@@ -217,14 +217,20 @@ __global__ void __launch_bounds__(1024) plan_kernel(const __grid_constant__ Deco
   const bool use_wide = W > 0 && nchunks * MP <= kPlanWideFlags;
   // rows are compared when items batch sequences or wide chunks are looked for
   const bool compare = p.kmax > 1 || use_wide;
+  // kmax, W and the slot strides below are powers of two: the indexing uses
+  // shifts and masks (a division by a variable costs tens of instructions,
+  // and this kernel is bound by the instructions it issues)
+  const int kmask = p.kmax - 1;
+  const int w_sh = W > 0 ? 31 - __clz(W) : 0;
+  const int mp_sh = 32 - __clz(MP - 1);  // partitions per sequence, padded: 2^mp_sh
   // a sequence may join its predecessor: within a group of kmax (batched
   // items), or anywhere when wide chunks are looked for
-  auto may_join = [&](int s) { return s > 0 && (use_wide || s % p.kmax != 0); };
+  auto may_join = [&](int s) { return s > 0 && (use_wide || (s & kmask) != 0); };
   // this CTA's run of sequences [s_lo, s_hi): whole kmax groups
   const int U = p.kmax;
   const int nu = (S + U - 1) / U;
-  const int s_lo = min(S, static_cast<int>(static_cast<long long>(rank) * nu / nranks) * U);
-  const int s_hi = min(S, static_cast<int>(static_cast<long long>(rank + 1) * nu / nranks) * U);
+  const int s_lo = min(S, (rank * nu / nranks) * U);  // (nu is at most the sequence count)
+  const int s_hi = min(S, ((rank + 1) * nu / nranks) * U);
   const int ns = s_hi - s_lo;
   // rows and lengths from r0: the run, and the sequence before it when its
   // first sequence is compared (wide chunks)
@@ -255,9 +261,10 @@ __global__ void __launch_bounds__(1024) plan_kernel(const __grid_constant__ Deco
   if (compare)  // (the workspace region is 256-byte aligned and padded: whole words)
     for (int i = tid * 4; i < nslots; i += 4 * 1024) *reinterpret_cast<uint32_t *>(mis + i) = 0u;
   if (use_wide) {  // every chunk's flags (a CTA's run may reach into a chunk another's starts)
-    for (int i = tid; i < nchunks * MP; i += 1024) {
-      const int n = min(W, S - (i / MP) * W);
-      s_wide[i] = (n >= p.wide_min && n >= 2) ? 1 : 0;
+    for (int i = tid; i < (nchunks << mp_sh); i += 1024) {
+      const int c = i >> mp_sh, q = i & ((1 << mp_sh) - 1);
+      const int n = min(W, S - c * W);
+      if (q < MP) s_wide[c * MP + q] = (n >= p.wide_min && n >= 2) ? 1 : 0;
     }
   }
   if (tbl_smem) cp_async_wait<0>();
@@ -267,9 +274,10 @@ __global__ void __launch_bounds__(1024) plan_kernel(const __grid_constant__ Deco
   asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
   // 2) the rows compared
   if (compare) {
-    const int cpp = (bpp + 3) >> 2;  // chunks per partition
-    const int cpr = MP * cpp;        // chunk slots per sequence
-    const int nch = ns * cpr;
+    const int cpp = (bpp + 3) >> 2;           // chunks per partition
+    const int cpp_sh = 32 - __clz(cpp - 1);  // ... padded: 2^cpp_sh
+    const int u_sh = mp_sh + cpp_sh;         // chunk slots per sequence: 2^u_sh
+    const int nch = ns << u_sh;
     // 16-byte loads when every chunk is four aligned entries
     const bool vec = (bpp & 3) == 0 && (p.max_blocks & 3) == 0 &&
                      (reinterpret_cast<uintptr_t>(p.block_tables) & 15) == 0;
@@ -285,14 +293,14 @@ __global__ void __launch_bounds__(1024) plan_kernel(const __grid_constant__ Deco
         jq[i] = jn[i] = 0;
         x[i] = y[i] = make_int4(0, 0, 0, 0);
         if (u < nch) {
-          const int sl = u / cpr;  // sequence s_lo + sl
-          const int c = u - sl * cpr;
-          const int q = c / cpp;
+          const int sl = u >> u_sh;  // sequence s_lo + sl, partition q, its chunk j
+          const int q = (u >> cpp_sh) & ((1 << mp_sh) - 1);
+          const int j = u & ((1 << cpp_sh) - 1);
           const int sq = s_lo + sl;
           // (a run's first sequence leads its kmax group: compared only for
           // the wide chunks)
-          if ((sl > 0 || use_wide) && may_join(sq) && full(sq, q) && full(sq - 1, q)) {
-            const int e0 = q * bpp + (c - q * cpp) * 4;  // first entry of the chunk
+          if (q < MP && j < cpp && (sl > 0 || use_wide) && may_join(sq) && full(sq, q) && full(sq - 1, q)) {
+            const int e0 = q * bpp + j * 4;              // first entry of the chunk
             const int nv = min(4, (q + 1) * bpp - e0);   // entries of the chunk (1..4)
             js[i] = sl;
             jq[i] = q;
@@ -316,14 +324,14 @@ __global__ void __launch_bounds__(1024) plan_kernel(const __grid_constant__ Deco
                             (jn[i] > 2 && x[i].z != y[i].z) || (jn[i] > 3 && x[i].w != y[i].w);
         if (differ) {  // several threads may write one flag, all the same value
           mis[js[i] * MP + jq[i]] = 1;
-          if (use_wide && (s_lo + js[i]) % W != 0) s_wide[((s_lo + js[i]) / W) * MP + jq[i]] = 0;
+          if (use_wide && ((s_lo + js[i]) & (W - 1)) != 0) s_wide[((s_lo + js[i]) >> w_sh) * MP + jq[i]] = 0;
         }
       }
     }
     if (use_wide) {  // every sequence of a wide chunk: the partition full, more than one
-      for (int i = tid; i < nslots; i += 1024) {
-        const int sl = i / MP, q = i - sl * MP;
-        if (!(length(s_lo + sl) > P && full(s_lo + sl, q))) s_wide[((s_lo + sl) / W) * MP + q] = 0;
+      for (int i = tid; i < (ns << mp_sh); i += 1024) {
+        const int sl = i >> mp_sh, q = i & ((1 << mp_sh) - 1);
+        if (q < MP && !(length(s_lo + sl) > P && full(s_lo + sl, q))) s_wide[((s_lo + sl) >> w_sh) * MP + q] = 0;
       }
     }
     __syncthreads();
@@ -333,7 +341,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(const __grid_constant__ Deco
     // the wide flags this CTA cleared, for the chunks its run reaches, into
     // every other CTA's copy (only zeros are stored, so the order of these
     // stores does not matter)
-    const int c0 = s_lo / W, nc = (s_hi - 1) / W - c0 + 1;
+    const int c0 = s_lo >> w_sh, nc = ((s_hi - 1) >> w_sh) - c0 + 1;
     for (int t = tid; t < nc * MP * nranks; t += 1024) {
       const int f = c0 * MP + t / nranks, r = t % nranks;
       if (r != rank && s_wide[f] == 0) {
@@ -348,8 +356,10 @@ __global__ void __launch_bounds__(1024) plan_kernel(const __grid_constant__ Deco
   auto joins = [&](int sq, int q) {
     return compare && may_join(sq) && full(sq, q) && full(sq - 1, q) && mis[(sq - s_lo) * MP + q] == 0;
   };
-  const int per = (nslots + 1023) / 1024;  // a run of slots per thread
-  const int i0 = min(nslots, tid * per), i1 = min(nslots, i0 + per);
+  // (slots indexed with the padded stride; q >= MP holds nothing)
+  const int nslots_p = ns << mp_sh;
+  const int per = (nslots_p + 1023) >> 10;  // a run of slots per thread
+  const int i0 = min(nslots_p, tid * per), i1 = min(nslots_p, i0 + per);
   // pass 0 counts the items the run leads, pass 1 writes them
   int nlead = 0, nwide = 0;
   int2 at = make_int2(0, 0), tot = make_int2(0, 0);
@@ -373,21 +383,21 @@ __global__ void __launch_bounds__(1024) plan_kernel(const __grid_constant__ Deco
         tot.y += t.y;
       }
     }
-    int sl = i0 / MP, q = i0 - sl * MP;
+    int sl = i0 >> mp_sh, q = i0 & ((1 << mp_sh) - 1);
     for (int i = i0; i < i1; ++i) {
       const int sq = s_lo + sl;
-      if (q * P < max(length(sq), 1)) {  // the slot exists
-        if (use_wide && s_wide[(sq / W) * MP + q] != 0) {
-          if (sq % W == 0) {  // the chunk's first sequence leads its wide item
+      if (q < MP && q * P < max(length(sq), 1)) {  // the slot exists
+        if (use_wide && s_wide[(sq >> w_sh) * MP + q] != 0) {
+          if ((sq & (W - 1)) == 0) {  // the chunk's first sequence leads its wide item
             if (pass == 0) ++nwide;
             else p.wide_items[at.y++] = make_int4(sq, q, min(W, S - sq), 0);
           }
-        } else if (p.kmax == 1 || sq % p.kmax == 0 || !joins(sq, q)) {
+        } else if (p.kmax == 1 || (sq & kmask) == 0 || !joins(sq, q)) {
           if (pass == 0) {
             ++nlead;
           } else {
             int ksz = 1;
-            for (int j = 1; j < p.kmax && sq + j < S && (sq + j) % p.kmax != 0; ++j) {
+            for (int j = 1; j < p.kmax && sq + j < S && ((sq + j) & kmask) != 0; ++j) {
               if (!joins(sq + j, q)) break;
               ++ksz;
             }
@@ -395,7 +405,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(const __grid_constant__ Deco
           }
         }
       }
-      if (++q == MP) {
+      if (++q == (1 << mp_sh)) {
         q = 0;
         ++sl;
       }
