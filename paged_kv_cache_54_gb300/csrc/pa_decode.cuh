@@ -149,8 +149,9 @@ __host__ __device__ constexpr int query_capacity(int G) { return G == 1 ? (PA_SH
 //     stored into every CTA's shared memory before one cluster barrier,
 //     place the CTA; the items are written in slot order.
 
-// Exclusive prefix sums of two counts over the 1024 threads of the block;
+// Exclusive prefix sums of two counts over the NW warps of the block;
 // *total = the block's sums.
+template <int NW>
 __device__ __forceinline__ int2 block_exclusive_scan2(int x, int y, int2 *warp_tot, int2 *total) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   int vx = x, vy = y;
@@ -165,7 +166,7 @@ __device__ __forceinline__ int2 block_exclusive_scan2(int x, int y, int2 *warp_t
   if (lane == 31) warp_tot[warp] = make_int2(vx, vy);
   __syncthreads();
   if (warp == 0) {
-    int2 t = warp_tot[lane];
+    int2 t = lane < NW ? warp_tot[lane] : make_int2(0, 0);
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const int ax = __shfl_up_sync(0xffffffffu, t.x, o), ay = __shfl_up_sync(0xffffffffu, t.y, o);
@@ -174,21 +175,22 @@ __device__ __forceinline__ int2 block_exclusive_scan2(int x, int y, int2 *warp_t
         t.y += ay;
       }
     }
-    warp_tot[lane] = t;  // inclusive over warps
+    if (lane < NW) warp_tot[lane] = t;  // inclusive over warps
   }
   __syncthreads();
   const int2 before = warp ? warp_tot[warp - 1] : make_int2(0, 0);
-  *total = warp_tot[31];
+  *total = warp_tot[NW - 1];
   return make_int2(before.x + vx - x, before.y + vy - y);
 }
 
-constexpr int kPlanCluster = 8;             // CTAs of the plan's cluster (1 if a cluster cannot be had)
+constexpr int kPlanCluster = 16;            // CTAs of the plan's cluster (1 if a cluster cannot be had)
+constexpr int kPlanThreads = 512;           // threads of a plan CTA
 constexpr int kPlanSmemSeqs = 2048;         // a CTA's lengths in shared memory up to this many
 constexpr int kPlanSmemSlots = 16384;       // a CTA's mismatch flags, one byte a slot
 constexpr int kPlanWideFlags = 4096;        // most (wide chunk, partition) flags
 constexpr int kPlanTableBytes = 96 * 1024;  // a CTA's block-table rows in shared memory up to this
 
-__global__ void __launch_bounds__(1024) plan_kernel(const __grid_constant__ DecodeParams p) {
+__global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constant__ DecodeParams p) {
   __shared__ int2 warp_tot[32];
   __shared__ int2 s_tot[kPlanCluster];  // the CTAs' item counts, stored by each CTA
   __shared__ int s_len[kPlanSmemSeqs];
@@ -250,18 +252,18 @@ __global__ void __launch_bounds__(1024) plan_kernel(const __grid_constant__ Deco
   const int32_t *tbl = p.block_tables + static_cast<size_t>(r0) * p.max_blocks;  // row s at (s - r0)
   if (tbl_smem) {
     const int4 *src = reinterpret_cast<const int4 *>(tbl);
-    for (int i = tid; i < tbl_words / 4; i += 1024) cp_async<16>(s_tbl + i, src + i);
+    for (int i = tid; i < tbl_words / 4; i += kPlanThreads) cp_async<16>(s_tbl + i, src + i);
     cp_async_commit();
     tbl = reinterpret_cast<const int32_t *>(s_tbl);
   }
-  for (int s = r0 + tid; s < s_hi; s += 1024) {
+  for (int s = r0 + tid; s < s_hi; s += kPlanThreads) {
     const int L = clamp_len(__ldg(p.seq_lens + s), p.len_cap, s >= s_lo ? p.err : nullptr);
     if (len_smem) s_len[s - r0] = L;
   }
   if (compare)  // (the workspace region is 256-byte aligned and padded: whole words)
-    for (int i = tid * 4; i < nslots; i += 4 * 1024) *reinterpret_cast<uint32_t *>(mis + i) = 0u;
+    for (int i = tid * 4; i < nslots; i += 4 * kPlanThreads) *reinterpret_cast<uint32_t *>(mis + i) = 0u;
   if (use_wide) {  // every chunk's flags (a CTA's run may reach into a chunk another's starts)
-    for (int i = tid; i < (nchunks << mp_sh); i += 1024) {
+    for (int i = tid; i < (nchunks << mp_sh); i += kPlanThreads) {
       const int c = i >> mp_sh, q = i & ((1 << mp_sh) - 1);
       const int n = min(W, S - c * W);
       if (q < MP) s_wide[c * MP + q] = (n >= p.wide_min && n >= 2) ? 1 : 0;
@@ -281,14 +283,14 @@ __global__ void __launch_bounds__(1024) plan_kernel(const __grid_constant__ Deco
     // 16-byte loads when every chunk is four aligned entries
     const bool vec = (bpp & 3) == 0 && (p.max_blocks & 3) == 0 &&
                      (reinterpret_cast<uintptr_t>(p.block_tables) & 15) == 0;
-    // Each thread takes chunks tid, tid + 1024, ... four at a time with all
-    // their loads in flight.
-    for (int u0 = 0; u0 < nch; u0 += 4 * 1024) {
+    // Each thread takes chunks tid, tid + kPlanThreads, ... four at a time
+    // with all their loads in flight.
+    for (int u0 = 0; u0 < nch; u0 += 4 * kPlanThreads) {
       int4 x[4], y[4];
       int js[4], jq[4], jn[4];
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        const int u = u0 + i * 1024 + tid;
+        const int u = u0 + i * kPlanThreads + tid;
         js[i] = -1;
         jq[i] = jn[i] = 0;
         x[i] = y[i] = make_int4(0, 0, 0, 0);
@@ -329,7 +331,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(const __grid_constant__ Deco
       }
     }
     if (use_wide) {  // every sequence of a wide chunk: the partition full, more than one
-      for (int i = tid; i < (ns << mp_sh); i += 1024) {
+      for (int i = tid; i < (ns << mp_sh); i += kPlanThreads) {
         const int sl = i >> mp_sh, q = i & ((1 << mp_sh) - 1);
         if (q < MP && !(length(s_lo + sl) > P && full(s_lo + sl, q))) s_wide[((s_lo + sl) >> w_sh) * MP + q] = 0;
       }
@@ -342,7 +344,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(const __grid_constant__ Deco
     // every other CTA's copy (only zeros are stored, so the order of these
     // stores does not matter)
     const int c0 = s_lo >> w_sh, nc = ((s_hi - 1) >> w_sh) - c0 + 1;
-    for (int t = tid; t < nc * MP * nranks; t += 1024) {
+    for (int t = tid; t < nc * MP * nranks; t += kPlanThreads) {
       const int f = c0 * MP + t / nranks, r = t % nranks;
       if (r != rank && s_wide[f] == 0) {
         uint32_t remote;
@@ -358,7 +360,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(const __grid_constant__ Deco
   };
   // (slots indexed with the padded stride; q >= MP holds nothing)
   const int nslots_p = ns << mp_sh;
-  const int per = (nslots_p + 1023) >> 10;  // a run of slots per thread
+  const int per = (nslots_p + kPlanThreads - 1) / kPlanThreads;  // a run of slots per thread
   const int i0 = min(nslots_p, tid * per), i1 = min(nslots_p, i0 + per);
   // pass 0 counts the items the run leads, pass 1 writes them
   int nlead = 0, nwide = 0;
@@ -366,7 +368,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(const __grid_constant__ Deco
   for (int pass = 0; pass < 2; ++pass) {
     if (pass == 1) {
       int2 cta;
-      at = block_exclusive_scan2(nlead, nwide, warp_tot, &cta);
+      at = block_exclusive_scan2<kPlanThreads / 32>(nlead, nwide, warp_tot, &cta);
       if (tid < nranks) {  // this CTA's counts into CTA tid's table
         uint32_t remote;
         asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_addr(&s_tot[rank])), "r"(tid));
@@ -1550,7 +1552,7 @@ pa_status launch_decode(DecodeParams p, const DeviceInfo &dev, cudaStream_t stre
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg = {};
-  cfg.blockDim = dim3(1024);
+  cfg.blockDim = dim3(kPlanThreads);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;
   // the plan: one cluster of up to kPlanCluster CTAs (no more than there
@@ -1562,9 +1564,11 @@ pa_status launch_decode(DecodeParams p, const DeviceInfo &dev, cudaStream_t stre
                       (reinterpret_cast<uintptr_t>(p.block_tables) & 15) == 0)
                          ? kPlanTableBytes
                          : 0;
-  static bool plan_configured[64];  // per device: the plan's dynamic shared memory allowed
+  static bool plan_configured[64];  // per device: the plan's dynamic shared memory and cluster size allowed
   if (dev_id < 0 || dev_id >= 64 || !plan_configured[dev_id]) {
     e = cudaFuncSetAttribute(plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kPlanTableBytes);
+    if (e != cudaSuccess) return cuda_fail(e);
+    e = cudaFuncSetAttribute(plan_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (e != cudaSuccess) return cuda_fail(e);
     if (dev_id >= 0 && dev_id < 64) plan_configured[dev_id] = true;
   }
@@ -1582,10 +1586,11 @@ pa_status launch_decode(DecodeParams p, const DeviceInfo &dev, cudaStream_t stre
     cfg.attrs = pattr;
     cfg.numAttrs = 2;
     e = cudaLaunchKernelEx(&cfg, plan_kernel, p);
-    if (e != cudaSuccess && nc > 1) {  // a cluster of one CTA
+    for (int smaller = nc > 8 ? 8 : 1; e != cudaSuccess && smaller >= 1 && smaller < static_cast<int>(cfg.gridDim.x);
+         smaller = smaller > 1 ? 1 : 0) {  // a smaller cluster: 8 CTAs, then one
       (void)cudaGetLastError();
-      pattr[1].val.clusterDim.x = 1;
-      cfg.gridDim = dim3(1);
+      pattr[1].val.clusterDim.x = smaller;
+      cfg.gridDim = dim3(smaller);
       e = cudaLaunchKernelEx(&cfg, plan_kernel, p);
     }
     if (e != cudaSuccess) return cuda_fail(e);
