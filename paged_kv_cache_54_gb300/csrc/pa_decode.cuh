@@ -185,6 +185,7 @@ __device__ __forceinline__ int2 block_exclusive_scan2(int x, int y, int2 *warp_t
 
 constexpr int kPlanCluster = 16;            // CTAs of the plan's cluster (1 if a cluster cannot be had)
 constexpr int kPlanThreads = 512;           // threads of a plan CTA
+constexpr int kPlanBuckets = kMaxPartition / kStageTok;  // item lengths in stages
 constexpr int kPlanSmemSeqs = 2048;         // a CTA's lengths in shared memory up to this many
 constexpr int kPlanSmemSlots = 16384;       // a CTA's mismatch flags, one byte a slot
 constexpr int kPlanWideFlags = 4096;        // most (wide chunk, partition) flags
@@ -192,7 +193,10 @@ constexpr int kPlanTableBytes = 96 * 1024;  // a CTA's block-table rows in share
 
 __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constant__ DecodeParams p) {
   __shared__ int2 warp_tot[32];
-  __shared__ int2 s_tot[kPlanCluster];  // the CTAs' item counts, stored by each CTA
+  // each CTA's counts, stored there by that CTA: its items, its wide items
+  // and (longest first) its items of each stage count
+  __shared__ int s_tab[kPlanCluster][2 + kPlanBuckets];
+  __shared__ int s_hist[kPlanBuckets], s_cur[kPlanBuckets];
   __shared__ int s_len[kPlanSmemSeqs];
   __shared__ __align__(4) uint8_t s_mis[kPlanSmemSlots];
   __shared__ uint8_t s_wide[kPlanWideFlags];
@@ -203,6 +207,12 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
   const int bpp = P / p.block_size;
   const int S = p.num_seqs;
   const int MP = p.max_parts;
+  // Items are listed in slot order, or longest first (by stage count, in
+  // any order within a count; the decode's claims then run from the longest
+  // items to the shortest, so its last ones are short).
+  const bool lf = p.longest_first != 0;
+  const int NB = P / kStageTok;
+  if (tid < kPlanBuckets) s_hist[tid] = 0;
   launch_dependents();  // the decode grid may become resident; it waits for us
   // This kernel is a programmatic dependent of whatever precedes it on the
   // stream: it reads only the block tables and lengths (which the cache
@@ -362,27 +372,58 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
   const int nslots_p = ns << mp_sh;
   const int per = (nslots_p + kPlanThreads - 1) / kPlanThreads;  // a run of slots per thread
   const int i0 = min(nslots_p, tid * per), i1 = min(nslots_p, i0 + per);
+  // the stage-count bucket of the item (s, q) leads: its partition's tokens
+  auto bucket = [&](int sq, int q) {
+    const int tok = min(P, length(sq) - q * P);
+    return max(1, (tok + kStageTok - 1) / kStageTok) - 1;
+  };
   // pass 0 counts the items the run leads, pass 1 writes them
   int nlead = 0, nwide = 0;
   int2 at = make_int2(0, 0), tot = make_int2(0, 0);
   for (int pass = 0; pass < 2; ++pass) {
     if (pass == 1) {
       int2 cta;
-      at = block_exclusive_scan2<kPlanThreads / 32>(nlead, nwide, warp_tot, &cta);
-      if (tid < nranks) {  // this CTA's counts into CTA tid's table
+      at = block_exclusive_scan2<kPlanThreads / 32>(nlead, nwide, warp_tot, &cta);  // (and the histogram is done)
+      if (tid < nranks) {  // this CTA's counts into row `rank` of CTA tid's table
         uint32_t remote;
-        asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_addr(&s_tot[rank])), "r"(tid));
-        asm volatile("st.shared::cluster.v2.s32 [%0], {%1, %2};" ::"r"(remote), "r"(cta.x), "r"(cta.y) : "memory");
+        asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_addr(&s_tab[rank][0])), "r"(tid));
+        for (int j = 0; j < (lf ? 2 + NB : 2); ++j) {
+          const int v = j == 0 ? cta.x : j == 1 ? cta.y : s_hist[j - 2];
+          asm volatile("st.shared::cluster.s32 [%0], %1;" ::"r"(remote + 4 * j), "r"(v) : "memory");
+        }
       }
       cluster_sync();  // every CTA's counts are here; no access to another CTA follows
       for (int r = 0; r < nranks; ++r) {
-        const int2 t = s_tot[r];
+        const int tx = s_tab[r][0], ty = s_tab[r][1];
         if (r < rank) {
-          at.x += t.x;
-          at.y += t.y;
+          at.x += tx;
+          at.y += ty;
         }
-        tot.x += t.x;
-        tot.y += t.y;
+        tot.x += tx;
+        tot.y += ty;
+      }
+      if (lf) {
+        // bucket b (b + 1 stages) starts after every longer bucket, and this
+        // CTA's part of it after the lower ranks' parts (one warp: lane b)
+        if (tid < 32) {
+          int all = 0, below = 0;
+          if (tid < NB) {
+            for (int r = 0; r < nranks; ++r) {
+              const int c = s_tab[r][2 + tid];
+              all += c;
+              if (r < rank) below += c;
+            }
+          }
+          int suf = all;  // items of buckets tid, tid + 1, ...
+#pragma unroll
+          for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_down_sync(0xffffffffu, suf, o);
+            if (tid + o < 32) suf += y;
+          }
+          if (tid < NB) s_cur[tid] = suf - all + below;
+          tot.x = __shfl_sync(0xffffffffu, suf, 0);
+        }
+        __syncthreads();
       }
     }
     int sl = i0 >> mp_sh, q = i0 & ((1 << mp_sh) - 1);
@@ -396,14 +437,16 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
           }
         } else if (p.kmax == 1 || (sq & kmask) == 0 || !joins(sq, q)) {
           if (pass == 0) {
-            ++nlead;
+            if (lf) atomicAdd(&s_hist[bucket(sq, q)], 1);
+            else ++nlead;
           } else {
             int ksz = 1;
             for (int j = 1; j < p.kmax && sq + j < S && ((sq + j) & kmask) != 0; ++j) {
               if (!joins(sq + j, q)) break;
               ++ksz;
             }
-            p.items[at.x++] = make_int4(sq, q, ksz, 0);
+            const int pos = lf ? atomicAdd(&s_cur[bucket(sq, q)], 1) : at.x++;
+            p.items[pos] = make_int4(sq, q, ksz, 0);
           }
         }
       }
@@ -1524,10 +1567,16 @@ pa_status launch_decode(DecodeParams p, const DeviceInfo &dev, cudaStream_t stre
   p.q_off = sp.q_off;
   p.stages_off = sp.stages_off;
   p.kmax = query_capacity(G) / G;
-  p.item_major = p.num_kv_heads >= 16;
   // runs of sequences sharing a whole partition's blocks go to the tensor
   // cores (16-bit caches, query groups of 2 or more, split sequences)
   const bool wide = !is_byte(KV) && G >= 2 && p.max_parts > 1;
+  // Claims take every KV head of an item in turn with 16 or more KV heads
+  // (neighbouring tiles of one block at a time), else head by head.  With
+  // wide items, the decode keeps the sequences' own tails, of varied
+  // lengths: those are listed longest first and claimed item by item, so
+  // that the last claims are short.
+  p.item_major = p.num_kv_heads >= 16 || wide;
+  p.longest_first = wide;
   p.wide_seqs = wide ? kWideRows / G : 0;
   p.wide_min = kWideMinRows / G;
   void (*kern)(DecodeParams);

@@ -85,6 +85,7 @@ struct DecodeParams {
   int num_stages, stage_bytes, k_off, v_off, q_off, stages_off;
   int kmax;   // most sequences one item may batch
   int item_major;  // claims take every KV head of an item in turn (else head by head)
+  int longest_first;  // items listed by stage count, longest first (else in slot order)
   int *work;  // [0] claim counter, [1] number of items, [2] number of wide items
   int4 *items;  // (first sequence, partition, sequences, 0)
   int4 *wide_items;  // the same, for the wide kernel
