@@ -121,7 +121,7 @@ __device__ __forceinline__ int clamp_len(int L, int cap, int *err) {
 __host__ __device__ constexpr int query_capacity(int G) { return G == 1 ? (PA_SHARE_G1 ? 4 : 1) : 8; }
 
 // ----------------------------------------------------------------------------
-// plan: list the work items in sequence order; reset the claim counter
+// plan: list the work items; reset the claim counter
 // ----------------------------------------------------------------------------
 // Work is indexed by slot (s, q), which exists when q is below the
 // sequence's partition count.  Partition q of sequence s is "full" when all
@@ -147,7 +147,9 @@ __host__ __device__ constexpr int query_capacity(int G) { return G == 1 ? (PA_SH
 //  3) each thread takes a run of consecutive slots and counts the items they
 //     lead; a block scan places them within the CTA, and the CTAs' totals,
 //     stored into every CTA's shared memory before one cluster barrier,
-//     place the CTA; the items are written in slot order.
+//     place the CTA; the items are written in slot order.  Longest first:
+//     each CTA counts its items by stage count instead, and each item takes
+//     a place in its count's range by a shared-memory atomic.
 
 // Exclusive prefix sums of two counts over the NW warps of the block;
 // *total = the block's sums.
